@@ -1,0 +1,34 @@
+"""Plain, slow, fp64 CPU oracle for the speculative-decoding verification pass.
+
+TEST INFRASTRUCTURE ONLY.  This package exists to check the CUDA library
+against the mathematics the pages define.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
+legs of ``bench.py`` may import it.  The product path (the C-ABI library and
+its Python binding) never imports, links or executes anything here, and this
+package imports nothing from the product package.
+
+Modules
+-------
+accept   -- temperature / nucleus distribution, the ratio test, residual
+            resampling, bonus token, greedy rule, inverse-CDF draw.
+model    -- the Llama-style decoder forward over the gamma+1 new positions
+            (RMSNorm, RoPE, GQA attention over a bf16 KV cache, SwiGLU,
+            LM head) and the KV rollback rule.
+weights  -- the seeded synthetic weights: Philox4x64-10 counter-based
+            generator + Box-Muller in fp64, rounded to bf16.
+bf16     -- round-to-nearest-even conversion of fp64 values to bf16.
+
+Every function cites the passage it follows.  Parity status per function:
+
+* accept.*                     pinned (worked example, exact enumeration,
+                               chi-square, alpha, E[tokens], greedy rule)
+* model.rmsnorm/rope/attention pinned against torch library routines and
+  /swiglu                      mathematical invariants
+* model.forward                pinned by invariants only (one pass equals
+                               sequential passes; rollback then re-verify
+                               equals a fresh pass; sublayers pinned above).
+                               The pages print no logits, so end-to-end
+                               values are otherwise unpinned.
+* weights                      pinned by the published Philox4x64-10
+                               known-answer vectors and normal moments.
+"""
