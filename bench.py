@@ -1,0 +1,452 @@
+"""Benchmark of one speculative-decoding verification pass on GB300.
+
+A step is the whole hot path on one batch: spec_verify_forward (the target's
+single pass over [t_last, x_1..x_gamma]) + spec_accept + spec_kv_truncate.
+Workload (default): 8B-shaped synthetic Llama decoder (32 layers, d 4096,
+32/8 heads of 128, SwiGLU 14336, vocab 128256, bf16 weights ~ N(0, 0.02^2)
+from seed), batch 1, gamma 4, 2048 cached tokens before every pass,
+temperature 1.0.  Drafts come from a noisy copy of the target (its own
+logits + N(0, 0.5^2) on the device, drawn with spec_draft_sample), produced
+outside the timed region.  Weights (15 GB) stream from HBM every step, so
+the inputs are larger than L2 and no flush is needed.
+
+The value is the verify pass's algorithmic HBM bytes per second (weights +
+KV read/write + logits + draft probabilities), with emitted tokens/s beside
+it.  Multi-GPU runs are independent replicas (the pass does not shard).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_pass_gb300 import binding as sb  # noqa: E402
+from speculative_decoding_verification_pass_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verify-pass HBM GB/s (% of peak) and emitted tokens/s, 8B-shape γ=4, batch 1"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p.get("bf16_tflops"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p:
+            time.sleep(0.25)
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        rows = [r.split(", ") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows]
+        mx = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+class Workload:
+    def __init__(self, cfg: sb.ModelConfig, B: int, gamma: int, ctx: int, T: float,
+                 top_p: float, sigma: float, seed: int, steps_cap: int):
+        self.cfg, self.B, self.gamma, self.ctx = cfg, B, gamma, ctx
+        self.T, self.top_p, self.sigma = T, top_p, sigma
+        self.n = gamma + 1
+        self.cap = ctx + self.n + 16
+        dev = "cuda"
+        self.model = sb.Model(cfg, 1000 + seed)
+        self.kv = sb.KVCache(cfg, B, self.cap)
+        hd = cfg.head_dim
+        K, V = wl.kv_prefix(seed, cfg.n_layers, B, cfg.n_kv_heads, ctx, hd)
+        self.kv.k[:, :, :, :ctx].copy_(torch.from_numpy(K.view(np.int16)).view(torch.bfloat16))
+        self.kv.v[:, :, :, :ctx].copy_(torch.from_numpy(V.view(np.int16)).view(torch.bfloat16))
+        del K, V
+        self.kv.len.fill_(ctx)
+        self.ws = sb.workspace(sb.spec_workspace_bytes(cfg, B, gamma, self.cap))
+        self.aws = sb.workspace(sb.spec_accept_workspace_bytes(B, gamma, cfg.vocab))
+        Vv = cfg.vocab
+        self.tokens = torch.zeros(B, self.n, dtype=torch.int32, device=dev)
+        self.logits = torch.empty(B, self.n, Vv, device=dev)
+        self.q = torch.zeros(B, gamma, Vv, device=dev)
+        self.x = torch.zeros(B, gamma, dtype=torch.int32, device=dev)
+        self.u = torch.zeros(B, self.n, device=dev)
+        self.out = torch.empty(B, self.n, dtype=torch.int32, device=dev)
+        self.nacc = torch.empty(B, dtype=torch.int32, device=dev)
+        self.zrow = torch.empty(B, 1, Vv, device=dev)
+        self.qrow = torch.empty(B, Vv, device=dev)
+        self.xrow = torch.empty(B, dtype=torch.int32, device=dev)
+        self.zeros = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.gen = torch.Generator(device=dev)
+        self.gen.manual_seed(seed)
+        self.t_last = torch.from_numpy(wl.tokens(seed, B, 1, Vv)).to(dev).view(B)
+        self.emitted = 0
+        self.accepted = 0
+
+    # ------------------------------------------------------------- harness
+    def draft(self):
+        """Untimed: gamma sequential single-token passes of the target give
+        its logits at each draft position; the draft distribution is
+        softmax((z + N(0, sigma^2)) / T) (+ top-p), x drawn from it."""
+        B, g = self.B, self.gamma
+        cur = self.t_last.view(B, 1).clone()
+        self.tokens[:, 0] = self.t_last
+        for i in range(g):
+            sb.spec_verify_forward(self.model.handle, cur, B, 0, self.kv, self.zrow, self.ws)
+            zq = self.zrow.view(B, -1) + self.sigma * torch.randn(B, self.cfg.vocab, device="cuda",
+                                                                  generator=self.gen)
+            ud = torch.rand(B, device="cuda", generator=self.gen)
+            sb.spec_draft_sample(zq.contiguous(), B, self.cfg.vocab, self.T, self.top_p, ud,
+                                 self.qrow, self.xrow, self.aws)
+            self.q[:, i] = self.qrow
+            self.x[:, i] = self.xrow
+            self.tokens[:, i + 1] = self.xrow
+            cur = self.xrow.view(B, 1).clone()
+        sb.spec_kv_truncate(self.kv, self.zeros, g, self.ws)      # back to the context
+        self.u.copy_(torch.rand(B, self.n, device="cuda", generator=self.gen))
+
+    def step(self, stream=None):
+        """The timed hot path."""
+        sb.spec_verify_forward(self.model.handle, self.tokens, self.B, self.gamma, self.kv,
+                               self.logits, self.ws, stream)
+        sb.spec_accept(self.logits, self.q, self.x, self.u, self.B, self.gamma, self.cfg.vocab,
+                       self.T, self.top_p, self.out, self.nacc, self.aws, stream)
+        sb.spec_kv_truncate(self.kv, self.nacc, self.gamma, self.ws, stream)
+
+    def finish(self):
+        """Untimed: count emitted tokens, take the last emitted token, and
+        return the cache to the fixed context for the next pass."""
+        n = self.nacc.cpu().numpy()
+        o = self.out.cpu().numpy()
+        self.emitted += int((n + 1).sum())
+        self.accepted += int(n.sum())
+        self.t_last = torch.from_numpy(o[np.arange(self.B), n].astype(np.int32)).cuda()
+        self.kv.len.fill_(self.ctx)
+
+    def check_status(self):
+        for ws in (self.ws, self.aws):
+            st, bits = sb.spec_device_status(ws)
+            if st != sb.SPEC_OK:
+                raise RuntimeError(f"device status {hex(bits)}")
+
+    # ---------------------------------------------------------- accounting
+    def bytes_per_step(self) -> float:
+        c = self.cfg
+        hd, d = c.head_dim, c.d_model
+        qkv = (c.n_heads + 2 * c.n_kv_heads) * hd
+        per_layer = (qkv * d + d * c.n_heads * hd + 2 * c.d_ffn * d + d * c.d_ffn) * 2
+        M = self.B * self.n
+        w = c.n_layers * per_layer + c.vocab * d * 2 + M * d * 2
+        kv_tok = c.n_layers * c.n_kv_heads * hd * 2 * 2
+        kv = self.B * ((self.ctx + self.n) * kv_tok + self.n * kv_tok)
+        logits = M * c.vocab * 4 * 2
+        q = self.B * self.gamma * c.vocab * 4
+        return float(w + kv + logits + q)
+
+    def gemm_bytes(self) -> float:
+        c = self.cfg
+        hd, d = c.head_dim, c.d_model
+        qkv = (c.n_heads + 2 * c.n_kv_heads) * hd
+        per_layer = (qkv * d + d * c.n_heads * hd + 2 * c.d_ffn * d + d * c.d_ffn) * 2
+        return float(c.n_layers * per_layer + c.vocab * d * 2)
+
+    def launches_per_step(self) -> int:
+        return 1 + 5 * self.cfg.n_layers + 1 + 2
+
+
+def time_steps(w: Workload, K: int):
+    """Per-step device time (CUDA events on the launch stream), synchronised
+    on both sides of each step; drafting happens between steps."""
+    st = torch.cuda.current_stream()
+    times = []
+    for _ in range(K):
+        w.draft()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        w.step()
+        b.record(st)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+        w.finish()
+    return times
+
+
+def time_e2e(w: Workload, K: int):
+    """The same step through the C ABI with host buffers: pinned host inputs
+    (tokens, draft probabilities, draft tokens, uniforms) copied in and the
+    emitted tokens + n_accepted copied out inside the timed region."""
+    st = torch.cuda.current_stream()
+    h_tok = torch.empty_like(w.tokens, device="cpu").pin_memory()
+    h_q = torch.empty_like(w.q, device="cpu").pin_memory()
+    h_x = torch.empty_like(w.x, device="cpu").pin_memory()
+    h_u = torch.empty_like(w.u, device="cpu").pin_memory()
+    h_out = torch.empty_like(w.out, device="cpu").pin_memory()
+    h_n = torch.empty_like(w.nacc, device="cpu").pin_memory()
+    times = []
+    for _ in range(K):
+        w.draft()
+        h_tok.copy_(w.tokens)
+        h_q.copy_(w.q)
+        h_x.copy_(w.x)
+        h_u.copy_(w.u)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        w.tokens.copy_(h_tok, non_blocking=True)
+        w.q.copy_(h_q, non_blocking=True)
+        w.x.copy_(h_x, non_blocking=True)
+        w.u.copy_(h_u, non_blocking=True)
+        w.step()
+        h_out.copy_(w.out, non_blocking=True)
+        h_n.copy_(w.nacc, non_blocking=True)
+        b.record(st)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+        w.finish()
+    h2d = sum(t.numel() * t.element_size() for t in (h_tok, h_q, h_x, h_u))
+    d2h = h_out.numel() * h_out.element_size() + h_n.numel() * h_n.element_size()
+    return times, h2d, d2h
+
+
+def instrumented(w: Workload, K: int):
+    """Per-kernel-kind device time of the GEMM and attention launches (events
+    around each launch, so launches are serialised; separate from the
+    headline timing)."""
+    sb.spec_timing_enable(w.model.handle, True)
+    sb.spec_timing_read(w.model.handle)
+    for _ in range(K):
+        w.draft()
+        sb.spec_timing_read(w.model.handle)     # drop the draft passes
+        w.step()
+        ms, n, by = sb.spec_timing_read(w.model.handle)
+        w.finish()
+        yield ms, n, by
+    sb.spec_timing_enable(w.model.handle, False)
+
+
+def accept_time(w: Workload, K: int):
+    st = torch.cuda.current_stream()
+    ts = []
+    for _ in range(K):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        sb.spec_accept(w.logits, w.q, w.x, w.u, w.B, w.gamma, w.cfg.vocab, w.T, w.top_p, w.out,
+                       w.nacc, w.aws)
+        b.record(st)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_step_estimate(cfg: sb.ModelConfig, B: int, gamma: int, ctx: int, T: float, seed: int,
+                         head_rows: int = 8192):
+    """The oracle timed on this host on a bounded sample of the same step:
+    one decoder layer of the 8B shape over the gamma+1 new positions at the
+    same context (cache contents from the same generator), an LM-head slice
+    of head_rows rows, and the accept rule on a full-vocabulary step; scaled
+    to a whole step as n_layers * layer + (V / head_rows) * head + accept."""
+    from oracle import accept as OA
+    from oracle import model as OM
+    from oracle import weights as OW
+    one = OM.Config(1, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn, head_rows,
+                    cfg.rms_eps, cfg.rope_theta)
+    W = OW.Weights(one, 1000 + seed)
+    W.layer(0)
+    W.head()
+    kvs = OM.KVState(one, B, ctx + gamma + 1)
+    K, V = wl.kv_prefix(seed, 1, B, cfg.n_kv_heads, ctx, cfg.head_dim)
+    from oracle.bf16 import from_bits
+    kvs.load_prefix([from_bits(K[0])], [from_bits(V[0])], [ctx] * B)
+    toks = wl.tokens(seed, B, gamma + 1, head_rows)
+    t0 = time.perf_counter()
+    OM.forward(one, W, toks, kvs)
+    t_fwd = time.perf_counter() - t0
+    x = np.random.default_rng(seed).standard_normal((B * (gamma + 1), cfg.d_model))
+    t0 = time.perf_counter()
+    OM.lm_head(x, W.head())
+    t_head = time.perf_counter() - t0
+    zq, zp = wl.accept_logits(seed, 1, gamma, cfg.vocab)
+    ud = wl.uniforms(seed, 1, gamma, stream=8)
+    q, xs, _ = OA.draft_sample(zq[0, :gamma], ud[0], T)
+    u = wl.uniforms(seed, 1, gamma + 1)[0]
+    t0 = time.perf_counter()
+    OA.accept(zp[0], q, xs, u, T)
+    t_acc = (time.perf_counter() - t0) * B
+    est = cfg.n_layers * max(t_fwd - t_head, 1e-9) + (cfg.vocab / head_rows) * t_head + t_acc
+    sample = (f"1 of {cfg.n_layers} decoder layers (M={B * (gamma + 1)}, context {ctx}), "
+              f"LM head {head_rows} of {cfg.vocab} rows, accept on one full-vocabulary step; "
+              f"scaled to a full step ({t_fwd + t_acc:.1f} s measured)")
+    return est, sample
+
+
+def blas_threads():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ main
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--gamma", type=int, default=4)
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--context", type=int, default=2048)
+    ap.add_argument("--temperature", type=float, default=1.0)
+    ap.add_argument("--top-p", type=float, default=1.0)
+    ap.add_argument("--sigma", type=float, default=0.5)
+    ap.add_argument("--shape", default="8b", choices=["8b", "1b"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = sb.LLAMA_8B if args.shape == "8b" else sb.LLAMA_1B
+    workload = (f"{args.shape.upper()}-shaped synthetic Llama decoder verify pass + accept + "
+                f"rollback, batch {args.batch}, gamma {args.gamma}, context {args.context}, "
+                f"T={args.temperature}, top_p={args.top_p}, noisy-target draft sigma {args.sigma}")
+    config = {"workload": workload, "batch": args.batch, "gamma": args.gamma,
+              "context": args.context, "temperature": args.temperature, "top_p": args.top_p,
+              "l2": "inputs larger than L2 (weights stream from HBM every step)",
+              "parallelism": f"replicas x{world}"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        est, sample = oracle_step_estimate(cfg, args.batch, args.gamma, args.context,
+                                           args.temperature, 3)
+        w_bytes = Workload.bytes_per_step.__get__(type("W", (), {
+            "cfg": cfg, "B": args.batch, "n": args.gamma + 1, "gamma": args.gamma,
+            "ctx": args.context}))()
+        val = w_bytes / est / 1e9
+        line = {"metric": METRIC, "value": val, "unit": "GB/s", "impl": "reference",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": blas_threads(),
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    __import__("__graft_entry__").build()
+    w = Workload(cfg, args.batch, args.gamma, args.context, args.temperature, args.top_p,
+                 args.sigma, seed=3 + rank, steps_cap=args.steps)
+    time_steps(w, args.warmup)
+    w.check_status()
+    w.emitted = w.accepted = 0
+    if world > 1:
+        torch.distributed.barrier()
+    with ClockSampler(local) as clk:
+        times = time_steps(w, args.steps)
+    w.check_status()
+    emitted, accepted = w.emitted, w.accepted
+    t_total = sum(times) / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t_total], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_total = float(tt)
+    step_bytes = w.bytes_per_step()
+    value = step_bytes * args.steps * world / t_total / 1e9
+    e2e_times, h2d, d2h = time_e2e(w, max(3, args.steps // 2))
+    e2e_val = step_bytes * len(e2e_times) * world / (sum(e2e_times) / 1e3) / 1e9
+    gm = gn = gb = am = an = 0.0
+    for ms, n, by in instrumented(w, 3):
+        gm += ms[0]; gn += n[0]; gb += by[0]; am += ms[1]; an += n[1]
+    acc_ms = accept_time(w, 10)
+    hbm, _, src = peaks()
+    achieved = gb / (gm / 1e3) / 1e9 if gm else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config,
+        "emitted_tokens_per_s": emitted * world / t_total,
+        "acceptance": accepted / max(1, args.steps * args.batch * args.gamma),
+        "hbm_frac_of_8tbs": value / world / 8000.0,
+        "hbm_frac_of_measured": value / world / hbm,
+        "bytes_per_step": step_bytes,
+        "accept_us": acc_ms * 1e3, "accept_frac_of_step": acc_ms / (t_total / args.steps * 1e3),
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": w.launches_per_step() * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": (achieved / hbm) if achieved else None, "traffic": None,
+                     "kernel": "gemm_tc_kernel", "peak_source": src,
+                     "launch_ms": gm / gn if gn else None,
+                     "attention_ms_per_launch": am / an if an else None},
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        est, sample = oracle_step_estimate(cfg, args.batch, args.gamma, args.context,
+                                           args.temperature, 3)
+        line["cpu_baseline"] = {"value": step_bytes / est / 1e9, "unit": "GB/s",
+                                "cores": blas_threads(), "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line))
+    w.model.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

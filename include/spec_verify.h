@@ -1,0 +1,243 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding
+ * verification pass.
+ *
+ * The library runs one verification pass of lossless speculative decoding
+ * on one GPU:
+ *   1. spec_verify_forward: the target model's single forward over the
+ *      gamma drafted tokens plus the bonus position (one weight read for all
+ *      gamma+1 positions), producing fp32 logits for the gamma+1 positions.
+ *   2. spec_accept: the acceptance rule -- temperature / top-p applied to the
+ *      target rows, accept x_i iff u_i < min(1, p(x_i)/q(x_i)), resample from
+ *      norm(max(0, p - q)) at the first rejection, or draw a bonus token from
+ *      p at position gamma+1 when every draft survives.
+ *   3. spec_kv_truncate: KV rollback by a length update (no memset).
+ *
+ * Sources (page title, section):
+ *   [pigeon]   "Speculative decoding" (pigeon guide): How it works (steps 1-5),
+ *              Why the output is exactly p, Speed, When it breaks.
+ *   [lattice]  "Speculative decoding" (lattice-ai-eng inference notes): the
+ *              rule, the worked example, the reference generation loop.
+ *   [engine]   "Build a Speculative Decoding Engine to Cut LLM Latency by 3x":
+ *              The Accept/Reject Mechanism, KV Cache Management for Dual
+ *              Models, Rollback Protocol, Batch-Level Speculation.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer named d_* is DEVICE memory owned by the caller (allocated
+ *   with cudaMalloc / a framework allocator).  The library never allocates,
+ *   frees or retains device memory.  `stream` is a cudaStream_t passed as
+ *   void* (NULL = the legacy default stream).
+ * - Calls are asynchronous on `stream`.  The return value reports argument
+ *   validation and launch errors only (spec_status, 0 = OK, negative =
+ *   error; nothing is enqueued on error).  Errors the device detects (a token
+ *   id outside the vocabulary, a cache that would overflow its capacity,
+ *   q(x) <= 0 for a drafted token, a bounded wait that ran out) set a status
+ *   word in the workspace; kernels never trap.  Read and clear it with
+ *   spec_device_status.
+ * - Every call is usable inside CUDA stream capture (no host synchronisation,
+ *   no allocation) except spec_device_status, which synchronises `stream`.
+ * - Layouts are row-major.  bf16 is IEEE bfloat16 stored as uint16.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ----------------------------------------------------------------- status */
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_EINVAL = -1,   /* a NULL pointer, a negative size, T < 0, top_p outside (0,1] */
+  SPEC_ESIZE = -2,    /* a size above a documented limit or a buffer too small */
+  SPEC_ECUDA = -3,    /* a CUDA launch / runtime error (see spec_last_cuda_error) */
+  SPEC_EDEVICE = -4,  /* returned by spec_device_status: the device set a status */
+  SPEC_ETIMEOUT = -5, /* device status: a bounded wait gave up */
+  SPEC_ENOTSUP = -6   /* the GPU is not sm_103 / the config is not supported */
+} spec_status;
+
+/* Device status bits (the value spec_device_status writes to *out). */
+#define SPEC_DEV_BAD_TOKEN     0x1   /* an input / draft token id outside [0, V) */
+#define SPEC_DEV_KV_OVERFLOW   0x2   /* len[b] + gamma + 1 > capacity, or truncate below 0 */
+#define SPEC_DEV_Q_ZERO        0x4   /* q(x_i) <= 0 for a drafted token (treated as a rejection) */
+#define SPEC_DEV_TIMEOUT       0x8   /* a bounded wait in a kernel gave up */
+#define SPEC_DEV_BAD_NACC      0x10  /* truncate: n_accepted outside [0, gamma] */
+
+/* Text for a spec_status value (static storage). */
+const char* spec_status_string(int status);
+/* The CUDA error string of the last SPEC_ECUDA on this thread. */
+const char* spec_last_cuda_error(void);
+
+/* ------------------------------------------------------------------ model */
+/* A Llama-style decoder ("8B-shaped": 32 layers, d 4096, 32 heads / 8 KV
+ * heads of 128, SwiGLU ffn 14336, vocab 128256; "1B-shaped": 16, 2048,
+ * 32/8 of 64, 8192, 32000).  Constraints: d_model = n_heads * head_dim,
+ * n_heads % n_kv_heads == 0, head_dim in {64, 128}, d_model, n_heads*head_dim,
+ * d_ffn multiples of 128 (d_ffn of 64 allowed), vocab >= 1.  n_layers = 0
+ * gives an LM-head-only model (embedding + head). */
+typedef struct {
+  int n_layers;
+  int d_model;
+  int n_heads;
+  int n_kv_heads;
+  int d_ffn;
+  int vocab;
+  float rms_eps;     /* RMSNorm epsilon, e.g. 1e-5 */
+  float rope_theta;  /* RoPE base, e.g. 500000 */
+} spec_model_config;
+
+typedef struct spec_model spec_model; /* opaque host-side handle */
+
+/* Bytes of the device buffer that holds all weights of `cfg` (bf16 matrices
+ * plus fp32 norm gains, each 256-byte aligned).  0 if cfg is invalid. */
+size_t spec_model_weight_bytes(const spec_model_config* cfg);
+
+/* Fill the caller's device buffer d_weights (>= spec_model_weight_bytes) with
+ * seeded synthetic weights and return a handle in *out.
+ * Every matrix element is bf16_round_nearest_even(0.02 * z) with z a standard
+ * normal from Box-Muller (fp64) over Philox4x64-10 (Salmon et al. 2011):
+ * logical tensor t, element e uses counter (e/4 + 1, t, 0, 0), key (seed, 0);
+ * outputs (0,1) and (2,3) of a block are the Box-Muller pairs of elements
+ * 4(e/4)+{0,1} and +{2,3}.  Tensor ids: 0 embedding [V][d], 1 LM head [V][d],
+ * layer l: 2+7l+{0 W_q, 1 W_k, 2 W_v, 3 W_o, 4 W_gate, 5 W_up, 6 W_down}, all
+ * [out][in].  RMSNorm gains are 1.0.  The generation is enqueued on `stream`.
+ * Requires an sm_103 device (else SPEC_ENOTSUP).  The handle keeps the
+ * pointer; the buffer must outlive the handle. */
+int spec_model_create(const spec_model_config* cfg, uint64_t seed, void* d_weights,
+                      size_t weight_bytes, void* stream, spec_model** out);
+
+/* Free the host handle (never the caller's device buffer). NULL is a no-op. */
+int spec_model_destroy(spec_model* model);
+
+/* Where a logical weight lives, for tests that compare the generator with an
+ * independent implementation.  which = 0..6 per layer as above (layer >= 0),
+ * or layer = -1 with which 0 = embedding, 1 = LM head.  The physical storage
+ * of W_gate/W_up is interleaved (blocks of 64 gate rows then 64 up rows), so
+ * for them *row_stride_rows = 128 and *block_rows = 64 with *d_ptr at the
+ * first row of the tensor's first block; for every other matrix the rows are
+ * contiguous (*row_stride_rows = *block_rows = rows).  shape = {rows, cols}. */
+int spec_model_tensor(const spec_model* model, int layer, int which, const void** d_ptr,
+                      int64_t shape[2], int* block_rows, int* row_stride_rows);
+
+/* ---------------------------------------------------------------- KV cache */
+/* The target KV cache, caller-owned:
+ *   k, v : bf16 [n_layers][batch][n_kv_heads][capacity][head_dim]
+ *   len  : int32 [batch] device array, the valid length of each sequence.
+ * A pass appends gamma+1 slots at len[b] .. len[b]+gamma and advances len;
+ * spec_kv_truncate moves len back ([engine] KV Cache Management: "a pointer
+ * update only"). */
+typedef struct {
+  void* k;
+  void* v;
+  int32_t* len;
+  int batch;
+  int capacity;
+} spec_kv_cache;
+
+/* Bytes of ONE of the k / v buffers. */
+size_t spec_kv_bytes(const spec_model_config* cfg, int batch, int capacity);
+
+/* ---------------------------------------------------------------- forward */
+/* Workspace bytes for spec_verify_forward / spec_lm_head on `batch`
+ * sequences of gamma+1 new tokens with a cache of `capacity` slots.  The
+ * workspace also holds the device status word; one workspace serves one
+ * stream at a time. */
+size_t spec_workspace_bytes(const spec_model_config* cfg, int batch, int gamma, int capacity);
+
+/* One verification forward ([pigeon] How it works, step 2; [lattice] the
+ * single target call over the k drafted positions and the next-token slot).
+ *   d_tokens  int32 [batch][gamma+1] = [t_last, x_1 .. x_gamma]: t_last is the
+ *             previous pass's emitted token, not yet in the cache.
+ *   kv        the cache; slots len[b] .. len[b]+gamma receive the new keys /
+ *             values (RoPE positions len[b]+j) and len[b] += gamma+1.
+ *   d_logits  fp32 [batch][gamma+1][vocab]; row j predicts the token after
+ *             input j (rows 0..gamma-1 score x_1..x_gamma, row gamma is the
+ *             bonus position).
+ * Limits: batch*(gamma+1) <= 512, gamma+1 <= 128; prefill uses the same call
+ * with gamma = prompt_len - 1 in chunks.  A token id outside [0, V) is read as
+ * 0 and sets SPEC_DEV_BAD_TOKEN; a sequence whose len[b]+gamma+1 exceeds the
+ * capacity sets SPEC_DEV_KV_OVERFLOW, its slots beyond the capacity are not
+ * written and its logits are unspecified. */
+int spec_verify_forward(const spec_model* model, const int32_t* d_tokens, int batch, int gamma,
+                        const spec_kv_cache* kv, float* d_logits, void* d_ws, size_t ws_bytes,
+                        void* stream);
+
+/* LM head alone on given activations: d_logits[m][v] = sum_k hidden[m][k] *
+ * W_head[v][k] (no norm).  d_hidden bf16 [rows][d_model], rows <= 512.
+ * Workspace: spec_workspace_bytes(cfg, rows, 0, 1) suffices. */
+int spec_lm_head(const spec_model* model, const uint16_t* d_hidden, int rows, float* d_logits,
+                 void* d_ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------- accept */
+/* Workspace bytes for spec_accept / spec_draft_sample (status word and
+ * per-row statistics). */
+size_t spec_accept_workspace_bytes(int batch, int gamma, int vocab);
+
+/* The acceptance step, one CTA per sequence ([pigeon] How it works, steps
+ * 3-5; [engine] The Accept/Reject Mechanism).
+ *   d_target_logits fp32 [batch][gamma+1][vocab]
+ *   d_draft_probs   fp32 [batch][gamma][vocab]: the distributions the drafts
+ *                   were drawn from, after the same temperature / top-p
+ *                   ([pigeon] When it breaks).  Unused when temperature = 0.
+ *   d_draft_tokens  int32 [batch][gamma]
+ *   d_uniforms      fp32 [batch][gamma+1] in [0,1): u_i (i < gamma) is the coin
+ *                   of draft i, u_gamma drives the one residual / bonus draw.
+ *                   Unused when temperature = 0.
+ *   temperature     >= 0; 0 is greedy: accept while x_i = argmax (lowest id on
+ *                   ties), emit the argmax at the first mismatch or the bonus.
+ *   top_p           in (0, 1]; 1 disables the nucleus.  The nucleus keeps every
+ *                   token whose probability is >= that of the token where the
+ *                   descending cumulative mass first reaches top_p.
+ *   d_out_tokens    int32 [batch][gamma+1]: x_1..x_n, then the correction or
+ *                   bonus token, then -1 padding.
+ *   d_n_accepted    int32 [batch].
+ * A draw is the inverse CDF in token-id order: the smallest id t with
+ * cumulative weight > u * total.  A rejection whose residual mass is <= 1e-8
+ * draws from p instead ([engine]'s numerical fallback). */
+int spec_accept(const float* d_target_logits, const float* d_draft_probs,
+                const int32_t* d_draft_tokens, const float* d_uniforms, int batch, int gamma,
+                int vocab, float temperature, float top_p, int32_t* d_out_tokens,
+                int32_t* d_n_accepted, void* d_ws, size_t ws_bytes, void* stream);
+
+/* The draft side of "applied identically": for each of `rows` logits rows,
+ * q = top-p(softmax(z / T)) written to d_probs (fp32 [rows][vocab], may be
+ * NULL) and one token drawn from q with d_uniforms[r] by the same inverse CDF
+ * (T = 0: the argmax; d_probs then one-hot).  Used to produce draft
+ * distributions for spec_accept. */
+int spec_draft_sample(const float* d_logits, int rows, int vocab, float temperature, float top_p,
+                      const float* d_uniforms, float* d_probs, int32_t* d_tokens, void* d_ws,
+                      size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------- rollback */
+/* KV rollback after a pass that appended gamma+1 slots ([engine] Rollback
+ * Protocol): len[b] -= gamma - n_accepted[b], so t_last and the accepted
+ * drafts stay and the rejected drafts' slots are dropped.  Nothing is
+ * cleared.  n_accepted outside [0, gamma] or a length that would go negative
+ * leaves len[b] unchanged and sets a device status bit in d_ws (which may be
+ * the forward's or the accept's workspace). */
+int spec_kv_truncate(const spec_kv_cache* kv, const int32_t* d_n_accepted, int gamma, void* d_ws,
+                     void* stream);
+
+/* ----------------------------------------------------------------- status */
+/* Synchronise `stream`, read the device status word of workspace d_ws into
+ * *out (a SPEC_DEV_* bit set), clear it, and return SPEC_OK if it was 0,
+ * SPEC_ETIMEOUT if the timeout bit was set, else SPEC_EDEVICE. */
+int spec_device_status(void* d_ws, void* stream, int32_t* out);
+
+/* ------------------------------------------------------------ diagnostics */
+/* Per-kernel-kind timing for benchmarks.  When enabled on a model, every
+ * subsequent forward records CUDA events around each launch of the GEMM and
+ * attention kernels (this serialises the launches it brackets).  spec_timing_read
+ * synchronises and returns, per kind (0 = GEMM, 1 = attention), the summed
+ * milliseconds, launch count and algorithmic bytes since the last read. */
+int spec_timing_enable(spec_model* model, int enable);
+int spec_timing_read(spec_model* model, double ms[2], int64_t launches[2], double bytes[2]);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -64,7 +64,7 @@ class NucleusInfo:
     boundary: bool = False   # cumulative mass within TOPP_MARGIN of top_p near k*
 
 
-def nucleus(P: np.ndarray, top_p: float) -> tuple[np.ndarray, NucleusInfo]:
+def nucleus(P: np.ndarray, top_p: float, margin: float = TOPP_MARGIN) -> tuple[np.ndarray, NucleusInfo]:
     """Top-p filter of one probability row, then renormalise.
 
     Reading of "top-p ... applied identically to p and q" (pigeon guide,
@@ -87,9 +87,9 @@ def nucleus(P: np.ndarray, top_p: float) -> tuple[np.ndarray, NucleusInfo]:
     out = np.where(keep, P, 0.0)
     out = out / out.sum()
     info.kstar, info.tau, info.kept = kstar, float(tau), int(keep.sum())
-    near = abs(c[kstar] - top_p) < TOPP_MARGIN
+    near = abs(c[kstar] - top_p) < margin
     if kstar > 0:
-        near = near or abs(c[kstar - 1] - top_p) < TOPP_MARGIN
+        near = near or abs(c[kstar - 1] - top_p) < margin
     # two probabilities that are distinct in fp64 may tie in fp32 right at the
     # threshold; then the device keeps both and the oracle one
     if kstar + 1 < P.size:
@@ -99,9 +99,9 @@ def nucleus(P: np.ndarray, top_p: float) -> tuple[np.ndarray, NucleusInfo]:
     return out, info
 
 
-def target_dist(z, temperature: float, top_p: float = 1.0):
+def target_dist(z, temperature: float, top_p: float = 1.0, margin: float = TOPP_MARGIN):
     """The distribution a row of logits stands for: softmax(z/T), then top-p."""
-    return nucleus(softmax_t(z, temperature), top_p)
+    return nucleus(softmax_t(z, temperature), top_p, margin)
 
 
 def argmax_lowest(z) -> int:
@@ -115,7 +115,7 @@ class Draw:
     boundary: bool
 
 
-def inverse_cdf(w, u: float) -> Draw:
+def inverse_cdf(w, u: float, margin: float = CDF_MARGIN) -> Draw:
     """Categorical draw from non-negative weights w with one uniform u in [0,1).
 
     Returns the smallest token id t with C_t = sum_{x<=t} w(x) > u * S,
@@ -133,9 +133,9 @@ def inverse_cdf(w, u: float) -> Draw:
     t = int(np.searchsorted(C, thr, side="right"))    # first C_t > thr
     if t >= w.size:                                    # u*S rounded up to S
         t = int(np.flatnonzero(w > 0)[-1])
-    near = abs(C[t] - thr) < CDF_MARGIN * S
+    near = abs(C[t] - thr) < margin * S
     if t > 0:
-        near = near or abs(C[t - 1] - thr) < CDF_MARGIN * S
+        near = near or abs(C[t - 1] - thr) < margin * S
     return Draw(t, bool(near))
 
 
@@ -158,7 +158,7 @@ class AcceptResult:
 
 
 def accept(z_target, q_draft, draft_tokens, uniforms, temperature: float,
-           top_p: float = 1.0) -> AcceptResult:
+           top_p: float = 1.0, margins: tuple | None = None) -> AcceptResult:
     """One sequence's verification outcome.
 
     z_target     [gamma+1][V] target logits (row i scores the token after
@@ -168,6 +168,8 @@ def accept(z_target, q_draft, draft_tokens, uniforms, temperature: float,
                  from, already after the same T / top-p (ignored for T = 0).
     draft_tokens [gamma] x_1..x_gamma.
     uniforms     [gamma+1] u_0..u_gamma in [0, 1) (ignored for T = 0).
+    margins      (ratio, cdf, top_p) widths of the boundary flags; the
+                 defaults cover fp32-vs-fp64 arithmetic on identical inputs.
 
     Follows pigeon *How it works* steps 3-5 and the lattice notes' rule.
     """
@@ -194,11 +196,12 @@ def accept(z_target, q_draft, draft_tokens, uniforms, temperature: float,
         out[gamma] = a
         return AcceptResult(out, gamma, a, True)
 
+    rm, cm, tm = margins if margins is not None else (RATIO_MARGIN, CDF_MARGIN, TOPP_MARGIN)
     q = np.asarray(q_draft, dtype=np.float64)
     u = np.asarray(uniforms, dtype=np.float64)
     res = AcceptResult(out, 0, -1, False)
     for i in range(gamma):
-        P, info = target_dist(z[i], temperature, top_p)
+        P, info = target_dist(z[i], temperature, top_p, tm)
         res.topp_boundary |= info.boundary
         x = int(draft_tokens[i])
         if not 0 <= x < V:
@@ -207,7 +210,7 @@ def accept(z_target, q_draft, draft_tokens, uniforms, temperature: float,
             raise ValueError("q(x) = 0 for a drafted token")
         a = min(1.0, P[x] / q[i, x])
         res.ratios.append(a)
-        if abs(u[i] - a) < RATIO_MARGIN:
+        if abs(u[i] - a) < rm:
             res.ratio_boundary = True
         if u[i] < a:
             out[i] = x
@@ -218,14 +221,14 @@ def accept(z_target, q_draft, draft_tokens, uniforms, temperature: float,
         S = r.sum()
         if RESIDUAL_FALLBACK * 0.1 < S < RESIDUAL_FALLBACK * 10:
             res.fallback_boundary = True
-        d = inverse_cdf(r if S > RESIDUAL_FALLBACK else P, u[gamma])
+        d = inverse_cdf(r if S > RESIDUAL_FALLBACK else P, u[gamma], cm)
         res.cdf_boundary = d.boundary
         out[i] = d.token
         res.emitted = d.token
         return res
-    P, info = target_dist(z[gamma], temperature, top_p)
+    P, info = target_dist(z[gamma], temperature, top_p, tm)
     res.topp_boundary |= info.boundary
-    d = inverse_cdf(P, u[gamma])
+    d = inverse_cdf(P, u[gamma], cm)
     res.cdf_boundary = d.boundary
     out[gamma] = d.token
     res.emitted = d.token

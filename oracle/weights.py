@@ -27,6 +27,10 @@ Matrices are [out][in], row-major.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import multiprocessing as mp
+import os
+
 import numpy as np
 
 from .bf16 import round_bf16
@@ -65,19 +69,51 @@ def normals(seed: int, tid: int, start: int, count: int) -> np.ndarray:
     return z[off:off + count]
 
 
+def _chunk(args):
+    seed, tid, start, count = args
+    return round_bf16(SCALE * normals(seed, tid, start, count)).astype(np.float32)
+
+
+_POOL = None
+
+
+def _pool():
+    """Worker processes for large tensors (spawned, never forked, so they are
+    safe to start after CUDA has been initialised in the parent)."""
+    global _POOL
+    if _POOL is None:
+        n = int(os.environ.get("ORACLE_WORKERS", min(16, os.cpu_count() or 1)))
+        if n > 1:
+            _POOL = cf.ProcessPoolExecutor(n, mp_context=mp.get_context("spawn"))
+        else:
+            _POOL = False
+    return _POOL
+
+
 def tensor(seed: int, tid: int, rows: int, cols: int,
            row0: int = 0, nrows: int | None = None,
-           chunk: int = 1 << 24) -> np.ndarray:
+           chunk: int = 1 << 22) -> np.ndarray:
     """Rows [row0, row0+nrows) of a [rows][cols] weight matrix as fp32
-    arrays holding bf16-exact values."""
+    arrays holding bf16-exact values (element order is independent of how
+    the range is split into chunks)."""
     if nrows is None:
         nrows = rows - row0
     out = np.empty(nrows * cols, dtype=np.float32)
     start = row0 * cols
     n = nrows * cols
-    for c0 in range(0, n, chunk):
-        c1 = min(n, c0 + chunk)
-        out[c0:c1] = round_bf16(SCALE * normals(seed, tid, start + c0, c1 - c0))
+    jobs = [(seed, tid, start + c0, min(n, c0 + chunk) - c0) for c0 in range(0, n, chunk)]
+    pool = _pool() if len(jobs) > 2 else False
+    parts = None
+    if pool:
+        try:
+            parts = list(pool.map(_chunk, jobs))
+        except cf.process.BrokenProcessPool:     # e.g. a parent without a main file
+            global _POOL
+            _POOL = False
+    if parts is None:
+        parts = map(_chunk, jobs)
+    for (_, _, s0, cnt), part in zip(jobs, parts):
+        out[s0 - start:s0 - start + cnt] = part
     return out.reshape(nrows, cols)
 
 

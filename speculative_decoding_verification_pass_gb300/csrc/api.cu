@@ -1,0 +1,747 @@
+// The C ABI declared in include/spec_verify.h: argument validation, the
+// weight and workspace layouts, TMA descriptors and the launch sequence of
+// one verification pass.  No device memory is allocated here.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using namespace spec;
+
+namespace {
+
+thread_local std::string g_cuda_error;
+
+int cuda_fail(cudaError_t e) {
+  g_cuda_error = cudaGetErrorString(e);
+  return SPEC_ECUDA;
+}
+
+#define SPEC_CUDA(call)                        \
+  do {                                         \
+    cudaError_t e_ = (call);                   \
+    if (e_ != cudaSuccess) return cuda_fail(e_); \
+  } while (0)
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxGrid = 192;      // stream-K grid cap (>= SM count of the part)
+constexpr int kMaxTok = 256;       // token rows per GEMM launch (UMMA N limit)
+constexpr int kMaxM = 512;         // token rows per pass
+constexpr int kMaxN = 128;         // gamma + 1 per pass
+constexpr size_t kGemmSmemBudget = 200 * 1024;
+
+size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+int round_up(int x, int a) { return (x + a - 1) / a * a; }
+
+bool cfg_ok(const spec_model_config* c) {
+  if (!c) return false;
+  if (c->n_layers < 0 || c->d_model <= 0 || c->vocab <= 0) return false;
+  if (c->d_model % 128) return false;
+  if (c->n_layers == 0) return true;
+  if (c->n_heads <= 0 || c->n_kv_heads <= 0 || c->n_heads % c->n_kv_heads) return false;
+  if (c->d_model % c->n_heads) return false;
+  const int hd = c->d_model / c->n_heads;
+  if (hd != 64 && hd != 128) return false;
+  if (c->d_ffn <= 0 || c->d_ffn % 64) return false;
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.f)) return false;
+  return true;
+}
+
+struct Layout {
+  size_t embed, head, gfinal, rope;
+  std::vector<size_t> g_attn, g_mlp, wqkv, wo, wgu, wd;
+  size_t total;
+};
+
+Layout layout_of(const spec_model_config& c) {
+  Layout L;
+  const size_t d = c.d_model, V = c.vocab;
+  const int hd = c.n_layers ? c.d_model / c.n_heads : 128;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.embed = take(V * d * 2);
+  L.head = take(V * d * 2);
+  L.gfinal = take(d * 4);
+  L.rope = take(static_cast<size_t>(hd / 2) * 8);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const size_t qkv = static_cast<size_t>(c.n_heads + 2 * c.n_kv_heads) * hd;
+    L.g_attn.push_back(take(d * 4));
+    L.g_mlp.push_back(take(d * 4));
+    L.wqkv.push_back(take(qkv * d * 2));
+    L.wo.push_back(take(d * static_cast<size_t>(c.n_heads) * hd * 2));
+    L.wgu.push_back(take(2ull * c.d_ffn * d * 2));
+    L.wd.push_back(take(d * c.d_ffn * 2));
+  }
+  L.total = o;
+  return L;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 [rows][cols] row-major, box = box_rows x 64 columns, 128-byte swizzle;
+// rows outside the tensor read as zero.
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct WsPlan {
+  size_t status, pos_base, seq_ok, counters, ssq, h, hb, hb_lo, q, q_lo, o, o_lo, act, act_lo,
+      gpart, apart_o, apart_ml;
+  size_t total;
+  int n_counters, attn_counter0, ssq_ld, splits, R, M, n;
+};
+
+int max_tiles(const spec_model_config& c) {
+  int t = (c.vocab + 127) / 128;
+  if (c.n_layers) {
+    const int hd = c.d_model / c.n_heads;
+    t = std::max(t, (c.n_heads + 2 * c.n_kv_heads) * hd / 128 + 1);
+    t = std::max(t, c.d_model / 128);
+    t = std::max(t, 2 * c.d_ffn / 128);
+  }
+  return t;
+}
+
+WsPlan plan_ws(const spec_model_config& c, int B, int gamma, int cap) {
+  WsPlan p{};
+  p.n = gamma + 1;
+  p.M = B * p.n;
+  const int M = p.M;
+  const int mpad = round_up(std::max(M, 1), 16);
+  const int ntok = std::min(kMaxTok, mpad);
+  const int hd = c.n_layers ? c.d_model / c.n_heads : 128;
+  const int Hkv = c.n_layers ? c.n_kv_heads : 1;
+  const int G = c.n_layers ? c.n_heads / c.n_kv_heads : 1;
+  p.ssq_ld = mpad;
+  p.splits = (std::max(cap, 1) + kAttnChunk - 1) / kAttnChunk;
+  p.R = p.n * G;
+  p.attn_counter0 = max_tiles(c);
+  p.n_counters = p.attn_counter0 + B * Hkv;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + std::max<size_t>(bytes, 1));
+    return at;
+  };
+  const size_t d = c.d_model;
+  const size_t qd = c.n_layers ? static_cast<size_t>(c.n_heads) * hd : 0;
+  p.status = take(4);
+  p.pos_base = take(static_cast<size_t>(B) * 4);
+  p.seq_ok = take(static_cast<size_t>(B) * 4);
+  p.counters = take(static_cast<size_t>(p.n_counters) * 4);
+  p.ssq = take(d / 128 * mpad * 4);
+  p.h = take(static_cast<size_t>(M) * d * 4);
+  p.hb = take(static_cast<size_t>(M) * d * 2);
+  p.hb_lo = take(static_cast<size_t>(M) * d * 2);
+  p.q = take(static_cast<size_t>(M) * qd * 2);
+  p.q_lo = take(static_cast<size_t>(M) * qd * 2);
+  p.o = take(static_cast<size_t>(M) * qd * 2);
+  p.o_lo = take(static_cast<size_t>(M) * qd * 2);
+  p.act = take(static_cast<size_t>(M) * c.d_ffn * 2);
+  p.act_lo = take(static_cast<size_t>(M) * c.d_ffn * 2);
+  p.gpart = take(static_cast<size_t>(kMaxGrid) * 2 * ntok * 128 * 4);  // summed partials: ntok columns
+  const size_t rows = c.n_layers ? static_cast<size_t>(B) * Hkv * p.splits * p.R : 0;
+  p.apart_o = take(rows * hd * 4);
+  p.apart_ml = take(rows * 2 * 4);
+  p.total = o;
+  return p;
+}
+
+struct TimedLaunch {
+  cudaEvent_t a, b;
+  int kind;
+  double bytes;
+};
+
+}  // namespace
+
+struct spec_model {
+  spec_model_config cfg;
+  int hd, G, qkv_rows, sm_count;
+  uint8_t* base;
+  size_t bytes;
+  Layout L;
+  std::vector<CUtensorMap> tm_qkv, tm_o, tm_gu, tm_d;
+  CUtensorMap tm_head;
+  bool timing = false;
+  std::vector<TimedLaunch> pending;
+  std::vector<cudaEvent_t> free_events;
+};
+
+namespace {
+
+cudaEvent_t take_event(spec_model* m) {
+  if (!m->free_events.empty()) {
+    cudaEvent_t e = m->free_events.back();
+    m->free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct Ctx {
+  const spec_model* m;
+  cudaStream_t st;
+  bool timing;
+};
+
+// Launch one GEMM over all token chunks of M rows.  With x_lo (the bf16
+// residual of the activations) both halves of x = hi + lo enter the MMA
+// (near-fp32 inputs at no extra weight traffic).
+int run_gemm(const Ctx& cx, const CUtensorMap* tmW, const void* x, const void* x_lo, int M, int N,
+             int K, GemmParams base) {
+  spec_model* mm = const_cast<spec_model*>(cx.m);
+  const int split = x_lo ? 1 : 0;
+  for (int tok0 = 0; tok0 < M; tok0 += kMaxTok) {
+    const int rows = std::min(kMaxTok, M - tok0);
+    GemmParams p = base;
+    p.N = N;
+    p.K = K;
+    p.M = M;
+    p.tok0 = tok0;
+    p.ntok = round_up(rows, 16);
+    p.split = split;
+    p.kc = K / 64;
+    p.n_tiles = (N + 127) / 128;
+    p.units = static_cast<long long>(p.n_tiles) * p.kc;
+    p.stages = gemm_max_stages(p.ntok << split, kGemmSmemBudget);
+    CUtensorMap tmX, tmXlo;
+    if (!make_tmap(&tmX, x, static_cast<uint64_t>(M), static_cast<uint64_t>(K),
+                   static_cast<uint32_t>(p.ntok)))
+      return SPEC_ECUDA;
+    if (split && !make_tmap(&tmXlo, x_lo, static_cast<uint64_t>(M), static_cast<uint64_t>(K),
+                            static_cast<uint32_t>(p.ntok)))
+      return SPEC_ECUDA;
+    if (!split) tmXlo = tmX;
+    const int grid = static_cast<int>(
+        std::min<long long>(std::min(cx.m->sm_count, kMaxGrid), p.units));
+    TimedLaunch t{};
+    if (cx.timing) {
+      t.a = take_event(mm);
+      t.b = take_event(mm);
+      t.kind = 0;
+      t.bytes = static_cast<double>(N) * K * 2 + static_cast<double>(rows) * K * 2;
+      cudaEventRecord(t.a, cx.st);
+    }
+    SPEC_CUDA(launch_gemm(tmW, &tmX, &tmXlo, p, grid, cx.st, !cx.timing));
+    if (cx.timing) {
+      cudaEventRecord(t.b, cx.st);
+      mm->pending.push_back(t);
+    }
+  }
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spec_status_string(int s) {
+  switch (s) {
+    case SPEC_OK: return "ok";
+    case SPEC_EINVAL: return "invalid argument";
+    case SPEC_ESIZE: return "size out of range or buffer too small";
+    case SPEC_ECUDA: return "CUDA error";
+    case SPEC_EDEVICE: return "the device reported an error (status word set)";
+    case SPEC_ETIMEOUT: return "a bounded device wait gave up";
+    case SPEC_ENOTSUP: return "unsupported device or configuration";
+    default: return "unknown status";
+  }
+}
+
+const char* spec_last_cuda_error(void) { return g_cuda_error.c_str(); }
+
+size_t spec_model_weight_bytes(const spec_model_config* cfg) {
+  if (!cfg_ok(cfg)) return 0;
+  return layout_of(*cfg).total;
+}
+
+int spec_model_create(const spec_model_config* cfg, uint64_t seed, void* d_weights,
+                      size_t weight_bytes, void* stream, spec_model** out) {
+  if (!out || !d_weights) return SPEC_EINVAL;
+  *out = nullptr;
+  if (!cfg_ok(cfg)) return SPEC_EINVAL;
+  const Layout L = layout_of(*cfg);
+  if (weight_bytes < L.total) return SPEC_ESIZE;
+  if (reinterpret_cast<uintptr_t>(d_weights) % kAlign) return SPEC_EINVAL;
+  int dev = 0;
+  SPEC_CUDA(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  SPEC_CUDA(cudaGetDeviceProperties(&prop, dev));
+  if (prop.major != 10 || prop.minor != 3) return SPEC_ENOTSUP;
+  if (!encode_fn()) return SPEC_ENOTSUP;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const spec_model_config& c = *cfg;
+  auto* m = new spec_model();
+  m->cfg = c;
+  m->hd = c.n_layers ? c.d_model / c.n_heads : 128;
+  m->G = c.n_layers ? c.n_heads / c.n_kv_heads : 1;
+  m->qkv_rows = c.n_layers ? (c.n_heads + 2 * c.n_kv_heads) * m->hd : 0;
+  m->sm_count = prop.multiProcessorCount;
+  m->base = static_cast<uint8_t*>(d_weights);
+  m->bytes = weight_bytes;
+  m->L = L;
+  uint8_t* B = m->base;
+  const long long d = c.d_model, V = c.vocab, hd = m->hd;
+  auto fail = [&](int code) {
+    delete m;
+    return code;
+  };
+  auto gen = [&](size_t off, long long rows, long long cols, int tid, int brows, int stride) {
+    return launch_init_weights(reinterpret_cast<uint16_t*>(B + off), rows, cols, tid, seed, brows,
+                               stride, st);
+  };
+  cudaError_t e;
+  if ((e = gen(L.embed, V, d, 0, static_cast<int>(V), static_cast<int>(V))) != cudaSuccess)
+    return fail(cuda_fail(e));
+  if ((e = gen(L.head, V, d, 1, static_cast<int>(V), static_cast<int>(V))) != cudaSuccess)
+    return fail(cuda_fail(e));
+  if ((e = launch_fill_f32(reinterpret_cast<float*>(B + L.gfinal), d, 1.0f, st)) != cudaSuccess)
+    return fail(cuda_fail(e));
+  if ((e = launch_rope_table(reinterpret_cast<float2*>(B + L.rope), static_cast<int>(hd),
+                             c.rope_theta, st)) != cudaSuccess)
+    return fail(cuda_fail(e));
+  const long long qd = static_cast<long long>(c.n_heads) * hd, kd = static_cast<long long>(c.n_kv_heads) * hd;
+  const long long ffn = c.d_ffn;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const int t0 = 2 + 7 * l;
+    const size_t qkv = L.wqkv[l];
+    struct G {
+      size_t off;
+      long long rows, cols;
+      int tid, brows, stride;
+    } gs[] = {
+        {qkv, qd, d, t0 + 0, static_cast<int>(qd), static_cast<int>(qd)},
+        {qkv + static_cast<size_t>(qd * d * 2), kd, d, t0 + 1, static_cast<int>(kd), static_cast<int>(kd)},
+        {qkv + static_cast<size_t>((qd + kd) * d * 2), kd, d, t0 + 2, static_cast<int>(kd), static_cast<int>(kd)},
+        {L.wo[l], d, qd, t0 + 3, static_cast<int>(d), static_cast<int>(d)},
+        {L.wgu[l], ffn, d, t0 + 4, 64, 128},
+        {L.wgu[l] + static_cast<size_t>(64 * d * 2), ffn, d, t0 + 5, 64, 128},
+        {L.wd[l], d, ffn, t0 + 6, static_cast<int>(d), static_cast<int>(d)},
+    };
+    for (const G& g : gs)
+      if ((e = gen(g.off, g.rows, g.cols, g.tid, g.brows, g.stride)) != cudaSuccess)
+        return fail(cuda_fail(e));
+    if ((e = launch_fill_f32(reinterpret_cast<float*>(B + L.g_attn[l]), d, 1.0f, st)) != cudaSuccess)
+      return fail(cuda_fail(e));
+    if ((e = launch_fill_f32(reinterpret_cast<float*>(B + L.g_mlp[l]), d, 1.0f, st)) != cudaSuccess)
+      return fail(cuda_fail(e));
+    CUtensorMap t;
+    if (!make_tmap(&t, B + L.wqkv[l], m->qkv_rows, d, 128)) return fail(SPEC_ECUDA);
+    m->tm_qkv.push_back(t);
+    if (!make_tmap(&t, B + L.wo[l], d, qd, 128)) return fail(SPEC_ECUDA);
+    m->tm_o.push_back(t);
+    if (!make_tmap(&t, B + L.wgu[l], 2 * ffn, d, 128)) return fail(SPEC_ECUDA);
+    m->tm_gu.push_back(t);
+    if (!make_tmap(&t, B + L.wd[l], d, ffn, 128)) return fail(SPEC_ECUDA);
+    m->tm_d.push_back(t);
+  }
+  if (!make_tmap(&m->tm_head, B + L.head, V, d, 128)) return fail(SPEC_ECUDA);
+  *out = m;
+  return SPEC_OK;
+}
+
+int spec_model_destroy(spec_model* m) {
+  if (!m) return SPEC_OK;
+  for (auto& t : m->pending) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  for (auto e : m->free_events) cudaEventDestroy(e);
+  delete m;
+  return SPEC_OK;
+}
+
+int spec_model_tensor(const spec_model* m, int layer, int which, const void** d_ptr,
+                      int64_t shape[2], int* block_rows, int* row_stride_rows) {
+  if (!m || !d_ptr || !shape || !block_rows || !row_stride_rows) return SPEC_EINVAL;
+  const spec_model_config& c = m->cfg;
+  const int64_t d = c.d_model, V = c.vocab, hd = m->hd;
+  const int64_t qd = static_cast<int64_t>(c.n_heads) * hd, kd = static_cast<int64_t>(c.n_kv_heads) * hd;
+  const uint8_t* B = m->base;
+  int64_t rows = 0, cols = 0;
+  const uint8_t* p = nullptr;
+  int brows = 0, stride = 0;
+  if (layer == -1) {
+    if (which == 0) p = B + m->L.embed;
+    else if (which == 1) p = B + m->L.head;
+    else return SPEC_EINVAL;
+    rows = V;
+    cols = d;
+  } else {
+    if (layer < 0 || layer >= c.n_layers) return SPEC_EINVAL;
+    const size_t qkv = m->L.wqkv[layer];
+    switch (which) {
+      case 0: p = B + qkv; rows = qd; cols = d; break;
+      case 1: p = B + qkv + qd * d * 2; rows = kd; cols = d; break;
+      case 2: p = B + qkv + (qd + kd) * d * 2; rows = kd; cols = d; break;
+      case 3: p = B + m->L.wo[layer]; rows = d; cols = qd; break;
+      case 4: p = B + m->L.wgu[layer]; rows = c.d_ffn; cols = d; brows = 64; stride = 128; break;
+      case 5: p = B + m->L.wgu[layer] + 64 * d * 2; rows = c.d_ffn; cols = d; brows = 64; stride = 128; break;
+      case 6: p = B + m->L.wd[layer]; rows = d; cols = c.d_ffn; break;
+      default: return SPEC_EINVAL;
+    }
+  }
+  if (!brows) brows = stride = static_cast<int>(rows);
+  *d_ptr = p;
+  shape[0] = rows;
+  shape[1] = cols;
+  *block_rows = brows;
+  *row_stride_rows = stride;
+  return SPEC_OK;
+}
+
+size_t spec_kv_bytes(const spec_model_config* cfg, int batch, int capacity) {
+  if (!cfg_ok(cfg) || batch < 0 || capacity < 0 || cfg->n_layers == 0) return 0;
+  const size_t hd = cfg->d_model / cfg->n_heads;
+  return static_cast<size_t>(cfg->n_layers) * batch * cfg->n_kv_heads * capacity * hd * 2;
+}
+
+size_t spec_workspace_bytes(const spec_model_config* cfg, int batch, int gamma, int capacity) {
+  if (!cfg_ok(cfg) || batch < 0 || gamma < 0 || capacity < 0) return 0;
+  return plan_ws(*cfg, batch, gamma, capacity).total;
+}
+
+int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch, int gamma,
+                        const spec_kv_cache* kv, float* d_logits, void* d_ws, size_t ws_bytes,
+                        void* stream) {
+  if (!m || !d_tokens || !kv || !d_logits || !d_ws) return SPEC_EINVAL;
+  if (batch < 0 || gamma < 0) return SPEC_EINVAL;
+  const spec_model_config& c = m->cfg;
+  if (c.n_layers == 0) return SPEC_ENOTSUP;
+  if (!kv->k || !kv->v || !kv->len) return SPEC_EINVAL;
+  if (kv->batch != batch || kv->capacity <= 0) return SPEC_EINVAL;
+  const int n = gamma + 1;
+  if (n > kMaxN || static_cast<long long>(batch) * n > kMaxM) return SPEC_ESIZE;
+  if (batch == 0) return SPEC_OK;
+  const WsPlan P = plan_ws(c, batch, gamma, kv->capacity);
+  if (ws_bytes < P.total) return SPEC_ESIZE;
+  if (reinterpret_cast<uintptr_t>(d_ws) % kAlign) return SPEC_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* W = static_cast<uint8_t*>(d_ws);
+  uint8_t* B = m->base;
+  const Layout& L = m->L;
+  const int M = P.M, d = c.d_model, hd = m->hd, H = c.n_heads, Hkv = c.n_kv_heads;
+  const int qd = H * hd;
+  int32_t* status = reinterpret_cast<int32_t*>(W + P.status);
+  int32_t* counters = reinterpret_cast<int32_t*>(W + P.counters);
+  float* ssq = reinterpret_cast<float*>(W + P.ssq);
+  float* h = reinterpret_cast<float*>(W + P.h);
+  uint16_t* hb = reinterpret_cast<uint16_t*>(W + P.hb);
+  uint16_t* hb_lo = reinterpret_cast<uint16_t*>(W + P.hb_lo);
+  uint16_t* q = reinterpret_cast<uint16_t*>(W + P.q);
+  uint16_t* q_lo = reinterpret_cast<uint16_t*>(W + P.q_lo);
+  uint16_t* o = reinterpret_cast<uint16_t*>(W + P.o);
+  uint16_t* o_lo = reinterpret_cast<uint16_t*>(W + P.o_lo);
+  uint16_t* act = reinterpret_cast<uint16_t*>(W + P.act);
+  uint16_t* act_lo = reinterpret_cast<uint16_t*>(W + P.act_lo);
+  int32_t* pos_base = reinterpret_cast<int32_t*>(W + P.pos_base);
+  int32_t* seq_ok = reinterpret_cast<int32_t*>(W + P.seq_ok);
+  const Ctx cx{m, st, m->timing};
+  const bool pdl = !m->timing;
+
+  EmbedParams ep{};
+  ep.tokens = d_tokens;
+  ep.embed = reinterpret_cast<const uint16_t*>(B + L.embed);
+  ep.g0 = reinterpret_cast<const float*>(B + L.g_attn[0]);
+  ep.h = h;
+  ep.hb = hb;
+  ep.hb_lo = hb_lo;
+  ep.ssq = ssq;
+  ep.ssq_ld = P.ssq_ld;
+  ep.len = kv->len;
+  ep.pos_base = pos_base;
+  ep.seq_ok = seq_ok;
+  ep.counters = counters;
+  ep.n_counters = P.n_counters;
+  ep.status = status;
+  ep.B = batch;
+  ep.n = n;
+  ep.d = d;
+  ep.V = c.vocab;
+  ep.cap = kv->capacity;
+  SPEC_CUDA(launch_embed(ep, st, pdl));
+
+  GemmParams g0{};
+  g0.inv_d = 1.0f / d;
+  g0.eps = c.rms_eps;
+  g0.ssq_tiles = d / 128;
+  g0.ssq_ld = P.ssq_ld;
+  g0.d = d;
+  g0.partials = reinterpret_cast<float*>(W + P.gpart);
+  g0.counters = counters;
+  g0.status = status;
+
+  const size_t layer_kv = static_cast<size_t>(batch) * Hkv * kv->capacity * hd;
+  for (int l = 0; l < c.n_layers; ++l) {
+    uint16_t* kc = static_cast<uint16_t*>(kv->k) + l * layer_kv;
+    uint16_t* vc = static_cast<uint16_t*>(kv->v) + l * layer_kv;
+    {  // QKV projection: RMSNorm scale, RoPE, KV append
+      GemmParams p = g0;
+      p.epi = EPI_QKV;
+      p.ssq_in = ssq;
+      p.q = q;
+      p.q_lo = q_lo;
+      p.kcache = kc;
+      p.vcache = vc;
+      p.pos_base = pos_base;
+      p.seq_ok = seq_ok;
+      p.rope = reinterpret_cast<const float2*>(B + L.rope);
+      p.n_per_seq = n;
+      p.H = H;
+      p.Hkv = Hkv;
+      p.hd = hd;
+      p.cap = kv->capacity;
+      int r = run_gemm(cx, &m->tm_qkv[l], hb, hb_lo, M, m->qkv_rows, d, p);
+      if (r) return r;
+    }
+    {  // attention over the cache
+      AttnParams a{};
+      a.q = q;
+      a.q_lo = q_lo;
+      a.kcache = kc;
+      a.vcache = vc;
+      a.o = o;
+      a.o_lo = o_lo;
+      a.pos_base = pos_base;
+      a.part_o = reinterpret_cast<float*>(W + P.apart_o);
+      a.part_ml = reinterpret_cast<float*>(W + P.apart_ml);
+      a.counters = counters + P.attn_counter0;
+      a.status = status;
+      a.B = batch;
+      a.n = n;
+      a.H = H;
+      a.Hkv = Hkv;
+      a.hd = hd;
+      a.cap = kv->capacity;
+      a.splits = P.splits;
+      a.R = P.R;
+      a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));
+      TimedLaunch t{};
+      if (cx.timing) {
+        t.a = take_event(const_cast<spec_model*>(m));
+        t.b = take_event(const_cast<spec_model*>(m));
+        t.kind = 1;
+        cudaEventRecord(t.a, st);
+      }
+      SPEC_CUDA(launch_attention(a, st, pdl));
+      if (cx.timing) {
+        cudaEventRecord(t.b, st);
+        const_cast<spec_model*>(m)->pending.push_back(t);
+      }
+    }
+    {  // O projection + residual
+      GemmParams p = g0;
+      p.epi = EPI_RESID;
+      p.h = h;
+      p.hb = hb;
+      p.hb_lo = hb_lo;
+      p.g_next = reinterpret_cast<const float*>(B + L.g_mlp[l]);
+      p.ssq_out = ssq;
+      int r = run_gemm(cx, &m->tm_o[l], o, o_lo, M, d, qd, p);
+      if (r) return r;
+    }
+    {  // gate/up + SwiGLU
+      GemmParams p = g0;
+      p.epi = EPI_SWIGLU;
+      p.ssq_in = ssq;
+      p.act = act;
+      p.act_lo = act_lo;
+      p.ffn = c.d_ffn;
+      int r = run_gemm(cx, &m->tm_gu[l], hb, hb_lo, M, 2 * c.d_ffn, d, p);
+      if (r) return r;
+    }
+    {  // down + residual; writes the next norm's input
+      GemmParams p = g0;
+      p.epi = EPI_RESID;
+      p.h = h;
+      p.hb = hb;
+      p.hb_lo = hb_lo;
+      p.g_next = reinterpret_cast<const float*>(B + (l + 1 < c.n_layers ? L.g_attn[l + 1] : L.gfinal));
+      p.ssq_out = ssq;
+      int r = run_gemm(cx, &m->tm_d[l], act, act_lo, M, d, c.d_ffn, p);
+      if (r) return r;
+    }
+  }
+  {  // final norm (scale in the epilogue) + LM head
+    GemmParams p = g0;
+    p.epi = EPI_STORE;
+    p.ssq_in = ssq;
+    p.out = d_logits;
+    p.ldo = c.vocab;
+    int r = run_gemm(cx, &m->tm_head, hb, hb_lo, M, c.vocab, d, p);
+    if (r) return r;
+  }
+  return SPEC_OK;
+}
+
+int spec_lm_head(const spec_model* m, const uint16_t* d_hidden, int rows, float* d_logits,
+                 void* d_ws, size_t ws_bytes, void* stream) {
+  if (!m || !d_hidden || !d_logits || !d_ws) return SPEC_EINVAL;
+  if (rows < 0) return SPEC_EINVAL;
+  if (rows > kMaxM) return SPEC_ESIZE;
+  if (rows == 0) return SPEC_OK;
+  const spec_model_config& c = m->cfg;
+  const WsPlan P = plan_ws(c, rows, 0, 1);
+  if (ws_bytes < P.total) return SPEC_ESIZE;
+  if (reinterpret_cast<uintptr_t>(d_ws) % kAlign) return SPEC_EINVAL;
+  if (reinterpret_cast<uintptr_t>(d_hidden) % 16) return SPEC_EINVAL;
+  uint8_t* W = static_cast<uint8_t*>(d_ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SPEC_CUDA(cudaMemsetAsync(W + P.counters, 0, static_cast<size_t>(P.n_counters) * 4, st));
+  GemmParams p{};
+  p.epi = EPI_STORE;
+  p.out = d_logits;
+  p.ldo = c.vocab;
+  p.partials = reinterpret_cast<float*>(W + P.gpart);
+  p.counters = reinterpret_cast<int32_t*>(W + P.counters);
+  p.status = reinterpret_cast<int32_t*>(W + P.status);
+  const Ctx cx{m, st, m->timing};
+  return run_gemm(cx, &m->tm_head, d_hidden, nullptr, rows, c.vocab, c.d_model, p);
+}
+
+size_t spec_accept_workspace_bytes(int batch, int gamma, int vocab) {
+  if (batch < 0 || gamma < 0 || vocab <= 0) return 0;
+  return kAlign;
+}
+
+static int accept_common_checks(int batch, int gamma, int vocab, float T, float top_p) {
+  if (batch < 0 || gamma < 0 || vocab <= 0) return SPEC_EINVAL;
+  if (!(T >= 0.f) || std::isinf(T)) return SPEC_EINVAL;
+  if (!(top_p > 0.f && top_p <= 1.f)) return SPEC_EINVAL;
+  return SPEC_OK;
+}
+
+int spec_accept(const float* d_target_logits, const float* d_draft_probs,
+                const int32_t* d_draft_tokens, const float* d_uniforms, int batch, int gamma,
+                int vocab, float temperature, float top_p, int32_t* d_out_tokens,
+                int32_t* d_n_accepted, void* d_ws, size_t ws_bytes, void* stream) {
+  int r = accept_common_checks(batch, gamma, vocab, temperature, top_p);
+  if (r) return r;
+  if (!d_target_logits || !d_out_tokens || !d_n_accepted || !d_ws) return SPEC_EINVAL;
+  if (gamma > 0 && !d_draft_tokens) return SPEC_EINVAL;
+  if (temperature > 0.f && ((gamma > 0 && !d_draft_probs) || !d_uniforms)) return SPEC_EINVAL;
+  if (ws_bytes < spec_accept_workspace_bytes(batch, gamma, vocab)) return SPEC_ESIZE;
+  if (batch == 0) return SPEC_OK;
+  AcceptParams p{};
+  p.logits = d_target_logits;
+  p.q = d_draft_probs;
+  p.draft = d_draft_tokens;
+  p.u = d_uniforms;
+  p.out = d_out_tokens;
+  p.n_acc = d_n_accepted;
+  p.status = static_cast<int32_t*>(d_ws);
+  p.B = batch;
+  p.gamma = gamma;
+  p.V = vocab;
+  p.T = temperature;
+  p.top_p = top_p;
+  SPEC_CUDA(launch_accept(p, static_cast<cudaStream_t>(stream), true));
+  return SPEC_OK;
+}
+
+int spec_draft_sample(const float* d_logits, int rows, int vocab, float temperature, float top_p,
+                      const float* d_uniforms, float* d_probs, int32_t* d_tokens, void* d_ws,
+                      size_t ws_bytes, void* stream) {
+  int r = accept_common_checks(rows, 0, vocab, temperature, top_p);
+  if (r) return r;
+  if (!d_logits || !d_tokens || !d_ws) return SPEC_EINVAL;
+  if (temperature > 0.f && !d_uniforms) return SPEC_EINVAL;
+  if (ws_bytes < spec_accept_workspace_bytes(rows, 0, vocab)) return SPEC_ESIZE;
+  if (rows == 0) return SPEC_OK;
+  SampleParams p{};
+  p.logits = d_logits;
+  p.u = d_uniforms;
+  p.probs = d_probs;
+  p.tokens = d_tokens;
+  p.status = static_cast<int32_t*>(d_ws);
+  p.R = rows;
+  p.V = vocab;
+  p.T = temperature;
+  p.top_p = top_p;
+  SPEC_CUDA(launch_sample(p, static_cast<cudaStream_t>(stream)));
+  return SPEC_OK;
+}
+
+int spec_kv_truncate(const spec_kv_cache* kv, const int32_t* d_n_accepted, int gamma, void* d_ws,
+                     void* stream) {
+  if (!kv || !kv->len || !d_n_accepted || !d_ws) return SPEC_EINVAL;
+  if (gamma < 0 || kv->batch < 0) return SPEC_EINVAL;
+  SPEC_CUDA(launch_truncate(kv->len, d_n_accepted, kv->batch, gamma, static_cast<int32_t*>(d_ws),
+                            static_cast<cudaStream_t>(stream), true));
+  return SPEC_OK;
+}
+
+int spec_device_status(void* d_ws, void* stream, int32_t* out) {
+  if (!d_ws || !out) return SPEC_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SPEC_CUDA(cudaStreamSynchronize(st));
+  int32_t v = 0;
+  SPEC_CUDA(cudaMemcpy(&v, d_ws, 4, cudaMemcpyDeviceToHost));
+  SPEC_CUDA(cudaMemset(d_ws, 0, 4));
+  *out = v;
+  if (v == 0) return SPEC_OK;
+  return (v & SPEC_DEV_TIMEOUT) ? SPEC_ETIMEOUT : SPEC_EDEVICE;
+}
+
+int spec_timing_enable(spec_model* m, int enable) {
+  if (!m) return SPEC_EINVAL;
+  m->timing = enable != 0;
+  return SPEC_OK;
+}
+
+int spec_timing_read(spec_model* m, double ms[2], int64_t launches[2], double bytes[2]) {
+  if (!m || !ms || !launches || !bytes) return SPEC_EINVAL;
+  for (int k = 0; k < 2; ++k) {
+    ms[k] = 0;
+    launches[k] = 0;
+    bytes[k] = 0;
+  }
+  for (auto& t : m->pending) {
+    SPEC_CUDA(cudaEventSynchronize(t.b));
+    float x = 0.f;
+    SPEC_CUDA(cudaEventElapsedTime(&x, t.a, t.b));
+    ms[t.kind] += x;
+    launches[t.kind] += 1;
+    bytes[t.kind] += t.bytes;
+    m->free_events.push_back(t.a);
+    m->free_events.push_back(t.b);
+  }
+  m->pending.clear();
+  return SPEC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,368 @@
+// Split-KV attention of the gamma+1 new positions over the bf16 KV cache.
+//
+// One verification pass feeds gamma+1 queries per sequence through attention
+// over the cached context plus the new block (lattice notes: the target
+// scores all k drafted positions and the next-token slot in one call; the
+// pass still reads "the KV cache" on top of the weights).  Query j of the
+// block sits at position len+j and sees keys 0..len+j (causal inside the
+// block).  Grouped-query attention: the G = n_heads / n_kv_heads query heads
+// of a KV head share its keys, so a CTA takes one (sequence, KV head, chunk
+// of 128 keys) and all n*G query rows of that group, reading each key and
+// value once.
+//
+// Per CTA: the key/value chunk is staged in shared memory with cp.async
+// (16-byte copies, XOR-swizzled rows so ldmatrix is conflict-free); query rows
+// go through in tiles of 16; each warp takes 32 of the 128 keys and computes
+// S = Q K^T and O = P V with mma.m16n8k16 (bf16 in, fp32 accumulate) and an
+// exp2-domain softmax; q and P enter as bf16 pairs (hi + lo, two MMAs each),
+// so only the cache itself is bf16-rounded; the four warps' (max, sum, O) are merged in shared
+// memory into the CTA's partial.  The last CTA of a (sequence, KV head) to
+// finish (atomic counter) merges all chunks' partials in chunk order by
+// log-sum-exp and writes the bf16 output rows: deterministic, no waits on
+// other CTAs.
+#include "common.cuh"
+#include "internal.h"
+
+namespace spec {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kChunk = kAttnChunk;  // keys per CTA
+constexpr int kKeysPerWarp = kChunk / 4;
+
+SPEC_DEVINL void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+SPEC_DEVINL void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+SPEC_DEVINL void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+SPEC_DEVINL void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+SPEC_DEVINL void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// byte offset of 16-byte chunk c of row i in a swizzled [rows][HD] bf16 tile
+template <int HD>
+SPEC_DEVINL uint32_t swz(int i, int c) {
+  return static_cast<uint32_t>(i * (HD * 2) + ((c ^ (i & 7)) << 4));
+}
+
+template <int HD>
+struct AttnSmem {
+  static constexpr int kRowB = HD * 2;
+  static constexpr int kOStride = HD + 8;  // floats per row of a warp partial
+  static constexpr size_t kK = 0;
+  static constexpr size_t kV = kK + static_cast<size_t>(kChunk) * kRowB;
+  static constexpr size_t kQ = kV + static_cast<size_t>(kChunk) * kRowB;
+  static constexpr size_t kQlo = kQ + 16 * kRowB;
+  static constexpr size_t kO = kQlo + 16 * kRowB;
+  static constexpr size_t kM = kO + 4ull * 16 * kOStride * 4;
+  static constexpr size_t kL = kM + 4 * 16 * 4;
+  static constexpr size_t kFlag = kL + 4 * 16 * 4;
+  static constexpr size_t kBytes = kFlag + 16;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads) attn_splitkv_kernel(const AttnParams p) {
+  using L = AttnSmem<HD>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.H / p.Hkv;
+  grid_dep_wait();
+  grid_dep_launch();
+
+  const int Lb = p.pos_base[b];
+  const int Tk = min(Lb + p.n, p.cap);
+  const int k0 = s * kChunk;
+  if (k0 >= Tk) return;  // this chunk is past the sequence
+  const int ns = (Tk + kChunk - 1) / kChunk;
+  const int nk = min(kChunk, Tk - k0);
+
+  const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV),
+                 sQ = smem_u32(smem + L::kQ), sQlo = smem_u32(smem + L::kQlo);
+  const bool lo = p.q_lo != nullptr;
+  float* Ow = reinterpret_cast<float*>(smem + L::kO);
+  float* Mw = reinterpret_cast<float*>(smem + L::kM);
+  float* Lw = reinterpret_cast<float*>(smem + L::kL);
+  int* flag = reinterpret_cast<int*>(smem + L::kFlag);
+
+  // ---- stage this chunk's keys and values (rows past the end are zero)
+  const long long head_base = (static_cast<long long>(b) * p.Hkv + kvh) * p.cap;
+  constexpr int kCPR = HD / 8;  // 16-byte chunks per row
+  for (int idx = tid; idx < kChunk * kCPR; idx += kThreads) {
+    const int i = idx / kCPR, c = idx % kCPR;
+    const int row = i < nk ? i : 0;
+    const long long g = (head_base + k0 + row) * HD + c * 8;
+    const int bytes = i < nk ? 16 : 0;
+    cp_async16(sK + swz<HD>(i, c), p.kcache + g, bytes);
+    cp_async16(sV + swz<HD>(i, c), p.vcache + g, bytes);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  const int R = p.R;
+  const int qdim = p.H * HD;
+  const int kw0 = warp * kKeysPerWarp;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  float* part_o = p.part_o + ((static_cast<long long>(b) * p.Hkv + kvh) * p.splits + s) * R * HD;
+  float* part_ml = p.part_ml + ((static_cast<long long>(b) * p.Hkv + kvh) * p.splits + s) * R * 2;
+
+  for (int qt = 0; qt * 16 < R; ++qt) {
+    // ---- query tile: rows r = qt*16 + i, r = j*G + g -> token b*n+j, head kvh*G+g
+    for (int idx = tid; idx < 16 * kCPR; idx += kThreads) {
+      const int i = idx / kCPR, c = idx % kCPR;
+      const int r = qt * 16 + i;
+      uint4 val = make_uint4(0, 0, 0, 0), vlo = make_uint4(0, 0, 0, 0);
+      if (r < R) {
+        const int j = r / G, g = r % G;
+        const long long off = (static_cast<long long>(b) * p.n + j) * qdim + (kvh * G + g) * HD + c * 8;
+        val = *reinterpret_cast<const uint4*>(p.q + off);
+        if (lo) vlo = *reinterpret_cast<const uint4*>(p.q_lo + off);
+      }
+      *reinterpret_cast<uint4*>(smem + L::kQ + swz<HD>(i, c)) = val;
+      *reinterpret_cast<uint4*>(smem + L::kQlo + swz<HD>(i, c)) = vlo;
+    }
+    __syncthreads();
+
+    float mrow[2] = {-INFINITY, -INFINITY};
+    float lrow[2] = {0.f, 0.f};
+    float oacc[HD / 8][4];
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+
+    if (kw0 < nk) {
+      // ---- S = Q K^T over this warp's 32 keys (4 n8 tiles)
+      float sacc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        uint32_t a0, a1, a2, a3, l0, l1, l2, l3;
+        ldsm_x4(sQ + swz<HD>(lane & 15, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+        if (lo) ldsm_x4(sQlo + swz<HD>(lane & 15, kk * 2 + (lane >> 4)), l0, l1, l2, l3);
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          const int key = kw0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(sK + swz<HD>(key, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
+          mma_bf16(sacc[np * 2], a0, a1, a2, a3, b0, b1);
+          mma_bf16(sacc[np * 2 + 1], a0, a1, a2, a3, b2, b3);
+          if (lo) {  // q = q_hi + q_lo
+            mma_bf16(sacc[np * 2], l0, l1, l2, l3, b0, b1);
+            mma_bf16(sacc[np * 2 + 1], l0, l1, l2, l3, b2, b3);
+          }
+        }
+      }
+      // ---- mask (causal within the block, chunk end) and exp2-domain softmax
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int r = qt * 16 + g8 + hr * 8;
+        const int qpos = r < R ? Lb + r / G : -1;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int kabs = k0 + kw0 + nt * 8 + t4 * 2 + e;
+            const bool ok = kabs < k0 + nk && kabs <= qpos;
+            const float v = ok ? sacc[nt][hr * 2 + e] * p.scale_log2 : -INFINITY;
+            sacc[nt][hr * 2 + e] = v;
+            mx = fmaxf(mx, v);
+          }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        float sum = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float v = sacc[nt][hr * 2 + e];
+            const float pe = mx == -INFINITY ? 0.f : exp2f(v - mx);
+            sacc[nt][hr * 2 + e] = pe;
+            sum += pe;
+          }
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        mrow[hr] = mx;
+        lrow[hr] = sum;
+      }
+      // ---- O = P V, with P = P_hi + P_lo (bf16 pair)
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const uint32_t a0 = pack_bf16x2(sacc[2 * k2][0], sacc[2 * k2][1]);
+        const uint32_t a1 = pack_bf16x2(sacc[2 * k2][2], sacc[2 * k2][3]);
+        const uint32_t a2 = pack_bf16x2(sacc[2 * k2 + 1][0], sacc[2 * k2 + 1][1]);
+        const uint32_t a3 = pack_bf16x2(sacc[2 * k2 + 1][2], sacc[2 * k2 + 1][3]);
+        const uint32_t l0 = pack_bf16x2(sacc[2 * k2][0] - bf16lo(a0), sacc[2 * k2][1] - bf16hi(a0));
+        const uint32_t l1 = pack_bf16x2(sacc[2 * k2][2] - bf16lo(a1), sacc[2 * k2][3] - bf16hi(a1));
+        const uint32_t l2 =
+            pack_bf16x2(sacc[2 * k2 + 1][0] - bf16lo(a2), sacc[2 * k2 + 1][1] - bf16hi(a2));
+        const uint32_t l3 =
+            pack_bf16x2(sacc[2 * k2 + 1][2] - bf16lo(a3), sacc[2 * k2 + 1][3] - bf16hi(a3));
+        const int key = kw0 + k2 * 16 + (lane & 15);
+#pragma unroll
+        for (int dn = 0; dn < HD / 16; ++dn) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(sV + swz<HD>(key, dn * 2 + (lane >> 4)), b0, b1, b2, b3);
+          mma_bf16(oacc[2 * dn], a0, a1, a2, a3, b0, b1);
+          mma_bf16(oacc[2 * dn + 1], a0, a1, a2, a3, b2, b3);
+          mma_bf16(oacc[2 * dn], l0, l1, l2, l3, b0, b1);
+          mma_bf16(oacc[2 * dn + 1], l0, l1, l2, l3, b2, b3);
+        }
+      }
+    }
+    // ---- this warp's partial to shared memory
+    if (t4 == 0) {
+      Mw[warp * 16 + g8] = mrow[0];
+      Mw[warp * 16 + g8 + 8] = mrow[1];
+      Lw[warp * 16 + g8] = lrow[0];
+      Lw[warp * 16 + g8 + 8] = lrow[1];
+    }
+#pragma unroll
+    for (int nd = 0; nd < HD / 8; ++nd) {
+      float* o0 = Ow + (warp * 16 + g8) * L::kOStride + nd * 8 + t4 * 2;
+      float* o1 = o0 + 8 * L::kOStride;
+      *reinterpret_cast<float2*>(o0) = make_float2(oacc[nd][0], oacc[nd][1]);
+      *reinterpret_cast<float2*>(o1) = make_float2(oacc[nd][2], oacc[nd][3]);
+    }
+    __syncthreads();
+    // ---- merge the four warps: thread -> (row tid/8, dims (tid%8)*HD/8 ..)
+    {
+      const int i = tid >> 3;
+      const int r = qt * 16 + i;
+      constexpr int kDims = HD / 8;
+      const int d0 = (tid & 7) * kDims;
+      float m = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) m = fmaxf(m, Mw[w * 16 + i]);
+      float wgt[4], l = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        wgt[w] = Mw[w * 16 + i] == -INFINITY ? 0.f : exp2f(Mw[w * 16 + i] - m);
+        l += wgt[w] * Lw[w * 16 + i];
+      }
+      if (r < R) {
+#pragma unroll
+        for (int dd = 0; dd < kDims; dd += 4) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const float4 v =
+                *reinterpret_cast<const float4*>(Ow + (w * 16 + i) * L::kOStride + d0 + dd);
+            acc.x += wgt[w] * v.x;
+            acc.y += wgt[w] * v.y;
+            acc.z += wgt[w] * v.z;
+            acc.w += wgt[w] * v.w;
+          }
+          __stcg(reinterpret_cast<float4*>(part_o + static_cast<long long>(r) * HD + d0 + dd), acc);
+        }
+        if ((tid & 7) == 0) {
+          __stcg(part_ml + r * 2, m);
+          __stcg(part_ml + r * 2 + 1, l);
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- last chunk to finish merges all chunks of this (sequence, KV head)
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    int32_t* ctr = p.counters + b * p.Hkv + kvh;
+    const int old = atomicAdd(ctr, 1);
+    const int last = old == ns - 1;
+    if (last) *ctr = 0;
+    *flag = last;
+  }
+  __syncthreads();
+  if (!*flag) return;
+  __threadfence();
+  const float* base_o = p.part_o + (static_cast<long long>(b) * p.Hkv + kvh) * p.splits * R * HD;
+  const float* base_ml = p.part_ml + (static_cast<long long>(b) * p.Hkv + kvh) * p.splits * R * 2;
+  for (int idx = tid; idx < R * (HD / 4); idx += kThreads) {
+    const int r = idx / (HD / 4), d4 = (idx % (HD / 4)) * 4;
+    float m = -INFINITY;
+    for (int c = 0; c < ns; ++c) m = fmaxf(m, __ldcg(base_ml + (static_cast<long long>(c) * R + r) * 2));
+    float l = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < ns; ++c) {
+      const float mc = __ldcg(base_ml + (static_cast<long long>(c) * R + r) * 2);
+      if (mc == -INFINITY) continue;
+      const float w = exp2f(mc - m);
+      l += w * __ldcg(base_ml + (static_cast<long long>(c) * R + r) * 2 + 1);
+      const float4 v =
+          __ldcg(reinterpret_cast<const float4*>(base_o + (static_cast<long long>(c) * R + r) * HD + d4));
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    const float inv = 1.0f / l;
+    const int j = r / G, g = r % G;
+    const long long off = (static_cast<long long>(b) * p.n + j) * qdim + (kvh * G + g) * HD + d4;
+    const float o0 = acc.x * inv, o1 = acc.y * inv, o2 = acc.z * inv, o3 = acc.w * inv;
+    uint2 pk;
+    pk.x = pack_bf16x2(o0, o1);
+    pk.y = pack_bf16x2(o2, o3);
+    *reinterpret_cast<uint2*>(p.o + off) = pk;
+    if (p.o_lo) {
+      uint2 lo;
+      lo.x = pack_bf16x2(o0 - bf16lo(pk.x), o1 - bf16hi(pk.x));
+      lo.y = pack_bf16x2(o2 - bf16lo(pk.y), o3 - bf16hi(pk.y));
+      *reinterpret_cast<uint2*>(p.o_lo + off) = lo;
+    }
+  }
+}
+
+template <int HD>
+cudaError_t launch_hd(const AttnParams& p, cudaStream_t stream, bool pdl) {
+  static bool configured = false;
+  const size_t smem = AttnSmem<HD>::kBytes;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_splitkv_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits, p.Hkv, p.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_splitkv_kernel<HD>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl) {
+  if (p.hd == 128) return launch_hd<128>(p, stream, pdl);
+  if (p.hd == 64) return launch_hd<64>(p, stream, pdl);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace spec

@@ -1,0 +1,522 @@
+// Skinny weight-streaming GEMM for the verification pass on sm_103a.
+//
+// One target pass multiplies every weight matrix by only M = batch*(gamma+1)
+// token rows, so the pass is a stream of the weights through HBM ("verifying
+// several tokens costs the same as one": pigeon guide, *The idea*; lattice
+// notes: the k-token pass turns the matrix-vector op into a matrix-matrix op
+// over the same weight read).  The kernel is built around that stream:
+//
+//  * swap-AB: the weight tile (128 output features x 64 K) is the UMMA "A"
+//    operand (M = 128), the M token rows padded to ntok (16..256) are "B";
+//    the accumulator D[feature][token] lives in tensor memory.  Activations
+//    arrive as a bf16 pair (x = hi + lo); both parts go through the MMA into
+//    the same accumulator, so the GEMM sees ~16-bit-mantissa inputs while the
+//    weights are still read once (the extra MMA is free in this regime).
+//  * warp 0 streams weight tiles and activation tiles with TMA
+//    (cp.async.bulk.tensor, 128-byte swizzle, evict-first L2 policy for the
+//    weights) through a ring of shared-memory stages guarded by mbarriers;
+//    weight loads for the first ring pass are issued before the
+//    programmatic-dependent-launch wait, i.e. while the previous kernel
+//    finishes.
+//  * warp 1 allocates TMEM and one lane issues tcgen05.mma (kind::f16, bf16 x
+//    bf16 -> fp32), committing each stage back to the producer and each
+//    finished accumulator to the epilogue (double-buffered in TMEM).
+//  * warps 2-5 drain TMEM with tcgen05.ld and run the fused epilogue.
+//  * Stream-K: the n_tiles x (K/64) work units are split into equal
+//    contiguous ranges, one per CTA (grid <= SM count), so every SM streams
+//    the same number of bytes.  A tile split across CTAs is finished by the
+//    last CTA to arrive (atomic counter), which sums every contributor's
+//    fp32 partial in CTA order: deterministic, no float atomics, no waits on
+//    other CTAs.
+//
+// Epilogues: EPI_STORE (fp32 logits), EPI_RESID (residual add + next norm's
+// bf16 input + sum-of-squares partials), EPI_QKV (RMSNorm scale, RoPE, q to
+// the workspace, k/v appended to the bf16 cache), EPI_SWIGLU.
+#include "common.cuh"
+#include "internal.h"
+
+namespace spec {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTileN = 128;             // weight rows per tile (UMMA M)
+constexpr int kTileK = 64;              // K elements per stage (one 128-byte swizzle row)
+constexpr int kATileBytes = kTileN * 128;
+constexpr int kMaxStages = 16;
+constexpr int kEpiThreads = 128;
+constexpr int kEpiBar = 1;
+
+struct Partition {
+  long long U;
+  int G;
+  int kc;
+  __device__ long long start(int c) const { return (static_cast<long long>(c) * U) / G; }
+  __device__ int cta_of(long long u) const {
+    return static_cast<int>(((u + 1) * static_cast<long long>(G) - 1) / U);
+  }
+  __device__ int tile_of(long long u) const { return static_cast<int>(u / kc); }
+  // Does CTA c cover units of more than one tile?
+  __device__ bool multi(int c) const {
+    long long s = start(c), e = start(c + 1);
+    return e > s && tile_of(s) != tile_of(e - 1);
+  }
+  // Partial-slot CTA c uses for its contribution to tile t.
+  __device__ int slot(int c, int t) const {
+    return (c == cta_of(static_cast<long long>(t) * kc) && multi(c)) ? 1 : 0;
+  }
+};
+
+struct Smem {
+  uint8_t* stage_base;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* accfull;
+  uint64_t* accempty;
+  uint32_t* tmem_slot;
+  int* abort;
+  int* flag;
+  float* rs;     // [256]
+  float* xbuf;   // [16][128]
+  float* red;    // [4][16]
+};
+
+__host__ __device__ inline size_t stage_bytes(int ntok) {
+  return static_cast<size_t>(kATileBytes) + static_cast<size_t>(ntok) * 128;
+}
+
+constexpr size_t kTailBytes = 1024 /*barriers*/ + 256 * 4 /*rs*/ + 16 * 128 * 4 /*xbuf*/ +
+                              4 * 16 * 4 /*red*/ + 64;
+
+__device__ Smem carve(uint8_t* raw, int ntok, int stages) {
+  uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023);
+  Smem s;
+  s.stage_base = reinterpret_cast<uint8_t*>(base);
+  uint8_t* t = s.stage_base + stage_bytes(ntok) * stages;
+  s.full = reinterpret_cast<uint64_t*>(t);
+  s.empty = s.full + kMaxStages;
+  s.accfull = s.empty + kMaxStages;
+  s.accempty = s.accfull + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.accempty + 2);
+  s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
+  s.flag = s.abort + 1;
+  s.rs = reinterpret_cast<float*>(t + 1024);
+  s.xbuf = s.rs + 256;
+  s.red = s.xbuf + 16 * 128;
+  return s;
+}
+
+__device__ __forceinline__ uint32_t tmem_cols_for(int ntok) {
+  uint32_t need = 2u * static_cast<uint32_t>(ntok);
+  uint32_t c = 32;
+  while (c < need) c <<= 1;
+  return c;
+}
+
+__device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
+
+// Accumulator columns [c0, c0+16) of this thread's row.
+__device__ __forceinline__ void load_acc(uint32_t tacc, int c0, float (&v)[16]) {
+  tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+}
+
+// --------------------------------------------------------------- epilogues
+// Apply the epilogue to 16 token columns [c0, c0+16) of this thread's row.
+__device__ void epilogue_chunk(const GemmParams& p, const Smem& sm, int tile, int r, int c0,
+                               const float (&acc)[16]) {
+  const int f = tile * kTileN + r;  // weight row = output feature (before SwiGLU pairing)
+  const int e = threadIdx.x - (kThreads - kEpiThreads);
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int m = p.tok0 + c0 + j;
+    v[j] = acc[j] * (p.ssq_in ? sm.rs[c0 + j] : 1.0f);
+    (void)m;
+  }
+  if (p.epi == EPI_STORE) {
+    if (f < p.N) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = p.tok0 + c0 + j;
+        if (m < p.M) p.out[static_cast<long long>(m) * p.ldo + f] = v[j];
+      }
+    }
+    return;
+  }
+  if (p.epi == EPI_RESID) {
+    float sq[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int m = p.tok0 + c0 + j;
+      sq[j] = 0.f;
+      if (m < p.M && f < p.N) {
+        const long long idx = static_cast<long long>(m) * p.d + f;
+        const float hn = p.h[idx] + v[j];
+        p.h[idx] = hn;
+        const float x = hn * p.g_next[f];
+        const uint16_t hi = f32_to_bf16(x);
+        p.hb[idx] = hi;
+        if (p.hb_lo) p.hb_lo[idx] = f32_to_bf16(x - bf16_to_f32(hi));
+        sq[j] = hn * hn;
+      }
+    }
+    const int warp = (threadIdx.x >> 5) & 3;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float s = warp_sum(sq[j]);
+      if ((threadIdx.x & 31) == 0) sm.red[warp * 16 + j] = s;
+    }
+    named_bar(kEpiBar, kEpiThreads);
+    if (e < 16) {
+      const int m = p.tok0 + c0 + e;
+      // quarters in row order 0..3 (warp w%4 holds rows 32*(w%4)..)
+      const float s = ((sm.red[0 * 16 + e] + sm.red[1 * 16 + e]) + sm.red[2 * 16 + e]) +
+                      sm.red[3 * 16 + e];
+      if (m < p.M) p.ssq_out[static_cast<long long>(tile) * p.ssq_ld + m] = s;
+    }
+    named_bar(kEpiBar, kEpiThreads);
+    return;
+  }
+  if (p.epi == EPI_QKV) {
+    // exchange the 16 columns of every row through shared memory for RoPE
+#pragma unroll
+    for (int j = 0; j < 16; ++j) sm.xbuf[j * kTileN + r] = v[j];
+    named_bar(kEpiBar, kEpiThreads);
+    const int hd = p.hd, half = hd >> 1;
+    const int qdim = p.H * hd, kdim = p.Hkv * hd;
+    const int dim = f % hd;
+    const bool rot = f < qdim + kdim;
+    const int pr = dim < half ? r + half : r - half;
+    const float2 fr = p.rope[dim < half ? dim : dim - half];
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+      const int m = p.tok0 + c0 + j;
+      if (m >= p.M || f >= p.N) continue;
+      const int b = m / p.n_per_seq, jj = m - b * p.n_per_seq;
+      float out = v[j];
+      const int pos = p.pos_base[b] + jj;
+      if (rot) {
+        // angle = pos * freq with the product kept to ~fp64 accuracy:
+        // freq = hi + lo, pos*hi = a + err exactly (fma), angle ~ a + (err + pos*lo)
+        const float fp = static_cast<float>(pos);
+        const float a = fp * fr.x;
+        const float err = fmaf(fp, fr.x, -a) + fp * fr.y;
+        float s, c;
+        sincosf(a, &s, &c);
+        const float sn = s + err * c, cs = c - err * s;
+        const float partner = sm.xbuf[j * kTileN + pr];
+        out = dim < half ? v[j] * cs - partner * sn : v[j] * cs + partner * sn;
+      }
+      if (f < qdim) {
+        const long long qi = static_cast<long long>(m) * qdim + f;
+        const uint16_t hi = f32_to_bf16(out);
+        p.q[qi] = hi;
+        if (p.q_lo) p.q_lo[qi] = f32_to_bf16(out - bf16_to_f32(hi));
+      } else if (p.seq_ok[b] && pos < p.cap) {
+        const int kf = f < qdim + kdim ? f - qdim : f - qdim - kdim;
+        const int kvh = kf / hd;
+        const long long idx =
+            ((static_cast<long long>(b) * p.Hkv + kvh) * p.cap + pos) * hd + (kf % hd);
+        if (f < qdim + kdim)
+          p.kcache[idx] = f32_to_bf16(out);
+        else
+          p.vcache[idx] = f32_to_bf16(out);
+      }
+    }
+    named_bar(kEpiBar, kEpiThreads);
+    return;
+  }
+  // EPI_SWIGLU
+  if (r >= 64) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) sm.xbuf[j * kTileN + r] = v[j];
+  }
+  named_bar(kEpiBar, kEpiThreads);
+  if (r < 64) {
+    const int fo = tile * 64 + r;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int m = p.tok0 + c0 + j;
+      if (m < p.M && fo < p.ffn) {
+        const float g = v[j], u = sm.xbuf[j * kTileN + r + 64];
+        const float sg = g / (1.0f + __expf(-g));
+        const float a = sg * u;
+        const uint16_t hi = f32_to_bf16(a);
+        const long long idx = static_cast<long long>(m) * p.ffn + fo;
+        p.act[idx] = hi;
+        if (p.act_lo) p.act_lo[idx] = f32_to_bf16(a - bf16_to_f32(hi));
+      }
+    }
+  }
+  named_bar(kEpiBar, kEpiThreads);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const __grid_constant__ CUtensorMap tmXlo, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const int nb = p.ntok << p.split;  // B rows per stage: hi rows, then (split) lo rows
+  const Smem sm = carve(smem_raw, nb, p.stages);
+  const int warp = threadIdx.x >> 5;
+  const int S = p.stages;
+  const Partition part{p.units, static_cast<int>(gridDim.x), p.kc};
+  const int me = blockIdx.x;
+  const long long u0 = part.start(me), u1 = part.start(me + 1);
+  const uint32_t tcols = tmem_cols_for(p.ntok);
+  const uint32_t sbytes = static_cast<uint32_t>(stage_bytes(nb));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sm.accfull[a], 1);
+      mbar_init(&sm.accempty[a], 4);
+    }
+    *sm.abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmX);
+    if (p.split) prefetch_tmap(&tmXlo);
+  }
+  if (warp == 1) {
+    tmem_alloc(sm.tmem_slot, tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_slot;
+  grid_dep_launch();
+
+  if (warp == 0) {
+    if (elect_lane0() && u1 > u0) {
+      // ------------------------------------------------------ TMA producer
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      uint32_t issued[kMaxStages];
+      for (int s = 0; s < S; ++s) issued[s] = 0;
+      const long long n = u1 - u0;
+      const int pre = static_cast<int>(n < S ? n : S);
+      for (int i = 0; i < pre; ++i) {
+        const long long u = u0 + i;
+        uint8_t* a = sm.stage_base + static_cast<size_t>(i) * sbytes;
+        mbar_arrive_expect_tx(&sm.full[i], sbytes);
+        tma_load_2d(a, &tmW, &sm.full[i], static_cast<int>(u % p.kc) * kTileK,
+                    part.tile_of(u) * kTileN, pol_w);
+      }
+      grid_dep_wait();  // activations are produced by the previous kernel
+      for (int i = 0; i < pre; ++i) {
+        const long long u = u0 + i;
+        uint8_t* b = sm.stage_base + static_cast<size_t>(i) * sbytes + kATileBytes;
+        tma_load_2d(b, &tmX, &sm.full[i], static_cast<int>(u % p.kc) * kTileK, p.tok0, pol_x);
+        if (p.split)
+          tma_load_2d(b + p.ntok * 128, &tmXlo, &sm.full[i], static_cast<int>(u % p.kc) * kTileK,
+                      p.tok0, pol_x);
+        issued[i] = 1;
+      }
+      int stage = pre % S;
+      uint32_t phase = pre == S ? 1u : 0u;
+      for (long long u = u0 + pre; u < u1; ++u) {
+        if (!mbar_wait(&sm.empty[stage], phase ^ 1u, sm.abort)) break;
+        uint8_t* a = sm.stage_base + static_cast<size_t>(stage) * sbytes;
+        mbar_arrive_expect_tx(&sm.full[stage], sbytes);
+        tma_load_2d(a, &tmW, &sm.full[stage], static_cast<int>(u % p.kc) * kTileK,
+                    part.tile_of(u) * kTileN, pol_w);
+        tma_load_2d(a + kATileBytes, &tmX, &sm.full[stage], static_cast<int>(u % p.kc) * kTileK,
+                    p.tok0, pol_x);
+        if (p.split)
+          tma_load_2d(a + kATileBytes + p.ntok * 128, &tmXlo, &sm.full[stage],
+                      static_cast<int>(u % p.kc) * kTileK, p.tok0, pol_x);
+        ++issued[stage];
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (*sm.abort) {
+        // let every copy still in flight land before the CTA may exit
+        volatile int never = 0;
+        for (int s = 0; s < S; ++s)
+          if (issued[s]) mbar_wait(&sm.full[s], (issued[s] - 1) & 1u, &never);
+      }
+    } else {
+      grid_dep_wait();
+    }
+  } else if (warp == 1) {
+    grid_dep_wait();
+    if (elect_lane0() && u1 > u0) {
+      // -------------------------------------------------------- MMA issuer
+      const uint32_t idesc = idesc_bf16(kTileN, p.ntok);
+      int stage = 0;
+      uint32_t phase = 0;
+      int seg = 0;
+      long long u = u0;
+      bool ok = true;
+      while (u < u1 && ok) {
+        const int t = part.tile_of(u);
+        const long long seg_end = min(u1, static_cast<long long>(t + 1) * p.kc);
+        const int a = seg & 1;
+        ok = mbar_wait(&sm.accempty[a], ((seg >> 1) & 1) ^ 1u, sm.abort);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t dcol = tmem_base + static_cast<uint32_t>(a * p.ntok);
+        for (long long v = u; v < seg_end; ++v) {
+          if (!mbar_wait(&sm.full[stage], phase, sm.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t abase = smem_u32(sm.stage_base + static_cast<size_t>(stage) * sbytes);
+          const uint32_t bbase = abase + kATileBytes;
+          const uint32_t lbase = bbase + static_cast<uint32_t>(p.ntok) * 128;
+#pragma unroll
+          for (int kk = 0; kk < kTileK / 16; ++kk) {
+            const uint64_t ad = sdesc_k128(abase + kk * 32);
+            umma_bf16(dcol, ad, sdesc_k128(bbase + kk * 32), idesc, (v > u || kk > 0) ? 1u : 0u);
+            // the bf16 residual of the activations into the same accumulator
+            if (p.split) umma_bf16(dcol, ad, sdesc_k128(lbase + kk * 32), idesc, 1u);
+          }
+          umma_commit(&sm.empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&sm.accfull[a]);
+        u = seg_end;
+        ++seg;
+      }
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    grid_dep_wait();
+    const int e = threadIdx.x - (kThreads - kEpiThreads);
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + (threadIdx.x & 31);
+    if (p.ssq_in) {
+      for (int c = e; c < p.ntok; c += kEpiThreads) {
+        const int m = p.tok0 + c;
+        float s = 0.f;
+        if (m < p.M)
+          for (int t = 0; t < p.ssq_tiles; ++t) s += p.ssq_in[static_cast<long long>(t) * p.ssq_ld + m];
+        sm.rs[c] = rsqrtf(s * p.inv_d + p.eps);
+      }
+    }
+    named_bar(kEpiBar, kEpiThreads);
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    int seg = 0;
+    long long u = u0;
+    while (u < u1) {
+      const int t = part.tile_of(u);
+      const long long seg_end = min(u1, static_cast<long long>(t + 1) * p.kc);
+      const int a = seg & 1;
+      mbar_wait(&sm.accfull[a], (seg >> 1) & 1, sm.abort);
+      named_bar(kEpiBar, kEpiThreads);  // all four warps leave together on abort
+      if (*sm.abort) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(a * p.ntok);
+      const int c_first = part.cta_of(static_cast<long long>(t) * p.kc);
+      const int c_last = part.cta_of(static_cast<long long>(t + 1) * p.kc - 1);
+      bool finisher = true;
+      if (c_first != c_last) {
+        const int slot = part.slot(me, t);
+        float* dst = p.partials + (static_cast<long long>(me) * 2 + slot) * p.ntok * kTileN;
+        for (int c0 = 0; c0 < p.ntok; c0 += 16) {
+          float v[16];
+          load_acc(tacc, c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) __stcg(dst + (c0 + j) * kTileN + r, v[j]);
+        }
+        __threadfence();
+        named_bar(kEpiBar, kEpiThreads);
+        if (e == 0) {
+          const int old = atomicAdd(&p.counters[t], 1);
+          const int last = old == c_last - c_first;
+          if (last) p.counters[t] = 0;
+          *sm.flag = last;
+        }
+        named_bar(kEpiBar, kEpiThreads);
+        finisher = *sm.flag != 0;
+        __threadfence();
+      }
+      if (finisher) {
+        for (int c0 = 0; c0 < p.ntok; c0 += 16) {
+          float own[16], acc[16];
+          load_acc(tacc, c0, own);
+          if (c_first == c_last) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = own[j];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+            for (int c = c_first; c <= c_last; ++c) {
+              if (c == me) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] += own[j];
+              } else {
+                const float* src =
+                    p.partials + (static_cast<long long>(c) * 2 + part.slot(c, t)) * p.ntok * kTileN;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] += ldcg(src + (c0 + j) * kTileN + r);
+              }
+            }
+          }
+          epilogue_chunk(p, sm, t, r, c0, acc);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.accempty[a]);
+      u = seg_end;
+      ++seg;
+    }
+  }
+
+  if (*sm.abort && threadIdx.x == 0) set_status(p.status, SPEC_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tcols);
+  }
+}
+
+size_t gemm_smem_bytes(int rows_b, int stages) {
+  return 1024 + stage_bytes(rows_b) * stages + kTailBytes;
+}
+
+int gemm_max_stages(int rows_b, size_t budget) {
+  int s = static_cast<int>((budget - 1024 - kTailBytes) / stage_bytes(rows_b));
+  if (s > kMaxStages) s = kMaxStages;
+  return s;
+}
+
+cudaError_t launch_gemm(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmXlo,
+                        const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
+  const size_t smem = gemm_smem_bytes(p.ntok << p.split, p.stages);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, *tmW, *tmX, *tmXlo, p);
+}
+
+}  // namespace spec

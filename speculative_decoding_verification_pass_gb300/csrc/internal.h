@@ -1,0 +1,144 @@
+// Host-side declarations shared by the C-ABI translation unit and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace spec {
+
+// ------------------------------------------------------------------ GEMM
+// Y[m][n] = sum_k X[m][k] * W[n][k]; W bf16 [N][K] (TMA map tmW), X bf16
+// [rows][K] (TMA map tmX); N-tiles of 128 rows, K-chunks of 64.
+enum EpiKind { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3 };
+
+struct GemmParams {
+  int N, K;        // weight rows (output features) and reduction length
+  int M;           // valid token rows in total (rows >= M are padding)
+  int tok0;        // first token row handled by this launch
+  int ntok;        // token tile (multiple of 16, <= 256)
+  int split;       // 1: B operand = [X_hi rows ; X_lo rows], both accumulated into D
+  int kc;          // K / 64
+  int n_tiles;     // ceil(N / 128)
+  long long units; // n_tiles * kc
+  int stages;      // smem ring depth
+  int epi;         // EpiKind
+  // RMSNorm of the consumer: rs[m] = rsqrt(sum_t ssq_in[t][m] / d + eps)
+  const float* ssq_in;  // nullptr: no norm scale
+  int ssq_tiles;
+  int ssq_ld;
+  float inv_d, eps;
+  // EPI_STORE
+  float* out;
+  int ldo;
+  // EPI_RESID: h[m][f] += y; hb[m][f] = bf16(h * g_next[f]); ssq_out[tile][m]
+  float* h;
+  uint16_t* hb;
+  uint16_t* hb_lo;        // bf16(x - bf16(x)) or nullptr
+  const float* g_next;
+  float* ssq_out;
+  int d;
+  // EPI_QKV
+  uint16_t* q;           // [M][H*hd]
+  uint16_t* q_lo;        // bf16 residual of q, or nullptr
+  uint16_t* kcache;      // this layer's K base [B][Hkv][cap][hd]
+  uint16_t* vcache;
+  const int32_t* pos_base;
+  const int32_t* seq_ok;  // per sequence: 1 if its slots fit in the cache
+  const float2* rope;     // [hd/2] frequency (hi, lo)
+  int n_per_seq, H, Hkv, hd, cap;
+  // EPI_SWIGLU: rows 0-63 of a tile are gate features, 64-127 up features
+  uint16_t* act;  // [M][ffn]
+  uint16_t* act_lo;
+  int ffn;
+  // stream-K workspace
+  float* partials;    // [grid][2][ntok][128]
+  int32_t* counters;  // [n_tiles], zero on entry, left zero
+  int32_t* status;
+};
+
+// Shared memory a launch needs for `stages` ring stages.
+// `rows_b` = token rows of the B operand per stage (ntok << split).
+size_t gemm_smem_bytes(int rows_b, int stages);
+int gemm_max_stages(int rows_b, size_t smem_budget);
+cudaError_t launch_gemm(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmXlo,
+                        const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
+
+// -------------------------------------------------------------- attention
+struct AttnParams {
+  const uint16_t* q;      // [M][H*hd] bf16 (RoPE applied)
+  const uint16_t* q_lo;   // bf16 residual of q, or nullptr
+  const uint16_t* kcache; // this layer's [B][Hkv][cap][hd]
+  const uint16_t* vcache;
+  uint16_t* o;            // [M][H*hd] bf16
+  uint16_t* o_lo;         // bf16 residual of o, or nullptr
+  const int32_t* pos_base;
+  float* part_o;          // [B][Hkv][splits][R][hd]
+  float* part_ml;         // [B][Hkv][splits][R][2]
+  int32_t* counters;      // [B*Hkv], zero on entry, left zero
+  int32_t* status;
+  int B, n, H, Hkv, hd, cap, splits, R;
+  float scale_log2;       // log2(e) / sqrt(hd)
+};
+constexpr int kAttnChunk = 128;  // keys per CTA
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl);
+
+// ------------------------------------------------------------ small kernels
+struct EmbedParams {
+  const int32_t* tokens;  // [B][n]
+  const uint16_t* embed;  // [V][d]
+  const float* g0;        // gain of the first consumer norm
+  float* h;
+  uint16_t* hb;
+  uint16_t* hb_lo;
+  float* ssq;             // [d/128][ld]
+  int ssq_ld;
+  int32_t* len;           // [B] cache lengths (advanced by n)
+  int32_t* pos_base;      // [B] out: length before this pass
+  int32_t* seq_ok;        // [B] out
+  int32_t* counters;      // zeroed here
+  int n_counters;
+  int32_t* status;
+  int B, n, d, V, cap;
+};
+cudaError_t launch_embed(const EmbedParams& p, cudaStream_t stream, bool pdl);
+
+cudaError_t launch_init_weights(uint16_t* dst, long long rows, long long cols, int tid,
+                                uint64_t seed, int block_rows, int row_stride_rows,
+                                cudaStream_t stream);
+cudaError_t launch_fill_f32(float* dst, long long n, float v, cudaStream_t stream);
+cudaError_t launch_rope_table(float2* dst, int hd, double theta, cudaStream_t stream);
+
+// ------------------------------------------------------------------ accept
+struct AcceptParams {
+  const float* logits;   // [B][gamma+1][V]
+  const float* q;        // [B][gamma][V]
+  const int32_t* draft;  // [B][gamma]
+  const float* u;        // [B][gamma+1]
+  int32_t* out;          // [B][gamma+1]
+  int32_t* n_acc;        // [B]
+  int32_t* status;
+  int B, gamma, V;
+  float T, top_p;
+};
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream, bool pdl);
+
+struct SampleParams {
+  const float* logits;  // [R][V]
+  const float* u;       // [R]
+  float* probs;         // [R][V] or nullptr
+  int32_t* tokens;      // [R]
+  int32_t* status;
+  int R, V;
+  float T, top_p;
+};
+cudaError_t launch_sample(const SampleParams& p, cudaStream_t stream);
+
+cudaError_t launch_truncate(int32_t* len, const int32_t* n_acc, int B, int gamma, int32_t* status,
+                            cudaStream_t stream, bool pdl);
+
+}  // namespace spec

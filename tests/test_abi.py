@@ -1,0 +1,89 @@
+"""The C-ABI library loads and exports every declared entry point; host-only
+calls (sizes, status strings, argument validation) work without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decoding_verification_pass_gb300 import binding
+    return binding
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "spec_verify.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    L = lib.lib()
+    names = _declared()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(lib.EXPORTED)
+
+
+def test_status_strings(lib):
+    L = lib.lib()
+    for s in range(0, -7, -1):
+        assert L.spec_status_string(s)
+    assert L.spec_status_string(-99) == b"unknown status"
+
+
+def test_sizes(lib):
+    c8 = lib.LLAMA_8B
+    wb = lib.spec_model_weight_bytes(c8)
+    # 32 layers x (6144+4096+28672+14336... ) -- matrices dominate: ~8.03e9 params
+    params = 2 * 128256 * 4096 + 32 * (6144 * 4096 + 4096 * 4096 + 2 * 14336 * 4096 + 4096 * 14336)
+    assert params * 2 <= wb < params * 2 + 2_000_000   # + fp32 norm gains, alignment
+    assert lib.spec_kv_bytes(c8, 1, 2064) == 32 * 1 * 8 * 2064 * 128 * 2
+    assert lib.spec_workspace_bytes(c8, 1, 4, 2064) > 0
+    bad = lib.ModelConfig(2, 100, 4, 2, 64, 10)      # d not a multiple of 128
+    assert lib.spec_model_weight_bytes(bad) == 0
+    bad = lib.ModelConfig(2, 256, 4, 3, 64, 10)      # heads not a multiple of kv heads
+    assert lib.spec_model_weight_bytes(bad) == 0
+
+
+def test_argument_validation_without_gpu(lib):
+    L = lib.lib()
+    P = ctypes.c_void_p
+    # NULL pointers are rejected before any CUDA call
+    assert L.spec_accept(None, None, None, None, 1, 4, 10, 1.0, 1.0, None, None, None, 0, None) == lib.SPEC_EINVAL
+    assert L.spec_draft_sample(None, 1, 10, 1.0, 1.0, None, None, None, None, 0, None) == lib.SPEC_EINVAL
+    assert L.spec_verify_forward(None, None, 1, 4, None, None, None, 0, None) == lib.SPEC_EINVAL
+    assert L.spec_kv_truncate(None, None, 4, None, None) == lib.SPEC_EINVAL
+    # bad temperature / top_p
+    fake = P(4096)
+    assert L.spec_accept(fake, fake, fake, fake, 1, 4, 10, -1.0, 1.0, fake, fake, fake, 256, None) == lib.SPEC_EINVAL
+    assert L.spec_accept(fake, fake, fake, fake, 1, 4, 10, 1.0, 0.0, fake, fake, fake, 256, None) == lib.SPEC_EINVAL
+    assert L.spec_accept(fake, fake, fake, fake, 1, 4, 10, 1.0, 1.5, fake, fake, fake, 256, None) == lib.SPEC_EINVAL
+    # workspace too small
+    assert L.spec_accept(fake, fake, fake, fake, 1, 4, 10, 1.0, 1.0, fake, fake, fake, 8, None) == lib.SPEC_ESIZE
+    # zero-size batch is a no-op
+    assert L.spec_accept(fake, fake, fake, fake, 0, 4, 10, 1.0, 1.0, fake, fake, fake, 256, None) == lib.SPEC_OK
+    out = P()
+    cfg = lib.LLAMA_1B.c()
+    assert L.spec_model_create(ctypes.byref(cfg), 1, None, 0, None, ctypes.byref(out)) == lib.SPEC_EINVAL
+    assert L.spec_model_destroy(None) == lib.SPEC_OK
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_pass_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle", src, re.M), f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith(".py"):
+            src = open(os.path.join(ROOT, "oracle", f)).read()
+            assert "speculative_decoding_verification_pass_gb300" not in src, f

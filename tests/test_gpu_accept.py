@@ -1,0 +1,172 @@
+"""GPU parity of the acceptance kernels against the fp64 oracle.
+
+Same seeded fp32 inputs on both sides (target logits, draft probabilities,
+draft tokens, uniforms); the draft side (q and x) is produced by the oracle.
+Emitted tokens and n_accepted must match exactly except where the oracle
+flags a decision within its fp32/fp64 margin (|u - min(1,p/q)| < 1e-4, an
+inverse-CDF point within 1e-5 of u*S, a nucleus threshold within 1e-5);
+such excused disagreements are counted and must stay below 0.1%.  Probabilities from
+spec_draft_sample must match the oracle within relative error 1e-5.
+"""
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+from oracle import accept as OA
+from speculative_decoding_verification_pass_gb300 import binding as sb
+from speculative_decoding_verification_pass_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _draft(zq, ud, T, top_p):
+    """Oracle-side draft: q = top-p(softmax(z_q/T)) in fp64 -> fp32, x ~ q."""
+    B, gamma, V = zq.shape
+    q = np.zeros((B, gamma, V), np.float32)
+    x = np.zeros((B, gamma), np.int32)
+    for b in range(B):
+        qs, ts, _ = OA.draft_sample(zq[b], ud[b], T, top_p)
+        q[b] = qs.astype(np.float32)
+        x[b] = ts
+    return q, x
+
+
+def _run_accept(zp, q, x, u, T, top_p):
+    B, n, V = zp.shape
+    gamma = n - 1
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = torch.full((B, n), -7, dtype=torch.int32, device="cuda")
+    nacc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    ws = sb.workspace(sb.spec_accept_workspace_bytes(B, gamma, V))
+    sb.spec_accept(dev(zp), dev(q) if gamma else None, dev(x) if gamma else None, dev(u), B, gamma,
+                   V, T, top_p, out, nacc, ws)
+    st, bits = sb.spec_device_status(ws)
+    assert st == sb.SPEC_OK, bits
+    return out.cpu().numpy(), nacc.cpu().numpy()
+
+
+def _compare(zp, q, x, u, T, top_p, out, nacc):
+    """Exact agreement required except where the oracle flags the decision
+    as within its margin; returns (excused mismatches, cases in a margin)."""
+    B = zp.shape[0]
+    excused = near = 0
+    for b in range(B):
+        r = OA.accept(zp[b], q[b] if T > 0 else None, x[b], u[b] if T > 0 else None, T, top_p)
+        same = int(nacc[b]) == r.n_accepted and out[b].tolist() == r.tokens
+        near += r.boundary
+        if not same:
+            assert r.boundary, (b, out[b].tolist(), r.tokens, int(nacc[b]), r.n_accepted)
+            excused += 1
+    return excused, near
+
+
+@pytest.mark.parametrize("B,gamma,V,T,top_p", [
+    (1000, 4, 4096, 1.0, 1.0),      # the spec_accept-only workload: 1000 steps of gamma=4, V=4096
+    (200, 4, 4096, 0.0, 1.0),       # greedy
+    (200, 4, 4096, 0.8, 0.9),       # temperature + nucleus on p and q
+    (100, 8, 1000, 1.0, 1.0),       # ragged vocabulary, longer draft
+    (64, 0, 777, 1.0, 1.0),         # no drafts: plain sampling of the bonus row
+    (64, 2, 3, 1.0, 1.0),           # tiny vocabulary
+    (16, 4, 32000, 0.7, 0.95),      # 1B vocabulary with nucleus
+])
+def test_accept_matches_oracle(B, gamma, V, T, top_p):
+    seed = 1000 + B + gamma + V
+    zq, zp = wl.accept_logits(seed, B, gamma, V)
+    ud = wl.uniforms(seed, B, gamma, stream=8)
+    u = wl.uniforms(seed, B, gamma + 1)
+    Tq = T if T > 0 else 1.0
+    q, x = _draft(zq[:, :gamma], ud, Tq, top_p)
+    if T == 0:
+        # greedy drafts: the draft's argmax, some of them agreeing with the target
+        x = zq[:, :gamma].argmax(-1).astype(np.int32)
+        agree = wl.uniforms(seed, B, gamma, stream=9) < 0.7
+        x = np.where(agree, zp[:, :gamma].argmax(-1), x).astype(np.int32)
+    out, nacc = _run_accept(zp, q, x, u, T, top_p)
+    excused, near = _compare(zp, q, x, u, T, top_p, out, nacc)
+    assert excused <= 0.001 * B, (excused, near)
+    if T > 0 and gamma > 0:
+        assert (nacc > 0).any()
+
+
+def test_accept_repeatable():
+    zq, zp = wl.accept_logits(5, 64, 4, 4096)
+    ud = wl.uniforms(5, 64, 4, stream=8)
+    u = wl.uniforms(5, 64, 5)
+    q, x = _draft(zq[:, :4], ud, 1.0, 0.9)
+    a = _run_accept(zp, q, x, u, 1.0, 0.9)
+    b = _run_accept(zp, q, x, u, 1.0, 0.9)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("R,V,T,top_p", [(64, 4096, 1.0, 1.0), (32, 4096, 0.8, 0.9),
+                                         (8, 128256, 1.0, 1.0), (8, 32000, 0.6, 0.5),
+                                         (16, 1000, 0.0, 1.0)])
+def test_draft_sample_probs_and_tokens(R, V, T, top_p):
+    seed = 77 + R + V
+    z = wl.accept_logits(seed, R, 0, V)[0][:, 0]
+    u = wl.uniforms(seed, R)
+    probs = torch.empty(R, V, device="cuda")
+    toks = torch.empty(R, dtype=torch.int32, device="cuda")
+    ws = sb.workspace(sb.spec_accept_workspace_bytes(R, 0, V))
+    sb.spec_draft_sample(torch.from_numpy(z).cuda(), R, V, T, top_p, torch.from_numpy(u).cuda(),
+                         probs, toks, ws)
+    P = probs.double().cpu().numpy()
+    t = toks.cpu().numpy()
+    qs, ts, bnd = OA.draft_sample(z, u, T, top_p)
+    mask = qs > 1e-30
+    rel = np.abs(P[mask] - qs[mask]) / qs[mask]
+    assert rel.max() <= 1e-5, rel.max()
+    assert (P[~mask] <= 1e-30).all()
+    ok = (t == ts) | bnd
+    assert ok.all(), np.flatnonzero(~ok)
+
+
+def test_worked_example_on_device():
+    """lattice notes worked example: ratio 0.5; r=0.42 accepts, r=0.71
+    rejects and the residual puts all its mass on 'green'."""
+    p = np.array([0.3, 0.4, 0.2, 0.1])
+    q = np.array([[[0.6, 0.05, 0.2, 0.15]]], np.float32)
+    z = np.log(np.array([[p, p]])).astype(np.float32)
+    x = np.array([[0]], np.int32)
+    out, nacc = _run_accept(z, q, x, np.array([[0.42, 0.5]], np.float32), 1.0, 1.0)
+    assert nacc[0] == 1 and out[0, 0] == 0
+    for ud in (0.0, 0.5, 0.99):
+        out, nacc = _run_accept(z, q, x, np.array([[0.71, ud]], np.float32), 1.0, 1.0)
+        assert nacc[0] == 0 and out[0].tolist() == [1, -1]
+
+
+def test_chi_square_v8_million_trials():
+    """V=8, gamma=4, fixed (p,q) rows per position, 10^6 independent trials on
+    the device: the token emitted at each position follows that position's p."""
+    V, gamma, N = 8, 4, 1_000_000
+    g = np.random.default_rng(7)
+    P = g.dirichlet(np.ones(V), size=gamma + 1)
+    Q = np.clip(P[:gamma] + g.normal(0, 0.08, size=(gamma, V)), 0.01, None)
+    Q /= Q.sum(1, keepdims=True)
+    zp = np.broadcast_to(np.log(P).astype(np.float32), (N, gamma + 1, V))
+    qf = Q.astype(np.float32)
+    ud = wl.uniforms(31, N, gamma, stream=8)
+    cq = np.cumsum(qf.astype(np.float64), axis=1)
+    x = np.stack([np.minimum((ud[:, i, None] >= cq[i][None, :] / cq[i][-1]).sum(1), V - 1)
+                  for i in range(gamma)], 1).astype(np.int32)
+    u = wl.uniforms(31, N, gamma + 1)
+    out, nacc = _run_accept(np.ascontiguousarray(zp), np.ascontiguousarray(np.broadcast_to(qf, (N, gamma, V))),
+                            x, u, 1.0, 1.0)
+    Pf = np.exp(np.log(P).astype(np.float32).astype(np.float64))
+    Pf /= Pf.sum(1, keepdims=True)
+    for k in range(gamma + 1):
+        col = out[:, k]
+        col = col[col >= 0]
+        chi = stats.chisquare(np.bincount(col, minlength=V), Pf[k] * col.size)
+        assert chi.pvalue > 1e-3, (k, chi)
+    alpha = np.minimum(Pf[0], Q[0]).sum()
+    acc0 = (nacc > 0).mean()
+    assert abs(acc0 - alpha) < 4 * np.sqrt(alpha * (1 - alpha) / N)

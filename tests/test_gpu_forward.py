@@ -1,0 +1,220 @@
+"""GPU parity of the verification forward, the LM head and the KV rollback.
+
+The oracle generates its own weights from the same seed with its own
+Philox4x64-10 + Box-Muller implementation and runs the fp64 decoder with its
+own cache; the device runs spec_model_create + spec_verify_forward.  Logits
+must agree within |d| <= 1e-2 * (1 + |logit|); the generator must agree
+bit-exactly on sampled elements (1-ulp slips allowed on at most 1e-4 of them,
+from last-bit differences in fp64 log/sin/cos).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import accept as OA
+from oracle import model as OM
+from oracle import weights as OW
+from oracle.bf16 import from_bits
+from speculative_decoding_verification_pass_gb300 import binding as sb
+from speculative_decoding_verification_pass_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _ocfg(c: sb.ModelConfig) -> OM.Config:
+    return OM.Config(c.n_layers, c.d_model, c.n_heads, c.n_kv_heads, c.d_ffn, c.vocab,
+                     c.rms_eps, c.rope_theta)
+
+
+def _close(got, ref, tol=TOL):
+    err = np.abs(got - ref) / (1.0 + np.abs(ref))
+    assert err.max() <= tol, f"max rel err {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}"
+    return err.max()
+
+
+class Pair:
+    """A device model + cache and the oracle's model + cache, same seed."""
+
+    def __init__(self, cfg, seed, B, cap):
+        self.cfg, self.B, self.cap = cfg, B, cap
+        self.model = sb.Model(cfg, seed)
+        self.kv = sb.KVCache(cfg, B, cap)
+        self.ws = sb.workspace(sb.spec_workspace_bytes(cfg, B, 127, cap))
+        self.ocfg = _ocfg(cfg)
+        self.W = OW.Weights(self.ocfg, seed)
+        self.okv = OM.KVState(self.ocfg, B, cap)
+
+    def gpu(self, toks):
+        B, n = toks.shape
+        out = torch.empty(B, n, self.cfg.vocab, device="cuda")
+        sb.spec_verify_forward(self.model.handle, torch.from_numpy(np.ascontiguousarray(toks)).cuda(),
+                               B, n - 1, self.kv, out, self.ws)
+        return out.double().cpu().numpy()
+
+    def oracle(self, toks):
+        return OM.forward(self.ocfg, self.W, toks, self.okv)
+
+    def prefill(self, toks, chunk=100):
+        for c0 in range(0, toks.shape[1], chunk):
+            blk = toks[:, c0:c0 + chunk]
+            g = self.gpu(blk)
+            o = self.oracle(blk)
+            _close(g, o)
+
+    def status_ok(self):
+        st, bits = sb.spec_device_status(self.ws)
+        assert st == sb.SPEC_OK, hex(bits)
+
+
+SMALL = [
+    sb.ModelConfig(2, 256, 4, 2, 256, 1000),        # hd 64, G 2, ragged vocab
+    sb.ModelConfig(2, 512, 4, 1, 384, 4099),        # hd 128, G 4, ragged vocab
+    sb.ModelConfig(3, 1024, 8, 8, 2048, 2048),      # hd 128, G 1 (MHA), several K tiles
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=["hd64", "hd128", "mha"])
+def test_generator_matches_oracle(cfg):
+    m = sb.Model(cfg, 9)
+    W = OW.Weights(_ocfg(cfg), 9)
+    torch.cuda.synchronize()
+    checks = [(-1, 0, None), (-1, 1, None)] + [(l, k, None) for l in range(cfg.n_layers) for k in range(7)]
+    slips = total = 0
+    for layer, which, _ in checks:
+        dev = m.tensor(layer, which).view(torch.int16).cpu().numpy().view(np.uint16)
+        if layer == -1:
+            ref = OW.tensor(9, which, cfg.vocab, cfg.d_model)
+        else:
+            ref = W.layer(layer)[which]
+        got = from_bits(dev)
+        diff = got != ref
+        total += got.size
+        if diff.any():
+            # at most one bf16 ulp apart
+            ulp = np.abs(got[diff] - ref[diff]) / np.maximum(np.abs(ref[diff]), 1e-30)
+            assert (ulp <= 2 ** -7 + 1e-12).all()
+            slips += int(diff.sum())
+    assert slips <= max(1, total // 10000), (slips, total)
+    m.close()
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=["hd64", "hd128", "mha"])
+def test_forward_matches_oracle_ragged_batch(cfg):
+    """Prefill 2 sequences (300 tokens: 3 key chunks, ragged), verify a
+    gamma=4 block, roll back different amounts per sequence, verify again."""
+    B, cap, gamma = 2, 320, 4
+    pr = Pair(cfg, 21, B, cap)
+    pr.prefill(wl.tokens(3, B, 300, cfg.vocab))
+    blk = wl.tokens(4, B, gamma + 1, cfg.vocab)
+    _close(pr.gpu(blk), pr.oracle(blk))
+    n_acc = np.array([1, 4], np.int32)[:B]
+    sb.spec_kv_truncate(pr.kv, torch.from_numpy(n_acc).cuda(), gamma, pr.ws)
+    pr.okv.lens = OM.truncate(pr.okv.lens, n_acc, gamma)
+    np.testing.assert_array_equal(pr.kv.len.cpu().numpy(), pr.okv.lens)
+    blk = wl.tokens(5, B, gamma + 1, cfg.vocab)
+    _close(pr.gpu(blk), pr.oracle(blk))
+    # the cache contents (bf16) agree with the oracle's cache
+    for l in range(cfg.n_layers):
+        for b in range(B):
+            Lb = int(pr.okv.lens[b])
+            kd = pr.kv.k[l, b, :, :Lb].double().cpu().numpy()
+            vd = pr.kv.v[l, b, :, :Lb].double().cpu().numpy()
+            _close(kd, pr.okv.K[l][b, :, :Lb])
+            _close(vd, pr.okv.V[l][b, :, :Lb])
+    pr.status_ok()
+    pr.model.close()
+
+
+def test_one_pass_equals_sequential_passes_on_device():
+    cfg = SMALL[1]
+    B, cap, gamma = 2, 200, 4
+    a = Pair(cfg, 8, B, cap)
+    b = Pair(cfg, 8, B, cap)
+    pre = wl.tokens(6, B, 150, cfg.vocab)
+    a.gpu(pre[:, :100]); a.gpu(pre[:, 100:])
+    b.gpu(pre[:, :100]); b.gpu(pre[:, 100:])
+    blk = wl.tokens(7, B, gamma + 1, cfg.vocab)
+    one = a.gpu(blk)
+    seq = np.concatenate([b.gpu(blk[:, j:j + 1]) for j in range(gamma + 1)], axis=1)
+    np.testing.assert_allclose(one, seq, rtol=1e-4, atol=1e-4)
+    np.testing.assert_array_equal(a.kv.len.cpu().numpy(), b.kv.len.cpu().numpy())
+
+
+def test_rollback_then_reverify_equals_fresh_pass_on_device():
+    cfg = SMALL[0]
+    B, cap, gamma = 1, 128, 4
+    a = Pair(cfg, 12, B, cap)
+    b = Pair(cfg, 12, B, cap)
+    pre = wl.tokens(9, B, 40, cfg.vocab)
+    a.gpu(pre)
+    b.gpu(pre)
+    blk = np.array([[7, 11, 13, 17, 19]], np.int32)
+    a.gpu(blk)
+    sb.spec_kv_truncate(a.kv, torch.tensor([1], dtype=torch.int32, device="cuda"), gamma, a.ws)
+    b.gpu(blk[:, :2])
+    nxt = np.array([[23, 29, 31, 37, 41]], np.int32)
+    np.testing.assert_allclose(a.gpu(nxt), b.gpu(nxt), rtol=1e-5, atol=1e-5)
+
+
+def test_device_status_on_overflow_and_bad_token():
+    cfg = SMALL[0]
+    B, cap = 2, 16
+    pr = Pair(cfg, 3, B, cap)
+    pr.kv.len.copy_(torch.tensor([10, 14], dtype=torch.int32))
+    toks = np.array([[1, 2, 3], [4, 5, cfg.vocab + 5]], np.int32)   # seq 1 overflows, bad id
+    pr.gpu(toks)
+    st, bits = sb.spec_device_status(pr.ws)
+    assert st == sb.SPEC_EDEVICE
+    assert bits & sb.DEV_KV_OVERFLOW and bits & sb.DEV_BAD_TOKEN
+    assert pr.kv.len.cpu().tolist() == [13, 14]
+    st, bits = sb.spec_device_status(pr.ws)      # cleared by the read
+    assert st == sb.SPEC_OK and bits == 0
+    # truncate with n_accepted out of range leaves len alone and flags it
+    sb.spec_kv_truncate(pr.kv, torch.tensor([5, -1], dtype=torch.int32, device="cuda"), 2, pr.ws)
+    st, bits = sb.spec_device_status(pr.ws)
+    assert bits & sb.DEV_BAD_NACC and pr.kv.len.cpu().tolist() == [13, 14]
+
+
+def test_lm_head_workload_and_accept():
+    """LM head 4096 x 32000 on 5 activation rows ~ N(0,1) (bf16), draft
+    probabilities from the same head on activations + N(0, 0.3^2), T = 1:
+    skinny GEMM then fused accept, checked against the oracle."""
+    cfg = sb.ModelConfig(0, 4096, 32, 8, 128, 32000)
+    seed = 41
+    m = sb.Model(cfg, seed)
+    head = OW.tensor(seed, OW.HEAD, cfg.vocab, cfg.d_model)
+    ws = sb.workspace(sb.spec_workspace_bytes(cfg, 5, 0, 1))
+    hb = wl.hidden_bf16(seed, 5, cfg.d_model)
+    h = from_bits(hb)
+    z = torch.empty(5, cfg.vocab, device="cuda")
+    sb.spec_lm_head(m.handle, torch.from_numpy(hb.view(np.int16)).cuda(), 5, z, ws)
+    zp = z.cpu().numpy()
+    ref = OM.lm_head(h, head)
+    _close(zp.astype(np.float64), ref, 1e-4)
+    # draft: the same head on noisy activations (oracle side, fp64)
+    noisy = h[:4] + wl.gauss(seed, (4, cfg.d_model), 0.3)
+    zq = OM.lm_head(noisy, head)
+    ud = wl.uniforms(seed, 1, 4, stream=8)[0]
+    q, x, _ = OA.draft_sample(zq, ud, 1.0)
+    u = wl.uniforms(seed, 1, 5)
+    out = torch.empty(1, 5, dtype=torch.int32, device="cuda")
+    nacc = torch.empty(1, dtype=torch.int32, device="cuda")
+    aws = sb.workspace(256)
+    sb.spec_accept(z.view(1, 5, -1), torch.from_numpy(q.astype(np.float32)[None]).cuda(),
+                   torch.from_numpy(x.astype(np.int32)[None]).cuda(), torch.from_numpy(u).cuda(),
+                   1, 4, cfg.vocab, 1.0, 1.0, out, nacc, aws)
+    # the oracle decides on its own logits; decisions closer to a boundary
+    # than the logits tolerance allows are not graded
+    r = OA.accept(ref.astype(np.float32), q.astype(np.float32), x, u[0], 1.0,
+                  margins=(5e-3, 5e-3, 5e-3))
+    if not r.boundary:
+        assert int(nacc[0]) == r.n_accepted and out[0].tolist() == r.tokens
+    m.close()

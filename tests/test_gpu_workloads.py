@@ -1,0 +1,193 @@
+"""The decoder workloads at their full sizes.
+
+* 1B-shaped decoder (16 layers, d 2048, 32/8 heads of 64, SwiGLU 8192, vocab
+  32000): a 512-token prefix uniform over the vocabulary is prefilled through
+  spec_verify_forward, then a gamma=4 pass is verified; every logit of every
+  pass is compared with the fp64 oracle running on its own weights and cache;
+  accept + rollback follow, then a second pass is compared again.
+* 8B-shaped decoder (32 layers, d 4096, 32/8 heads of 128, SwiGLU 14336,
+  vocab 128256) with 2048 cached tokens, the launch configuration the
+  benchmark times: properties that hold at any size (one pass over gamma+1
+  equals gamma+1 single-token passes; rollback then re-verify equals a fresh
+  pass; the greedy rule reproduces the argmax walk of the logits).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import accept as OA
+from oracle import model as OM
+from oracle import weights as OW
+from speculative_decoding_verification_pass_gb300 import binding as sb
+from speculative_decoding_verification_pass_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _rel(got, ref):
+    return (np.abs(got - ref) / (1.0 + np.abs(ref))).max()
+
+
+def test_1b_workload_matches_oracle():
+    cfg = sb.LLAMA_1B
+    ocfg = OM.Config(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn, cfg.vocab)
+    seed, B, gamma, L0 = 1002, 1, 4, 512
+    cap = L0 + 2 * (gamma + 1) + 8
+    m = sb.Model(cfg, seed)
+    kv = sb.KVCache(cfg, B, cap)
+    ws = sb.workspace(sb.spec_workspace_bytes(cfg, B, 127, cap))
+    W = OW.Weights(ocfg, seed)
+    okv = OM.KVState(ocfg, B, cap)
+    prefix = wl.tokens(seed, B, L0, cfg.vocab)
+    worst = 0.0
+    for c0 in range(0, L0, 128):
+        blk = prefix[:, c0:c0 + 128]
+        z = torch.empty(B, blk.shape[1], cfg.vocab, device="cuda")
+        sb.spec_verify_forward(m.handle, torch.from_numpy(np.ascontiguousarray(blk)).cuda(), B,
+                               blk.shape[1] - 1, kv, z, ws)
+        ref = OM.forward(ocfg, W, blk, okv)
+        worst = max(worst, _rel(z.double().cpu().numpy(), ref))
+    assert worst <= 1e-2, worst
+    # the verify pass: t_last + 4 drafts drawn as in the accept-only workload
+    zq, _ = wl.accept_logits(seed, B, gamma, cfg.vocab)
+    ud = wl.uniforms(seed, B, gamma, stream=8)
+    q, x, _ = OA.draft_sample(zq[0, :gamma], ud[0], 1.0)
+    t_last = wl.tokens(seed + 1, B, 1, cfg.vocab)
+    block = np.concatenate([t_last, x[None].astype(np.int32)], axis=1)
+    z = torch.empty(B, gamma + 1, cfg.vocab, device="cuda")
+    sb.spec_verify_forward(m.handle, torch.from_numpy(block).cuda(), B, gamma, kv, z, ws)
+    ref = OM.forward(ocfg, W, block, okv)
+    zg = z.cpu().numpy()
+    err = _rel(zg.astype(np.float64), ref)
+    assert err <= 1e-2, err
+    # accept on each side's own logits; decisions closer to a boundary than
+    # the logits tolerance are not graded
+    u = wl.uniforms(seed, B, gamma + 1)
+    out = torch.empty(B, gamma + 1, dtype=torch.int32, device="cuda")
+    nacc = torch.empty(B, dtype=torch.int32, device="cuda")
+    aws = sb.workspace(256)
+    sb.spec_accept(z, torch.from_numpy(q.astype(np.float32)[None]).cuda(),
+                   torch.from_numpy(x.astype(np.int32)[None]).cuda(), torch.from_numpy(u).cuda(),
+                   B, gamma, cfg.vocab, 1.0, 1.0, out, nacc, aws)
+    r = OA.accept(ref[0].astype(np.float32), q.astype(np.float32), x, u[0], 1.0,
+                  margins=(5e-3, 5e-3, 5e-3))
+    n_dev = int(nacc[0])
+    if not r.boundary:
+        assert n_dev == r.n_accepted and out[0].tolist() == r.tokens
+    sb.spec_kv_truncate(kv, nacc, gamma, ws)
+    okv.lens = OM.truncate(okv.lens, [n_dev], gamma)
+    assert kv.len.cpu().tolist() == okv.lens.tolist() == [L0 + 1 + n_dev]
+    # next pass from the device's emitted token
+    nxt = np.array([[int(out[0, n_dev])] + list(wl.tokens(seed + 2, 1, gamma, cfg.vocab)[0])],
+                   np.int32)
+    sb.spec_verify_forward(m.handle, torch.from_numpy(nxt).cuda(), B, gamma, kv, z, ws)
+    ref = OM.forward(ocfg, W, nxt, okv)
+    assert _rel(z.double().cpu().numpy(), ref) <= 1e-2
+    st, bits = sb.spec_device_status(ws)
+    assert st == sb.SPEC_OK, bits
+    m.close()
+
+
+@pytest.fixture(scope="module")
+def big():
+    cfg = sb.LLAMA_8B
+    seed, B, ctx = 1003, 1, 2048
+    cap = ctx + 64
+    m = sb.Model(cfg, seed)
+    K, V = wl.kv_prefix(seed, cfg.n_layers, B, cfg.n_kv_heads, ctx, cfg.head_dim)
+    kv = sb.KVCache(cfg, B, cap)
+    kv.k[:, :, :, :ctx].copy_(torch.from_numpy(K.view(np.int16)).view(torch.bfloat16))
+    kv.v[:, :, :, :ctx].copy_(torch.from_numpy(V.view(np.int16)).view(torch.bfloat16))
+    del K, V
+    ws = sb.workspace(sb.spec_workspace_bytes(cfg, B, 8, cap))
+    yield cfg, m, kv, ws, ctx
+    m.close()
+
+
+def _run(cfg, m, kv, ws, toks):
+    B, n = toks.shape
+    z = torch.empty(B, n, cfg.vocab, device="cuda")
+    sb.spec_verify_forward(m.handle, torch.from_numpy(np.ascontiguousarray(toks)).cuda(), B, n - 1,
+                           kv, z, ws)
+    return z
+
+
+@pytest.mark.parametrize("gamma", [2, 4, 8])
+def test_8b_one_pass_equals_sequential(big, gamma):
+    cfg, m, kv, ws, ctx = big
+    toks = wl.tokens(50 + gamma, 1, gamma + 1, cfg.vocab)
+    kv.len.fill_(ctx)
+    one = _run(cfg, m, kv, ws, toks).double().cpu().numpy()
+    kv.len.fill_(ctx)
+    seq = np.concatenate([_run(cfg, m, kv, ws, toks[:, j:j + 1]).double().cpu().numpy()
+                          for j in range(gamma + 1)], axis=1)
+    assert np.isfinite(one).all()
+    assert _rel(one, seq) <= 1e-3
+    st, bits = sb.spec_device_status(ws)
+    assert st == sb.SPEC_OK, bits
+
+
+def test_8b_rollback_then_reverify_equals_fresh(big):
+    cfg, m, kv, ws, ctx = big
+    gamma = 4
+    blk = wl.tokens(60, 1, gamma + 1, cfg.vocab)
+    nxt = wl.tokens(61, 1, gamma + 1, cfg.vocab)
+    kv.len.fill_(ctx)
+    _run(cfg, m, kv, ws, blk)
+    sb.spec_kv_truncate(kv, torch.tensor([2], dtype=torch.int32, device="cuda"), gamma, ws)
+    assert int(kv.len[0]) == ctx + 3
+    a = _run(cfg, m, kv, ws, nxt).double().cpu().numpy()
+    kv.len.fill_(ctx)
+    _run(cfg, m, kv, ws, blk[:, :3])
+    b = _run(cfg, m, kv, ws, nxt).double().cpu().numpy()
+    assert _rel(a, b) <= 1e-5
+
+
+@pytest.mark.parametrize("gamma", [2, 4, 8])
+def test_8b_greedy_walks_the_argmax(big, gamma):
+    cfg, m, kv, ws, ctx = big
+    kv.len.fill_(ctx)
+    toks = wl.tokens(70 + gamma, 1, gamma + 1, cfg.vocab)
+    z = _run(cfg, m, kv, ws, toks)
+    am = z[0].argmax(-1).cpu().numpy()
+    # drafts: agree with the argmax for the first two positions, then not
+    x = am[:gamma].copy()
+    if gamma > 2:
+        x[2] = (x[2] + 1) % cfg.vocab
+    out = torch.empty(1, gamma + 1, dtype=torch.int32, device="cuda")
+    nacc = torch.empty(1, dtype=torch.int32, device="cuda")
+    aws = sb.workspace(256)
+    sb.spec_accept(z, None, torch.from_numpy(x[None].astype(np.int32)).cuda(), None, 1, gamma,
+                   cfg.vocab, 0.0, 1.0, out, nacc, aws)
+    n = int(nacc[0])
+    exp_n = 2 if gamma > 2 else gamma
+    assert n == exp_n
+    assert out[0, :n + 1].tolist() == am[:n + 1].tolist()
+    sb.spec_kv_truncate(kv, nacc, gamma, ws)
+    assert int(kv.len[0]) == ctx + 1 + n
+
+
+def test_8b_pass_matches_oracle(big):
+    """The benchmark's pass at full size (8B shape, 2048 cached tokens,
+    gamma=4) against the fp64 oracle on its own weights (generated layer by
+    layer, not kept) and the same cache contents: all 5 x 128256 logits."""
+    cfg, m, kv, ws, ctx = big
+    ocfg = OM.Config(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn, cfg.vocab)
+    W = OW.Weights(ocfg, 1003, cache_layers=False)
+    okv = OM.KVState(ocfg, 1, ctx + 64)
+    K, V = wl.kv_prefix(1003, cfg.n_layers, 1, cfg.n_kv_heads, ctx, cfg.head_dim)
+    from oracle.bf16 import from_bits
+    okv.load_prefix([from_bits(K[l]) for l in range(cfg.n_layers)],
+                    [from_bits(V[l]) for l in range(cfg.n_layers)], [ctx])
+    del K, V
+    toks = wl.tokens(80, 1, 5, cfg.vocab)
+    kv.len.fill_(ctx)
+    z = _run(cfg, m, kv, ws, toks).double().cpu().numpy()
+    ref = OM.forward(ocfg, W, toks, okv)
+    assert _rel(z, ref) <= 1e-2, _rel(z, ref)
