@@ -345,6 +345,8 @@ def parse():
     ap.add_argument("--top-p", type=float, default=1.0)
     ap.add_argument("--sigma", type=float, default=0.5)
     ap.add_argument("--shape", default="8b", choices=["8b", "1b"])
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the decoder depth (profiling a smaller model)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -357,6 +359,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = sb.LLAMA_8B if args.shape == "8b" else sb.LLAMA_1B
+    if args.layers:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, n_layers=args.layers)
     workload = (f"{args.shape.upper()}-shaped synthetic Llama decoder verify pass + accept + "
                 f"rollback, batch {args.batch}, gamma {args.gamma}, context {args.context}, "
                 f"T={args.temperature}, top_p={args.top_p}, noisy-target draft sigma {args.sigma}")

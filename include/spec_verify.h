@@ -157,7 +157,8 @@ size_t spec_workspace_bytes(const spec_model_config* cfg, int batch, int gamma, 
  *   d_logits  fp32 [batch][gamma+1][vocab]; row j predicts the token after
  *             input j (rows 0..gamma-1 score x_1..x_gamma, row gamma is the
  *             bonus position).
- * Limits: batch*(gamma+1) <= 512, gamma+1 <= 128; prefill uses the same call
+ * Limits: batch*(gamma+1) <= 512, gamma+1 <= 128, capacity <= 32768 slots
+ * (SPEC_ESIZE otherwise); prefill uses the same call
  * with gamma = prompt_len - 1 in chunks.  A token id outside [0, V) is read as
  * 0 and sets SPEC_DEV_BAD_TOKEN; a sequence whose len[b]+gamma+1 exceeds the
  * capacity sets SPEC_DEV_KV_OVERFLOW, its slots beyond the capacity are not

@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -30,11 +31,42 @@ int cuda_fail(cudaError_t e) {
   } while (0)
 
 constexpr size_t kAlign = 256;
-constexpr int kMaxGrid = 192;      // stream-K grid cap (>= SM count of the part)
+constexpr int kMaxGrid = 512;      // stream-K grid cap (>= 3 x SM count of the part)
 constexpr int kMaxTok = 256;       // token rows per GEMM launch (UMMA N limit)
 constexpr int kMaxM = 512;         // token rows per pass
 constexpr int kMaxN = 128;         // gamma + 1 per pass
-constexpr size_t kGemmSmemBudget = 200 * 1024;
+// Shared-memory budget of one GEMM CTA (ring stages).  Two ~100 KB CTAs per SM
+// stream faster than one CTA with a ring twice as deep (each CTA's stage
+// round trip, not the bytes in flight, caps its rate).  Tunable with the
+// environment variable SPEC_GEMM_SMEM_KB for sweeps.
+size_t gemm_smem_budget() {
+  static size_t v = [] {
+    const char* e = getenv("SPEC_GEMM_SMEM_KB");
+    long kb = e ? atol(e) : 100;
+    if (kb < 48) kb = 48;
+    if (kb > 220) kb = 220;
+    return static_cast<size_t>(kb) * 1024;
+  }();
+  return v;
+}
+// K sub-tiles of 64 per pipeline stage (SPEC_GEMM_KSUB, default 2).
+int gemm_ksub() {
+  static int v = [] {
+    const char* e = getenv("SPEC_GEMM_KSUB");
+    int x = e ? atoi(e) : 2;
+    return x == 1 ? 1 : 2;
+  }();
+  return v;
+}
+// Stream-K grid: SM count x SPEC_GEMM_CTAS_PER_SM (default 2).
+int gemm_ctas_per_sm() {
+  static int v = [] {
+    const char* e = getenv("SPEC_GEMM_CTAS_PER_SM");
+    int x = e ? atoi(e) : 2;
+    return x < 1 ? 1 : (x > 3 ? 3 : x);
+  }();
+  return v;
+}
 
 size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 int round_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -234,10 +266,26 @@ int run_gemm(const Ctx& cx, const CUtensorMap* tmW, const void* x, const void* x
     p.tok0 = tok0;
     p.ntok = round_up(rows, 16);
     p.split = split;
-    p.kc = K / 64;
+    p.ksub = (K % 128 == 0) ? gemm_ksub() : 1;
+    p.kc = K / (64 * p.ksub);
     p.n_tiles = (N + 127) / 128;
     p.units = static_cast<long long>(p.n_tiles) * p.kc;
-    p.stages = gemm_max_stages(p.ntok << split, kGemmSmemBudget);
+    // wide token tiles (prefill) need a bigger ring budget: one CTA per SM then
+    size_t budget = gemm_smem_budget();
+    int cps = gemm_ctas_per_sm();
+    p.stages = gemm_max_stages(p.ntok << split, budget, p.ksub);
+    if (p.stages < 2) {
+      p.ksub = 1;
+      p.kc = K / 64;
+      p.units = static_cast<long long>(p.n_tiles) * p.kc;
+      p.stages = gemm_max_stages(p.ntok << split, budget, 1);
+    }
+    if (p.stages < 2) {
+      budget = 220 * 1024;
+      cps = 1;
+      p.stages = gemm_max_stages(p.ntok << split, budget, 1);
+    }
+    if (p.stages < 2) return SPEC_ESIZE;
     CUtensorMap tmX, tmXlo;
     if (!make_tmap(&tmX, x, static_cast<uint64_t>(M), static_cast<uint64_t>(K),
                    static_cast<uint32_t>(p.ntok)))
@@ -246,8 +294,10 @@ int run_gemm(const Ctx& cx, const CUtensorMap* tmW, const void* x, const void* x
                             static_cast<uint32_t>(p.ntok)))
       return SPEC_ECUDA;
     if (!split) tmXlo = tmX;
-    const int grid = static_cast<int>(
-        std::min<long long>(std::min(cx.m->sm_count, kMaxGrid), p.units));
+    int grid = static_cast<int>(std::min<long long>(std::min(cx.m->sm_count * cps, kMaxGrid), p.units));
+    // 32-bit partition arithmetic in the kernel; at most 64 CTAs per tile
+    if (static_cast<unsigned long long>(p.units) * grid >= (1ull << 32)) return SPEC_ESIZE;
+    while (grid > 1 && (static_cast<long long>(grid) * p.kc + p.units - 1) / p.units + 1 > 64) --grid;
     TimedLaunch t{};
     if (cx.timing) {
       t.a = take_event(mm);
@@ -444,6 +494,7 @@ int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch,
   if (c.n_layers == 0) return SPEC_ENOTSUP;
   if (!kv->k || !kv->v || !kv->len) return SPEC_EINVAL;
   if (kv->batch != batch || kv->capacity <= 0) return SPEC_EINVAL;
+  if (kv->capacity > kAttnChunk * kAttnMaxChunks) return SPEC_ESIZE;
   const int n = gamma + 1;
   if (n > kMaxN || static_cast<long long>(batch) * n > kMaxM) return SPEC_ESIZE;
   if (batch == 0) return SPEC_OK;
@@ -550,6 +601,9 @@ int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch,
       a.splits = P.splits;
       a.R = P.R;
       a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));
+      // decode shapes (<= 32 query rows per KV head) take the cluster path when
+      // a rank's slice of the cache fits in shared memory
+      a.cluster = P.R <= 32 ? attention_cluster_size(hd, kv->capacity, 200 * 1024) : 0;
       TimedLaunch t{};
       if (cx.timing) {
         t.a = take_event(const_cast<spec_model*>(m));

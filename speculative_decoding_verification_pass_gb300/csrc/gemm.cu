@@ -47,23 +47,23 @@ constexpr int kMaxStages = 16;
 constexpr int kEpiThreads = 128;
 constexpr int kEpiBar = 1;
 
+// Contiguous equal split of the U = n_tiles * kc work units over G CTAs
+// (32-bit: the host guarantees U * G < 2^32).
 struct Partition {
-  long long U;
-  int G;
-  int kc;
-  __device__ long long start(int c) const { return (static_cast<long long>(c) * U) / G; }
-  __device__ int cta_of(long long u) const {
-    return static_cast<int>(((u + 1) * static_cast<long long>(G) - 1) / U);
-  }
-  __device__ int tile_of(long long u) const { return static_cast<int>(u / kc); }
+  uint32_t U;
+  uint32_t G;
+  uint32_t kc;
+  __device__ uint32_t start(uint32_t c) const { return (c * U) / G; }
+  __device__ uint32_t cta_of(uint32_t u) const { return ((u + 1) * G - 1) / U; }
+  __device__ uint32_t tile_of(uint32_t u) const { return u / kc; }
   // Does CTA c cover units of more than one tile?
-  __device__ bool multi(int c) const {
-    long long s = start(c), e = start(c + 1);
+  __device__ bool multi(uint32_t c) const {
+    const uint32_t s = start(c), e = start(c + 1);
     return e > s && tile_of(s) != tile_of(e - 1);
   }
   // Partial-slot CTA c uses for its contribution to tile t.
-  __device__ int slot(int c, int t) const {
-    return (c == cta_of(static_cast<long long>(t) * kc) && multi(c)) ? 1 : 0;
+  __device__ int slot(uint32_t c, uint32_t t) const {
+    return (c == cta_of(t * kc) && multi(c)) ? 1 : 0;
   }
 };
 
@@ -76,23 +76,26 @@ struct Smem {
   uint32_t* tmem_slot;
   int* abort;
   int* flag;
+  int* slots;    // [kMaxContrib] partial-slot index of each contributor of a tile
   float* rs;     // [256]
   float* xbuf;   // [16][128]
   float* red;    // [4][16]
 };
 
-__host__ __device__ inline size_t stage_bytes(int ntok) {
-  return static_cast<size_t>(kATileBytes) + static_cast<size_t>(ntok) * 128;
+// One stage = ksub K-sub-tiles of 64: [A_0 .. A_{ksub-1}][B_0 .. B_{ksub-1}], each
+// B sub-tile holding `rows_b` token rows (hi rows, then lo rows).
+__host__ __device__ inline size_t stage_bytes(int rows_b, int ksub = 1) {
+  return (static_cast<size_t>(kATileBytes) + static_cast<size_t>(rows_b) * 128) * ksub;
 }
 
 constexpr size_t kTailBytes = 1024 /*barriers*/ + 256 * 4 /*rs*/ + 16 * 128 * 4 /*xbuf*/ +
-                              4 * 16 * 4 /*red*/ + 64;
+                              4 * 16 * 4 /*red*/ + 64 * 4 /*slots*/ + 64;
 
-__device__ Smem carve(uint8_t* raw, int ntok, int stages) {
+__device__ Smem carve(uint8_t* raw, int rows_b, int stages, int ksub) {
   uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023);
   Smem s;
   s.stage_base = reinterpret_cast<uint8_t*>(base);
-  uint8_t* t = s.stage_base + stage_bytes(ntok) * stages;
+  uint8_t* t = s.stage_base + stage_bytes(rows_b, ksub) * stages;
   s.full = reinterpret_cast<uint64_t*>(t);
   s.empty = s.full + kMaxStages;
   s.accfull = s.empty + kMaxStages;
@@ -103,6 +106,7 @@ __device__ Smem carve(uint8_t* raw, int ntok, int stages) {
   s.rs = reinterpret_cast<float*>(t + 1024);
   s.xbuf = s.rs + 256;
   s.red = s.xbuf + 16 * 128;
+  s.slots = reinterpret_cast<int*>(s.red + 4 * 16);
   return s;
 }
 
@@ -122,9 +126,9 @@ __device__ __forceinline__ void load_acc(uint32_t tacc, int c0, float (&v)[16]) 
 
 // --------------------------------------------------------------- epilogues
 // Apply the epilogue to 16 token columns [c0, c0+16) of this thread's row.
-__device__ void epilogue_chunk(const GemmParams& p, const Smem& sm, int tile, int r, int c0,
+__device__ void epilogue_chunk(const GemmParams& p, const Smem& sm, uint32_t tile, int r, int c0,
                                const float (&acc)[16]) {
-  const int f = tile * kTileN + r;  // weight row = output feature (before SwiGLU pairing)
+  const int f = static_cast<int>(tile) * kTileN + r;  // weight row = output feature
   const int e = threadIdx.x - (kThreads - kEpiThreads);
   float v[16];
 #pragma unroll
@@ -233,7 +237,7 @@ __device__ void epilogue_chunk(const GemmParams& p, const Smem& sm, int tile, in
   }
   named_bar(kEpiBar, kEpiThreads);
   if (r < 64) {
-    const int fo = tile * 64 + r;
+    const int fo = static_cast<int>(tile) * 64 + r;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int m = p.tok0 + c0 + j;
@@ -257,15 +261,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmXlo, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
-  const int nb = p.ntok << p.split;  // B rows per stage: hi rows, then (split) lo rows
-  const Smem sm = carve(smem_raw, nb, p.stages);
+  const int nb = p.ntok << p.split;  // B rows per sub-tile: hi rows, then (split) lo rows
+  const int ksub = p.ksub;
+  const Smem sm = carve(smem_raw, nb, p.stages, ksub);
   const int warp = threadIdx.x >> 5;
   const int S = p.stages;
-  const Partition part{p.units, static_cast<int>(gridDim.x), p.kc};
-  const int me = blockIdx.x;
-  const long long u0 = part.start(me), u1 = part.start(me + 1);
+  const Partition part{static_cast<uint32_t>(p.units), gridDim.x, static_cast<uint32_t>(p.kc)};
+  const uint32_t me = blockIdx.x;
+  const uint32_t u0 = part.start(me), u1 = part.start(me + 1);
+  const uint32_t kc = static_cast<uint32_t>(p.kc);
   const uint32_t tcols = tmem_cols_for(p.ntok);
-  const uint32_t sbytes = static_cast<uint32_t>(stage_bytes(nb));
+  const uint32_t sbytes = static_cast<uint32_t>(stage_bytes(nb, ksub));
+  const uint32_t boff = static_cast<uint32_t>(kATileBytes) * ksub;  // B sub-tiles after the A ones
+  const uint32_t bsub = static_cast<uint32_t>(nb) * 128;            // bytes of one B sub-tile
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -299,39 +307,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_x = l2_policy_evict_last();
       uint32_t issued[kMaxStages];
       for (int s = 0; s < S; ++s) issued[s] = 0;
-      const long long n = u1 - u0;
-      const int pre = static_cast<int>(n < S ? n : S);
+      const uint32_t n = u1 - u0;
+      const int pre = static_cast<int>(n < static_cast<uint32_t>(S) ? n : static_cast<uint32_t>(S));
+      // (tile, k-chunk) of the next unit, advanced without divisions
+      uint32_t tile = u0 / kc, kci = u0 - tile * kc;
+      uint32_t kci_b = kci;
+      auto load_a = [&](uint8_t* st, uint64_t* bar) {
+        for (int s = 0; s < ksub; ++s)
+          tma_load_2d(st + s * kATileBytes, &tmW, bar, static_cast<int>((kci * ksub + s) * kTileK),
+                      static_cast<int>(tile * kTileN), pol_w);
+      };
+      auto load_b = [&](uint8_t* st, uint64_t* bar, uint32_t k) {
+        for (int s = 0; s < ksub; ++s) {
+          uint8_t* b = st + boff + s * bsub;
+          const int x = static_cast<int>((k * ksub + s) * kTileK);
+          tma_load_2d(b, &tmX, bar, x, p.tok0, pol_x);
+          if (p.split) tma_load_2d(b + p.ntok * 128, &tmXlo, bar, x, p.tok0, pol_x);
+        }
+      };
       for (int i = 0; i < pre; ++i) {
-        const long long u = u0 + i;
-        uint8_t* a = sm.stage_base + static_cast<size_t>(i) * sbytes;
+        uint8_t* st = sm.stage_base + static_cast<size_t>(i) * sbytes;
         mbar_arrive_expect_tx(&sm.full[i], sbytes);
-        tma_load_2d(a, &tmW, &sm.full[i], static_cast<int>(u % p.kc) * kTileK,
-                    part.tile_of(u) * kTileN, pol_w);
+        load_a(st, &sm.full[i]);
+        if (++kci == kc) {
+          kci = 0;
+          ++tile;
+        }
       }
       grid_dep_wait();  // activations are produced by the previous kernel
       for (int i = 0; i < pre; ++i) {
-        const long long u = u0 + i;
-        uint8_t* b = sm.stage_base + static_cast<size_t>(i) * sbytes + kATileBytes;
-        tma_load_2d(b, &tmX, &sm.full[i], static_cast<int>(u % p.kc) * kTileK, p.tok0, pol_x);
-        if (p.split)
-          tma_load_2d(b + p.ntok * 128, &tmXlo, &sm.full[i], static_cast<int>(u % p.kc) * kTileK,
-                      p.tok0, pol_x);
+        load_b(sm.stage_base + static_cast<size_t>(i) * sbytes, &sm.full[i], kci_b);
         issued[i] = 1;
+        if (++kci_b == kc) kci_b = 0;
       }
       int stage = pre % S;
       uint32_t phase = pre == S ? 1u : 0u;
-      for (long long u = u0 + pre; u < u1; ++u) {
+      for (uint32_t u = u0 + pre; u < u1; ++u) {
         if (!mbar_wait(&sm.empty[stage], phase ^ 1u, sm.abort)) break;
-        uint8_t* a = sm.stage_base + static_cast<size_t>(stage) * sbytes;
+        uint8_t* st = sm.stage_base + static_cast<size_t>(stage) * sbytes;
         mbar_arrive_expect_tx(&sm.full[stage], sbytes);
-        tma_load_2d(a, &tmW, &sm.full[stage], static_cast<int>(u % p.kc) * kTileK,
-                    part.tile_of(u) * kTileN, pol_w);
-        tma_load_2d(a + kATileBytes, &tmX, &sm.full[stage], static_cast<int>(u % p.kc) * kTileK,
-                    p.tok0, pol_x);
-        if (p.split)
-          tma_load_2d(a + kATileBytes + p.ntok * 128, &tmXlo, &sm.full[stage],
-                      static_cast<int>(u % p.kc) * kTileK, p.tok0, pol_x);
+        load_a(st, &sm.full[stage]);
+        load_b(st, &sm.full[stage], kci);
         ++issued[stage];
+        if (++kci == kc) {
+          kci = 0;
+          ++tile;
+        }
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
@@ -354,31 +375,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int seg = 0;
-      long long u = u0;
+      uint32_t u = u0;
       bool ok = true;
       while (u < u1 && ok) {
-        const int t = part.tile_of(u);
-        const long long seg_end = min(u1, static_cast<long long>(t + 1) * p.kc);
+        const uint32_t t = part.tile_of(u);
+        const uint32_t seg_end = min(u1, (t + 1) * kc);
         const int a = seg & 1;
         ok = mbar_wait(&sm.accempty[a], ((seg >> 1) & 1) ^ 1u, sm.abort);
         if (!ok) break;
         tc_fence_after();
         const uint32_t dcol = tmem_base + static_cast<uint32_t>(a * p.ntok);
-        for (long long v = u; v < seg_end; ++v) {
+        for (uint32_t v = u; v < seg_end; ++v) {
           if (!mbar_wait(&sm.full[stage], phase, sm.abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t abase = smem_u32(sm.stage_base + static_cast<size_t>(stage) * sbytes);
-          const uint32_t bbase = abase + kATileBytes;
-          const uint32_t lbase = bbase + static_cast<uint32_t>(p.ntok) * 128;
+          const uint32_t sbase = smem_u32(sm.stage_base + static_cast<size_t>(stage) * sbytes);
+          for (int s = 0; s < ksub; ++s) {
+            const uint32_t abase = sbase + s * kATileBytes;
+            const uint32_t bbase = sbase + boff + s * bsub;
+            const uint32_t lbase = bbase + static_cast<uint32_t>(p.ntok) * 128;
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk) {
-            const uint64_t ad = sdesc_k128(abase + kk * 32);
-            umma_bf16(dcol, ad, sdesc_k128(bbase + kk * 32), idesc, (v > u || kk > 0) ? 1u : 0u);
-            // the bf16 residual of the activations into the same accumulator
-            if (p.split) umma_bf16(dcol, ad, sdesc_k128(lbase + kk * 32), idesc, 1u);
+            for (int kk = 0; kk < kTileK / 16; ++kk) {
+              const uint64_t ad = sdesc_k128(abase + kk * 32);
+              umma_bf16(dcol, ad, sdesc_k128(bbase + kk * 32), idesc,
+                        (v > u || s > 0 || kk > 0) ? 1u : 0u);
+              // the bf16 residual of the activations into the same accumulator
+              if (p.split) umma_bf16(dcol, ad, sdesc_k128(lbase + kk * 32), idesc, 1u);
+            }
           }
           umma_commit(&sm.empty[stage]);
           if (++stage == S) {
@@ -410,20 +435,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar(kEpiBar, kEpiThreads);
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     int seg = 0;
-    long long u = u0;
+    uint32_t u = u0;
     while (u < u1) {
-      const int t = part.tile_of(u);
-      const long long seg_end = min(u1, static_cast<long long>(t + 1) * p.kc);
+      const uint32_t t = part.tile_of(u);
+      const uint32_t seg_end = min(u1, (t + 1) * kc);
       const int a = seg & 1;
       mbar_wait(&sm.accfull[a], (seg >> 1) & 1, sm.abort);
       named_bar(kEpiBar, kEpiThreads);  // all four warps leave together on abort
       if (*sm.abort) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(a * p.ntok);
-      const int c_first = part.cta_of(static_cast<long long>(t) * p.kc);
-      const int c_last = part.cta_of(static_cast<long long>(t + 1) * p.kc - 1);
+      const uint32_t c_first = part.cta_of(t * kc);
+      const uint32_t c_last = part.cta_of((t + 1) * kc - 1);
+      const int nc = static_cast<int>(c_last - c_first + 1);
       bool finisher = true;
-      if (c_first != c_last) {
+      if (nc > 1) {
         const int slot = part.slot(me, t);
         float* dst = p.partials + (static_cast<long long>(me) * 2 + slot) * p.ntok * kTileN;
         for (int c0 = 0; c0 < p.ntok; c0 += 16) {
@@ -432,11 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) __stcg(dst + (c0 + j) * kTileN + r, v[j]);
         }
+        if (e < nc) sm.slots[e] = part.slot(c_first + e, t);  // for the finisher
         __threadfence();
         named_bar(kEpiBar, kEpiThreads);
         if (e == 0) {
           const int old = atomicAdd(&p.counters[t], 1);
-          const int last = old == c_last - c_first;
+          const int last = old == nc - 1;
           if (last) p.counters[t] = 0;
           *sm.flag = last;
         }
@@ -448,22 +475,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c0 = 0; c0 < p.ntok; c0 += 16) {
           float own[16], acc[16];
           load_acc(tacc, c0, own);
-          if (c_first == c_last) {
+          if (nc == 1) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[j] = own[j];
           } else {
+            // contributors in CTA order (deterministic), loads in flight together
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-            for (int c = c_first; c <= c_last; ++c) {
+            for (int i = 0; i < nc; ++i) {
+              const uint32_t c = c_first + i;
+              float v[16];
               if (c == me) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] += own[j];
+                for (int j = 0; j < 16; ++j) v[j] = own[j];
               } else {
                 const float* src =
-                    p.partials + (static_cast<long long>(c) * 2 + part.slot(c, t)) * p.ntok * kTileN;
+                    p.partials + (static_cast<long long>(c) * 2 + sm.slots[i]) * p.ntok * kTileN +
+                    c0 * kTileN + r;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] += ldcg(src + (c0 + j) * kTileN + r);
+                for (int j = 0; j < 16; ++j) v[j] = ldcg(src + j * kTileN);
               }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) acc[j] += v[j];
             }
           }
           epilogue_chunk(p, sm, t, r, c0, acc);
@@ -486,19 +519,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-size_t gemm_smem_bytes(int rows_b, int stages) {
-  return 1024 + stage_bytes(rows_b) * stages + kTailBytes;
+size_t gemm_smem_bytes(int rows_b, int stages, int ksub) {
+  return 1024 + stage_bytes(rows_b, ksub) * stages + kTailBytes;
 }
 
-int gemm_max_stages(int rows_b, size_t budget) {
-  int s = static_cast<int>((budget - 1024 - kTailBytes) / stage_bytes(rows_b));
+int gemm_max_stages(int rows_b, size_t budget, int ksub) {
+  int s = static_cast<int>((budget - 1024 - kTailBytes) / stage_bytes(rows_b, ksub));
   if (s > kMaxStages) s = kMaxStages;
   return s;
 }
 
 cudaError_t launch_gemm(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmXlo,
                         const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
-  const size_t smem = gemm_smem_bytes(p.ntok << p.split, p.stages);
+  const size_t smem = gemm_smem_bytes(p.ntok << p.split, p.stages, p.ksub);
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -22,7 +22,8 @@ struct GemmParams {
   int tok0;        // first token row handled by this launch
   int ntok;        // token tile (multiple of 16, <= 256)
   int split;       // 1: B operand = [X_hi rows ; X_lo rows], both accumulated into D
-  int kc;          // K / 64
+  int ksub;        // 64-wide K sub-tiles per stage (1 or 2)
+  int kc;          // K / (64 * ksub): K-chunks per tile
   int n_tiles;     // ceil(N / 128)
   long long units; // n_tiles * kc
   int stages;      // smem ring depth
@@ -63,8 +64,8 @@ struct GemmParams {
 
 // Shared memory a launch needs for `stages` ring stages.
 // `rows_b` = token rows of the B operand per stage (ntok << split).
-size_t gemm_smem_bytes(int rows_b, int stages);
-int gemm_max_stages(int rows_b, size_t smem_budget);
+size_t gemm_smem_bytes(int rows_b, int stages, int ksub);
+int gemm_max_stages(int rows_b, size_t smem_budget, int ksub);
 cudaError_t launch_gemm(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmXlo,
                         const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 
@@ -82,10 +83,15 @@ struct AttnParams {
   int32_t* counters;      // [B*Hkv], zero on entry, left zero
   int32_t* status;
   int B, n, H, Hkv, hd, cap, splits, R;
+  int cluster;            // > 0: decode path, clusters of this many CTAs (R <= 32)
   float scale_log2;       // log2(e) / sqrt(hd)
 };
-constexpr int kAttnChunk = 128;  // keys per CTA
+constexpr int kAttnChunk = 128;      // keys per CTA
+constexpr int kAttnMaxChunks = 256;  // capacity <= 32768 slots
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl);
+// Cluster size of the decode attention path for this cache capacity (0: the
+// cache slice per CTA would not fit in smem_limit, or no cluster can be placed).
+int attention_cluster_size(int hd, int cap, size_t smem_limit);
 
 // ------------------------------------------------------------ small kernels
 struct EmbedParams {
