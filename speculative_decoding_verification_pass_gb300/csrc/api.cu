@@ -256,7 +256,7 @@ struct Ctx {
 int run_gemm(const Ctx& cx, const CUtensorMap* tmW, const void* x, const void* x_lo, int M, int N,
              int K, GemmParams base) {
   spec_model* mm = const_cast<spec_model*>(cx.m);
-  const int split = x_lo ? 1 : 0;
+  const int split_req = x_lo ? 1 : 0;
   for (int tok0 = 0; tok0 < M; tok0 += kMaxTok) {
     const int rows = std::min(kMaxTok, M - tok0);
     GemmParams p = base;
@@ -265,6 +265,7 @@ int run_gemm(const Ctx& cx, const CUtensorMap* tmW, const void* x, const void* x
     p.M = M;
     p.tok0 = tok0;
     p.ntok = round_up(rows, 16);
+    const int split = split_req ? (p.ntok <= 128 ? 1 : 2) : 0;
     p.split = split;
     p.ksub = (K % 128 == 0) ? gemm_ksub() : 1;
     p.kc = K / (64 * p.ksub);
@@ -273,17 +274,17 @@ int run_gemm(const Ctx& cx, const CUtensorMap* tmW, const void* x, const void* x
     // wide token tiles (prefill) need a bigger ring budget: one CTA per SM then
     size_t budget = gemm_smem_budget();
     int cps = gemm_ctas_per_sm();
-    p.stages = gemm_max_stages(p.ntok << split, budget, p.ksub);
+    p.stages = gemm_max_stages(p.ntok << (split ? 1 : 0), budget, p.ksub);
     if (p.stages < 2) {
       p.ksub = 1;
       p.kc = K / 64;
       p.units = static_cast<long long>(p.n_tiles) * p.kc;
-      p.stages = gemm_max_stages(p.ntok << split, budget, 1);
+      p.stages = gemm_max_stages(p.ntok << (split ? 1 : 0), budget, 1);
     }
     if (p.stages < 2) {
       budget = 220 * 1024;
       cps = 1;
-      p.stages = gemm_max_stages(p.ntok << split, budget, 1);
+      p.stages = gemm_max_stages(p.ntok << (split ? 1 : 0), budget, 1);
     }
     if (p.stages < 2) return SPEC_ESIZE;
     CUtensorMap tmX, tmXlo;

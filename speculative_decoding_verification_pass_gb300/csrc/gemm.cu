@@ -9,9 +9,11 @@
 //  * swap-AB: the weight tile (128 output features x 64 K) is the UMMA "A"
 //    operand (M = 128), the M token rows padded to ntok (16..256) are "B";
 //    the accumulator D[feature][token] lives in tensor memory.  Activations
-//    arrive as a bf16 pair (x = hi + lo); both parts go through the MMA into
-//    the same accumulator, so the GEMM sees ~16-bit-mantissa inputs while the
-//    weights are still read once (the extra MMA is free in this regime).
+//    arrive as a bf16 pair (x = hi + lo) so the GEMM sees ~16-bit-mantissa
+//    inputs while the weights are still read once: for ntok <= 128 the lo rows
+//    are stacked under the hi rows in one B operand (UMMA N = 2 ntok, summed in
+//    the epilogue; an N=32 MMA issues as fast as an N=16 one), for wider tiles
+//    a second MMA accumulates the lo rows.
 //  * warp 0 streams weight tiles and activation tiles with TMA
 //    (cp.async.bulk.tensor, 128-byte swizzle, evict-first L2 policy for the
 //    weights) through a ring of shared-memory stages guarded by mbarriers;
@@ -119,9 +121,18 @@ __device__ __forceinline__ uint32_t tmem_cols_for(int ntok) {
 
 __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
 
-// Accumulator columns [c0, c0+16) of this thread's row.
-__device__ __forceinline__ void load_acc(uint32_t tacc, int c0, float (&v)[16]) {
+// Accumulator columns [c0, c0+16) of this thread's row.  With the stacked
+// split (split == 1) the lo half of the activations sits in columns ntok..,
+// added here.
+__device__ __forceinline__ void load_acc(uint32_t tacc, int c0, int ntok, int split,
+                                         float (&v)[16]) {
   tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+  if (split == 1) {
+    float lo[16];
+    tmem_ld16(tacc + static_cast<uint32_t>(ntok + c0), lo);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] += lo[j];
+  }
 }
 
 // --------------------------------------------------------------- epilogues
@@ -261,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmXlo, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
-  const int nb = p.ntok << p.split;  // B rows per sub-tile: hi rows, then (split) lo rows
+  const int nb = p.split ? 2 * p.ntok : p.ntok;  // B rows per sub-tile: hi rows, then lo rows
+  const int ncols = p.split == 1 ? 2 * p.ntok : p.ntok;  // accumulator columns (UMMA N)
   const int ksub = p.ksub;
   const Smem sm = carve(smem_raw, nb, p.stages, ksub);
   const int warp = threadIdx.x >> 5;
@@ -270,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t me = blockIdx.x;
   const uint32_t u0 = part.start(me), u1 = part.start(me + 1);
   const uint32_t kc = static_cast<uint32_t>(p.kc);
-  const uint32_t tcols = tmem_cols_for(p.ntok);
+  const uint32_t tcols = tmem_cols_for(ncols);
   const uint32_t sbytes = static_cast<uint32_t>(stage_bytes(nb, ksub));
   const uint32_t boff = static_cast<uint32_t>(kATileBytes) * ksub;  // B sub-tiles after the A ones
   const uint32_t bsub = static_cast<uint32_t>(nb) * 128;            // bytes of one B sub-tile
@@ -371,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_dep_wait();
     if (elect_lane0() && u1 > u0) {
       // -------------------------------------------------------- MMA issuer
-      const uint32_t idesc = idesc_bf16(kTileN, p.ntok);
+      const uint32_t idesc = idesc_bf16(kTileN, ncols);
       int stage = 0;
       uint32_t phase = 0;
       int seg = 0;
@@ -384,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&sm.accempty[a], ((seg >> 1) & 1) ^ 1u, sm.abort);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t dcol = tmem_base + static_cast<uint32_t>(a * p.ntok);
+        const uint32_t dcol = tmem_base + static_cast<uint32_t>(a * ncols);
         for (uint32_t v = u; v < seg_end; ++v) {
           if (!mbar_wait(&sm.full[stage], phase, sm.abort)) {
             ok = false;
@@ -401,8 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t ad = sdesc_k128(abase + kk * 32);
               umma_bf16(dcol, ad, sdesc_k128(bbase + kk * 32), idesc,
                         (v > u || s > 0 || kk > 0) ? 1u : 0u);
-              // the bf16 residual of the activations into the same accumulator
-              if (p.split) umma_bf16(dcol, ad, sdesc_k128(lbase + kk * 32), idesc, 1u);
+              // split == 2: the bf16 residual of the activations into the same
+              // accumulator (split == 1 has it stacked in the same MMA's N)
+              if (p.split == 2) umma_bf16(dcol, ad, sdesc_k128(lbase + kk * 32), idesc, 1u);
             }
           }
           umma_commit(&sm.empty[stage]);
@@ -444,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar(kEpiBar, kEpiThreads);  // all four warps leave together on abort
       if (*sm.abort) break;
       tc_fence_after();
-      const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(a * p.ntok);
+      const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(a * ncols);
       const uint32_t c_first = part.cta_of(t * kc);
       const uint32_t c_last = part.cta_of((t + 1) * kc - 1);
       const int nc = static_cast<int>(c_last - c_first + 1);
@@ -454,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* dst = p.partials + (static_cast<long long>(me) * 2 + slot) * p.ntok * kTileN;
         for (int c0 = 0; c0 < p.ntok; c0 += 16) {
           float v[16];
-          load_acc(tacc, c0, v);
+          load_acc(tacc, c0, p.ntok, p.split, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) __stcg(dst + (c0 + j) * kTileN + r, v[j]);
         }
@@ -474,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (finisher) {
         for (int c0 = 0; c0 < p.ntok; c0 += 16) {
           float own[16], acc[16];
-          load_acc(tacc, c0, own);
+          load_acc(tacc, c0, p.ntok, p.split, own);
           if (nc == 1) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[j] = own[j];
@@ -531,7 +544,7 @@ int gemm_max_stages(int rows_b, size_t budget, int ksub) {
 
 cudaError_t launch_gemm(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmXlo,
                         const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
-  const size_t smem = gemm_smem_bytes(p.ntok << p.split, p.stages, p.ksub);
+  const size_t smem = gemm_smem_bytes(p.split ? 2 * p.ntok : p.ntok, p.stages, p.ksub);
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

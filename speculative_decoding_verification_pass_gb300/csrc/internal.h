@@ -21,7 +21,8 @@ struct GemmParams {
   int M;           // valid token rows in total (rows >= M are padding)
   int tok0;        // first token row handled by this launch
   int ntok;        // token tile (multiple of 16, <= 256)
-  int split;       // 1: B operand = [X_hi rows ; X_lo rows], both accumulated into D
+  int split;       // 0: bf16 X only; 1: [X_hi ; X_lo] stacked in N (2*ntok <= 256);
+                   // 2: X_lo accumulated by a second MMA
   int ksub;        // 64-wide K sub-tiles per stage (1 or 2)
   int kc;          // K / (64 * ksub): K-chunks per tile
   int n_tiles;     // ceil(N / 128)
