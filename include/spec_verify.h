@@ -173,6 +173,28 @@ int spec_verify_forward(const spec_model* model, const int32_t* d_tokens, int ba
 int spec_lm_head(const spec_model* model, const uint16_t* d_hidden, int rows, float* d_logits,
                  void* d_ws, size_t ws_bytes, void* stream);
 
+/* LM head for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call; it exists for hosts that own every device
+ * allocation and hand a plug-in only its input and output buffers, or that
+ * run the call where no allocator may be used.  It computes exactly what
+ * spec_lm_head computes (same kernel), but its scratch memory -- the stream-K
+ * partial sums and tile counters spec_lm_head keeps in the caller's workspace
+ * -- is a fixed 8.4 MiB device array inside the library, held by every GPU
+ * that loads the library until the process exits.
+ *   d_hidden  bf16 [rows][d_model], 16-byte aligned; rows <= 16 (else
+ *             SPEC_ESIZE); a model vocabulary above 262144 gives SPEC_ESIZE.
+ *   d_logits  fp32 [rows][vocab].
+ * It allocates and frees nothing.  The first call on a device looks up the
+ * array's device address on that device (the current device at the call);
+ * make that first call before any stream capture.  All calls share the one
+ * array and leave their contents in it: calls whose work overlaps on the GPU
+ * (two streams, two host threads) race and produce wrong logits -- serialise
+ * them.  The tile counters are cleared on `stream` at the start of every
+ * call.  A device-side bounded-wait timeout is recorded in the library's own
+ * scratch, not in a caller workspace, and is not reported. */
+int spec_lm_head_noalloc(const spec_model* model, const uint16_t* d_hidden, int rows,
+                         float* d_logits, void* stream);
+
 /* ----------------------------------------------------------------- accept */
 /* Workspace bytes for spec_accept / spec_draft_sample (status word and
  * per-row statistics). */

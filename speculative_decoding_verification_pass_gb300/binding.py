@@ -60,6 +60,7 @@ _SIGS = {
     "spec_workspace_bytes": (_SZ, [ctypes.POINTER(spec_model_config), _I, _I, _I]),
     "spec_verify_forward": (_I, [_P, _P, _I, _I, ctypes.POINTER(spec_kv_cache), _P, _P, _SZ, _P]),
     "spec_lm_head": (_I, [_P, _P, _I, _P, _P, _SZ, _P]),
+    "spec_lm_head_noalloc": (_I, [_P, _P, _I, _P, _P]),
     "spec_accept_workspace_bytes": (_SZ, [_I, _I, _I]),
     "spec_accept": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _F, _P, _P, _P, _SZ, _P]),
     "spec_draft_sample": (_I, [_P, _I, _I, _F, _F, _P, _P, _P, _P, _SZ, _P]),
@@ -187,6 +188,12 @@ def spec_verify_forward(handle: int, tokens, batch: int, gamma: int, kv: "KVCach
 def spec_lm_head(handle: int, hidden, rows: int, logits, ws, stream=None):
     _check(lib().spec_lm_head(handle, _ptr(hidden), rows, _ptr(logits), _ptr(ws), ws.numel(),
                               _stream(stream)), "spec_lm_head")
+
+
+def spec_lm_head_noalloc(handle: int, hidden, rows: int, logits, stream=None):
+    """LM head with the library's own scratch (no workspace argument)."""
+    _check(lib().spec_lm_head_noalloc(handle, _ptr(hidden), rows, _ptr(logits), _stream(stream)),
+           "spec_lm_head_noalloc")
 
 
 def spec_accept_workspace_bytes(batch: int, gamma: int, vocab: int) -> int:

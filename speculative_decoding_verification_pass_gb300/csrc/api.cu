@@ -688,6 +688,26 @@ int spec_lm_head(const spec_model* m, const uint16_t* d_hidden, int rows, float*
   return run_gemm(cx, &m->tm_head, d_hidden, nullptr, rows, c.vocab, c.d_model, p);
 }
 
+// LM head on caller-supplied stream-K scratch (used by the entry point that
+// keeps its scratch in a static device array instead of a workspace).
+int spec_internal_lm_head(const spec_model* m, const uint16_t* d_hidden, int rows, float* d_logits,
+                          float* partials, int32_t* counters, int32_t* status, int max_vocab,
+                          int max_grid, void* stream) {
+  if (!m || !d_hidden || !d_logits || !partials || !counters || !status) return SPEC_EINVAL;
+  if (rows <= 0) return rows == 0 ? SPEC_OK : SPEC_EINVAL;
+  if (m->cfg.vocab > max_vocab || kMaxGrid > max_grid || rows > 16) return SPEC_ESIZE;
+  if (reinterpret_cast<uintptr_t>(d_hidden) % 16) return SPEC_EINVAL;
+  GemmParams p{};
+  p.epi = EPI_STORE;
+  p.out = d_logits;
+  p.ldo = m->cfg.vocab;
+  p.partials = partials;
+  p.counters = counters;
+  p.status = status;
+  const Ctx cx{m, static_cast<cudaStream_t>(stream), false};
+  return run_gemm(cx, &m->tm_head, d_hidden, nullptr, rows, m->cfg.vocab, m->cfg.d_model, p);
+}
+
 size_t spec_accept_workspace_bytes(int batch, int gamma, int vocab) {
   if (batch < 0 || gamma < 0 || vocab <= 0) return 0;
   return kAlign;

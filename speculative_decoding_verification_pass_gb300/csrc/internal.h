@@ -145,6 +145,16 @@ struct SampleParams {
 };
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t stream);
 
+// LM head with explicit stream-K scratch sized for rows <= 16: partials >=
+// max_grid x 2 x 16 x 128 floats, counters >= ceil(vocab/128) ints (zero on
+// entry).  SPEC_ESIZE when the model's vocabulary exceeds max_vocab or the
+// launcher's grid cap exceeds max_grid.
+}  // namespace spec
+extern "C" int spec_internal_lm_head(const spec_model* m, const uint16_t* d_hidden, int rows,
+                                     float* d_logits, float* partials, int32_t* counters,
+                                     int32_t* status, int max_vocab, int max_grid, void* stream);
+namespace spec {
+
 cudaError_t launch_truncate(int32_t* len, const int32_t* n_acc, int B, int gamma, int32_t* status,
                             cudaStream_t stream, bool pdl);
 
