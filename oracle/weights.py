@@ -27,6 +27,7 @@ Matrices are [out][in], row-major.
 """
 from __future__ import annotations
 
+import atexit
 import concurrent.futures as cf
 import multiprocessing as mp
 import os
@@ -85,6 +86,7 @@ def _pool():
         n = int(os.environ.get("ORACLE_WORKERS", min(16, os.cpu_count() or 1)))
         if n > 1:
             _POOL = cf.ProcessPoolExecutor(n, mp_context=mp.get_context("spawn"))
+            atexit.register(_POOL.shutdown, wait=True)
         else:
             _POOL = False
     return _POOL
