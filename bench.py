@@ -35,6 +35,20 @@ from speculative_decoding_verification_pass_gb300 import workloads as wl  # noqa
 
 METRIC = "verify-pass HBM GB/s (% of peak) and emitted tokens/s, 8B-shape γ=4, batch 1"
 
+# DRAM bytes (read + write) per GEMM launch over one 8B verify step, from the
+# ncu capture summarised in profiles/gemm_tc_kernel_8b_dims.md (one 8B-dims
+# layer's four GEMMs x 32 + the LM head, / 129 launches).  Reported only while
+# the kernel source is the one that capture measured.
+GEMM_TRAFFIC = {"source_sha1": "8e216fc32ca40f7636d65c01def4ef52f68a3a17", "bytes_per_launch": 118288036}
+
+
+def gemm_traffic():
+    import hashlib
+    src = os.path.join(ROOT, "speculative_decoding_verification_pass_gb300", "csrc", "gemm.cu")
+    with open(src, "rb") as f:
+        ok = hashlib.sha1(f.read()).hexdigest() == GEMM_TRAFFIC["source_sha1"]
+    return GEMM_TRAFFIC["bytes_per_launch"] if ok else None
+
 
 def peaks():
     try:
@@ -435,7 +449,8 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": w.launches_per_step() * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": (achieved / hbm) if achieved else None, "traffic": None,
+                     "frac": (achieved / hbm) if achieved else None, "traffic": gemm_traffic(),
+                     "algorithmic_bytes_per_launch": gb / gn if gn else None,
                      "kernel": "gemm_tc_kernel", "peak_source": src,
                      "launch_ms": gm / gn if gn else None,
                      "attention_ms_per_launch": am / an if an else None},
