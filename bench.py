@@ -35,19 +35,24 @@ from speculative_decoding_verification_pass_gb300 import workloads as wl  # noqa
 
 METRIC = "verify-pass HBM GB/s (% of peak) and emitted tokens/s, 8B-shape γ=4, batch 1"
 
-# DRAM bytes (read + write) per GEMM launch over one 8B verify step, from the
-# ncu capture summarised in profiles/gemm_tc_kernel_8b_dims.md (one 8B-dims
-# layer's four GEMMs x 32 + the LM head, / 129 launches).  Reported only while
-# the kernel source is the one that capture measured.
-GEMM_TRAFFIC = {"source_sha1": "8e216fc32ca40f7636d65c01def4ef52f68a3a17", "bytes_per_launch": 118288036}
+# DRAM bytes (read + write) per launch of the dominant kernel, from ncu
+# captures summarised under profiles/, keyed by the sha1 of the kernel's
+# source file: reported only while the source is the one that was measured.
+TRAFFIC = {
+    # one 8B-dims layer's four GEMMs x 32 + the LM head, / 129 launches
+    "gemm_tc_kernel": {"file": "gemm.cu", "source_sha1": "8e216fc32ca40f7636d65c01def4ef52f68a3a17",
+                       "bytes_per_launch": 118288036},
+    "forward_kernel": {"file": "forward.cu", "source_sha1": None, "bytes_per_launch": None},
+}
 
 
-def gemm_traffic():
+def kernel_traffic(kernel: str):
     import hashlib
-    src = os.path.join(ROOT, "speculative_decoding_verification_pass_gb300", "csrc", "gemm.cu")
+    t = TRAFFIC[kernel]
+    src = os.path.join(ROOT, "speculative_decoding_verification_pass_gb300", "csrc", t["file"])
     with open(src, "rb") as f:
-        ok = hashlib.sha1(f.read()).hexdigest() == GEMM_TRAFFIC["source_sha1"]
-    return GEMM_TRAFFIC["bytes_per_launch"] if ok else None
+        ok = hashlib.sha1(f.read()).hexdigest() == t["source_sha1"]
+    return t["bytes_per_launch"] if ok else None
 
 
 def peaks():
@@ -204,8 +209,16 @@ class Workload:
         per_layer = (qkv * d + d * c.n_heads * hd + 2 * c.d_ffn * d + d * c.d_ffn) * 2
         return float(c.n_layers * per_layer + c.vocab * d * 2)
 
-    def launches_per_step(self) -> int:
-        return 1 + 5 * self.cfg.n_layers + 1 + 2
+    def forward_bytes(self) -> float:
+        """Algorithmic HBM bytes of one verify forward: every weight once, the
+        new tokens' embedding rows, the attended keys/values (context + the
+        gamma+1 new slots, every layer), the appended slots and the logits."""
+        c = self.cfg
+        hd, d = c.head_dim, c.d_model
+        M = self.B * self.n
+        kv_tok = c.n_layers * c.n_kv_heads * hd * 2 * 2
+        kv = self.B * ((self.ctx + self.n) * kv_tok + self.n * kv_tok)
+        return float(self.gemm_bytes() + M * d * 2 + kv + M * c.vocab * 4)
 
 
 def time_steps(w: Workload, K: int):
@@ -428,12 +441,21 @@ def main():
     value = step_bytes * args.steps * world / t_total / 1e9
     e2e_times, h2d, d2h = time_e2e(w, max(3, args.steps // 2))
     e2e_val = step_bytes * len(e2e_times) * world / (sum(e2e_times) / 1e3) / 1e9
-    gm = gn = gb = am = an = 0.0
-    for ms, n, by in instrumented(w, 3):
-        gm += ms[0]; gn += n[0]; gb += by[0]; am += ms[1]; an += n[1]
+    gm = gn = gb = am = an = pm = pn = 0.0
+    k_inst = 3
+    for ms, n, by in instrumented(w, k_inst):
+        gm += ms[0]; gn += n[0]; gb += by[0]; am += ms[1]; an += n[1]; pm += ms[2]; pn += n[2]
     acc_ms = accept_time(w, 10)
     hbm, _, src = peaks()
-    achieved = gb / (gm / 1e3) / 1e9 if gm else None
+    # launches of this library's kernels per step: the forward's (one
+    # persistent kernel, or embedding + per-step GEMM / attention kernels),
+    # then accept and the rollback
+    launches = int(round((gn + an + pn) / k_inst)) + (1 if gn else 0) + 2
+    if pn:
+        kernel, k_ms, k_n, k_bytes = "forward_kernel", pm, pn, w.forward_bytes() * pn
+    else:
+        kernel, k_ms, k_n, k_bytes = "gemm_tc_kernel", gm, gn, gb
+    achieved = k_bytes / (k_ms / 1e3) / 1e9 if k_ms else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_total / args.steps * 1e3,
@@ -447,13 +469,13 @@ def main():
         "accept_us": acc_ms * 1e3, "accept_frac_of_step": acc_ms / (t_total / args.steps * 1e3),
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": w.launches_per_step() * args.steps,
+        "gpu_launches": launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": (achieved / hbm) if achieved else None, "traffic": gemm_traffic(),
-                     "algorithmic_bytes_per_launch": gb / gn if gn else None,
-                     "kernel": "gemm_tc_kernel", "peak_source": src,
-                     "launch_ms": gm / gn if gn else None,
-                     "attention_ms_per_launch": am / an if an else None},
+                     "frac": (achieved / hbm) if achieved else None,
+                     "traffic": kernel_traffic(kernel),
+                     "algorithmic_bytes_per_launch": k_bytes / k_n if k_n else None,
+                     "kernel": kernel, "peak_source": src,
+                     "launch_ms": k_ms / k_n if k_n else None},
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -162,7 +162,15 @@ size_t spec_workspace_bytes(const spec_model_config* cfg, int batch, int gamma, 
  * with gamma = prompt_len - 1 in chunks.  A token id outside [0, V) is read as
  * 0 and sets SPEC_DEV_BAD_TOKEN; a sequence whose len[b]+gamma+1 exceeds the
  * capacity sets SPEC_DEV_KV_OVERFLOW, its slots beyond the capacity are not
- * written and its logits are unspecified. */
+ * written and its logits are unspecified.
+ * Schedule: a decode-shaped pass (batch*(gamma+1) <= 128, (gamma+1) x query
+ * heads per KV head <= 32, <= 48 layers, d_model/128 a power of two) runs as
+ * ONE persistent cooperative kernel (one CTA per SM, grid-wide barriers
+ * between the pass's steps, weights streaming ahead across them); every
+ * other pass (prefill chunks) runs as one kernel per step.  Setting the
+ * environment variable SPEC_FORWARD_PERSISTENT=0 forces the per-step
+ * schedule (read on every call).  Both give the same results up to fp32
+ * summation order. */
 int spec_verify_forward(const spec_model* model, const int32_t* d_tokens, int batch, int gamma,
                         const spec_kv_cache* kv, float* d_logits, void* d_ws, size_t ws_bytes,
                         void* stream);
@@ -253,12 +261,14 @@ int spec_device_status(void* d_ws, void* stream, int32_t* out);
 
 /* ------------------------------------------------------------ diagnostics */
 /* Per-kernel-kind timing for benchmarks.  When enabled on a model, every
- * subsequent forward records CUDA events around each launch of the GEMM and
- * attention kernels (this serialises the launches it brackets).  spec_timing_read
- * synchronises and returns, per kind (0 = GEMM, 1 = attention), the summed
- * milliseconds, launch count and algorithmic bytes since the last read. */
+ * subsequent forward records CUDA events around each launch of the GEMM,
+ * attention and persistent forward kernels (this serialises the launches it
+ * brackets).  spec_timing_read synchronises and returns, per kind (0 = GEMM,
+ * 1 = attention, 2 = persistent forward), the summed milliseconds, launch
+ * count and weight bytes streamed (kinds 0 and 2; 0 for kind 1) since the
+ * last read. */
 int spec_timing_enable(spec_model* model, int enable);
-int spec_timing_read(spec_model* model, double ms[2], int64_t launches[2], double bytes[2]);
+int spec_timing_read(spec_model* model, double ms[3], int64_t launches[3], double bytes[3]);
 
 #ifdef __cplusplus
 }

@@ -235,9 +235,9 @@ def spec_timing_enable(handle: int, enable: bool):
 
 
 def spec_timing_read(handle: int):
-    ms = (ctypes.c_double * 2)()
-    n = (ctypes.c_int64 * 2)()
-    by = (ctypes.c_double * 2)()
+    ms = (ctypes.c_double * 3)()
+    n = (ctypes.c_int64 * 3)()
+    by = (ctypes.c_double * 3)()
     _check(lib().spec_timing_read(handle, ms, n, by), "spec_timing_read")
     return list(ms), list(n), list(by)
 

@@ -68,6 +68,24 @@ int gemm_ctas_per_sm() {
   return v;
 }
 
+// Shared-memory budget of the persistent decode forward's CTA (one per SM):
+// SPEC_MK_SMEM_KB, default 220.
+int mk_smem_kb() {
+  static int v = [] {
+    const char* e = getenv("SPEC_MK_SMEM_KB");
+    int x = e ? atoi(e) : 220;
+    return x < 64 ? 64 : (x > 224 ? 224 : x);
+  }();
+  return v;
+}
+// Decode-shaped passes run as one persistent kernel unless the environment
+// sets SPEC_FORWARD_PERSISTENT=0 (read per call: the per-kernel schedule
+// stays selectable for comparison).
+bool mk_enabled() {
+  const char* e = getenv("SPEC_FORWARD_PERSISTENT");
+  return !(e && e[0] == '0');
+}
+
 size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -148,10 +166,10 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
 }
 
 struct WsPlan {
-  size_t status, pos_base, seq_ok, counters, ssq, h, hb, hb_lo, q, q_lo, o, o_lo, act, act_lo,
-      gpart, apart_o, apart_ml;
+  size_t status, pos_base, seq_ok, mk_bar, counters, ssq, h, hb, hb_lo, q, q_lo, o, o_lo, act,
+      act_lo, gpart, apart_o, apart_ml, mk_att_o, mk_att_ml;
   size_t total;
-  int n_counters, attn_counter0, ssq_ld, splits, R, M, n;
+  int n_counters, attn_counter0, ssq_ld, splits, R, M, n, att_pairs;
 };
 
 int max_tiles(const spec_model_config& c) {
@@ -191,6 +209,7 @@ WsPlan plan_ws(const spec_model_config& c, int B, int gamma, int cap) {
   p.status = take(4);
   p.pos_base = take(static_cast<size_t>(B) * 4);
   p.seq_ok = take(static_cast<size_t>(B) * 4);
+  p.mk_bar = take(256);  // directly before the counters: one memset clears both
   p.counters = take(static_cast<size_t>(p.n_counters) * 4);
   p.ssq = take(d / 128 * mpad * 4);
   p.h = take(static_cast<size_t>(M) * d * 4);
@@ -206,6 +225,10 @@ WsPlan plan_ws(const spec_model_config& c, int B, int gamma, int cap) {
   const size_t rows = c.n_layers ? static_cast<size_t>(B) * Hkv * p.splits * p.R : 0;
   p.apart_o = take(rows * hd * 4);
   p.apart_ml = take(rows * 2 * 4);
+  p.att_pairs = (std::max(cap, 1) + 63) / 64;
+  const size_t urows = c.n_layers ? static_cast<size_t>(B) * Hkv * p.att_pairs * 32 : 0;
+  p.mk_att_o = take(urows * hd * 4);
+  p.mk_att_ml = take(urows * 2 * 4);
   p.total = o;
   return p;
 }
@@ -525,6 +548,115 @@ int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch,
   const Ctx cx{m, st, m->timing};
   const bool pdl = !m->timing;
 
+  // ---- decode shapes: the whole pass as one persistent cooperative kernel
+  {
+    const int ntok = round_up(M, 16);
+    const int fpt = d / 128;
+    const bool shape_ok = mk_enabled() && M <= 128 && P.R <= 32 && c.n_layers <= kMkMaxLayers &&
+                          (fpt & (fpt - 1)) == 0 && fpt <= 128;
+    // one CTA per SM with a deep ring (the ring also absorbs grid barriers)
+    int stages = shape_ok ? forward_max_stages(ntok, hd, static_cast<size_t>(mk_smem_kb()) * 1024) : 0;
+    const int cps = stages >= 2 ? forward_ctas_per_sm(ntok, stages, hd) : 0;
+    const long long stride = c.n_layers > 1 ? static_cast<long long>(L.g_attn[1] - L.g_attn[0]) : 0;
+    bool uniform = true;
+    for (int l = 1; l < c.n_layers; ++l)
+      uniform = uniform && static_cast<long long>(L.g_attn[l] - L.g_attn[0]) == stride * l &&
+                static_cast<long long>(L.g_mlp[l] - L.g_mlp[0]) == stride * l;
+    if (shape_ok && cps >= 1 && uniform) {
+      MkParams* mp = new MkParams();
+      MkParams& Q = *mp;
+      const void* xs[6] = {hb, hb_lo, o, o_lo, act, act_lo};
+      const int xk[6] = {d, d, qd, qd, c.d_ffn, c.d_ffn};
+      bool ok = true;
+      for (int i = 0; i < 6 && ok; ++i)
+        ok = make_tmap(&Q.xmap[i], xs[i], static_cast<uint64_t>(M), static_cast<uint64_t>(xk[i]),
+                       static_cast<uint32_t>(ntok));
+      if (!ok) {
+        delete mp;
+        return SPEC_ECUDA;
+      }
+      for (int l = 0; l < c.n_layers; ++l) {
+        Q.wmap[4 * l + 0] = m->tm_qkv[l];
+        Q.wmap[4 * l + 1] = m->tm_o[l];
+        Q.wmap[4 * l + 2] = m->tm_gu[l];
+        Q.wmap[4 * l + 3] = m->tm_d[l];
+      }
+      Q.wmap[4 * c.n_layers] = m->tm_head;
+      Q.L = c.n_layers;
+      Q.d = d;
+      Q.H = H;
+      Q.Hkv = Hkv;
+      Q.hd = hd;
+      Q.ffn = c.d_ffn;
+      Q.V = c.vocab;
+      Q.qkv_rows = m->qkv_rows;
+      Q.B = batch;
+      Q.n = n;
+      Q.M = M;
+      Q.ntok = ntok;
+      Q.cap = kv->capacity;
+      Q.stages = stages;
+      Q.ssq_ld = P.ssq_ld;
+      const int grid = std::min(m->sm_count * cps, kMaxGrid);
+      // key chunks per (sequence, KV head): about one attention unit per CTA
+      Q.att_nch = std::max(1, std::min(P.att_pairs, grid / std::max(1, batch * Hkv)));
+      Q.eps = c.rms_eps;
+      Q.inv_d = 1.0f / d;
+      Q.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));
+      Q.embed = reinterpret_cast<const uint16_t*>(B + L.embed);
+      Q.rope = reinterpret_cast<const float2*>(B + L.rope);
+      Q.gfinal = reinterpret_cast<const float*>(B + L.gfinal);
+      Q.g_attn0 = reinterpret_cast<const float*>(B + L.g_attn[0]);
+      Q.g_mlp0 = reinterpret_cast<const float*>(B + L.g_mlp[0]);
+      Q.layer_stride = stride;
+      Q.kc = static_cast<uint16_t*>(kv->k);
+      Q.vc = static_cast<uint16_t*>(kv->v);
+      Q.layer_kv = static_cast<long long>(batch) * Hkv * kv->capacity * hd;
+      Q.len = kv->len;
+      Q.tokens = d_tokens;
+      Q.logits = d_logits;
+      Q.h = h;
+      Q.hb = hb;
+      Q.hb_lo = hb_lo;
+      Q.q = q;
+      Q.q_lo = q_lo;
+      Q.o = o;
+      Q.o_lo = o_lo;
+      Q.act = act;
+      Q.act_lo = act_lo;
+      Q.ssq = ssq;
+      Q.partials = reinterpret_cast<float*>(W + P.gpart);
+      Q.counters = counters;
+      Q.bar = reinterpret_cast<unsigned*>(W + P.mk_bar);
+      Q.status = status;
+      Q.pos_base = pos_base;
+      Q.seq_ok = seq_ok;
+      Q.att_o = reinterpret_cast<float*>(W + P.mk_att_o);
+      Q.att_ml = reinterpret_cast<float*>(W + P.mk_att_ml);
+      cudaError_t e = cudaMemsetAsync(W + P.mk_bar, 0, P.counters + P.n_counters * 4 - P.mk_bar, st);
+      TimedLaunch t{};
+      if (e == cudaSuccess && cx.timing) {
+        t.a = take_event(const_cast<spec_model*>(m));
+        t.b = take_event(const_cast<spec_model*>(m));
+        t.kind = 2;
+        double wbytes = static_cast<double>(c.vocab) * d * 2;
+        for (int l = 0; l < c.n_layers; ++l)
+          wbytes += (static_cast<double>(m->qkv_rows) * d + static_cast<double>(d) * qd +
+                     2.0 * c.d_ffn * d + static_cast<double>(d) * c.d_ffn) * 2;
+        t.bytes = wbytes;
+        cudaEventRecord(t.a, st);
+      }
+      if (e == cudaSuccess) e = launch_forward(Q, grid, hd, st);
+      if (e == cudaSuccess && cx.timing) {
+        cudaEventRecord(t.b, st);
+        const_cast<spec_model*>(m)->pending.push_back(t);
+      }
+      delete mp;
+      if (e != cudaSuccess) return cuda_fail(e);
+      return SPEC_OK;
+    }
+  }
+
   EmbedParams ep{};
   ep.tokens = d_tokens;
   ep.embed = reinterpret_cast<const uint16_t*>(B + L.embed);
@@ -798,9 +930,9 @@ int spec_timing_enable(spec_model* m, int enable) {
   return SPEC_OK;
 }
 
-int spec_timing_read(spec_model* m, double ms[2], int64_t launches[2], double bytes[2]) {
+int spec_timing_read(spec_model* m, double ms[3], int64_t launches[3], double bytes[3]) {
   if (!m || !ms || !launches || !bytes) return SPEC_EINVAL;
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < 3; ++k) {
     ms[k] = 0;
     launches[k] = 0;
     bytes[k] = 0;

@@ -1,0 +1,914 @@
+// Persistent decode forward: the whole verification pass of a decode-shaped
+// batch (M = B*(gamma+1) <= 128 token rows, <= 32 query rows per KV head) in
+// one cooperative kernel.
+//
+// Why: the pass is a stream of 15 GB of weights through HBM ([lattice] /
+// [pigeon] *The idea*: one weight read scores every drafted position), cut
+// into ~160 dependent steps (4 projections + attention per layer).  As
+// separate kernels every boundary drains the weight stream (tail of one
+// kernel, launch and pipeline fill of the next).  Here every CTA stays
+// resident; the steps become phases separated by grid-wide barriers, and the
+// weight producer never waits on a barrier: the next phase's weight tiles keep
+// streaming into the shared-memory ring while the dependency resolves, only
+// the activation loads (which need the previous phase's output) wait.
+//
+// Phases: EMBED, then per layer QKV -> ATT -> CMB -> O -> GU -> DOWN, then
+// HEAD.  Warp roles (224 threads):
+//   warp 0 lane 0  weight producer (TMA, runs ahead across phases)
+//   warp 1         TMEM owner; lane 0 issues tcgen05.mma
+//   warps 2-5      GEMM epilogues (TMEM -> fused epilogue), embedding,
+//                  attention partials (ATT) and their merge (CMB); they arrive
+//                  on the grid barrier for every phase
+//   warp 6 lane 0  activation producer (TMA after each phase's barrier)
+// Grid barrier: one monotonic counter; phase k is complete when it holds
+// (k+1) * gridDim.x arrivals.  All waits are bounded (~2 s); a CTA that times
+// out sets the status bit, drains its own copies, frees TMEM and returns.
+#include "attn_common.cuh"
+#include "common.cuh"
+#include "gemm_common.cuh"
+#include "internal.h"
+
+namespace spec {
+namespace {
+
+constexpr int kMkThreads = 224;
+static_assert(sizeof(MkParams) <= 32764, "kernel parameter space");
+constexpr int kAttBlockKeys = 32;   // keys per attention warp block
+constexpr int kAttUnitKeys = 64;    // keys per attention work unit (2 blocks)
+constexpr int kArriveBar = 2;       // named barrier of the epilogue warps for arrivals
+
+enum PhaseKind { PH_EMBED, PH_QKV, PH_ATT, PH_CMB, PH_O, PH_GU, PH_D, PH_HEAD };
+
+SPEC_DEVINL int ph_kind(int ph, int L) {
+  if (ph == 0) return PH_EMBED;
+  if (ph == 1 + 6 * L) return PH_HEAD;
+  return PH_QKV + (ph - 1) % 6;
+}
+SPEC_DEVINL bool is_gemm(int k) {
+  return k == PH_QKV || k == PH_O || k == PH_GU || k == PH_D || k == PH_HEAD;
+}
+
+struct GPh {
+  int wmap, xmap, N, K, epi, l;
+};
+
+SPEC_DEVINL GPh gph(const MkParams& P, int ph) {
+  const int k = ph_kind(ph, P.L);
+  const int l = k == PH_HEAD ? P.L : (ph - 1) / 6;
+  GPh g;
+  g.l = l;
+  switch (k) {
+    case PH_QKV: g = {4 * l + 0, 0, P.qkv_rows, P.d, EPI_QKV, l}; break;
+    case PH_O: g = {4 * l + 1, 2, P.d, P.H * P.hd, EPI_RESID, l}; break;
+    case PH_GU: g = {4 * l + 2, 0, 2 * P.ffn, P.d, EPI_SWIGLU, l}; break;
+    case PH_D: g = {4 * l + 3, 4, P.d, P.ffn, EPI_RESID, l}; break;
+    default: g = {4 * P.L, 0, P.V, P.d, EPI_STORE, l}; break;
+  }
+  return g;
+}
+
+// Work split of one GEMM phase.  The phase uses only the first G CTAs of the
+// grid: at most one per work unit, so every CTA of the split owns units (the
+// fixup counts contributors by CTA index), and at most 63 contributors per
+// tile (the fixup's slot table).  CTAs past the split idle in that phase.
+struct PhaseSplit {
+  Partition part;
+  uint32_t u0, u1;
+};
+
+SPEC_DEVINL PhaseSplit phase_split(const GPh& g, uint32_t me, uint32_t GR) {
+  const uint32_t kc = static_cast<uint32_t>(g.K) / 64;
+  const uint32_t tiles = static_cast<uint32_t>(g.N + 127) / 128;
+  const uint32_t U = tiles * kc;
+  const uint32_t G = min(min(GR, U), 63u * tiles);
+  PhaseSplit s{Partition{U, G, kc}, 0u, 0u};
+  if (me < G) {
+    s.u0 = s.part.start(me);
+    s.u1 = s.part.start(me + 1);
+  }
+  return s;
+}
+
+// Position in the sequence of weight tiles one CTA streams: GEMM phase, work
+// unit, and the unit's (tile, K chunk).
+struct WCursor {
+  int ph = -1;
+  uint32_t u = 0, u1 = 0, kc = 1, tile = 0, kci = 0;
+  int wmap = 0;
+  SPEC_DEVINL void step() {
+    ++u;
+    if (++kci == kc) {
+      kci = 0;
+      ++tile;
+    }
+  }
+};
+
+// Move `c` onto a unit it still has to stream; false past the last phase.
+SPEC_DEVINL bool wcur_seek(const MkParams& P, WCursor& c, int nph, uint32_t me, uint32_t GR) {
+  while (c.u >= c.u1) {
+    if (++c.ph >= nph) return false;
+    if (!is_gemm(ph_kind(c.ph, P.L))) continue;
+    const GPh g = gph(P, c.ph);
+    const PhaseSplit ps = phase_split(g, me, GR);
+    c.kc = static_cast<uint32_t>(g.K) / 64;
+    c.u = ps.u0;
+    c.u1 = ps.u1;
+    c.tile = c.u / c.kc;
+    c.kci = c.u - c.tile * c.kc;
+    c.wmap = g.wmap;
+  }
+  return true;
+}
+
+template <typename T>
+SPEC_DEVINL const T* layer_ptr(const T* base0, long long stride, int l) {
+  return reinterpret_cast<const T*>(reinterpret_cast<const char*>(base0) + stride * l);
+}
+
+// Epilogue parameters of one GEMM phase.
+SPEC_DEVINL GemmParams phase_params(const MkParams& P, const GPh& g) {
+  GemmParams p{};
+  p.N = g.N;
+  p.K = g.K;
+  p.M = P.M;
+  p.tok0 = 0;
+  p.ntok = P.ntok;
+  p.split = 1;
+  p.ksub = 1;
+  p.kc = g.K / 64;
+  p.n_tiles = (g.N + 127) / 128;
+  p.units = static_cast<long long>(p.n_tiles) * p.kc;
+  p.epi = g.epi;
+  p.ssq_tiles = P.d / 128;
+  p.ssq_ld = P.ssq_ld;
+  p.inv_d = P.inv_d;
+  p.eps = P.eps;
+  p.d = P.d;
+  p.partials = P.partials;
+  p.counters = P.counters;
+  p.status = P.status;
+  if (g.epi == EPI_QKV) {
+    p.ssq_in = P.ssq;
+    p.q = P.q;
+    p.q_lo = P.q_lo;
+    p.kcache = P.kc + P.layer_kv * g.l;
+    p.vcache = P.vc + P.layer_kv * g.l;
+    p.pos_base = P.pos_base;
+    p.seq_ok = P.seq_ok;
+    p.rope = P.rope;
+    p.n_per_seq = P.n;
+    p.H = P.H;
+    p.Hkv = P.Hkv;
+    p.hd = P.hd;
+    p.cap = P.cap;
+  } else if (g.epi == EPI_RESID) {
+    p.h = P.h;
+    p.hb = P.hb;
+    p.hb_lo = P.hb_lo;
+    p.ssq_out = P.ssq;
+    const bool o_proj = g.wmap % 4 == 1;
+    p.g_next = o_proj ? layer_ptr(P.g_mlp0, P.layer_stride, g.l)
+                      : (g.l + 1 < P.L ? layer_ptr(P.g_attn0, P.layer_stride, g.l + 1) : P.gfinal);
+  } else if (g.epi == EPI_SWIGLU) {
+    p.ssq_in = P.ssq;
+    p.act = P.act;
+    p.act_lo = P.act_lo;
+    p.ffn = P.ffn;
+  } else {
+    p.ssq_in = P.ssq;
+    p.out = P.logits;
+    p.ldo = P.V;
+  }
+  return p;
+}
+
+SPEC_DEVINL uint32_t ld_acquire(const unsigned* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+SPEC_DEVINL void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Wait (one thread) until `target` arrivals; bounded.
+SPEC_DEVINL bool grid_wait(const unsigned* bar, unsigned target, volatile int* abort,
+                           int32_t* status) {
+  if (ld_acquire(bar) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    if (ld_acquire(bar) >= target) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      set_status(status, SPEC_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(32);
+  }
+}
+
+struct MkSmem {
+  uint8_t* ring;
+  uint8_t* att;  // attention staging; also the epilogue exchange buffer
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* accfull;
+  uint64_t* accempty;
+  uint32_t* tmem_slot;
+  int* abort;
+  int* flag;
+  unsigned* aseq;   // weight stages issued (read by the activation producer)
+  float* rs;
+  float* red;
+  int* slots;
+  float* sq;        // [128] embedding partial sums
+};
+
+__host__ __device__ inline size_t mk_att_bytes(int hd) { return static_cast<size_t>(384) * hd; }
+constexpr size_t kMkBarBytes = 512;
+constexpr size_t kMkTail = kMkBarBytes + 256 * 4 + 64 * 4 + 64 * 4 + 128 * 4 + 64;
+
+SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
+  uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023);
+  MkSmem s;
+  s.ring = reinterpret_cast<uint8_t*>(base);
+  s.att = s.ring + ring_bytes;
+  uint8_t* t = s.att + mk_att_bytes(hd);
+  s.full = reinterpret_cast<uint64_t*>(t);
+  s.empty = s.full + kMaxStages;
+  s.accfull = s.empty + kMaxStages;
+  s.accempty = s.accfull + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.accempty + 2);
+  s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
+  s.flag = s.abort + 1;
+  s.aseq = reinterpret_cast<unsigned*>(s.flag + 1);
+  s.rs = reinterpret_cast<float*>(t + kMkBarBytes);
+  s.red = s.rs + 256;
+  s.slots = reinterpret_cast<int*>(s.red + 64);
+  s.sq = reinterpret_cast<float*>(s.slots + 64);
+  return s;
+}
+
+// Every epilogue thread publishes its writes; one thread arrives.
+SPEC_DEVINL void phase_arrive(const MkParams& P) {
+  __threadfence();
+  fence_proxy_async();
+  named_bar(kArriveBar, kEpiThreads);
+  if (threadIdx.x == kEpiFirstThread) atomicAdd(P.bar, 1u);
+}
+
+// All epilogue threads wait for phase `ph - 1` to be complete.
+SPEC_DEVINL bool epi_wait(const MkParams& P, const MkSmem& sm, int ph) {
+  if (threadIdx.x == kEpiFirstThread)
+    grid_wait(P.bar, static_cast<unsigned>(ph) * gridDim.x, sm.abort, P.status);
+  named_bar(kArriveBar, kEpiThreads);
+  __threadfence();
+  return *sm.abort == 0;
+}
+
+// ------------------------------------------------------------------ embed
+SPEC_DEVINL void embed_phase(const MkParams& P, const MkSmem& sm) {
+  const int e = threadIdx.x - kEpiFirstThread;
+  if (blockIdx.x == 0) {
+    for (int b = e; b < P.B; b += kEpiThreads) {
+      const int L = P.len[b];
+      const bool ok = L >= 0 && L + P.n <= P.cap;
+      P.pos_base[b] = L < 0 ? 0 : L;
+      P.seq_ok[b] = ok ? 1 : 0;
+      if (ok)
+        P.len[b] = L + P.n;
+      else
+        set_status(P.status, SPEC_DEV_KV_OVERFLOW);
+    }
+  }
+  const int fpt = P.d / 128;  // features per thread (a tile of 128 = 128/fpt threads)
+  for (int m = blockIdx.x; m < P.M; m += gridDim.x) {
+    int tok = P.tokens[m];
+    if (tok < 0 || tok >= P.V) {
+      if (e == 0) set_status(P.status, SPEC_DEV_BAD_TOKEN);
+      tok = 0;
+    }
+    const uint16_t* row = P.embed + static_cast<long long>(tok) * P.d;
+    float sq = 0.f;
+    for (int i = 0; i < fpt; ++i) {
+      const int f = e * fpt + i;
+      const float x = bf16_to_f32(row[f]);
+      const long long idx = static_cast<long long>(m) * P.d + f;
+      P.h[idx] = x;
+      const float y = x * P.g_attn0[f];
+      const uint16_t hi = f32_to_bf16(y);
+      P.hb[idx] = hi;
+      P.hb_lo[idx] = f32_to_bf16(y - bf16_to_f32(hi));
+      sq += x * x;
+    }
+    sm.sq[e] = sq;
+    named_bar(kArriveBar, kEpiThreads);
+    if (e < fpt) {  // fpt tiles of 128 features, 128/fpt threads each, in order
+      const int tpt = kEpiThreads / fpt;
+      float s = 0.f;
+      for (int k = 0; k < tpt; ++k) s += sm.sq[e * tpt + k];
+      P.ssq[static_cast<long long>(e) * P.ssq_ld + m] = s;
+    }
+    named_bar(kArriveBar, kEpiThreads);
+  }
+}
+
+// ------------------------------------------------------------- attention
+// The keys of (sequence b, KV head) are cut into P.att_nch chunks of a
+// multiple of 64 keys; a unit is one chunk, so a decode batch needs at most
+// one unit per CTA.  A unit walks its chunk in blocks of 64 keys: warp
+// (slot s, query tile qt) takes keys [32 s, 32 s + 32) of every block for the
+// 16 query rows of tile qt and keeps its own online softmax state; the two
+// slots merge in shared memory into the unit's partial (max, sum, O).
+SPEC_DEVINL int att_chunk_keys(int Tk, int nch) {
+  const int per = (Tk + nch - 1) / nch;
+  return ((per + kAttUnitKeys - 1) / kAttUnitKeys) * kAttUnitKeys;
+}
+
+template <int HD>
+SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
+  const int e = threadIdx.x - kEpiFirstThread;
+  const int w = e >> 5, lane = e & 31;
+  const int slot = w >> 1, qt = w & 1;
+  const int G = P.H / P.Hkv;
+  const int R = P.n * G;
+  const int qdim = P.H * HD;
+  constexpr int kRowB = HD * 2;
+  uint8_t* sQ = sm.att;
+  uint8_t* sQlo = sQ + 32 * kRowB;
+  uint8_t* sK = sQlo + 32 * kRowB;  // [slot][K 32 rows | V 32 rows]
+  const uint32_t aQ = smem_u32(sQ), aQlo = smem_u32(sQlo);
+  const uint32_t aK = smem_u32(sK + slot * 64 * kRowB), aV = aK + 32 * kRowB;
+  float* merge = reinterpret_cast<float*>(sm.att);  // [2 tiles][16][HD], reuses the Q area
+  const uint16_t* kc = P.kc + P.layer_kv * l;
+  const uint16_t* vc = P.vc + P.layer_kv * l;
+  const int nch = P.att_nch;
+  const int units = P.B * P.Hkv * nch;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  constexpr int kCPR = HD / 8;
+  const bool active = qt * 16 < R;
+  for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const int b = unit / (P.Hkv * nch);
+    const int kvh = (unit / nch) % P.Hkv;
+    const int ch = unit % nch;
+    const int Lb = __ldcg(P.pos_base + b);
+    const int Tk = min(Lb + P.n, P.cap);
+    const int ck = att_chunk_keys(Tk, nch);
+    const int kbeg = ch * ck, kend = min(kbeg + ck, Tk);
+    if (kbeg >= kend) continue;  // uniform across the CTA
+    const long long head_base = (static_cast<long long>(b) * P.Hkv + kvh) * P.cap;
+    auto load_block = [&](int kb) {
+      for (int idx = e; idx < kAttUnitKeys * kCPR; idx += kEpiThreads) {
+        const int i = idx / kCPR, c = idx % kCPR;  // key kb + i
+        const int s = i >> 5, ii = i & 31;
+        const bool valid = kb + i < kend;
+        const long long g = (head_base + (valid ? kb + i : kb)) * HD + c * 8;
+        const uint32_t dk = smem_u32(sK + s * 64 * kRowB) + swz<HD>(ii, c);
+        cp_async16(dk, kc + g, valid ? 16 : 0);
+        cp_async16(dk + 32 * kRowB, vc + g, valid ? 16 : 0);
+      }
+    };
+    load_block(kbeg);  // in flight while q is staged
+    // ---- stage q (hi, lo) rows
+    for (int idx = e; idx < 32 * kCPR; idx += kEpiThreads) {
+      const int r = idx / kCPR, c = idx % kCPR;
+      uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
+      if (r < R) {
+        const int j = r / G, g = r % G;
+        const long long off = (static_cast<long long>(b) * P.n + j) * qdim + (kvh * G + g) * HD + c * 8;
+        hi = __ldcg(reinterpret_cast<const uint4*>(P.q + off));
+        lo = __ldcg(reinterpret_cast<const uint4*>(P.q_lo + off));
+      }
+      *reinterpret_cast<uint4*>(sQ + swz<HD>(r, c)) = hi;
+      *reinterpret_cast<uint4*>(sQlo + swz<HD>(r, c)) = lo;
+    }
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+    float oacc[HD / 8][4];
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+    for (int kb = kbeg; kb < kend; kb += kAttUnitKeys) {
+      if (kb > kbeg) {
+        named_bar(kArriveBar, kEpiThreads);  // previous block consumed
+        load_block(kb);
+      }
+      cp_async_wait_all();
+      named_bar(kArriveBar, kEpiThreads);
+      const int k0 = kb + slot * kAttBlockKeys;
+      if (!active || k0 >= kend) continue;
+      float sacc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        uint32_t a0, a1, a2, a3, q0, q1, q2, q3;
+        const int qrow = qt * 16 + (lane & 15);
+        ldsm_x4(aQ + swz<HD>(qrow, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+        ldsm_x4(aQlo + swz<HD>(qrow, kk * 2 + (lane >> 4)), q0, q1, q2, q3);
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(aK + swz<HD>(key, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
+          mma_bf16(sacc[np * 2], a0, a1, a2, a3, b0, b1);
+          mma_bf16(sacc[np * 2 + 1], a0, a1, a2, a3, b2, b3);
+          mma_bf16(sacc[np * 2], q0, q1, q2, q3, b0, b1);
+          mma_bf16(sacc[np * 2 + 1], q0, q1, q2, q3, b2, b3);
+        }
+      }
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int r = qt * 16 + g8 + hr * 8;
+        const int qpos = r < R ? Lb + r / G : -1;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const int kabs = k0 + nt * 8 + t4 * 2 + x;
+            const bool ok = kabs < kend && kabs <= qpos;
+            const float v = ok ? sacc[nt][hr * 2 + x] * P.scale_log2 : -INFINITY;
+            sacc[nt][hr * 2 + x] = v;
+            mx = fmaxf(mx, v);
+          }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(mrow[hr], mx);
+        const float alpha = mrow[hr] == -INFINITY ? 0.f : exp2f(mrow[hr] - mn);
+        float sum = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const float pe = mn == -INFINITY ? 0.f : exp2f(sacc[nt][hr * 2 + x] - mn);
+            sacc[nt][hr * 2 + x] = pe;
+            sum += pe;
+          }
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        mrow[hr] = mn;
+        lrow[hr] = lrow[hr] * alpha + sum;
+#pragma unroll
+        for (int nd = 0; nd < HD / 8; ++nd) {
+          oacc[nd][hr * 2] *= alpha;
+          oacc[nd][hr * 2 + 1] *= alpha;
+        }
+      }
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const uint32_t a0 = pack_bf16x2(sacc[2 * k2][0], sacc[2 * k2][1]);
+        const uint32_t a1 = pack_bf16x2(sacc[2 * k2][2], sacc[2 * k2][3]);
+        const uint32_t a2 = pack_bf16x2(sacc[2 * k2 + 1][0], sacc[2 * k2 + 1][1]);
+        const uint32_t a3 = pack_bf16x2(sacc[2 * k2 + 1][2], sacc[2 * k2 + 1][3]);
+        const uint32_t p0 = pack_bf16x2(sacc[2 * k2][0] - bf16lo(a0), sacc[2 * k2][1] - bf16hi(a0));
+        const uint32_t p1 = pack_bf16x2(sacc[2 * k2][2] - bf16lo(a1), sacc[2 * k2][3] - bf16hi(a1));
+        const uint32_t p2 =
+            pack_bf16x2(sacc[2 * k2 + 1][0] - bf16lo(a2), sacc[2 * k2 + 1][1] - bf16hi(a2));
+        const uint32_t p3 =
+            pack_bf16x2(sacc[2 * k2 + 1][2] - bf16lo(a3), sacc[2 * k2 + 1][3] - bf16hi(a3));
+        const int key = k2 * 16 + (lane & 15);
+#pragma unroll
+        for (int dn = 0; dn < HD / 16; ++dn) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(aV + swz<HD>(key, dn * 2 + (lane >> 4)), b0, b1, b2, b3);
+          mma_bf16(oacc[2 * dn], a0, a1, a2, a3, b0, b1);
+          mma_bf16(oacc[2 * dn + 1], a0, a1, a2, a3, b2, b3);
+          mma_bf16(oacc[2 * dn], p0, p1, p2, p3, b0, b1);
+          mma_bf16(oacc[2 * dn + 1], p0, p1, p2, p3, b2, b3);
+        }
+      }
+    }
+    // ---- merge the two slots: slot 1 through shared memory
+    named_bar(kArriveBar, kEpiThreads);  // the Q area becomes the merge buffer
+    float* mb = merge + qt * 16 * HD;
+    float* mm = sm.red + qt * 32;  // [16] max, [16] sum
+    if (slot == 1 && active) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int rr = g8 + hr * 8;
+#pragma unroll
+        for (int nd = 0; nd < HD / 8; ++nd) {
+          mb[rr * HD + nd * 8 + t4 * 2] = oacc[nd][hr * 2];
+          mb[rr * HD + nd * 8 + t4 * 2 + 1] = oacc[nd][hr * 2 + 1];
+        }
+        if (t4 == 0) {
+          mm[rr] = mrow[hr];
+          mm[16 + rr] = lrow[hr];
+        }
+      }
+    }
+    named_bar(kArriveBar, kEpiThreads);
+    if (slot == 0 && active) {
+      const long long ubase = (static_cast<long long>(b) * P.Hkv + kvh) * nch + ch;
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int rr = g8 + hr * 8;
+        const int r = qt * 16 + rr;
+        const float m1 = mm[rr], l1 = mm[16 + rr];
+        const float mn = fmaxf(mrow[hr], m1);
+        const float s0 = mrow[hr] == -INFINITY ? 0.f : exp2f(mrow[hr] - mn);
+        const float s1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mn);
+        if (r < R) {
+          float* dst = P.att_o + (ubase * 32 + r) * HD;
+#pragma unroll
+          for (int nd = 0; nd < HD / 8; ++nd) {
+            const int c = nd * 8 + t4 * 2;
+            float2 v;
+            v.x = oacc[nd][hr * 2] * s0 + mb[rr * HD + c] * s1;
+            v.y = oacc[nd][hr * 2 + 1] * s0 + mb[rr * HD + c + 1] * s1;
+            __stcg(reinterpret_cast<float2*>(dst + c), v);
+          }
+          if (t4 == 0) {
+            float2 ml;
+            ml.x = mn;
+            ml.y = lrow[hr] * s0 + l1 * s1;
+            __stcg(reinterpret_cast<float2*>(P.att_ml + (ubase * 32 + r) * 2), ml);
+          }
+        }
+      }
+    }
+    named_bar(kArriveBar, kEpiThreads);  // shared memory free for the next unit
+  }
+}
+
+// Merge the chunk partials of each query row by log-sum-exp; one warp per
+// (sequence, KV head, row), each lane owning HD/32 consecutive dimensions.
+template <int HD>
+SPEC_DEVINL void cmb_phase(const MkParams& P) {
+  const int e = threadIdx.x - kEpiFirstThread;
+  const int w = e >> 5, lane = e & 31;
+  const int G = P.H / P.Hkv;
+  const int R = P.n * G;
+  const int qdim = P.H * HD;
+  const int nch = P.att_nch;
+  constexpr int kV = HD / 32;
+  const int items = P.B * P.Hkv * R;
+  const float2* mlp = reinterpret_cast<const float2*>(P.att_ml);
+  for (int it = blockIdx.x * 4 + w; it < items; it += gridDim.x * 4) {
+    const int r = it % R;
+    const int kvh = (it / R) % P.Hkv;
+    const int b = it / (R * P.Hkv);
+    const int Tk = min(__ldcg(P.pos_base + b) + P.n, P.cap);
+    const int nu = (Tk + att_chunk_keys(Tk, nch) - 1) / att_chunk_keys(Tk, nch);
+    const long long ubase = (static_cast<long long>(b) * P.Hkv + kvh) * nch;
+    const float2 mv0 = lane < nu ? __ldcg(&mlp[(ubase + lane) * 32 + r]) : make_float2(-INFINITY, 0.f);
+    float m = mv0.x;
+    for (int u = 32 + lane; u < nu; u += 32) m = fmaxf(m, __ldcg(&mlp[(ubase + u) * 32 + r]).x);
+    m = warp_max(m);
+    float acc[kV];
+#pragma unroll
+    for (int k = 0; k < kV; ++k) acc[k] = 0.f;
+    float l = 0.f;
+    for (int u0 = 0; u0 < nu; u0 += 32) {
+      const float2 mv = u0 == 0 ? mv0
+                                : (u0 + lane < nu ? __ldcg(&mlp[(ubase + u0 + lane) * 32 + r])
+                                                  : make_float2(-INFINITY, 0.f));
+      const float wgt = mv.x == -INFINITY ? 0.f : exp2f(mv.x - m);
+      l += wgt * mv.y;
+      const int cnt = min(32, nu - u0);
+      const float* src = P.att_o + ((ubase + u0) * 32 + r) * HD + lane * kV;
+#pragma unroll 8
+      for (int k = 0; k < cnt; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, wgt, k);
+        const float* s = src + static_cast<long long>(k) * 32 * HD;
+        if constexpr (kV == 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(s));
+          acc[0] += wk * v.x;
+          acc[1] += wk * v.y;
+          acc[2] += wk * v.z;
+          acc[3] += wk * v.w;
+        } else {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(s));
+          acc[0] += wk * v.x;
+          acc[1] += wk * v.y;
+        }
+      }
+    }
+    const float inv = 1.f / warp_sum(l);
+    const int j = r / G, g = r % G;
+    const long long off = (static_cast<long long>(b) * P.n + j) * qdim + (kvh * G + g) * HD + lane * kV;
+#pragma unroll
+    for (int k = 0; k < kV; ++k) {
+      const float o = acc[k] * inv;
+      const uint16_t hi = f32_to_bf16(o);
+      P.o[off + k] = hi;
+      P.o_lo[off + k] = f32_to_bf16(o - bf16_to_f32(hi));
+    }
+  }
+}
+
+// -------------------------------------------------------------- the kernel
+template <int HD>
+__global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_constant__ MkParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  const int nb = 2 * P.ntok;  // B rows per stage: hi rows then lo rows
+  const int ncols = 2 * P.ntok;
+  const uint32_t sbytes = static_cast<uint32_t>(stage_bytes(nb, 1));
+  const int S = P.stages;
+  const MkSmem sm = mk_carve(smem_raw, static_cast<size_t>(sbytes) * S, HD);
+  const int warp = threadIdx.x >> 5;
+  const uint32_t me = blockIdx.x, GR = gridDim.x;
+  const int nph = 2 + 6 * P.L;
+  const uint32_t tcols = tmem_cols_for(ncols);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sm.accfull[a], 1);
+      mbar_init(&sm.accempty[a], 4);
+    }
+    *sm.abort = 0;
+    *sm.aseq = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sm.tmem_slot, tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_slot;
+
+  if (warp == 0) {
+    if (elect_lane0()) {
+      // ------------------------------------------------- weight producer
+      // Streams every GEMM phase's weight tiles of this CTA into the ring,
+      // running ahead across phases (only the ring's free stages limit it).
+      const uint64_t pol_w = l2_policy_evict_first();
+      uint32_t issued[kMaxStages];
+      for (int s = 0; s < S; ++s) issued[s] = 0;
+      uint32_t n = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      WCursor cur;
+      while (wcur_seek(P, cur, nph, me, GR)) {
+        if (n >= static_cast<uint32_t>(S) && !mbar_wait(&sm.empty[stage], phase ^ 1u, sm.abort)) break;
+        uint8_t* st = sm.ring + static_cast<size_t>(stage) * sbytes;
+        mbar_arrive_expect_tx(&sm.full[stage], sbytes);
+        tma_load_2d(st, &P.wmap[cur.wmap], &sm.full[stage], static_cast<int>(cur.kci * kTileK),
+                    static_cast<int>(cur.tile * kTileN), pol_w);
+        ++issued[stage];
+        ++n;
+        atomicExch(sm.aseq, n);
+        cur.step();
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (*sm.abort) {
+        volatile int never = 0;
+        for (int s = 0; s < S; ++s)
+          if (issued[s]) mbar_wait(&sm.full[s], (issued[s] - 1) & 1u, &never);
+      }
+    }
+  } else if (warp == 6) {
+    if (elect_lane0()) {
+      // --------------------------------------------- activation producer
+      const uint64_t pol_x = l2_policy_evict_last();
+      uint32_t n = 0;
+      int stage = 0;
+      bool ok = true;
+      for (int ph = 0; ph < nph && ok; ++ph) {
+        if (!is_gemm(ph_kind(ph, P.L))) continue;
+        const GPh g = gph(P, ph);
+        const uint32_t kc = g.K / 64;
+        const PhaseSplit ps = phase_split(g, me, GR);
+        const uint32_t u0 = ps.u0, u1 = ps.u1;
+        if (u1 == u0) continue;
+        if (!grid_wait(P.bar, static_cast<unsigned>(ph) * GR, sm.abort, P.status)) break;
+        fence_proxy_async();  // the previous phase's generic-proxy writes, then TMA reads
+        uint32_t kci = u0 % kc;
+        for (uint32_t u = u0; u < u1; ++u) {
+          // the weight producer has claimed this stage (expect_tx registered)
+          const unsigned long long t0 = globaltimer();
+          while (*reinterpret_cast<volatile unsigned*>(sm.aseq) <= n) {
+            if (*sm.abort || globaltimer() - t0 > kWaitLimitNs) {
+              *sm.abort = 1;
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          uint8_t* b = sm.ring + static_cast<size_t>(stage) * sbytes + kATileBytes;
+          const int x = static_cast<int>(kci * kTileK);
+          tma_load_2d(b, &P.xmap[g.xmap], &sm.full[stage], x, 0, pol_x);
+          tma_load_2d(b + P.ntok * 128, &P.xmap[g.xmap + 1], &sm.full[stage], x, 0, pol_x);
+          ++n;
+          if (++kci == kc) kci = 0;
+          if (++stage == S) stage = 0;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (elect_lane0()) {
+      // ----------------------------------------------------- MMA issuer
+      const uint32_t idesc = idesc_bf16(kTileN, ncols);
+      int stage = 0;
+      uint32_t phase = 0;
+      int seg = 0;
+      bool ok = true;
+      for (int ph = 0; ph < nph && ok; ++ph) {
+        if (!is_gemm(ph_kind(ph, P.L))) continue;
+        const GPh g = gph(P, ph);
+        const uint32_t kc = g.K / 64;
+        const PhaseSplit ps = phase_split(g, me, GR);
+        const uint32_t u0 = ps.u0, u1 = ps.u1;
+        uint32_t u = u0;
+        while (u < u1 && ok) {
+          const uint32_t t = u / kc;
+          const uint32_t seg_end = min(u1, (t + 1) * kc);
+          const int a = seg & 1;
+          if (!mbar_wait(&sm.accempty[a], ((seg >> 1) & 1) ^ 1u, sm.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dcol = tmem_base + static_cast<uint32_t>(a * ncols);
+          for (uint32_t v = u; v < seg_end; ++v) {
+            if (!mbar_wait(&sm.full[stage], phase, sm.abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t abase = smem_u32(sm.ring + static_cast<size_t>(stage) * sbytes);
+            const uint32_t bbase = abase + kATileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kTileK / 16; ++kk)
+              umma_bf16(dcol, sdesc_k128(abase + kk * 32), sdesc_k128(bbase + kk * 32), idesc,
+                        (v > u || kk > 0) ? 1u : 0u);
+            umma_commit(&sm.empty[stage]);
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&sm.accfull[a]);
+          u = seg_end;
+          ++seg;
+        }
+      }
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ------------------------------------ epilogue / embedding / attention
+    const int e = threadIdx.x - kEpiFirstThread;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + (threadIdx.x & 31);
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    Smem gs;  // the GEMM epilogue's view of shared memory
+    gs.rs = sm.rs;
+    gs.xbuf = reinterpret_cast<float*>(sm.att);
+    gs.red = sm.red;
+    gs.slots = sm.slots;
+    gs.flag = sm.flag;
+    int seg = 0;
+    for (int ph = 0; ph < nph; ++ph) {
+      const int kind = ph_kind(ph, P.L);
+      if (kind == PH_EMBED) {
+        embed_phase(P, sm);
+      } else if (kind == PH_ATT) {
+        if (!epi_wait(P, sm, ph)) break;
+        att_phase<HD>(P, sm, (ph - 1) / 6);
+      } else if (kind == PH_CMB) {
+        if (!epi_wait(P, sm, ph)) break;
+        cmb_phase<HD>(P);
+      } else {
+        if (!epi_wait(P, sm, ph)) break;
+        const GPh g = gph(P, ph);
+        const GemmParams p = phase_params(P, g);
+        const uint32_t kc = g.K / 64;
+        const PhaseSplit ps = phase_split(g, me, GR);
+        const Partition& part = ps.part;
+        const uint32_t u0 = ps.u0, u1 = ps.u1;
+        if (p.ssq_in) {
+          for (int c = e; c < p.ntok; c += kEpiThreads) {
+            float s = 0.f;
+            if (c < p.M)
+              for (int t = 0; t < p.ssq_tiles; ++t) s += __ldcg(p.ssq_in + static_cast<long long>(t) * p.ssq_ld + c);
+            sm.rs[c] = rsqrtf(s * p.inv_d + p.eps);
+          }
+        }
+        named_bar(kEpiBar, kEpiThreads);
+        uint32_t u = u0;
+        while (u < u1) {
+          const uint32_t t = u / kc;
+          const uint32_t seg_end = min(u1, (t + 1) * kc);
+          const int a = seg & 1;
+          mbar_wait(&sm.accfull[a], (seg >> 1) & 1, sm.abort);
+          named_bar(kEpiBar, kEpiThreads);
+          if (*sm.abort) break;
+          tc_fence_after();
+          const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(a * ncols);
+          const uint32_t c_first = part.cta_of(t * kc);
+          const uint32_t c_last = part.cta_of((t + 1) * kc - 1);
+          const int nc = static_cast<int>(c_last - c_first + 1);
+          bool finisher = true;
+          if (nc > 1) {
+            const int slot = part.slot(me, t);
+            float* dst = p.partials + (static_cast<long long>(me) * 2 + slot) * p.ntok * kTileN;
+            for (int c0 = 0; c0 < p.ntok; c0 += 16) {
+              float v[16];
+              load_acc(tacc, c0, p.ntok, 1, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) __stcg(dst + (c0 + j) * kTileN + r, v[j]);
+            }
+            if (e < nc) sm.slots[e] = part.slot(c_first + e, t);
+            __threadfence();
+            named_bar(kEpiBar, kEpiThreads);
+            if (e == 0) {
+              const int old = atomicAdd(&p.counters[t], 1);
+              const int last = old == nc - 1;
+              if (last) p.counters[t] = 0;
+              *sm.flag = last;
+            }
+            named_bar(kEpiBar, kEpiThreads);
+            finisher = *sm.flag != 0;
+            __threadfence();
+          }
+          if (finisher) {
+            for (int c0 = 0; c0 < p.ntok; c0 += 16) {
+              float own[16], acc[16];
+              load_acc(tacc, c0, p.ntok, 1, own);
+              if (nc == 1) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] = own[j];
+              } else {
+                fixup_sum<4>(p.partials, p.ntok, c0, r, c_first, nc, me, sm.slots, own, acc);
+              }
+              epilogue_chunk(p, gs, t, r, c0, acc);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.accempty[a]);
+          u = seg_end;
+          ++seg;
+        }
+        if (*sm.abort) break;
+      }
+      phase_arrive(P);
+    }
+  }
+
+  if (*sm.abort && threadIdx.x == 0) set_status(P.status, SPEC_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tcols);
+  }
+}
+
+}  // namespace
+
+size_t forward_smem_bytes(int ntok, int stages, int hd) {
+  return 1024 + stage_bytes(2 * ntok, 1) * stages + mk_att_bytes(hd) + kMkTail;
+}
+
+int forward_max_stages(int ntok, int hd, size_t budget) {
+  const size_t fixed = 1024 + mk_att_bytes(hd) + kMkTail;
+  if (budget <= fixed) return 0;
+  int s = static_cast<int>((budget - fixed) / stage_bytes(2 * ntok, 1));
+  return s > kMaxStages ? kMaxStages : s;
+}
+
+// CTAs per SM the persistent forward can keep resident (0: not launchable).
+int forward_ctas_per_sm(int ntok, int stages, int hd) {
+  const size_t smem = forward_smem_bytes(ntok, stages, hd);
+  const void* fn = hd == 128 ? reinterpret_cast<const void*>(forward_kernel<128>)
+                             : reinterpret_cast<const void*>(forward_kernel<64>);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kMkThreads, smem) != cudaSuccess) return 0;
+  // every resident CTA holds its accumulators in TMEM (512 columns per SM)
+  uint32_t need = 2u * 2u * static_cast<uint32_t>(ntok), cols = 32;
+  while (cols < need) cols <<= 1;
+  const int by_tmem = static_cast<int>(512 / cols);
+  return n < by_tmem ? n : by_tmem;
+}
+
+cudaError_t launch_forward(const MkParams& P, int grid, int hd, cudaStream_t stream) {
+  const size_t smem = forward_smem_bytes(P.ntok, P.stages, hd);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (hd == 128) return cudaLaunchKernelEx(&cfg, forward_kernel<128>, P);
+  return cudaLaunchKernelEx(&cfg, forward_kernel<64>, P);
+}
+
+}  // namespace spec

@@ -94,6 +94,44 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl)
 // cache slice per CTA would not fit in smem_limit, or no cluster can be placed).
 int attention_cluster_size(int hd, int cap, size_t smem_limit);
 
+// --------------------------------------------------- persistent decode forward
+constexpr int kMkMaxLayers = 48;
+struct MkParams {
+  CUtensorMap xmap[6];                    // hb, hb_lo, o, o_lo, act, act_lo (box rows = ntok)
+  CUtensorMap wmap[4 * kMkMaxLayers + 1]; // per layer W_qkv, W_o, W_gu, W_d; then the LM head
+  int L, d, H, Hkv, hd, ffn, V, qkv_rows;
+  int B, n, M, ntok, cap, stages, ssq_ld;
+  int att_nch;                            // key chunks per (sequence, KV head)
+  float eps, inv_d, scale_log2;
+  const uint16_t* embed;
+  const float2* rope;
+  const float* gfinal;
+  const float* g_attn0;                   // layer 0's gains; layer l is + l * layer_stride bytes
+  const float* g_mlp0;
+  long long layer_stride;
+  uint16_t* kc;                           // KV cache base; layer l is + l * layer_kv elements
+  uint16_t* vc;
+  long long layer_kv;
+  int32_t* len;
+  const int32_t* tokens;
+  float* logits;
+  float* h;
+  uint16_t *hb, *hb_lo, *q, *q_lo, *o, *o_lo, *act, *act_lo;
+  float* ssq;
+  float* partials;
+  int32_t* counters;
+  unsigned* bar;                          // grid-barrier arrivals, zero at launch
+  int32_t* status;
+  int32_t* pos_base;
+  int32_t* seq_ok;
+  float* att_o;                           // [B][Hkv][att_nch][32][hd] chunk partials
+  float* att_ml;                          // [B][Hkv][att_nch][32][2] (max, sum)
+};
+size_t forward_smem_bytes(int ntok, int stages, int hd);
+int forward_max_stages(int ntok, int hd, size_t budget);
+int forward_ctas_per_sm(int ntok, int stages, int hd);
+cudaError_t launch_forward(const MkParams& P, int grid, int hd, cudaStream_t stream);
+
 // ------------------------------------------------------------ small kernels
 struct EmbedParams {
   const int32_t* tokens;  // [B][n]

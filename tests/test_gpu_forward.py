@@ -218,3 +218,52 @@ def test_lm_head_workload_and_accept():
     if not r.boundary:
         assert int(nacc[0]) == r.n_accepted and out[0].tolist() == r.tokens
     m.close()
+
+
+def _device_pass(cfg, seed, B, cap, prompt, blk, persistent, monkeypatch):
+    """Prefill `prompt` (per-step schedule: more than 32 query rows per KV
+    head), then verify `blk` under the chosen schedule; returns the block's
+    logits, the caches and the per-kind launch counts of the block's pass."""
+    monkeypatch.setenv("SPEC_FORWARD_PERSISTENT", "1" if persistent else "0")
+    m = sb.Model(cfg, seed)
+    kv = sb.KVCache(cfg, B, cap)
+    ws = sb.workspace(sb.spec_workspace_bytes(cfg, B, 127, cap))
+
+    def run(toks):
+        Bn, n = toks.shape
+        out = torch.empty(Bn, n, cfg.vocab, device="cuda")
+        sb.spec_verify_forward(m.handle, torch.from_numpy(np.ascontiguousarray(toks)).cuda(), Bn,
+                               n - 1, kv, out, ws)
+        return out.double().cpu().numpy()
+
+    run(prompt)
+    sb.spec_timing_enable(m.handle, True)
+    sb.spec_timing_read(m.handle)
+    z = run(blk)
+    _, launches, _ = sb.spec_timing_read(m.handle)
+    sb.spec_timing_enable(m.handle, False)
+    st, bits = sb.spec_device_status(ws)
+    assert st == sb.SPEC_OK, hex(bits)
+    res = (z, kv.k.double().cpu().numpy(), kv.v.double().cpu().numpy(), kv.len.cpu().numpy(),
+           launches)
+    m.close()
+    return res
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=["hd64", "hd128", "mha"])
+def test_persistent_and_per_step_schedules_agree(cfg, monkeypatch):
+    """A decode-shaped pass runs as ONE persistent kernel (timing kind 2);
+    forcing the per-step schedule on an identical model and cache gives the
+    same logits up to fp32 summation order (the two split the GEMMs'
+    K dimension differently) and the same cache up to one bf16 rounding."""
+    B, cap, gamma = 3, 200, 4
+    prompt = wl.tokens(51, B, 97, cfg.vocab)
+    blk = wl.tokens(52, B, gamma + 1, cfg.vocab)
+    zp, kp, vp, lp, np_ = _device_pass(cfg, 61, B, cap, prompt, blk, True, monkeypatch)
+    zs, ks, vs, ls, ns_ = _device_pass(cfg, 61, B, cap, prompt, blk, False, monkeypatch)
+    assert np_[2] == 1 and np_[0] == 0 and np_[1] == 0, np_
+    assert ns_[2] == 0 and ns_[0] == 4 * cfg.n_layers + 1 and ns_[1] == cfg.n_layers, ns_
+    np.testing.assert_array_equal(lp, ls)
+    _close(zp, zs, tol=1e-3)
+    _close(kp, ks, tol=8e-3)
+    _close(vp, vs, tol=8e-3)
