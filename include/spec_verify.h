@@ -204,12 +204,20 @@ int spec_lm_head_noalloc(const spec_model* model, const uint16_t* d_hidden, int 
                          float* d_logits, void* stream);
 
 /* ----------------------------------------------------------------- accept */
-/* Workspace bytes for spec_accept / spec_draft_sample (status word and
- * per-row statistics). */
+/* Workspace bytes for spec_accept / spec_draft_sample: the device status
+ * word, a grid-barrier counter and the per-chunk partial statistics of the
+ * accept grid (about 8.3 MiB for batch 64, gamma 7, vocab 128256).  The
+ * workspace must be 16-byte aligned; one workspace serves one stream at a
+ * time. */
 size_t spec_accept_workspace_bytes(int batch, int gamma, int vocab);
 
-/* The acceptance step, one CTA per sequence ([pigeon] How it works, steps
- * 3-5; [engine] The Accept/Reject Mechanism).
+/* The acceptance step ([pigeon] How it works, steps 3-5; [engine] The
+ * Accept/Reject Mechanism); gamma + 1 <= 128 (else SPEC_ESIZE).  Batches of
+ * up to 1024 rows (batch x (gamma+1)) run as one cooperative grid over
+ * (sequence, row, vocabulary chunk) work units; larger batches run one CTA
+ * per sequence (also forced by the environment variable SPEC_ACCEPT_GRID=0,
+ * read per call).  Both give the same result up to fp32 summation order in
+ * the softmax normaliser.
  *   d_target_logits fp32 [batch][gamma+1][vocab]
  *   d_draft_probs   fp32 [batch][gamma][vocab]: the distributions the drafts
  *                   were drawn from, after the same temperature / top-p

@@ -11,7 +11,7 @@
 // pigeon guide, *When it breaks*).  T = 0 is the greedy rule: accept while
 // the draft equals the argmax.
 //
-// Structure per CTA (1024 threads):
+// Draft sampling (sample_kernel), per CTA (1024 threads):
 //  * row statistics in one pass: per-thread online (max, sum of exp2) merged
 //    by a fixed-order block reduction; rows are visited lazily, so only the
 //    rows up to the first rejection (plus the bonus row) are read;
@@ -22,6 +22,9 @@
 //    tiles of 4096 ids in id order, the smallest id whose cumulative weight
 //    exceeds u * total (exact integer arithmetic, so the selected id is
 //    consistent with its own cumulative sums and deterministic).
+#include <algorithm>
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -365,13 +368,14 @@ __device__ void weights_total(const DrawWeights& dw, int V, Red& r, unsigned lon
   last_pos = block_max_i(lp, r);
 }
 
-__global__ void __launch_bounds__(kT, 1) accept_kernel(const AcceptParams p) {
+// ------------------------------------------------------- accept per sequence
+// One CTA per sequence (batches with more than kAcceptGridRows rows): rows are
+// visited lazily up to the first rejection.
+__global__ void __launch_bounds__(kT, 1) accept_seq_kernel(const AcceptParams p) {
   __shared__ Red red;
   __shared__ int s_flag;
   const int b = blockIdx.x;
   const int gamma = p.gamma, V = p.V, n = gamma + 1;
-  grid_dep_wait();
-  grid_dep_launch();
   const float* zb = p.logits + static_cast<long long>(b) * n * V;
   const int32_t* xb = p.draft + static_cast<long long>(b) * gamma;
   int32_t* out = p.out + static_cast<long long>(b) * n;
@@ -445,6 +449,598 @@ __global__ void __launch_bounds__(kT, 1) accept_kernel(const AcceptParams p) {
   }
 }
 
+// ------------------------------------------------------------- accept grid
+// The acceptance step as one cooperative grid over (sequence, row, vocabulary
+// chunk) units, phases separated by grid-wide barriers:
+//   P1  per chunk: online (max, sum exp2) of z / T, or (greedy) the chunk's
+//       argmax; with top_p < 1 the nucleus histograms and totals are cleared.
+//   N0..N3, NZ (top_p < 1 only)  the mass-weighted radix select of the
+//       nucleus threshold over global integer histograms (one 8-bit digit per
+//       phase), then each chunk's kept mass.
+//   P2  per (sequence, chunk): every unit takes the same accept decisions
+//       (they only need the merged row statistics and one id per row) and
+//       sums the chunk's 2^-52 fixed-point draw weights (residual and p).
+//   P3  per sequence: the chunk where the cumulative weight crosses
+//       u * total, then one block scan of that chunk.
+// Row statistics are merged from the chunk partials in a fixed order by one
+// warp, so every CTA derives bit-identical values; the fixed-point sums are
+// exact integers, so the draw is the single-scan inverse CDF in id order.
+constexpr int kAT = 512;
+constexpr int kAW = kAT / 32;
+constexpr int kAPer = kAcceptMaxChunk / kAT;  // ids per thread in a chunk scan
+constexpr int kMaxRows = 128;
+
+struct ASmem {
+  float f[kAW];
+  float g[kAW];
+  int i[kAW];
+  unsigned long long u[kAW];
+  unsigned long long hist[256];
+  float rm[kMaxRows];   // row max (greedy: argmax value)
+  float rz[kMaxRows];   // row normaliser (kept mass with a nucleus)
+  float rtau[kMaxRows]; // nucleus threshold on e(x) (0: none)
+  int ri[kMaxRows];     // greedy: argmax id
+  float bf[2];
+  unsigned long long bu[3];
+  int bi[3];
+  uint32_t prefix;
+  int j, tok, abort;
+};
+
+SPEC_DEVINL bool agrid_sync(const AcceptParams& p, unsigned target, ASmem& s) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(p.bar, 1u);
+    if (ld_acquire(p.bar) < target) {
+      const unsigned long long t0 = globaltimer();
+      while (ld_acquire(p.bar) < target) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          set_status(p.status, SPEC_DEV_TIMEOUT);
+          s.abort = 1;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+  }
+  __syncthreads();
+  return s.abort == 0;
+}
+
+// Block (max, sum exp2((z - max) c)) over ids [x0, x1), fixed merge order.
+__device__ float2 chunk_ms(const float* z, int x0, int x1, float c, ASmem& s) {
+  float m = -INFINITY, sum = 0.f;
+  for (int x = x0 + threadIdx.x; x < x1; x += kAT) {
+    const float v = __ldcg(z + x);
+    if (v > m) {
+      sum = (m == -INFINITY ? 0.f : sum * exp2f((m - v) * c)) + 1.0f;
+      m = v;
+    } else {
+      sum += exp2f((v - m) * c);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    ms_merge(m, sum, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, sum, o), c);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    s.f[w] = m;
+    s.g[w] = sum;
+  }
+  __syncthreads();
+  if (w == 0) {
+    m = l < kAW ? s.f[l] : -INFINITY;
+    sum = l < kAW ? s.g[l] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      ms_merge(m, sum, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, sum, o), c);
+    if (l == 0) {
+      s.bf[0] = m;
+      s.bf[1] = sum;
+    }
+  }
+  __syncthreads();
+  const float2 r = make_float2(s.bf[0], s.bf[1]);
+  __syncthreads();
+  return r;
+}
+
+SPEC_DEVINL void arg_merge(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+// Block argmax over [x0, x1), lowest id on ties.
+__device__ float2 chunk_argmax(const float* z, int x0, int x1, ASmem& s) {
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int x = x0 + threadIdx.x; x < x1; x += kAT) arg_merge(best, bi, __ldcg(z + x), x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    arg_merge(best, bi, __shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bi, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    s.f[w] = best;
+    s.i[w] = bi;
+  }
+  __syncthreads();
+  if (w == 0) {
+    best = l < kAW ? s.f[l] : -INFINITY;
+    bi = l < kAW ? s.i[l] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      arg_merge(best, bi, __shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bi, o));
+    if (l == 0) {
+      s.bf[0] = best;
+      s.bi[0] = bi;
+    }
+  }
+  __syncthreads();
+  const float2 r = make_float2(s.bf[0], __int_as_float(s.bi[0]));
+  __syncthreads();
+  return r;
+}
+
+// Block sums (fixed order): a uint64 and a float.
+__device__ unsigned long long ablock_sum_u64(unsigned long long v, ASmem& s) {
+  v = warp_sum_u64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) s.u[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    unsigned long long t = l < kAW ? s.u[l] : 0ull;
+    t = warp_sum_u64(t);
+    if (l == 0) s.bu[0] = t;
+  }
+  __syncthreads();
+  const unsigned long long r = s.bu[0];
+  __syncthreads();
+  return r;
+}
+
+__device__ float ablock_sum_f(float v, ASmem& s) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) s.f[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    float t = l < kAW ? s.f[l] : 0.f;
+    t = warp_sum(t);
+    if (l == 0) s.bf[0] = t;
+  }
+  __syncthreads();
+  const float r = s.bf[0];
+  __syncthreads();
+  return r;
+}
+
+__device__ int ablock_max_i(int v, ASmem& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) s.i[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int t = l < kAW ? s.i[l] : INT_MIN;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+    if (l == 0) s.bi[0] = t;
+  }
+  __syncthreads();
+  const int r = s.bi[0];
+  __syncthreads();
+  return r;
+}
+
+// One warp: merged (max, sum) of a row from its S chunk partials.
+SPEC_DEVINL float2 warp_row_ms(const float2* part, int S, float c) {
+  float m = -INFINITY, sum = 0.f;
+  for (int k = threadIdx.x & 31; k < S; k += 32) {
+    const float2 v = __ldcg(part + k);
+    ms_merge(m, sum, v.x, v.y, c);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    ms_merge(m, sum, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, sum, o), c);
+  return make_float2(m, sum);
+}
+
+// One warp: fixed-order sum of S floats.
+SPEC_DEVINL float warp_sum_parts(const float* part, int S) {
+  float t = 0.f;
+  for (int k = threadIdx.x & 31; k < S; k += 32) t += __ldcg(part + k);
+  return warp_sum(t);
+}
+
+// One warp: one digit of the mass-weighted radix select.  Among the 256
+// buckets of `hist` (values sharing the digits chosen so far), scanning from
+// the top with `above` = the mass strictly above them, pick the first bucket
+// at which the cumulative mass reaches `target`; `above` becomes the mass
+// strictly above that bucket.  If rounding leaves the target unreached, the
+// lowest nonempty bucket (0 if none) with `above` = the whole mass.
+SPEC_DEVINL int warp_select(const unsigned long long* hist, double target,
+                            unsigned long long& above) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long h[8], ls = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    h[k] = __ldcg(hist + 255 - 8 * lane - k);
+    ls += h[k];
+  }
+  unsigned long long incl = ls;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  unsigned long long acc = above + incl - ls;
+  int cand = -1;
+  unsigned long long cacc = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (cand < 0) {
+      if (h[k] && static_cast<double>(acc + h[k]) >= target) {
+        cand = 255 - 8 * lane - k;
+        cacc = acc;
+      } else {
+        acc += h[k];
+      }
+    }
+  }
+  const unsigned ball = __ballot_sync(0xffffffffu, cand >= 0);
+  const unsigned long long total = above + __shfl_sync(0xffffffffu, incl, 31);
+  if (ball) {
+    const int src = __ffs(ball) - 1;
+    above = __shfl_sync(0xffffffffu, cacc, src);
+    return __shfl_sync(0xffffffffu, cand, src);
+  }
+  int low = -1;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (h[k]) low = 255 - 8 * lane - k;
+  const unsigned nb = __ballot_sync(0xffffffffu, low >= 0);
+  above = total;
+  return nb ? __shfl_sync(0xffffffffu, low, 31 - __clz(nb)) : 0;
+}
+
+struct ARow {  // the distribution of one row: e = exp2((z - m) c), kept iff e >= tau
+  const float* z;
+  float m, c, tau, Z;
+  SPEC_DEVINL float p(int x) const {
+    const float e = exp2f((__ldcg(z + x) - m) * c);
+    return e >= tau ? e / Z : 0.f;
+  }
+};
+
+// Statistics of every row of sequence b into shared memory (all warps).
+__device__ void seq_stats(const AcceptParams& p, int b, float c, bool nucleus, ASmem& s) {
+  const int n = p.gamma + 1;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  for (int i = w; i < n; i += kAW) {
+    const long long row = static_cast<long long>(b) * n + i;
+    const float2 ms = warp_row_ms(p.part_ms + row * p.S, p.S, c);
+    float Z = ms.y, tau = 0.f;
+    if (nucleus) {
+      Z = warp_sum_parts(p.part_z + row * p.S, p.S);
+      tau = __uint_as_float(static_cast<uint32_t>(__ldcg(p.sel + (row * 4 + 3) * 2)));
+    }
+    if (l == 0) {
+      s.rm[i] = ms.x;
+      s.rz[i] = Z;
+      s.rtau[i] = tau;
+    }
+  }
+  __syncthreads();
+}
+
+SPEC_DEVINL ARow arow(const AcceptParams& p, int b, int i, float c, const ASmem& s) {
+  ARow r;
+  r.z = p.logits + (static_cast<long long>(b) * (p.gamma + 1) + i) * p.V;
+  r.m = s.rm[i];
+  r.c = c;
+  r.tau = s.rtau[i];
+  r.Z = s.rz[i];
+  return r;
+}
+
+// Thread 0: the first rejected draft of sequence b (gamma if none), with the
+// device status flags when `flag`.
+__device__ int decide(const AcceptParams& p, int b, float c, const ASmem& s, bool flag) {
+  const int32_t* xb = p.draft + static_cast<long long>(b) * p.gamma;
+  const float* qb = p.q + static_cast<long long>(b) * p.gamma * p.V;
+  const float* ub = p.u + static_cast<long long>(b) * (p.gamma + 1);
+  for (int i = 0; i < p.gamma; ++i) {
+    const int x = __ldg(xb + i);
+    if (x < 0 || x >= p.V) {
+      if (flag) set_status(p.status, SPEC_DEV_BAD_TOKEN);
+      return i;
+    }
+    const float qx = __ldg(qb + static_cast<long long>(i) * p.V + x);
+    if (!(qx > 0.f)) {
+      if (flag) set_status(p.status, SPEC_DEV_Q_ZERO);
+      return i;
+    }
+    const float a = fminf(1.0f, arow(p, b, i, c, s).p(x) / qx);
+    if (!(__ldg(ub + i) < a)) return i;
+  }
+  return p.gamma;
+}
+
+// Fixed-point draw weights of id x: k = 0 residual max(0, p_j - q_j), k = 1 p_r.
+SPEC_DEVINL unsigned long long fx_weight(const ARow& r, const float* qrow, int x, int k) {
+  const float pv = r.p(x);
+  const float w = k == 0 ? fmaxf(pv - __ldcg(qrow + x), 0.f) : pv;
+  return static_cast<unsigned long long>(w * kFix52);
+}
+
+__global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) {
+  __shared__ ASmem s;
+  const int n = p.gamma + 1, S = p.S, C = p.C, V = p.V, B = p.B;
+  const int G = gridDim.x;
+  const bool greedy = !(p.T > 0.f);
+  const bool nucleus = !greedy && p.top_p < 1.0f;
+  const float c = greedy ? 0.f : kLog2e / p.T;
+  unsigned nbar = 0;
+  if (threadIdx.x == 0) s.abort = 0;
+  __syncthreads();
+
+  // ---- P1: chunk statistics
+  if (nucleus) {
+    const long long nh = static_cast<long long>(B) * n * 4 * 256;
+    for (long long k = static_cast<long long>(blockIdx.x) * kAT + threadIdx.x; k < nh;
+         k += static_cast<long long>(G) * kAT)
+      p.hist[k] = 0ull;
+    for (long long k = static_cast<long long>(blockIdx.x) * kAT + threadIdx.x;
+         k < static_cast<long long>(B) * n; k += static_cast<long long>(G) * kAT)
+      p.tot40[k] = 0ull;
+  }
+  const long long units1 = static_cast<long long>(B) * n * S;
+  for (long long u = blockIdx.x; u < units1; u += G) {
+    const int ch = static_cast<int>(u % S);
+    const long long row = u / S;
+    const float* z = p.logits + row * V;
+    const int x0 = ch * C, x1 = min(x0 + C, V);
+    p.part_ms[u] = greedy ? chunk_argmax(z, x0, x1, s) : chunk_ms(z, x0, x1, c, s);
+  }
+  if (!agrid_sync(p, ++nbar * G, s)) return;
+
+  if (greedy) {
+    for (int b = blockIdx.x; b < B; b += G) {
+      const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+      for (int i = w; i < n; i += kAW) {
+        const float2* part = p.part_ms + (static_cast<long long>(b) * n + i) * S;
+        float best = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int k = l; k < S; k += 32) {
+          const float2 v = __ldcg(part + k);
+          arg_merge(best, bi, v.x, __float_as_int(v.y));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+          arg_merge(best, bi, __shfl_xor_sync(0xffffffffu, best, o),
+                    __shfl_xor_sync(0xffffffffu, bi, o));
+        if (l == 0) s.ri[i] = bi == 0x7fffffff ? 0 : bi;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const int32_t* xb = p.draft + static_cast<long long>(b) * p.gamma;
+        int32_t* out = p.out + static_cast<long long>(b) * n;
+        int acc = 0, i = 0;
+        for (; i <= p.gamma; ++i) {
+          out[i] = s.ri[i];
+          if (i < p.gamma && __ldg(xb + i) == s.ri[i]) {
+            ++acc;
+            continue;
+          }
+          break;
+        }
+        for (++i; i < n; ++i) out[i] = -1;
+        p.n_acc[b] = acc;
+      }
+      __syncthreads();
+    }
+    return;
+  }
+
+  // ---- N0..N3, NZ: the nucleus threshold of every row
+  if (nucleus) {
+    for (int level = 0; level <= 4; ++level) {
+      for (long long u = blockIdx.x; u < units1; u += G) {
+        const int ch = static_cast<int>(u % S);
+        const long long row = u / S;
+        const float* z = p.logits + row * V;
+        const int x0 = ch * C, x1 = min(x0 + C, V);
+        if (threadIdx.x < 32) {
+          const float2 ms = warp_row_ms(p.part_ms + row * S, S, c);
+          uint32_t prefix = 0;
+          if (level >= 1) {
+            unsigned long long above = 0;
+            if (level >= 2) {
+              prefix = static_cast<uint32_t>(__ldcg(p.sel + (row * 4 + level - 2) * 2));
+              above = __ldcg(p.sel + (row * 4 + level - 2) * 2 + 1);
+            }
+            const double target = static_cast<double>(p.top_p) * static_cast<double>(__ldcg(p.tot40 + row));
+            const int chosen = warp_select(p.hist + (row * 4 + level - 1) * 256, target, above);
+            prefix |= static_cast<uint32_t>(chosen) << (24 - 8 * (level - 1));
+            if (threadIdx.x == 0 && ch == 0) {
+              p.sel[(row * 4 + level - 1) * 2] = prefix;
+              p.sel[(row * 4 + level - 1) * 2 + 1] = above;
+            }
+          }
+          if (threadIdx.x == 0) {
+            s.bf[0] = ms.x;
+            s.prefix = prefix;
+          }
+        }
+        for (int k = threadIdx.x; k < 256; k += kAT) s.hist[k] = 0ull;
+        __syncthreads();
+        const float m = s.bf[0];
+        const uint32_t prefix = s.prefix;
+        if (level < 4) {
+          const int shift = 24 - 8 * level;
+          const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
+          unsigned long long mass = 0;
+          for (int x = x0 + threadIdx.x; x < x1; x += kAT) {
+            const float e = exp2f((__ldcg(z + x) - m) * c);
+            const uint32_t bits = __float_as_uint(e);
+            const unsigned long long fx = static_cast<unsigned long long>(e * kFix40);
+            mass += fx;
+            if ((bits & hi_mask) == prefix) atomicAdd(&s.hist[(bits >> shift) & 0xFFu], fx);
+          }
+          if (level == 0) {
+            mass = ablock_sum_u64(mass, s);
+            if (threadIdx.x == 0) atomicAdd(p.tot40 + row, mass);
+          }
+          __syncthreads();
+          for (int k = threadIdx.x; k < 256; k += kAT)
+            if (s.hist[k]) atomicAdd(p.hist + (row * 4 + level) * 256 + k, s.hist[k]);
+        } else {
+          const float tau = __uint_as_float(prefix);
+          float kept = 0.f;
+          for (int x = x0 + threadIdx.x; x < x1; x += kAT) {
+            const float e = exp2f((__ldcg(z + x) - m) * c);
+            kept += e >= tau ? e : 0.f;
+          }
+          kept = ablock_sum_f(kept, s);
+          if (threadIdx.x == 0) p.part_z[u] = kept;
+        }
+        __syncthreads();
+      }
+      if (!agrid_sync(p, ++nbar * G, s)) return;
+    }
+  }
+
+  // ---- P2: decisions and the chunk sums of the draw weights
+  const long long units2 = static_cast<long long>(B) * S;
+  for (long long u = blockIdx.x; u < units2; u += G) {
+    const int b = static_cast<int>(u / S), ch = static_cast<int>(u % S);
+    seq_stats(p, b, c, nucleus, s);
+    if (threadIdx.x == 0) s.j = decide(p, b, c, s, ch == 0);
+    __syncthreads();
+    const int j = s.j;
+    const ARow r = arow(p, b, j, c, s);
+    const float* qrow = p.q + (static_cast<long long>(b) * p.gamma + (j < p.gamma ? j : 0)) * V;
+    const int x0 = ch * C, x1 = min(x0 + C, V);
+    unsigned long long tr = 0, tp = 0;
+    int lr = -1, lp = -1;
+    for (int x = x0 + threadIdx.x; x < x1; x += kAT) {
+      const unsigned long long fp = fx_weight(r, qrow, x, 1);
+      tp += fp;
+      if (fp) lp = x;
+      if (j < p.gamma) {
+        const unsigned long long fr = fx_weight(r, qrow, x, 0);
+        tr += fr;
+        if (fr) lr = x;
+      }
+    }
+    tr = ablock_sum_u64(tr, s);
+    tp = ablock_sum_u64(tp, s);
+    lr = ablock_max_i(lr, s);
+    lp = ablock_max_i(lp, s);
+    if (threadIdx.x == 0) {
+      p.part_tot[u * 2] = tr;
+      p.part_tot[u * 2 + 1] = tp;
+      p.part_last[u * 2] = lr;
+      p.part_last[u * 2 + 1] = lp;
+    }
+    __syncthreads();
+  }
+  if (!agrid_sync(p, ++nbar * G, s)) return;
+
+  // ---- P3: the draw
+  for (int b = blockIdx.x; b < B; b += G) {
+    seq_stats(p, b, c, nucleus, s);
+    if (threadIdx.x == 0) {
+      const int j = decide(p, b, c, s, false);
+      const unsigned long long* tot = p.part_tot + static_cast<long long>(b) * S * 2;
+      const int* last = p.part_last + static_cast<long long>(b) * S * 2;
+      unsigned long long total_r = 0, total_p = 0;
+      for (int k = 0; k < S; ++k) {
+        total_r += __ldcg(tot + 2 * k);
+        total_p += __ldcg(tot + 2 * k + 1);
+      }
+      int kind = 1;
+      if (j < p.gamma && !(static_cast<double>(total_r) <= kResidualFallback * 4503599627370496.0))
+        kind = 0;
+      const unsigned long long total = kind == 0 ? total_r : total_p;
+      const float uu = __ldg(p.u + static_cast<long long>(b) * n + p.gamma);
+      const unsigned long long thr =
+          static_cast<unsigned long long>(static_cast<double>(uu) * static_cast<double>(total));
+      unsigned long long run = 0;
+      int found = -1, lastpos = -1;
+      for (int k = 0; k < S; ++k) {
+        const unsigned long long t = __ldcg(tot + 2 * k + kind);
+        lastpos = max(lastpos, __ldcg(last + 2 * k + kind));
+        if (found < 0) {
+          if (thr < run + t)
+            found = k;
+          else
+            run += t;
+        }
+      }
+      s.j = j;
+      s.bi[0] = found;
+      s.bi[1] = kind;
+      s.bi[2] = lastpos;
+      s.bu[1] = run;
+      s.bu[2] = thr;
+      s.tok = -1;
+    }
+    __syncthreads();
+    const int j = s.j, found = s.bi[0], kind = s.bi[1];
+    int tok = s.bi[2];
+    if (found >= 0) {
+      const ARow r = arow(p, b, j, c, s);
+      const float* qrow = p.q + (static_cast<long long>(b) * p.gamma + (j < p.gamma ? j : 0)) * V;
+      const int x0 = found * C + threadIdx.x * kAPer;
+      const int x1 = min(found * C + C, V);
+      unsigned long long f[kAPer], mine = 0;
+#pragma unroll
+      for (int k = 0; k < kAPer; ++k) {
+        f[k] = x0 + k < x1 ? fx_weight(r, qrow, x0 + k, kind) : 0ull;
+        mine += f[k];
+      }
+      const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+      unsigned long long incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (l >= o) incl += t;
+      }
+      if (l == 31) s.u[w] = incl;
+      __syncthreads();
+      unsigned long long wex = 0;
+      for (int k = 0; k < w; ++k) wex += s.u[k];
+      const unsigned long long thr = s.bu[2];
+      unsigned long long acc = s.bu[1] + wex + (incl - mine);
+      if (acc <= thr && thr < acc + mine) {
+#pragma unroll
+        for (int k = 0; k < kAPer; ++k) {
+          acc += f[k];
+          if (acc > thr) {
+            s.tok = x0 + k;
+            break;
+          }
+        }
+      }
+      __syncthreads();
+      if (s.tok >= 0) tok = s.tok;
+    }
+    if (threadIdx.x == 0) {
+      const int32_t* xb = p.draft + static_cast<long long>(b) * p.gamma;
+      int32_t* out = p.out + static_cast<long long>(b) * n;
+      for (int i = 0; i < j; ++i) out[i] = __ldg(xb + i);
+      out[j] = tok < 0 ? 0 : tok;
+      for (int i = j + 1; i < n; ++i) out[i] = -1;
+      p.n_acc[b] = j;
+    }
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(kT, 1) sample_kernel(const SampleParams p) {
   __shared__ Red red;
   const int row = blockIdx.x;
@@ -506,12 +1102,41 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, cudaS
 
 }  // namespace
 
-cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream, bool pdl) {
+int accept_grid_capacity() {
+  static int cap = [] {
+    int dev = 0, sms = 0, per = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, accept_grid_kernel, kAT, 0) != cudaSuccess)
+      return 0;
+    return sms * per;
+  }();
+  return cap;
+}
+
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream) {
   if (p.B == 0) return cudaSuccess;
-  AcceptParams a = p;
-  void* args[] = {&a};
-  return launch_pdl(reinterpret_cast<const void*>(accept_kernel), dim3(p.B), dim3(kT), args,
-                    stream, pdl);
+  const long long rows = static_cast<long long>(p.B) * (p.gamma + 1);
+  const int cap = accept_grid_capacity();
+  if (!p.grid || rows > kAcceptGridRows || cap <= 0) {
+    AcceptParams a = p;
+    accept_seq_kernel<<<p.B, kT, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
+  const long long units = rows * p.S;
+  const int grid = static_cast<int>(std::min<long long>(cap, std::max<long long>(units, 1)));
+  cudaError_t e = cudaMemsetAsync(p.bar, 0, sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kAT);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, accept_grid_kernel, p);
 }
 
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t stream) {

@@ -840,9 +840,67 @@ int spec_internal_lm_head(const spec_model* m, const uint16_t* d_hidden, int row
   return run_gemm(cx, &m->tm_head, d_hidden, nullptr, rows, m->cfg.vocab, m->cfg.d_model, p);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Accept workspace: status word and grid-barrier counter, then the chunk
+// partials of the cooperative accept grid, sized for the largest chunk count
+// a launch may choose.
+struct AcceptWs {
+  size_t bar, part_ms, tot40, hist, sel, part_z, part_tot, part_last, total;
+  int s_max;
+};
+
+int accept_chunks_max(int V) {
+  const int by_size = (V + kAcceptMaxChunk - 1) / kAcceptMaxChunk;
+  return std::min(V, std::max(512, by_size));
+}
+
+AcceptWs plan_accept(int B, int gamma, int V) {
+  AcceptWs w{};
+  const size_t n = static_cast<size_t>(gamma) + 1;
+  w.s_max = accept_chunks_max(V);
+  const size_t S = static_cast<size_t>(w.s_max);
+  // the grid schedule serves batches of up to kAcceptGridRows rows; larger
+  // ones run one CTA per sequence and need only the status word
+  if (static_cast<long long>(B) * static_cast<long long>(n) > kAcceptGridRows) B = 0;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  take(64);  // status word
+  w.bar = take(64);
+  w.part_ms = take(B * n * S * 8);
+  w.tot40 = take(B * n * 8);
+  w.hist = take(B * n * 4 * 256 * 8);
+  w.sel = take(B * n * 4 * 2 * 8);
+  w.part_z = take(B * n * S * 4);
+  w.part_tot = take(B * S * 2 * 8);
+  w.part_last = take(B * S * 2 * 4);
+  w.total = off;
+  return w;
+}
+
+int device_sm_count() {
+  static int v = [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+  }();
+  return v;
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t spec_accept_workspace_bytes(int batch, int gamma, int vocab) {
   if (batch < 0 || gamma < 0 || vocab <= 0) return 0;
-  return kAlign;
+  return plan_accept(batch, gamma, vocab).total;
 }
 
 static int accept_common_checks(int batch, int gamma, int vocab, float T, float top_p) {
@@ -861,9 +919,31 @@ int spec_accept(const float* d_target_logits, const float* d_draft_probs,
   if (!d_target_logits || !d_out_tokens || !d_n_accepted || !d_ws) return SPEC_EINVAL;
   if (gamma > 0 && !d_draft_tokens) return SPEC_EINVAL;
   if (temperature > 0.f && ((gamma > 0 && !d_draft_probs) || !d_uniforms)) return SPEC_EINVAL;
-  if (ws_bytes < spec_accept_workspace_bytes(batch, gamma, vocab)) return SPEC_ESIZE;
+  if (gamma + 1 > kAcceptMaxRows) return SPEC_ESIZE;
+  const AcceptWs A = plan_accept(batch, gamma, vocab);
+  if (ws_bytes < A.total) return SPEC_ESIZE;
+  if (reinterpret_cast<uintptr_t>(d_ws) % 16) return SPEC_EINVAL;
   if (batch == 0) return SPEC_OK;
+  uint8_t* W = static_cast<uint8_t*>(d_ws);
   AcceptParams p{};
+  const char* ge = getenv("SPEC_ACCEPT_GRID");  // 0: one CTA per sequence (read per call)
+  p.grid = (ge && ge[0] == '0') ? 0 : 1;
+  // chunks: at most kAcceptMaxChunk ids each, and about two units per SM
+  const int rows = batch * (gamma + 1);
+  const int want = std::max(1, (2 * device_sm_count() + rows - 1) / rows);
+  int S = std::min(A.s_max, std::max((vocab + kAcceptMaxChunk - 1) / kAcceptMaxChunk, want));
+  const int C = (vocab + S - 1) / S;
+  S = (vocab + C - 1) / C;
+  p.S = S;
+  p.C = C;
+  p.bar = reinterpret_cast<unsigned*>(W + A.bar);
+  p.part_ms = reinterpret_cast<float2*>(W + A.part_ms);
+  p.tot40 = reinterpret_cast<unsigned long long*>(W + A.tot40);
+  p.hist = reinterpret_cast<unsigned long long*>(W + A.hist);
+  p.sel = reinterpret_cast<unsigned long long*>(W + A.sel);
+  p.part_z = reinterpret_cast<float*>(W + A.part_z);
+  p.part_tot = reinterpret_cast<unsigned long long*>(W + A.part_tot);
+  p.part_last = reinterpret_cast<int*>(W + A.part_last);
   p.logits = d_target_logits;
   p.q = d_draft_probs;
   p.draft = d_draft_tokens;
@@ -876,7 +956,7 @@ int spec_accept(const float* d_target_logits, const float* d_draft_probs,
   p.V = vocab;
   p.T = temperature;
   p.top_p = top_p;
-  SPEC_CUDA(launch_accept(p, static_cast<cudaStream_t>(stream), true));
+  SPEC_CUDA(launch_accept(p, static_cast<cudaStream_t>(stream)));
   return SPEC_OK;
 }
 

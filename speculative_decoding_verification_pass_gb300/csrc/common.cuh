@@ -19,6 +19,13 @@ SPEC_DEVINL void set_status(int32_t* status, int32_t bit) {
   if (status) atomicOr(status, bit);
 }
 
+// Load with acquire semantics at GPU scope (grid-barrier counters).
+SPEC_DEVINL uint32_t ld_acquire(const unsigned* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Wall-clock bound for every spin-wait in a kernel: about two seconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 

@@ -183,11 +183,6 @@ SPEC_DEVINL GemmParams phase_params(const MkParams& P, const GPh& g) {
   return p;
 }
 
-SPEC_DEVINL uint32_t ld_acquire(const unsigned* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 SPEC_DEVINL void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // Wait (one thread) until `target` arrivals; bounded.

@@ -159,6 +159,9 @@ cudaError_t launch_fill_f32(float* dst, long long n, float v, cudaStream_t strea
 cudaError_t launch_rope_table(float2* dst, int hd, double theta, cudaStream_t stream);
 
 // ------------------------------------------------------------------ accept
+constexpr int kAcceptMaxChunk = 4096;  // vocabulary ids per accept work unit
+constexpr int kAcceptMaxRows = 128;    // gamma + 1 per sequence
+constexpr int kAcceptGridRows = 1024;  // batch * (gamma + 1) of the grid schedule
 struct AcceptParams {
   const float* logits;   // [B][gamma+1][V]
   const float* q;        // [B][gamma][V]
@@ -167,10 +170,19 @@ struct AcceptParams {
   int32_t* out;          // [B][gamma+1]
   int32_t* n_acc;        // [B]
   int32_t* status;
-  int B, gamma, V;
+  unsigned* bar;                 // grid-barrier arrivals, zeroed before launch
+  float2* part_ms;               // [B][n][S] chunk (max, sum) or (value, id)
+  unsigned long long* tot40;     // [B][n] nucleus mass (2^-40 fixed point)
+  unsigned long long* hist;      // [B][n][4][256] radix-select histograms
+  unsigned long long* sel;       // [B][n][4][2] (prefix, mass above) per digit
+  float* part_z;                 // [B][n][S] kept mass per chunk
+  unsigned long long* part_tot;  // [B][S][2] draw-weight sums (residual, p)
+  int* part_last;                // [B][S][2] last id with positive weight
+  int B, gamma, V, S, C;         // S chunks of C ids (C <= kAcceptMaxChunk)
+  int grid;                      // 1: the cooperative grid schedule when it fits
   float T, top_p;
 };
-cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
 
 struct SampleParams {
   const float* logits;  // [R][V]

@@ -69,7 +69,16 @@ def test_argument_validation_without_gpu(lib):
     # workspace too small
     assert L.spec_accept(fake, fake, fake, fake, 1, 4, 10, 1.0, 1.0, fake, fake, fake, 8, None) == lib.SPEC_ESIZE
     # zero-size batch is a no-op
-    assert L.spec_accept(fake, fake, fake, fake, 0, 4, 10, 1.0, 1.0, fake, fake, fake, 256, None) == lib.SPEC_OK
+    ws0 = lib.spec_accept_workspace_bytes(0, 4, 10)
+    assert L.spec_accept(fake, fake, fake, fake, 0, 4, 10, 1.0, 1.0, fake, fake, fake, ws0, None) == lib.SPEC_OK
+    # more than 128 rows per sequence, or a misaligned workspace
+    big = lib.spec_accept_workspace_bytes(1, 128, 10)
+    assert L.spec_accept(fake, fake, fake, fake, 1, 128, 10, 1.0, 1.0, fake, fake, fake, big, None) == lib.SPEC_ESIZE
+    ws1 = lib.spec_accept_workspace_bytes(1, 4, 10)
+    assert L.spec_accept(fake, fake, fake, fake, 1, 4, 10, 1.0, 1.0, fake, fake, P(4100), ws1, None) == lib.SPEC_EINVAL
+    # the accept workspace grows with the batch and the draft length
+    assert lib.spec_accept_workspace_bytes(2, 4, 32000) > lib.spec_accept_workspace_bytes(1, 4, 32000)
+    assert lib.spec_accept_workspace_bytes(1, 7, 32000) > lib.spec_accept_workspace_bytes(1, 4, 32000)
     out = P()
     cfg = lib.LLAMA_1B.c()
     assert L.spec_model_create(ctypes.byref(cfg), 1, None, 0, None, ctypes.byref(out)) == lib.SPEC_EINVAL

@@ -170,3 +170,46 @@ def test_chi_square_v8_million_trials():
     alpha = np.minimum(Pf[0], Q[0]).sum()
     acc0 = (nacc > 0).mean()
     assert abs(acc0 - alpha) < 4 * np.sqrt(alpha * (1 - alpha) / N)
+
+
+@pytest.mark.parametrize("T,top_p", [(1.0, 1.0), (0.8, 0.9), (0.0, 1.0)])
+def test_accept_grid_and_per_sequence_schedules_agree(T, top_p, monkeypatch):
+    """The cooperative grid (batches up to 1024 rows) and the per-sequence
+    kernel take the same decisions and draws: each matches the oracle under
+    the boundary rule, and they differ on at most 0.1% of the sequences
+    (only where fp32 summation order crosses a boundary)."""
+    B, gamma, V = 96, 4, 32000
+    seed = 77 + int(10 * T) + int(100 * top_p)
+    zq, zp = wl.accept_logits(seed, B, gamma, V)
+    ud = wl.uniforms(seed, B, gamma, stream=8)
+    u = wl.uniforms(seed, B, gamma + 1)
+    q, x = _draft(zq[:, :gamma], ud, T if T > 0 else 1.0, top_p)
+    if T == 0:
+        x = zp[:, :gamma].argmax(-1).astype(np.int32)
+        x[:, 2] = (x[:, 2] + 1) % V
+    res = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("SPEC_ACCEPT_GRID", mode)
+        res[mode] = _run_accept(zp, q, x, u, T, top_p)
+        excused, near = _compare(zp, q, x, u, T, top_p, *res[mode])
+        assert excused <= max(1, 0.001 * B), (mode, excused, near)
+    diff = (res["1"][0] != res["0"][0]).any(1) | (res["1"][1] != res["0"][1])
+    assert diff.sum() <= max(1, 0.001 * B), np.nonzero(diff)
+
+
+@pytest.mark.parametrize("top_p", [1.0, 0.9])
+def test_accept_llama3_vocabulary_batch_one(top_p):
+    """The verify step's own shape: one sequence, gamma 4, V = 128256 (the
+    grid schedule spreads each row over the SMs), 40 independent steps."""
+    gamma, V, steps = 4, 128256, 40
+    excused = 0
+    for k in range(steps):
+        seed = 5000 + k
+        zq, zp = wl.accept_logits(seed, 1, gamma, V)
+        ud = wl.uniforms(seed, 1, gamma, stream=8)
+        u = wl.uniforms(seed, 1, gamma + 1)
+        q, x = _draft(zq[:, :gamma], ud, 1.0, top_p)
+        out, nacc = _run_accept(zp, q, x, u, 1.0, top_p)
+        e, _ = _compare(zp, q, x, u, 1.0, top_p, out, nacc)
+        excused += e
+    assert excused <= 1, excused
