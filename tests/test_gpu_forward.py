@@ -207,7 +207,7 @@ def test_lm_head_workload_and_accept():
     u = wl.uniforms(seed, 1, 5)
     out = torch.empty(1, 5, dtype=torch.int32, device="cuda")
     nacc = torch.empty(1, dtype=torch.int32, device="cuda")
-    aws = sb.workspace(256)
+    aws = sb.workspace(sb.spec_accept_workspace_bytes(1, 4, cfg.vocab))
     sb.spec_accept(z.view(1, 5, -1), torch.from_numpy(q.astype(np.float32)[None]).cuda(),
                    torch.from_numpy(x.astype(np.int32)[None]).cuda(), torch.from_numpy(u).cuda(),
                    1, 4, cfg.vocab, 1.0, 1.0, out, nacc, aws)

@@ -71,7 +71,7 @@ def test_1b_workload_matches_oracle():
     u = wl.uniforms(seed, B, gamma + 1)
     out = torch.empty(B, gamma + 1, dtype=torch.int32, device="cuda")
     nacc = torch.empty(B, dtype=torch.int32, device="cuda")
-    aws = sb.workspace(256)
+    aws = sb.workspace(sb.spec_accept_workspace_bytes(B, gamma, cfg.vocab))
     sb.spec_accept(z, torch.from_numpy(q.astype(np.float32)[None]).cuda(),
                    torch.from_numpy(x.astype(np.int32)[None]).cuda(), torch.from_numpy(u).cuda(),
                    B, gamma, cfg.vocab, 1.0, 1.0, out, nacc, aws)
@@ -162,7 +162,7 @@ def test_8b_greedy_walks_the_argmax(big, gamma):
         x[2] = (x[2] + 1) % cfg.vocab
     out = torch.empty(1, gamma + 1, dtype=torch.int32, device="cuda")
     nacc = torch.empty(1, dtype=torch.int32, device="cuda")
-    aws = sb.workspace(256)
+    aws = sb.workspace(sb.spec_accept_workspace_bytes(1, gamma, cfg.vocab))
     sb.spec_accept(z, None, torch.from_numpy(x[None].astype(np.int32)).cuda(), None, 1, gamma,
                    cfg.vocab, 0.0, 1.0, out, nacc, aws)
     n = int(nacc[0])
