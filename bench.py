@@ -42,7 +42,10 @@ TRAFFIC = {
     # one 8B-dims layer's four GEMMs x 32 + the LM head, / 129 launches
     "gemm_tc_kernel": {"file": "gemm.cu", "source_sha1": "8e216fc32ca40f7636d65c01def4ef52f68a3a17",
                        "bytes_per_launch": 118288036},
-    "forward_kernel": {"file": "forward.cu", "source_sha1": None, "bytes_per_launch": None},
+    # 2-layer 8B-dims capture scaled to 32 layers by the algorithmic bytes
+    # (profiles/forward_kernel_8b_2layers.md)
+    "forward_kernel": {"file": "forward.cu", "source_sha1": "32656b28ccacbb51d79e6b575fd8320b1c3cafce",
+                       "bytes_per_launch": 15348201291},
 }
 
 
