@@ -17,8 +17,9 @@
 //   warp 0 lane 0  weight producer (TMA, runs ahead across phases)
 //   warp 1         TMEM owner; lane 0 issues tcgen05.mma
 //   warps 2-5      GEMM epilogues (TMEM -> fused epilogue), embedding,
-//                  attention partials (ATT) and their merge (CMB); they arrive
-//                  on the grid barrier for every phase
+//                  attention partials (ATT; the first key block prefetched
+//                  before the QKV phase ends) and their merge (CMB); they
+//                  arrive on the grid barrier for every phase
 //   warp 6 lane 0  activation producer (TMA after each phase's barrier)
 // Grid barrier: one monotonic counter; phase k is complete when it holds
 // (k+1) * gridDim.x arrivals.  All waits are bounded (~2 s); a CTA that times
@@ -38,11 +39,12 @@ constexpr int kAttUnitKeys = 64;    // keys per attention work unit (2 blocks)
 constexpr int kArriveBar = 2;       // named barrier of the epilogue warps for arrivals
 
 enum PhaseKind { PH_EMBED, PH_QKV, PH_ATT, PH_CMB, PH_O, PH_GU, PH_D, PH_HEAD };
+constexpr int kPhPerLayer = 6;
 
 SPEC_DEVINL int ph_kind(int ph, int L) {
   if (ph == 0) return PH_EMBED;
-  if (ph == 1 + 6 * L) return PH_HEAD;
-  return PH_QKV + (ph - 1) % 6;
+  if (ph == 1 + kPhPerLayer * L) return PH_HEAD;
+  return PH_QKV + (ph - 1) % kPhPerLayer;
 }
 SPEC_DEVINL bool is_gemm(int k) {
   return k == PH_QKV || k == PH_O || k == PH_GU || k == PH_D || k == PH_HEAD;
@@ -54,7 +56,7 @@ struct GPh {
 
 SPEC_DEVINL GPh gph(const MkParams& P, int ph) {
   const int k = ph_kind(ph, P.L);
-  const int l = k == PH_HEAD ? P.L : (ph - 1) / 6;
+  const int l = k == PH_HEAD ? P.L : (ph - 1) / kPhPerLayer;
   GPh g;
   g.l = l;
   switch (k) {
@@ -320,6 +322,106 @@ SPEC_DEVINL int att_chunk_keys(int Tk, int nch) {
   return ((per + kAttUnitKeys - 1) / kAttUnitKeys) * kAttUnitKeys;
 }
 
+// Issue the cp.async copies of the 64-key block at kb (keys and values) into
+// the K/V stage: `what` = 0 every row (zero fill past kend), 1 the rows this
+// pass does not write (cached keys below Lb; zero fill past kend), 2 the rows
+// this pass writes (keys Lb .. kend-1).
+template <int HD>
+SPEC_DEVINL void att_load_block(uint8_t* sK, const uint16_t* kc, const uint16_t* vc, long long head_base,
+                                int kb, int kend, int Lb, int what, int e) {
+  constexpr int kRowB = HD * 2;
+  constexpr int kCPR = HD / 8;
+  for (int idx = e; idx < kAttUnitKeys * kCPR; idx += kEpiThreads) {
+    const int i = idx / kCPR, c = idx % kCPR;  // key kb + i
+    const int s = i >> 5, ii = i & 31;
+    const int key = kb + i;
+    const bool valid = key < kend;
+    const bool fresh = valid && key >= Lb;
+    if ((what == 1 && fresh) || (what == 2 && !fresh)) continue;
+    const long long g = (head_base + (valid ? key : kb)) * HD + c * 8;
+    const uint32_t dk = smem_u32(sK + s * 64 * kRowB) + swz<HD>(ii, c);
+    cp_async16(dk, kc + g, valid ? 16 : 0);
+    cp_async16(dk + 32 * kRowB, vc + g, valid ? 16 : 0);
+  }
+}
+
+// Before the QKV phase completes: start loading the cached keys / values of
+// the first 64-key block of this CTA's first attention unit of layer l (they
+// do not depend on the pass).
+template <int HD>
+SPEC_DEVINL void att_prefetch(const MkParams& P, const MkSmem& sm, int l) {
+  const int e = threadIdx.x - kEpiFirstThread;
+  const int nch = P.att_nch;
+  const int unit = blockIdx.x;
+  if (unit >= P.B * P.Hkv * nch) return;
+  const int b = unit / (P.Hkv * nch);
+  const int kvh = (unit / nch) % P.Hkv;
+  const int ch = unit % nch;
+  const int Lb = __ldcg(P.pos_base + b);
+  const int Tk = min(Lb + P.n, P.cap);
+  const int ck = att_chunk_keys(Tk, nch);
+  const int kbeg = ch * ck, kend = min(kbeg + ck, Tk);
+  if (kbeg >= kend) return;
+  const long long head_base = (static_cast<long long>(b) * P.Hkv + kvh) * P.cap;
+  uint8_t* sK = sm.att + 64 * HD * 2;
+  att_load_block<HD>(sK, P.kc + P.layer_kv * l, P.vc + P.layer_kv * l, head_base, kbeg, kend, Lb, 1, e);
+}
+
+// Merge the chunk partials of every query row by log-sum-exp into the
+// attention output (bf16 hi/lo).  One warp per (sequence, KV head, row,
+// 32-dimension group): each lane owns one dimension, so every partial load of
+// a lane is in flight at once.
+template <int HD>
+SPEC_DEVINL void cmb_phase(const MkParams& P) {
+  const int e = threadIdx.x - kEpiFirstThread;
+  const int w = e >> 5, lane = e & 31;
+  const int G = P.H / P.Hkv;
+  const int R = P.n * G;
+  const int qdim = P.H * HD;
+  const int nch = P.att_nch;
+  constexpr int kDG = HD / 32;
+  const int items = P.B * P.Hkv * R * kDG;
+  const float2* mlp = reinterpret_cast<const float2*>(P.att_ml);
+  for (int it = blockIdx.x * 4 + w; it < items; it += gridDim.x * 4) {
+    const int dg = it % kDG;
+    const int r = (it / kDG) % R;
+    const int kvh = (it / (kDG * R)) % P.Hkv;
+    const int b = it / (kDG * R * P.Hkv);
+    const int Tk = min(__ldcg(P.pos_base + b) + P.n, P.cap);
+    const int ck = att_chunk_keys(Tk, nch);
+    const int nu = (Tk + ck - 1) / ck;
+    const long long ubase = (static_cast<long long>(b) * P.Hkv + kvh) * nch;
+    const float* ob = P.att_o + (ubase * 32 + r) * HD + dg * 32 + lane;
+    float acc = 0.f, lsum = 0.f, m = -INFINITY;
+    for (int u0 = 0; u0 < nu; u0 += 32) {
+      // lane k holds unit u0 + k's (max, sum); the o loads of the 32 units
+      // below do not depend on them
+      const int cnt = min(32, nu - u0);
+      const float2 mv = lane < cnt ? __ldcg(&mlp[(ubase + u0 + lane) * 32 + r]) : make_float2(-INFINITY, 0.f);
+      float ov[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) ov[k] = k < cnt ? __ldcg(ob + static_cast<long long>(u0 + k) * 32 * HD) : 0.f;
+      const float mb = warp_max(mv.x);
+      const float mn = fmaxf(m, mb);
+      const float scale = m == -INFINITY ? 0.f : exp2f(m - mn);
+      const float wgt = mv.x == -INFINITY ? 0.f : exp2f(mv.x - mn);
+      float a2 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) a2 += __shfl_sync(0xffffffffu, wgt, k) * ov[k];
+      acc = acc * scale + a2;
+      lsum = lsum * scale + warp_sum(wgt * mv.y);
+      m = mn;
+    }
+    const float o = acc / lsum;
+    const int j = r / G, g = r % G;
+    const long long off =
+        (static_cast<long long>(b) * P.n + j) * qdim + (kvh * G + g) * HD + dg * 32 + lane;
+    const uint16_t hi = f32_to_bf16(o);
+    P.o[off] = hi;
+    P.o_lo[off] = f32_to_bf16(o - bf16_to_f32(hi));
+  }
+}
+
 template <int HD>
 SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
   const int e = threadIdx.x - kEpiFirstThread;
@@ -352,18 +454,9 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
     const int kbeg = ch * ck, kend = min(kbeg + ck, Tk);
     if (kbeg >= kend) continue;  // uniform across the CTA
     const long long head_base = (static_cast<long long>(b) * P.Hkv + kvh) * P.cap;
-    auto load_block = [&](int kb) {
-      for (int idx = e; idx < kAttUnitKeys * kCPR; idx += kEpiThreads) {
-        const int i = idx / kCPR, c = idx % kCPR;  // key kb + i
-        const int s = i >> 5, ii = i & 31;
-        const bool valid = kb + i < kend;
-        const long long g = (head_base + (valid ? kb + i : kb)) * HD + c * 8;
-        const uint32_t dk = smem_u32(sK + s * 64 * kRowB) + swz<HD>(ii, c);
-        cp_async16(dk, kc + g, valid ? 16 : 0);
-        cp_async16(dk + 32 * kRowB, vc + g, valid ? 16 : 0);
-      }
-    };
-    load_block(kbeg);  // in flight while q is staged
+    // the first block of the CTA's first unit was prefetched except the rows
+    // this pass wrote; they are in flight while q is staged
+    att_load_block<HD>(sK, kc, vc, head_base, kbeg, kend, Lb, unit == static_cast<int>(blockIdx.x) ? 2 : 0, e);
     // ---- stage q (hi, lo) rows
     for (int idx = e; idx < 32 * kCPR; idx += kEpiThreads) {
       const int r = idx / kCPR, c = idx % kCPR;
@@ -384,7 +477,7 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
     for (int kb = kbeg; kb < kend; kb += kAttUnitKeys) {
       if (kb > kbeg) {
         named_bar(kArriveBar, kEpiThreads);  // previous block consumed
-        load_block(kb);
+        att_load_block<HD>(sK, kc, vc, head_base, kb, kend, Lb, 0, e);
       }
       cp_async_wait_all();
       named_bar(kArriveBar, kEpiThreads);
@@ -527,72 +620,6 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
   }
 }
 
-// Merge the chunk partials of each query row by log-sum-exp; one warp per
-// (sequence, KV head, row), each lane owning HD/32 consecutive dimensions.
-template <int HD>
-SPEC_DEVINL void cmb_phase(const MkParams& P) {
-  const int e = threadIdx.x - kEpiFirstThread;
-  const int w = e >> 5, lane = e & 31;
-  const int G = P.H / P.Hkv;
-  const int R = P.n * G;
-  const int qdim = P.H * HD;
-  const int nch = P.att_nch;
-  constexpr int kV = HD / 32;
-  const int items = P.B * P.Hkv * R;
-  const float2* mlp = reinterpret_cast<const float2*>(P.att_ml);
-  for (int it = blockIdx.x * 4 + w; it < items; it += gridDim.x * 4) {
-    const int r = it % R;
-    const int kvh = (it / R) % P.Hkv;
-    const int b = it / (R * P.Hkv);
-    const int Tk = min(__ldcg(P.pos_base + b) + P.n, P.cap);
-    const int nu = (Tk + att_chunk_keys(Tk, nch) - 1) / att_chunk_keys(Tk, nch);
-    const long long ubase = (static_cast<long long>(b) * P.Hkv + kvh) * nch;
-    const float2 mv0 = lane < nu ? __ldcg(&mlp[(ubase + lane) * 32 + r]) : make_float2(-INFINITY, 0.f);
-    float m = mv0.x;
-    for (int u = 32 + lane; u < nu; u += 32) m = fmaxf(m, __ldcg(&mlp[(ubase + u) * 32 + r]).x);
-    m = warp_max(m);
-    float acc[kV];
-#pragma unroll
-    for (int k = 0; k < kV; ++k) acc[k] = 0.f;
-    float l = 0.f;
-    for (int u0 = 0; u0 < nu; u0 += 32) {
-      const float2 mv = u0 == 0 ? mv0
-                                : (u0 + lane < nu ? __ldcg(&mlp[(ubase + u0 + lane) * 32 + r])
-                                                  : make_float2(-INFINITY, 0.f));
-      const float wgt = mv.x == -INFINITY ? 0.f : exp2f(mv.x - m);
-      l += wgt * mv.y;
-      const int cnt = min(32, nu - u0);
-      const float* src = P.att_o + ((ubase + u0) * 32 + r) * HD + lane * kV;
-#pragma unroll 8
-      for (int k = 0; k < cnt; ++k) {
-        const float wk = __shfl_sync(0xffffffffu, wgt, k);
-        const float* s = src + static_cast<long long>(k) * 32 * HD;
-        if constexpr (kV == 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(s));
-          acc[0] += wk * v.x;
-          acc[1] += wk * v.y;
-          acc[2] += wk * v.z;
-          acc[3] += wk * v.w;
-        } else {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(s));
-          acc[0] += wk * v.x;
-          acc[1] += wk * v.y;
-        }
-      }
-    }
-    const float inv = 1.f / warp_sum(l);
-    const int j = r / G, g = r % G;
-    const long long off = (static_cast<long long>(b) * P.n + j) * qdim + (kvh * G + g) * HD + lane * kV;
-#pragma unroll
-    for (int k = 0; k < kV; ++k) {
-      const float o = acc[k] * inv;
-      const uint16_t hi = f32_to_bf16(o);
-      P.o[off + k] = hi;
-      P.o_lo[off + k] = f32_to_bf16(o - bf16_to_f32(hi));
-    }
-  }
-}
-
 // -------------------------------------------------------------- the kernel
 template <int HD>
 __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_constant__ MkParams P) {
@@ -604,7 +631,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
   const MkSmem sm = mk_carve(smem_raw, static_cast<size_t>(sbytes) * S, HD);
   const int warp = threadIdx.x >> 5;
   const uint32_t me = blockIdx.x, GR = gridDim.x;
-  const int nph = 2 + 6 * P.L;
+  const int nph = 2 + kPhPerLayer * P.L;
   const uint32_t tcols = tmem_cols_for(ncols);
 
   if (threadIdx.x == 0) {
@@ -768,8 +795,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
       if (kind == PH_EMBED) {
         embed_phase(P, sm);
       } else if (kind == PH_ATT) {
+        att_prefetch<HD>(P, sm, (ph - 1) / kPhPerLayer);
         if (!epi_wait(P, sm, ph)) break;
-        att_phase<HD>(P, sm, (ph - 1) / 6);
+        att_phase<HD>(P, sm, (ph - 1) / kPhPerLayer);
       } else if (kind == PH_CMB) {
         if (!epi_wait(P, sm, ph)) break;
         cmb_phase<HD>(P);
@@ -795,6 +823,15 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
           const uint32_t t = u / kc;
           const uint32_t seg_end = min(u1, (t + 1) * kc);
           const int a = seg & 1;
+          // the residual stream of this tile's rows, loaded while the MMAs run
+          float hv[16];
+          const bool pre_h = p.epi == EPI_RESID && p.ntok <= 16;
+          if (pre_h) {
+            const int f = static_cast<int>(t) * kTileN + r;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              hv[j] = (j < p.M && f < p.N) ? __ldcg(p.h + static_cast<long long>(j) * p.d + f) : 0.f;
+          }
           mbar_wait(&sm.accfull[a], (seg >> 1) & 1, sm.abort);
           named_bar(kEpiBar, kEpiThreads);
           if (*sm.abort) break;
@@ -836,7 +873,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
               } else {
                 fixup_sum<4>(p.partials, p.ntok, c0, r, c_first, nc, me, sm.slots, own, acc);
               }
-              epilogue_chunk(p, gs, t, r, c0, acc);
+              epilogue_chunk_h(p, gs, t, r, c0, acc, hv, pre_h);
             }
           }
           tc_fence_before();

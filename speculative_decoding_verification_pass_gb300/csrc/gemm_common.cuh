@@ -141,8 +141,10 @@ __device__ __forceinline__ void fixup_sum(const float* partials, int ntok, int c
 
 // --------------------------------------------------------------- epilogues
 // Apply the epilogue to 16 token columns [c0, c0+16) of this thread's row.
-__device__ void epilogue_chunk(const GemmParams& p, const Smem& sm, uint32_t tile, int r, int c0,
-                               const float (&acc)[16]) {
+// With have_h the residual-stream values of these columns were loaded
+// beforehand (hv); otherwise the residual epilogue loads them.
+__device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t tile, int r, int c0,
+                                 const float (&acc)[16], const float (&hv_in)[16], bool have_h) {
   const int f = static_cast<int>(tile) * kTileN + r;  // weight row = output feature
   const int e = threadIdx.x - kEpiFirstThread;
   float v[16];
@@ -171,7 +173,7 @@ __device__ void epilogue_chunk(const GemmParams& p, const Smem& sm, uint32_t til
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int m = p.tok0 + c0 + j;
-      hv[j] = (m < p.M && fok) ? ldcg(p.h + static_cast<long long>(m) * p.d + f) : 0.f;
+      hv[j] = have_h ? hv_in[j] : ((m < p.M && fok) ? ldcg(p.h + static_cast<long long>(m) * p.d + f) : 0.f);
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -285,6 +287,12 @@ __device__ void epilogue_chunk(const GemmParams& p, const Smem& sm, uint32_t til
     }
   }
   named_bar(kEpiBar, kEpiThreads);
+}
+
+__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Smem& sm, uint32_t tile, int r,
+                                               int c0, const float (&acc)[16]) {
+  const float none[16] = {};
+  epilogue_chunk_h(p, sm, tile, r, c0, acc, none, false);
 }
 
 }  // namespace
