@@ -5,6 +5,8 @@
   spec_verify_forward, then a gamma=4 pass is verified; every logit of every
   pass is compared with the fp64 oracle running on its own weights and cache;
   accept + rollback follow, then a second pass is compared again.
+* Batched workload at the 1B shape (batch 16 and 64, ragged cached lengths,
+  T 0.8, top-p 0.9): logits, accept and rollback against the oracle.
 * 8B-shaped decoder (32 layers, d 4096, 32/8 heads of 128, SwiGLU 14336,
   vocab 128256) with 2048 cached tokens, the launch configuration the
   benchmark times: properties that hold at any size (one pass over gamma+1
@@ -191,3 +193,97 @@ def test_8b_pass_matches_oracle(big):
     z = _run(cfg, m, kv, ws, toks).double().cpu().numpy()
     ref = OM.forward(ocfg, W, toks, okv)
     assert _rel(z, ref) <= 1e-2, _rel(z, ref)
+
+
+def _batched_topp(B, steps, seed, lo, hi):
+    """The batched workload (ragged cached lengths ~ U{lo..hi}, capacity
+    hi+16, gamma 4, T 0.8, top-p 0.9 on p and q; draft logits independent
+    N(0, 2^2), so that no device output enters the oracle) at the 1B shape:
+    every logit of every pass against the fp64 oracle on its own weights and
+    the same cache bytes; the accept kernel against the oracle on identical
+    (oracle) logits, and end to end outside margins widened to the logits
+    tolerance; rollback by the oracle's decisions."""
+    cfg = sb.LLAMA_1B
+    gamma, T, top_p, cap = 4, 0.8, 0.9, hi + 16
+    n = gamma + 1
+    ocfg = OM.Config(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn, cfg.vocab)
+    lens = wl.context_lengths(seed, B, lo, hi)
+    Lmax = int(lens.max())
+    m = sb.Model(cfg, seed)
+    kv = sb.KVCache(cfg, B, cap)
+    W = OW.Weights(ocfg, seed)
+    okv = OM.KVState(ocfg, B, cap)
+    K, V = wl.kv_prefix(seed, cfg.n_layers, B, cfg.n_kv_heads, Lmax, cfg.head_dim)
+    from oracle.bf16 import from_bits
+    okv.load_prefix([from_bits(K[l]) for l in range(cfg.n_layers)],
+                    [from_bits(V[l]) for l in range(cfg.n_layers)], lens)
+    kv.k[:, :, :, :Lmax].copy_(torch.from_numpy(K.view(np.int16)).view(torch.bfloat16))
+    kv.v[:, :, :, :Lmax].copy_(torch.from_numpy(V.view(np.int16)).view(torch.bfloat16))
+    del K, V
+    kv.len.copy_(torch.from_numpy(lens))
+    ws = sb.workspace(sb.spec_workspace_bytes(cfg, B, gamma, cap))
+    aws = sb.workspace(sb.spec_accept_workspace_bytes(B, gamma, cfg.vocab))
+    t_last = wl.tokens(seed + 1, B, 1, cfg.vocab)[:, 0]
+    excused = 0
+    for step in range(steps):
+        x = np.zeros((B, gamma), np.int32)
+        q = np.zeros((B, gamma, cfg.vocab), np.float32)
+        ud = wl.uniforms(seed + 10 * step, B, gamma, stream=8)
+        # drafts from independent noisy logits (no device output enters the oracle)
+        zq = wl.gauss(seed + 10 * step, (B, gamma, cfg.vocab), 2.0)
+        for b in range(B):
+            qs, ts, _ = OA.draft_sample(zq[b], ud[b], T, top_p)
+            q[b] = qs.astype(np.float32)
+            x[b] = ts
+        block = np.concatenate([t_last[:, None], x], axis=1).astype(np.int32)
+        z = torch.empty(B, n, cfg.vocab, device="cuda")
+        sb.spec_verify_forward(m.handle, torch.from_numpy(block).cuda(), B, gamma, kv, z, ws)
+        st, bits = sb.spec_device_status(ws)
+        assert st == sb.SPEC_OK, hex(bits)
+        zd = z.double().cpu().numpy()
+        ref = OM.forward(ocfg, W, block, okv)
+        assert _rel(zd, ref) <= 1e-2, (step, _rel(zd, ref))
+        np.testing.assert_array_equal(kv.len.cpu().numpy(), okv.lens)
+        u = wl.uniforms(seed + 10 * step, B, n)
+        # accept on identical (oracle) fp32 logits: exact except boundary cases
+        ref32 = ref.astype(np.float32)
+        out = torch.empty(B, n, dtype=torch.int32, device="cuda")
+        nacc = torch.empty(B, dtype=torch.int32, device="cuda")
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        sb.spec_accept(dev(ref32), dev(q), dev(x), dev(u), B, gamma, cfg.vocab, T, top_p, out, nacc, aws)
+        o, na = out.cpu().numpy(), nacc.cpu().numpy()
+        oracle_n = np.zeros(B, np.int32)
+        for b in range(B):
+            r = OA.accept(ref32[b], q[b], x[b], u[b], T, top_p)
+            oracle_n[b] = r.n_accepted
+            if not (int(na[b]) == r.n_accepted and o[b].tolist() == r.tokens):
+                assert r.boundary, (step, b)
+                excused += 1
+        # end to end: the device's accept on the device's logits
+        sb.spec_accept(z, dev(q), dev(x), dev(u), B, gamma, cfg.vocab, T, top_p, out, nacc, aws)
+        o2, na2 = out.cpu().numpy(), nacc.cpu().numpy()
+        for b in range(B):
+            r = OA.accept(ref32[b], q[b], x[b], u[b], T, top_p, margins=(5e-3, 5e-3, 5e-3))
+            if not r.boundary:
+                assert int(na2[b]) == r.n_accepted and o2[b].tolist() == r.tokens, (step, b)
+        # roll both caches back by the oracle's decisions; emitted token = next t_last
+        sb.spec_kv_truncate(kv, dev(oracle_n), gamma, ws)
+        okv.lens = OM.truncate(okv.lens, oracle_n, gamma)
+        np.testing.assert_array_equal(kv.len.cpu().numpy(), okv.lens)
+        t_last = np.array([OA.accept(ref32[b], q[b], x[b], u[b], T, top_p).tokens[oracle_n[b]]
+                           for b in range(B)], np.int32)
+    assert excused <= max(1, 0.001 * B * steps), excused
+    m.close()
+
+
+def test_batched_topp_workload_b16_two_steps():
+    """Batch 16, cached lengths U{512..4096} (80 token rows: the persistent
+    kernel), two verify steps."""
+    _batched_topp(16, 2, 2016, 512, 4096)
+
+
+def test_batched_topp_workload_b64():
+    """Batch 64 (320 token rows: one kernel per step), cached lengths
+    U{512..1024} (the oracle's fp64 cache at 4096 slots would need ~34 GB of
+    host memory), one verify step."""
+    _batched_topp(64, 1, 2064, 512, 1024)
