@@ -287,16 +287,66 @@ SPEC_DEVINL void embed_phase(const MkParams& P, const MkSmem& sm) {
     }
     const uint16_t* row = P.embed + static_cast<long long>(tok) * P.d;
     float sq = 0.f;
-    for (int i = 0; i < fpt; ++i) {
-      const int f = e * fpt + i;
-      const float x = bf16_to_f32(row[f]);
-      const long long idx = static_cast<long long>(m) * P.d + f;
-      P.h[idx] = x;
-      const float y = x * P.g_attn0[f];
-      const uint16_t hi = f32_to_bf16(y);
-      P.hb[idx] = hi;
-      P.hb_lo[idx] = f32_to_bf16(y - bf16_to_f32(hi));
-      sq += x * x;
+    if (fpt % 8 == 0) {
+      // batches of up to 32 features: every load issued before any store
+      // (the stores could alias the loads, which would serialise them)
+      for (int i0 = 0; i0 < fpt; i0 += 32) {
+        const int nck = min(32, fpt - i0) / 8;
+        uint4 raw[4];
+        float4 gg[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (c < nck) {
+            const int f = e * fpt + i0 + c * 8;
+            raw[c] = __ldg(reinterpret_cast<const uint4*>(row + f));
+            gg[2 * c] = __ldg(reinterpret_cast<const float4*>(P.g_attn0 + f));
+            gg[2 * c + 1] = __ldg(reinterpret_cast<const float4*>(P.g_attn0 + f + 4));
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (c < nck) {
+            const int f = e * fpt + i0 + c * 8;
+            const long long idx = static_cast<long long>(m) * P.d + f;
+            const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+            const float g[8] = {gg[2 * c].x, gg[2 * c].y, gg[2 * c].z, gg[2 * c].w,
+                                gg[2 * c + 1].x, gg[2 * c + 1].y, gg[2 * c + 1].z, gg[2 * c + 1].w};
+            float x[8];
+            uint32_t hi2[4], lo2[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              x[2 * k] = bf16lo(w[k]);
+              x[2 * k + 1] = bf16hi(w[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float y0 = x[2 * k] * g[2 * k], y1 = x[2 * k + 1] * g[2 * k + 1];
+              const uint16_t b0 = f32_to_bf16(y0), b1 = f32_to_bf16(y1);
+              hi2[k] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
+              const uint16_t l0 = f32_to_bf16(y0 - bf16_to_f32(b0)), l1 = f32_to_bf16(y1 - bf16_to_f32(b1));
+              lo2[k] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sq += x[k] * x[k];
+            *reinterpret_cast<float4*>(P.h + idx) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(P.h + idx + 4) = make_float4(x[4], x[5], x[6], x[7]);
+            *reinterpret_cast<uint4*>(P.hb + idx) = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
+            *reinterpret_cast<uint4*>(P.hb_lo + idx) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+          }
+        }
+      }
+    } else {
+      for (int i = 0; i < fpt; ++i) {
+        const int f = e * fpt + i;
+        const float x = bf16_to_f32(row[f]);
+        const long long idx = static_cast<long long>(m) * P.d + f;
+        P.h[idx] = x;
+        const float y = x * P.g_attn0[f];
+        const uint16_t hi = f32_to_bf16(y);
+        P.hb[idx] = hi;
+        P.hb_lo[idx] = f32_to_bf16(y - bf16_to_f32(hi));
+        sq += x * x;
+      }
     }
     sm.sq[e] = sq;
     named_bar(kArriveBar, kEpiThreads);
@@ -457,18 +507,14 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
     // the first block of the CTA's first unit was prefetched except the rows
     // this pass wrote; they are in flight while q is staged
     att_load_block<HD>(sK, kc, vc, head_base, kbeg, kend, Lb, unit == static_cast<int>(blockIdx.x) ? 2 : 0, e);
-    // ---- stage q (hi, lo) rows
+    // ---- stage q (hi, lo) rows with async copies (zero rows past R)
     for (int idx = e; idx < 32 * kCPR; idx += kEpiThreads) {
       const int r = idx / kCPR, c = idx % kCPR;
-      uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
-      if (r < R) {
-        const int j = r / G, g = r % G;
-        const long long off = (static_cast<long long>(b) * P.n + j) * qdim + (kvh * G + g) * HD + c * 8;
-        hi = __ldcg(reinterpret_cast<const uint4*>(P.q + off));
-        lo = __ldcg(reinterpret_cast<const uint4*>(P.q_lo + off));
-      }
-      *reinterpret_cast<uint4*>(sQ + swz<HD>(r, c)) = hi;
-      *reinterpret_cast<uint4*>(sQlo + swz<HD>(r, c)) = lo;
+      const bool valid = r < R;
+      const int j = valid ? r / G : 0, g = valid ? r % G : 0;
+      const long long off = (static_cast<long long>(b) * P.n + j) * qdim + (kvh * G + g) * HD + c * 8;
+      cp_async16(aQ + swz<HD>(r, c), P.q + off, valid ? 16 : 0);
+      cp_async16(aQlo + swz<HD>(r, c), P.q_lo + off, valid ? 16 : 0);
     }
     float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
     float oacc[HD / 8][4];

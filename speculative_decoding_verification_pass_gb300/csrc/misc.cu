@@ -47,6 +47,15 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedParams p) {
       const uint4 a = *reinterpret_cast<const uint4*>(row + f0);
       const uint4 c = *reinterpret_cast<const uint4*>(row + f0 + 8);
       const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+      float g[16];  // gains loaded before any store (the stores could alias them)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(p.g0 + f0) + k);
+        g[4 * k] = v.x;
+        g[4 * k + 1] = v.y;
+        g[4 * k + 2] = v.z;
+        g[4 * k + 3] = v.w;
+      }
       float* h = p.h + static_cast<long long>(m) * p.d + f0;
       uint16_t* hb = p.hb + static_cast<long long>(m) * p.d + f0;
 #pragma unroll
@@ -54,7 +63,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedParams p) {
         const float lo = bf16lo(w[k]), hi = bf16hi(w[k]);
         h[2 * k] = lo;
         h[2 * k + 1] = hi;
-        const float x0 = lo * p.g0[f0 + 2 * k], x1 = hi * p.g0[f0 + 2 * k + 1];
+        const float x0 = lo * g[2 * k], x1 = hi * g[2 * k + 1];
         const uint16_t b0 = f32_to_bf16(x0), b1 = f32_to_bf16(x1);
         hb[2 * k] = b0;
         hb[2 * k + 1] = b1;
