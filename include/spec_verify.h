@@ -20,7 +20,13 @@
  *              rule, the worked example, the reference generation loop.
  *   [engine]   "Build a Speculative Decoding Engine to Cut LLM Latency by 3x":
  *              The Accept/Reject Mechanism, KV Cache Management for Dual
- *              Models, Rollback Protocol, Batch-Level Speculation.
+ *              Models, Rollback Protocol, Batch-Level Speculation,
+ *              Speculation Depth Tuning and Tree Drafting.
+ *   [aci]      "Speculative Decoding: Speeding Sequential Generation":
+ *              Tree-Based Drafting, Constructing the Tree Attention Mask in
+ *              Code, Expected Tokens per Verification Round: Chain vs. Tree.
+ *   [kishorek] "Speculative Decoding: How to Make an LLM 3x Faster...":
+ *              verifying a whole tree in one pass.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -66,6 +72,7 @@ typedef enum {
 #define SPEC_DEV_Q_ZERO        0x4   /* q(x_i) <= 0 for a drafted token (treated as a rejection) */
 #define SPEC_DEV_TIMEOUT       0x8   /* a bounded wait in a kernel gave up */
 #define SPEC_DEV_BAD_NACC      0x10  /* truncate: n_accepted outside [0, gamma] */
+#define SPEC_DEV_BAD_TREE      0x20  /* tree accept / commit: bad parents, path or n_accepted */
 
 /* Text for a spec_status value (static storage). */
 const char* spec_status_string(int status);
@@ -260,6 +267,99 @@ int spec_draft_sample(const float* d_logits, int rows, int vocab, float temperat
  * the forward's or the accept's workspace). */
 int spec_kv_truncate(const spec_kv_cache* kv, const int32_t* d_n_accepted, int gamma, void* d_ws,
                      void* stream);
+
+/* ------------------------------------------------------------ draft trees */
+/* Verification of a draft TREE instead of a chain ([aci] Tree-Based Drafting;
+ * [engine] Speculation Depth Tuning and Tree Drafting): several candidates
+ * per position, all scored by one target pass.  A tree of n_nodes <= 64
+ * nodes (else SPEC_ESIZE) is given by parent pointers: node 0 is the root --
+ * the previous pass's emitted token, not yet in the cache -- with parent -1,
+ * and node i > 0 has a parent p(i) < i (parents are listed before their
+ * children).  A chain of gamma drafts is the tree parents = [-1, 0, 1, ..,
+ * gamma-1], and every tree call below then computes what the chain call
+ * computes. */
+
+/* Host-only (no device access): the attention mask and rotary positions of a
+ * tree ([aci] Constructing the Tree Attention Mask in Code).  For each node i
+ * out_anc[i] has bit j set iff node j is i itself or one of its ancestors
+ * (node i sees the cached prefix and exactly those new slots) and
+ * out_depth[i] is its depth (root 0), its rotary position offset.  Returns
+ * SPEC_EINVAL for parents[0] != -1 or any parents[i] outside [0, i), and
+ * SPEC_ESIZE for n_nodes > 64. */
+int spec_tree_masks(const int32_t* parents, int n_nodes, uint64_t* out_anc, int32_t* out_depth);
+
+/* One verification forward over a tree per sequence.
+ *   d_tokens  int32 [batch][n_nodes] node tokens (node 0 the root).
+ *   d_anc     uint64 [batch][n_nodes] ancestor masks (spec_tree_masks),
+ *   d_depth   int32 [batch][n_nodes] depths; each sequence may have its own
+ *             tree of the same node count.
+ *   kv        node i's key / value goes to the flattened slot len[b] + i,
+ *             rotated at position len[b] + depth(i); len[b] += n_nodes.
+ *   d_logits  fp32 [batch][n_nodes][vocab]: row i scores the token after
+ *             node i (its children's target distribution).
+ * Workspace, limits, schedules and device errors as spec_verify_forward with
+ * gamma = n_nodes - 1 (the persistent schedule applies when n_nodes x query
+ * heads per KV head <= 32).  The masks and depths are not checked on the
+ * device: a mask bit at or above n_nodes is ignored, and a node whose mask
+ * lacks its own bit does not see itself. */
+int spec_verify_forward_tree(const spec_model* model, const int32_t* d_tokens,
+                             const uint64_t* d_anc, const int32_t* d_depth, int batch,
+                             int n_nodes, const spec_kv_cache* kv, float* d_logits, void* d_ws,
+                             size_t ws_bytes, void* stream);
+
+/* Workspace bytes for spec_tree_accept: the status word and one fp32
+ * vocabulary row per sequence (the current residual distribution). */
+size_t spec_tree_accept_workspace_bytes(int batch, int vocab);
+
+/* The acceptance walk over each sequence's tree ([aci] Tree-Based Drafting:
+ * the accept/reject test applied per node; [kishorek] accept the longest
+ * valid root-to-node path), one CTA per sequence.  Starting at the root, at
+ * the current node c with target distribution p' (softmax(z_c / T) after
+ * top-p) the children are tried in index order: child j (token x_j) is
+ * accepted iff u_j < min(1, p'(x_j) / q_c(x_j)); after each rejected child p'
+ * becomes norm(max(0, p' - q_c)) (unchanged when that mass is <= 1e-8).  The
+ * first accepted child becomes the current node; when no child is accepted
+ * (or c is a leaf) one token is drawn from p' with u_0 by the inverse CDF in
+ * id order and the walk ends.  Siblings are independent draws from their
+ * parent's q, so the emitted tokens follow the target exactly as in the
+ * chain rule, which is the case of one child per node.
+ *   d_target_logits fp32 [batch][n_nodes][vocab] (spec_verify_forward_tree)
+ *   d_draft_probs   fp32 [batch][n_nodes][vocab]: row c is the distribution
+ *                   node c's children were drawn from (after the same T /
+ *                   top-p); rows of leaves are not read.  Unused at T = 0.
+ *   d_node_tokens   int32 [batch][n_nodes]; d_parents int32 [batch][n_nodes].
+ *   d_uniforms      fp32 [batch][n_nodes] in [0,1): u_j (j >= 1) is the coin
+ *                   of node j, u_0 drives the final draw.  Unused at T = 0.
+ *   temperature     >= 0; 0 is greedy: move to the first child whose token is
+ *                   the argmax (lowest id on ties), else emit the argmax.
+ *   d_out_tokens    int32 [batch][n_nodes]: the accepted nodes' tokens, the
+ *                   emitted token, then -1.
+ *   d_out_path      int32 [batch][n_nodes]: the accepted nodes (root
+ *                   excluded) in depth order, then -1.
+ *   d_n_accepted    int32 [batch]: accepted nodes m (the round emits m + 1).
+ * A sequence whose parents are not a valid tree sets SPEC_DEV_BAD_TREE and
+ * gets m = 0 and no tokens (-1); a child token outside [0, V) or with
+ * q_c(x) <= 0 is a rejection and sets SPEC_DEV_BAD_TOKEN / SPEC_DEV_Q_ZERO. */
+int spec_tree_accept(const float* d_target_logits, const float* d_draft_probs,
+                     const int32_t* d_node_tokens, const int32_t* d_parents,
+                     const float* d_uniforms, int batch, int n_nodes, int vocab, float temperature,
+                     float top_p, int32_t* d_out_tokens, int32_t* d_out_path,
+                     int32_t* d_n_accepted, void* d_ws, size_t ws_bytes, void* stream);
+
+/* The tree round's KV commit, run after spec_tree_accept (the tree
+ * counterpart of spec_kv_truncate; [engine] Rollback Protocol): with
+ * L0 = len[b] - n_nodes, the accepted path's keys / values move from the
+ * flattened slots L0 + path[d-1] to L0 + d (d = 1 .. m, every layer and KV
+ * head), and len[b] = L0 + 1 + m, so the root and the accepted path are
+ * contiguous and the other nodes' slots are dropped.
+ *   d_path, d_n_accepted  spec_tree_accept's outputs.
+ *   kv->k, kv->v          16-byte aligned.
+ * A path that is not strictly increasing within [1, n_nodes) or an m outside
+ * [0, n_nodes) leaves the sequence unchanged and sets SPEC_DEV_BAD_TREE; a
+ * length below n_nodes or above the capacity sets SPEC_DEV_KV_OVERFLOW.
+ * d_ws is any workspace of this library (its status word is used). */
+int spec_kv_tree_commit(const spec_model* model, const spec_kv_cache* kv, const int32_t* d_path,
+                        const int32_t* d_n_accepted, int n_nodes, void* d_ws, void* stream);
 
 /* ----------------------------------------------------------------- status */
 /* Synchronise `stream`, read the device status word of workspace d_ws into

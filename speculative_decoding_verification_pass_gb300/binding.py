@@ -18,7 +18,8 @@ from . import _build
 
 SPEC_OK, SPEC_EINVAL, SPEC_ESIZE, SPEC_ECUDA, SPEC_EDEVICE, SPEC_ETIMEOUT, SPEC_ENOTSUP = (
     0, -1, -2, -3, -4, -5, -6)
-DEV_BAD_TOKEN, DEV_KV_OVERFLOW, DEV_Q_ZERO, DEV_TIMEOUT, DEV_BAD_NACC = 0x1, 0x2, 0x4, 0x8, 0x10
+DEV_BAD_TOKEN, DEV_KV_OVERFLOW, DEV_Q_ZERO, DEV_TIMEOUT, DEV_BAD_NACC, DEV_BAD_TREE = (
+    0x1, 0x2, 0x4, 0x8, 0x10, 0x20)
 
 
 class SpecError(RuntimeError):
@@ -65,6 +66,13 @@ _SIGS = {
     "spec_accept": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _F, _P, _P, _P, _SZ, _P]),
     "spec_draft_sample": (_I, [_P, _I, _I, _F, _F, _P, _P, _P, _P, _SZ, _P]),
     "spec_kv_truncate": (_I, [ctypes.POINTER(spec_kv_cache), _P, _I, _P, _P]),
+    "spec_tree_masks": (_I, [ctypes.POINTER(ctypes.c_int32), _I, ctypes.POINTER(ctypes.c_uint64),
+                             ctypes.POINTER(ctypes.c_int32)]),
+    "spec_verify_forward_tree": (_I, [_P, _P, _P, _P, _I, _I, ctypes.POINTER(spec_kv_cache), _P, _P,
+                                      _SZ, _P]),
+    "spec_tree_accept_workspace_bytes": (_SZ, [_I, _I]),
+    "spec_tree_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _F, _P, _P, _P, _P, _SZ, _P]),
+    "spec_kv_tree_commit": (_I, [_P, ctypes.POINTER(spec_kv_cache), _P, _P, _I, _P, _P]),
     "spec_device_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "spec_timing_enable": (_I, [_P, _I]),
     "spec_timing_read": (_I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
@@ -219,6 +227,44 @@ def spec_draft_sample(logits, rows: int, vocab: int, temperature: float, top_p: 
 def spec_kv_truncate(kv: "KVCache", n_accepted, gamma: int, ws, stream=None):
     _check(lib().spec_kv_truncate(ctypes.byref(kv.c()), _ptr(n_accepted), gamma, _ptr(ws),
                                   _stream(stream)), "spec_kv_truncate")
+
+
+def spec_tree_masks(parents) -> tuple[list, list]:
+    """(ancestor masks, depths) of a tree given by parent pointers (host only)."""
+    n = len(parents)
+    par = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in parents])
+    anc = (ctypes.c_uint64 * max(n, 1))()
+    depth = (ctypes.c_int32 * max(n, 1))()
+    _check(lib().spec_tree_masks(par, n, anc, depth), "spec_tree_masks")
+    return list(anc)[:n], list(depth)[:n]
+
+
+def spec_verify_forward_tree(handle: int, tokens, anc, depth, batch: int, n_nodes: int,
+                             kv: "KVCache", logits, ws, stream=None):
+    _check(lib().spec_verify_forward_tree(handle, _ptr(tokens), _ptr(anc), _ptr(depth), batch,
+                                          n_nodes, ctypes.byref(kv.c()), _ptr(logits), _ptr(ws),
+                                          ws.numel(), _stream(stream)),
+           "spec_verify_forward_tree")
+
+
+def spec_tree_accept_workspace_bytes(batch: int, vocab: int) -> int:
+    return int(lib().spec_tree_accept_workspace_bytes(batch, vocab))
+
+
+def spec_tree_accept(target_logits, draft_probs, node_tokens, parents, uniforms, batch: int,
+                     n_nodes: int, vocab: int, temperature: float, top_p: float, out_tokens,
+                     out_path, n_accepted, ws, stream=None):
+    _check(lib().spec_tree_accept(_ptr(target_logits), _ptr(draft_probs), _ptr(node_tokens),
+                                  _ptr(parents), _ptr(uniforms), batch, n_nodes, vocab,
+                                  temperature, top_p, _ptr(out_tokens), _ptr(out_path),
+                                  _ptr(n_accepted), _ptr(ws), ws.numel(), _stream(stream)),
+           "spec_tree_accept")
+
+
+def spec_kv_tree_commit(handle: int, kv: "KVCache", path, n_accepted, n_nodes: int, ws,
+                        stream=None):
+    _check(lib().spec_kv_tree_commit(handle, ctypes.byref(kv.c()), _ptr(path), _ptr(n_accepted),
+                                     n_nodes, _ptr(ws), _stream(stream)), "spec_kv_tree_commit")
 
 
 def spec_device_status(ws, stream=None) -> tuple[int, int]:

@@ -305,8 +305,8 @@ SPEC_DEVINL unsigned long long warp_incl_scan_u64(unsigned long long v) {
 
 // Inverse-CDF draw: the smallest id t with sum_{x<=t} fx(x) > floor(u * total).
 // `total` is the exact fixed-point sum; `last_pos` the last id with fx > 0.
-__device__ int draw(const DrawWeights& dw, int V, float u, unsigned long long total,
-                    int last_pos, Red& r) {
+template <class DW>
+__device__ int draw(const DW& dw, int V, float u, unsigned long long total, int last_pos, Red& r) {
   const unsigned long long thr =
       static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(total));
   unsigned long long run = 0;  // exact prefix before the current tile
@@ -355,7 +355,8 @@ __device__ int draw(const DrawWeights& dw, int V, float u, unsigned long long to
 }
 
 // Exact fixed-point total and last positive id of the draw weights.
-__device__ void weights_total(const DrawWeights& dw, int V, Red& r, unsigned long long& total,
+template <class DW>
+__device__ void weights_total(const DW& dw, int V, Red& r, unsigned long long& total,
                               int& last_pos) {
   unsigned long long s = 0;
   int lp = -1;
@@ -1067,6 +1068,238 @@ __global__ void __launch_bounds__(kT, 1) sample_kernel(const SampleParams p) {
   if (threadIdx.x == 0) p.tokens[row] = t < 0 ? 0 : t;
 }
 
+// ------------------------------------------------------------- tree accept
+// The acceptance walk over one sequence's draft tree ("Speculative Decoding:
+// Speeding Sequential Generation", Tree-Based Drafting: the accept/reject test
+// applied per node), one CTA per sequence.  At the current node the children
+// are tried in index order with the node's target distribution p' (after T /
+// top-p): child c is accepted iff u[c] < min(1, p'(x_c) / q(x_c)), q being the
+// distribution the siblings were drawn from; after each rejected child p' is
+// replaced by norm(max(0, p' - q)) (kept when that mass is <= 1e-8).  The
+// first accepted child becomes the current node; when none is (or the node is
+// a leaf) one token is drawn from p' with u[0] and the walk ends.  T = 0: move
+// to the first child whose token is the argmax, else emit the argmax.
+//
+// p' starts as the softmax row itself (recomputed from the logits); the first
+// residual is materialised in pbuf (fp32) and later residuals replace it in
+// place.  Sums and the draw use the same 2^-52 fixed-point weights as the
+// chain rule.
+
+// Draw weights of the tree walk: p' (the row, or pbuf once materialised),
+// minus q for a residual.
+struct TreeWeights {
+  RowDist p;
+  const float* pb;  // materialised p', or nullptr
+  const float* q;   // residual against q, or nullptr
+  SPEC_DEVINL float base(int x) const { return pb ? __ldcg(pb + x) : p.p(x); }
+  SPEC_DEVINL float w(int x) const {
+    const float v = base(x);
+    return q ? fmaxf(v - __ldcg(q + x), 0.f) : v;
+  }
+  SPEC_DEVINL unsigned long long fx(int x) const {
+    return static_cast<unsigned long long>(w(x) * kFix52);
+  }
+};
+
+__global__ void __launch_bounds__(kT, 1) tree_accept_kernel(const TreeAcceptParams p) {
+  __shared__ Red red;
+  __shared__ int s_flag;
+  const int b = blockIdx.x;
+  const int n = p.n, V = p.V;
+  const long long row0 = static_cast<long long>(b) * n;
+  const float* zb = p.logits + row0 * V;
+  const int32_t* tok = p.tokens + row0;
+  const int32_t* par = p.parents + row0;
+  int32_t* out = p.out + row0;
+  int32_t* path = p.path + row0;
+  for (int i = threadIdx.x; i < n; i += kT) {
+    out[i] = -1;
+    path[i] = -1;
+  }
+  if (threadIdx.x == 0) {
+    bool ok = __ldg(par) == -1;
+    for (int i = 1; i < n; ++i) {
+      const int pi = __ldg(par + i);
+      ok = ok && pi >= 0 && pi < i;
+    }
+    if (!ok) {
+      set_status(p.status, SPEC_DEV_BAD_TREE);
+      p.n_acc[b] = 0;
+    }
+    s_flag = ok;
+  }
+  __syncthreads();
+  if (!s_flag) return;
+
+  int cur = 0, m = 0;
+  if (p.T == 0.f) {
+    for (;;) {
+      const int a = row_argmax(zb + static_cast<long long>(cur) * V, V, red);
+      if (threadIdx.x == 0) {
+        int nxt = -1;
+        for (int c = cur + 1; c < n && nxt < 0; ++c)
+          if (__ldg(par + c) == cur && __ldg(tok + c) == a) nxt = c;
+        out[m] = a;
+        if (nxt >= 0) path[m] = nxt;
+        else p.n_acc[b] = m;
+        s_flag = nxt;
+      }
+      __syncthreads();
+      if (s_flag < 0) return;
+      cur = s_flag;
+      ++m;
+    }
+  }
+
+  const float* ub = p.u + row0;
+  float* pb = p.pbuf + static_cast<long long>(b) * V;
+  for (;;) {
+    const float* qrow = p.q + (row0 + cur) * V;
+    TreeWeights tw;
+    tw.p = make_dist(zb + static_cast<long long>(cur) * V, V, p.T, p.top_p, red);
+    tw.pb = nullptr;
+    tw.q = nullptr;
+    int nxt = -1;
+    for (int c = cur + 1; c < n; ++c) {
+      if (__ldg(par + c) != cur) continue;
+      if (threadIdx.x == 0) {
+        const int x = __ldg(tok + c);
+        bool accept = false;
+        if (x < 0 || x >= V) {
+          set_status(p.status, SPEC_DEV_BAD_TOKEN);
+        } else {
+          const float qx = __ldcg(qrow + x);
+          if (!(qx > 0.f)) {
+            set_status(p.status, SPEC_DEV_Q_ZERO);
+          } else {
+            const float a = fminf(1.0f, tw.base(x) / qx);
+            accept = __ldg(ub + c) < a;
+          }
+        }
+        s_flag = accept;
+      }
+      __syncthreads();
+      if (s_flag) {
+        nxt = c;
+        break;
+      }
+      // rejected: p' <- norm(max(0, p' - q)) unless that mass is ~0
+      tw.q = qrow;
+      unsigned long long total;
+      int last_pos;
+      weights_total(tw, V, red, total, last_pos);
+      if (static_cast<double>(total) > kResidualFallback * 4503599627370496.0) {
+        const float inv = static_cast<float>(4503599627370496.0 / static_cast<double>(total));
+        for (int x = threadIdx.x; x < V; x += kT) pb[x] = tw.w(x) * inv;
+        __syncthreads();
+        tw.pb = pb;
+      }
+      tw.q = nullptr;
+    }
+    if (nxt >= 0) {
+      if (threadIdx.x == 0) {
+        path[m] = nxt;
+        out[m] = __ldg(tok + nxt);
+      }
+      cur = nxt;
+      ++m;
+      continue;
+    }
+    unsigned long long total;
+    int last_pos;
+    weights_total(tw, V, red, total, last_pos);
+    const int t = draw(tw, V, __ldg(ub), total, last_pos, red);
+    if (threadIdx.x == 0) {
+      out[m] = t < 0 ? 0 : t;
+      p.n_acc[b] = m;
+    }
+    return;
+  }
+}
+
+// ------------------------------------------------------------- tree commit
+// Moves the accepted path's keys / values from the flattened slots L0 + node
+// to L0 + 1 .. L0 + m (depth order); one CTA per (layer, sequence, KV head).
+// A destination may be the source of an earlier path entry (path [2, 5]
+// reads slot 2 and writes it), so every source row is loaded before any row
+// is stored.
+constexpr int kCommitThreads = 256;
+constexpr int kCommitPer = 8;  // uint4 per thread: 64 nodes x (K, V) x 128 dims / 256 threads
+
+SPEC_DEVINL bool tree_path_ok(const int32_t* path, int m, int n) {
+  int prev = 0;
+  for (int d = 0; d < m; ++d) {
+    const int s = __ldg(path + d);
+    if (s <= prev || s >= n) return false;
+    prev = s;
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kCommitThreads) tree_commit_kernel(const TreeCommitParams p) {
+  const int layer = blockIdx.y;
+  const int b = blockIdx.x / p.Hkv, h = blockIdx.x % p.Hkv;
+  const int n = p.n;
+  const int m = __ldg(p.n_acc + b);
+  const int len = p.len[b];
+  const int L0 = len - n;
+  const int32_t* path = p.path + static_cast<long long>(b) * n;
+  if (m < 0 || m >= n || L0 < 0 || len > p.cap || !tree_path_ok(path, m, n)) return;
+  const long long base =
+      ((static_cast<long long>(layer) * p.B + b) * p.Hkv + h) * p.cap * p.hd;
+  const int vec = p.hd / 8;  // uint4 per row
+  const int per_side = m * vec;
+  uint4 r[kCommitPer];
+  int dst[kCommitPer];
+#pragma unroll
+  for (int k = 0; k < kCommitPer; ++k) {
+    const int e = threadIdx.x + k * kCommitThreads;  // over [side][depth][vec]
+    dst[k] = -1;
+    if (e < 2 * per_side) {
+      const int side = e / per_side, rem = e % per_side;
+      const int d = rem / vec, c = rem % vec;
+      const int src = __ldg(path + d);
+      if (src != d + 1) {
+        const uint4* s = reinterpret_cast<const uint4*>((side ? p.v : p.k) + base +
+                                                         static_cast<long long>(L0 + src) * p.hd) + c;
+        r[k] = *s;
+        dst[k] = e;
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kCommitPer; ++k) {
+    const int e = dst[k];
+    if (e < 0) continue;
+    const int side = e / per_side, rem = e % per_side;
+    const int d = rem / vec, c = rem % vec;
+    uint4* t = reinterpret_cast<uint4*>((side ? p.v : p.k) + base +
+                                        static_cast<long long>(L0 + d + 1) * p.hd) + c;
+    *t = r[k];
+  }
+}
+
+// len = L0 + 1 + m after the copies (a separate launch: the copies read len).
+__global__ void tree_len_kernel(int32_t* len, const int32_t* path, const int32_t* n_acc, int B,
+                                int n, int cap, int32_t* status) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int m = n_acc[b];
+  const int l = len[b];
+  if (m < 0 || m >= n || !tree_path_ok(path + static_cast<long long>(b) * n, m, n)) {
+    set_status(status, SPEC_DEV_BAD_TREE);
+    return;
+  }
+  if (l < n || l > cap) {
+    set_status(status, SPEC_DEV_KV_OVERFLOW);
+    return;
+  }
+  len[b] = l - n + 1 + m;
+}
+
 __global__ void truncate_kernel(int32_t* len, const int32_t* n_acc, int B, int gamma,
                                 int32_t* status) {
   grid_dep_wait();
@@ -1151,6 +1384,30 @@ cudaError_t launch_truncate(int32_t* len, const int32_t* n_acc, int B, int gamma
   void* args[] = {&len, const_cast<int32_t**>(&n_acc), &B, &gamma, &status};
   return launch_pdl(reinterpret_cast<const void*>(truncate_kernel), dim3((B + 127) / 128),
                     dim3(128), args, stream, pdl);
+}
+
+cudaError_t launch_tree_accept(const TreeAcceptParams& p, cudaStream_t stream) {
+  if (p.B == 0) return cudaSuccess;
+  tree_accept_kernel<<<p.B, kT, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tree_commit(const TreeCommitParams& p, cudaStream_t stream) {
+  if (p.B == 0) return cudaSuccess;
+  if (p.n > 1 && p.L > 0 && p.Hkv > 0) {
+    tree_commit_kernel<<<dim3(p.B * p.Hkv, p.L), kCommitThreads, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  int32_t* len = p.len;
+  const int32_t* path = p.path;
+  const int32_t* n_acc = p.n_acc;
+  int B = p.B, n = p.n, cap = p.cap;
+  int32_t* status = p.status;
+  void* args[] = {&len, const_cast<int32_t**>(&path), const_cast<int32_t**>(&n_acc), &B, &n, &cap,
+                  &status};
+  return launch_pdl(reinterpret_cast<const void*>(tree_len_kernel), dim3((B + 127) / 128),
+                    dim3(128), args, stream, true);
 }
 
 }  // namespace spec

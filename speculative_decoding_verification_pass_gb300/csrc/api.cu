@@ -509,9 +509,12 @@ size_t spec_workspace_bytes(const spec_model_config* cfg, int batch, int gamma, 
   return plan_ws(*cfg, batch, gamma, capacity).total;
 }
 
-int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch, int gamma,
-                        const spec_kv_cache* kv, float* d_logits, void* d_ws, size_t ws_bytes,
-                        void* stream) {
+// The verification forward; d_anc / d_depth describe a draft tree per
+// sequence (nullptr: the chain, node j at position len + j seeing new slots
+// 0..j).
+static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, const uint64_t* d_anc,
+                               const int32_t* d_depth, int batch, int gamma, const spec_kv_cache* kv,
+                               float* d_logits, void* d_ws, size_t ws_bytes, void* stream) {
   if (!m || !d_tokens || !kv || !d_logits || !d_ws) return SPEC_EINVAL;
   if (batch < 0 || gamma < 0) return SPEC_EINVAL;
   const spec_model_config& c = m->cfg;
@@ -605,6 +608,8 @@ int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch,
       Q.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));
       Q.embed = reinterpret_cast<const uint16_t*>(B + L.embed);
       Q.rope = reinterpret_cast<const float2*>(B + L.rope);
+      Q.anc = d_anc;
+      Q.depth = d_depth;
       Q.gfinal = reinterpret_cast<const float*>(B + L.gfinal);
       Q.g_attn0 = reinterpret_cast<const float*>(B + L.g_attn[0]);
       Q.g_mlp0 = reinterpret_cast<const float*>(B + L.g_mlp[0]);
@@ -704,6 +709,7 @@ int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch,
       p.pos_base = pos_base;
       p.seq_ok = seq_ok;
       p.rope = reinterpret_cast<const float2*>(B + L.rope);
+      p.depth = d_depth;
       p.n_per_seq = n;
       p.H = H;
       p.Hkv = Hkv;
@@ -721,6 +727,7 @@ int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch,
       a.o = o;
       a.o_lo = o_lo;
       a.pos_base = pos_base;
+      a.anc = d_anc;
       a.part_o = reinterpret_cast<float*>(W + P.apart_o);
       a.part_ml = reinterpret_cast<float*>(W + P.apart_ml);
       a.counters = counters + P.attn_counter0;
@@ -793,6 +800,41 @@ int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch,
     if (r) return r;
   }
   return SPEC_OK;
+}
+
+int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch, int gamma,
+                        const spec_kv_cache* kv, float* d_logits, void* d_ws, size_t ws_bytes,
+                        void* stream) {
+  return verify_forward_impl(m, d_tokens, nullptr, nullptr, batch, gamma, kv, d_logits, d_ws, ws_bytes,
+                             stream);
+}
+
+int spec_tree_masks(const int32_t* parents, int n_nodes, uint64_t* out_anc, int32_t* out_depth) {
+  if (!parents || !out_anc || !out_depth || n_nodes < 1) return SPEC_EINVAL;
+  if (n_nodes > kTreeMaxNodes) return SPEC_ESIZE;
+  if (parents[0] != -1) return SPEC_EINVAL;
+  for (int i = 1; i < n_nodes; ++i)
+    if (parents[i] < 0 || parents[i] >= i) return SPEC_EINVAL;
+  for (int i = 0; i < n_nodes; ++i) {
+    uint64_t mask = 0;
+    int depth = -1;
+    for (int j = i; j != -1; j = parents[j]) {
+      mask |= 1ull << j;
+      ++depth;
+    }
+    out_anc[i] = mask;
+    out_depth[i] = depth;
+  }
+  return SPEC_OK;
+}
+
+int spec_verify_forward_tree(const spec_model* m, const int32_t* d_tokens, const uint64_t* d_anc,
+                             const int32_t* d_depth, int batch, int n_nodes, const spec_kv_cache* kv,
+                             float* d_logits, void* d_ws, size_t ws_bytes, void* stream) {
+  if (!d_anc || !d_depth || n_nodes < 1) return SPEC_EINVAL;
+  if (n_nodes > kTreeMaxNodes) return SPEC_ESIZE;
+  return verify_forward_impl(m, d_tokens, d_anc, d_depth, batch, n_nodes - 1, kv, d_logits, d_ws,
+                             ws_bytes, stream);
 }
 
 int spec_lm_head(const spec_model* m, const uint16_t* d_hidden, int rows, float* d_logits,
@@ -989,6 +1031,73 @@ int spec_kv_truncate(const spec_kv_cache* kv, const int32_t* d_n_accepted, int g
   if (gamma < 0 || kv->batch < 0) return SPEC_EINVAL;
   SPEC_CUDA(launch_truncate(kv->len, d_n_accepted, kv->batch, gamma, static_cast<int32_t*>(d_ws),
                             static_cast<cudaStream_t>(stream), true));
+  return SPEC_OK;
+}
+
+size_t spec_tree_accept_workspace_bytes(int batch, int vocab) {
+  if (batch < 0 || vocab <= 0) return 0;
+  return 64 + align_up(static_cast<size_t>(batch) * static_cast<size_t>(vocab) * 4);
+}
+
+int spec_tree_accept(const float* d_target_logits, const float* d_draft_probs,
+                     const int32_t* d_node_tokens, const int32_t* d_parents,
+                     const float* d_uniforms, int batch, int n_nodes, int vocab, float temperature,
+                     float top_p, int32_t* d_out_tokens, int32_t* d_out_path,
+                     int32_t* d_n_accepted, void* d_ws, size_t ws_bytes, void* stream) {
+  int r = accept_common_checks(batch, 0, vocab, temperature, top_p);
+  if (r) return r;
+  if (n_nodes < 1) return SPEC_EINVAL;
+  if (n_nodes > kTreeMaxNodes) return SPEC_ESIZE;
+  if (!d_target_logits || !d_node_tokens || !d_parents || !d_out_tokens || !d_out_path ||
+      !d_n_accepted || !d_ws)
+    return SPEC_EINVAL;
+  if (temperature > 0.f && (!d_draft_probs || !d_uniforms)) return SPEC_EINVAL;
+  if (ws_bytes < spec_tree_accept_workspace_bytes(batch, vocab)) return SPEC_ESIZE;
+  if (reinterpret_cast<uintptr_t>(d_ws) % 16) return SPEC_EINVAL;
+  if (batch == 0) return SPEC_OK;
+  TreeAcceptParams p{};
+  p.logits = d_target_logits;
+  p.q = d_draft_probs;
+  p.tokens = d_node_tokens;
+  p.parents = d_parents;
+  p.u = d_uniforms;
+  p.pbuf = reinterpret_cast<float*>(static_cast<uint8_t*>(d_ws) + 64);
+  p.out = d_out_tokens;
+  p.path = d_out_path;
+  p.n_acc = d_n_accepted;
+  p.status = static_cast<int32_t*>(d_ws);
+  p.B = batch;
+  p.n = n_nodes;
+  p.V = vocab;
+  p.T = temperature;
+  p.top_p = top_p;
+  SPEC_CUDA(launch_tree_accept(p, static_cast<cudaStream_t>(stream)));
+  return SPEC_OK;
+}
+
+int spec_kv_tree_commit(const spec_model* m, const spec_kv_cache* kv, const int32_t* d_path,
+                        const int32_t* d_n_accepted, int n_nodes, void* d_ws, void* stream) {
+  if (!m || !kv || !kv->k || !kv->v || !kv->len || !d_path || !d_n_accepted || !d_ws)
+    return SPEC_EINVAL;
+  if (n_nodes < 1 || kv->batch < 0 || kv->capacity < 0) return SPEC_EINVAL;
+  if (n_nodes > kTreeMaxNodes) return SPEC_ESIZE;
+  if (reinterpret_cast<uintptr_t>(kv->k) % 16 || reinterpret_cast<uintptr_t>(kv->v) % 16)
+    return SPEC_EINVAL;
+  const spec_model_config& c = m->cfg;
+  TreeCommitParams p{};
+  p.k = static_cast<uint16_t*>(kv->k);
+  p.v = static_cast<uint16_t*>(kv->v);
+  p.len = kv->len;
+  p.path = d_path;
+  p.n_acc = d_n_accepted;
+  p.status = static_cast<int32_t*>(d_ws);
+  p.L = c.n_layers;
+  p.B = kv->batch;
+  p.Hkv = c.n_kv_heads;
+  p.hd = m->hd;
+  p.cap = kv->capacity;
+  p.n = n_nodes;
+  SPEC_CUDA(launch_tree_commit(p, static_cast<cudaStream_t>(stream)));
   return SPEC_OK;
 }
 

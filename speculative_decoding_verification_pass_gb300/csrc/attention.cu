@@ -146,14 +146,16 @@ __global__ void __launch_bounds__(kThreads) attn_splitkv_kernel(const AttnParams
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int r = qt * 16 + g8 + hr * 8;
-        const int qpos = r < R ? Lb + r / G : -1;
+        const bool rv = r < R;
+        const int jn = rv ? r / G : 0;
+        const uint64_t am = (p.anc && rv) ? __ldg(p.anc + static_cast<long long>(b) * p.n + jn) : 0ull;
         float mx = -INFINITY;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int kabs = k0 + kw0 + nt * 8 + t4 * 2 + e;
-            const bool ok = kabs < k0 + nk && kabs <= qpos;
+            const bool ok = rv && kabs < k0 + nk && key_visible(kabs, Lb, jn, p.anc, am);
             const float v = ok ? sacc[nt][hr * 2 + e] * p.scale_log2 : -INFINITY;
             sacc[nt][hr * 2 + e] = v;
             mx = fmaxf(mx, v);
@@ -493,7 +495,9 @@ __global__ void __launch_bounds__(kClusterThreads)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int r = qt * 16 + g8 + hr * 8;
-        const int qpos = r < R ? Lb + r / G : -1;
+        const bool rv = r < R;
+        const int jn = rv ? r / G : 0;
+        const uint64_t am = (p.anc && rv) ? __ldg(p.anc + static_cast<long long>(b) * p.n + jn) : 0ull;
         float mx = -INFINITY;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
@@ -501,7 +505,7 @@ __global__ void __launch_bounds__(kClusterThreads)
           for (int e = 0; e < 2; ++e) {
             const int kl = kw0 + nt * 8 + t4 * 2 + e;
             const int kabs = k_lo + kl;
-            const bool ok = kl < nk && kabs <= qpos;
+            const bool ok = rv && kl < nk && key_visible(kabs, Lb, jn, p.anc, am);
             const float v = ok ? sacc[nt][hr * 2 + e] * p.scale_log2 : -INFINITY;
             sacc[nt][hr * 2 + e] = v;
             mx = fmaxf(mx, v);

@@ -26,6 +26,16 @@ SPEC_DEVINL uint32_t ld_acquire(const unsigned* p) {
   return v;
 }
 
+// May the query of new-block node j see key slot kabs?  The block starts at
+// slot Lb: cached keys always; a new slot Lb + s by the causal order (s <= j)
+// for a chain, or, with a draft tree (anc != nullptr), iff bit s of the
+// node's ancestor mask `am` is set (the node itself or one of its ancestors).
+SPEC_DEVINL bool key_visible(int kabs, int Lb, int j, const uint64_t* anc, uint64_t am) {
+  if (kabs < Lb) return true;
+  const int s = kabs - Lb;
+  return anc ? (s < 64 && ((am >> s) & 1ull) != 0) : s <= j;
+}
+
 // Wall-clock bound for every spin-wait in a kernel: about two seconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 

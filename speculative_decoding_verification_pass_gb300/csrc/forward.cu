@@ -159,6 +159,7 @@ SPEC_DEVINL GemmParams phase_params(const MkParams& P, const GPh& g) {
     p.pos_base = P.pos_base;
     p.seq_ok = P.seq_ok;
     p.rope = P.rope;
+    p.depth = P.depth;
     p.n_per_seq = P.n;
     p.H = P.H;
     p.Hkv = P.Hkv;
@@ -552,14 +553,16 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int r = qt * 16 + g8 + hr * 8;
-        const int qpos = r < R ? Lb + r / G : -1;
+        const bool rv = r < R;
+        const int jn = rv ? r / G : 0;
+        const uint64_t am = (P.anc && rv) ? __ldg(P.anc + static_cast<long long>(b) * P.n + jn) : 0ull;
         float mx = -INFINITY;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             const int kabs = k0 + nt * 8 + t4 * 2 + x;
-            const bool ok = kabs < kend && kabs <= qpos;
+            const bool ok = rv && kabs < kend && key_visible(kabs, Lb, jn, P.anc, am);
             const float v = ok ? sacc[nt][hr * 2 + x] * P.scale_log2 : -INFINITY;
             sacc[nt][hr * 2 + x] = v;
             mx = fmaxf(mx, v);

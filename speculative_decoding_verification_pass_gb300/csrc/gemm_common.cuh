@@ -218,12 +218,16 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
     const bool rot = f < qdim + kdim;
     const int pr = dim < half ? r + half : r - half;
     const float2 fr = p.rope[dim < half ? dim : dim - half];
-    int posv[16], okv[16];
+    // slot = len + node index; rotary position = len + node depth (the node
+    // index itself for a chain)
+    int slotv[16], posv[16], okv[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {  // sequence bookkeeping, loads in flight together
       const int m = min(p.tok0 + c0 + j, p.M - 1);
       const int b = m / p.n_per_seq;
-      posv[j] = ldcg_i(p.pos_base + b) + (m - b * p.n_per_seq);
+      const int base = ldcg_i(p.pos_base + b), node = m - b * p.n_per_seq;
+      slotv[j] = base + node;
+      posv[j] = base + (p.depth ? __ldg(p.depth + m) : node);
       okv[j] = ldcg_i(p.seq_ok + b);
     }
 #pragma unroll 4
@@ -250,11 +254,11 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
         const uint16_t hi = f32_to_bf16(out);
         p.q[qi] = hi;
         if (p.q_lo) p.q_lo[qi] = f32_to_bf16(out - bf16_to_f32(hi));
-      } else if (okv[j] && pos < p.cap) {
+      } else if (okv[j] && slotv[j] < p.cap) {
         const int kf = f < qdim + kdim ? f - qdim : f - qdim - kdim;
         const int kvh = kf / hd;
         const long long idx =
-            ((static_cast<long long>(b) * p.Hkv + kvh) * p.cap + pos) * hd + (kf % hd);
+            ((static_cast<long long>(b) * p.Hkv + kvh) * p.cap + slotv[j]) * hd + (kf % hd);
         if (f < qdim + kdim)
           p.kcache[idx] = f32_to_bf16(out);
         else

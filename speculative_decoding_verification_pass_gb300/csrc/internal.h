@@ -52,6 +52,7 @@ struct GemmParams {
   const int32_t* pos_base;
   const int32_t* seq_ok;  // per sequence: 1 if its slots fit in the cache
   const float2* rope;     // [hd/2] frequency (hi, lo)
+  const int32_t* depth;   // [M] draft-tree node depths (position = base + depth), or nullptr
   int n_per_seq, H, Hkv, hd, cap;
   // EPI_SWIGLU: rows 0-63 of a tile are gate features, 64-127 up features
   uint16_t* act;  // [M][ffn]
@@ -79,6 +80,7 @@ struct AttnParams {
   uint16_t* o;            // [M][H*hd] bf16
   uint16_t* o_lo;         // bf16 residual of o, or nullptr
   const int32_t* pos_base;
+  const uint64_t* anc;    // [B][n] draft-tree ancestor masks, or nullptr (chain)
   float* part_o;          // [B][Hkv][splits][R][hd]
   float* part_ml;         // [B][Hkv][splits][R][2]
   int32_t* counters;      // [B*Hkv], zero on entry, left zero
@@ -124,6 +126,8 @@ struct MkParams {
   int32_t* status;
   int32_t* pos_base;
   int32_t* seq_ok;
+  const uint64_t* anc;                    // [B][n] draft-tree ancestor masks, or nullptr (chain)
+  const int32_t* depth;                   // [B][n] draft-tree node depths, or nullptr (chain)
   float* att_o;                           // [B][Hkv][att_nch][32][hd] chunk partials
   float* att_ml;                          // [B][Hkv][att_nch][32][2] (max, sum)
 };
@@ -207,5 +211,34 @@ namespace spec {
 
 cudaError_t launch_truncate(int32_t* len, const int32_t* n_acc, int B, int gamma, int32_t* status,
                             cudaStream_t stream, bool pdl);
+
+// ------------------------------------------------------------- draft trees
+constexpr int kTreeMaxNodes = 64;  // one 64-bit ancestor mask per node
+struct TreeAcceptParams {
+  const float* logits;     // [B][n][V] target logits per node
+  const float* q;          // [B][n][V] each node's draft distribution (its children's)
+  const int32_t* tokens;   // [B][n] node tokens (node 0: the root)
+  const int32_t* parents;  // [B][n] parent index, -1 for node 0
+  const float* u;          // [B][n]: u[c] coin of child c, u[0] the final draw
+  float* pbuf;             // [B][V] the current node's residual target distribution
+  int32_t* out;            // [B][n] accepted tokens, then the emitted token, -1 padding
+  int32_t* path;           // [B][n] accepted nodes in depth order, -1 padding
+  int32_t* n_acc;          // [B]
+  int32_t* status;
+  int B, n, V;
+  float T, top_p;
+};
+cudaError_t launch_tree_accept(const TreeAcceptParams& p, cudaStream_t stream);
+
+struct TreeCommitParams {
+  uint16_t* k;             // [L][B][Hkv][cap][hd]
+  uint16_t* v;
+  int32_t* len;            // [B], len = L0 + n on entry
+  const int32_t* path;     // [B][n]
+  const int32_t* n_acc;    // [B]
+  int32_t* status;
+  int L, B, Hkv, hd, cap, n;
+};
+cudaError_t launch_tree_commit(const TreeCommitParams& p, cudaStream_t stream);
 
 }  // namespace spec

@@ -80,3 +80,10 @@ def kv_prefix(seed: int, n_layers: int, batch: int, n_kv_heads: int,
 
 def context_lengths(seed: int, batch: int, lo: int, hi: int, stream: int = 7) -> np.ndarray:
     return rng(seed, stream).integers(lo, hi + 1, size=batch, dtype=np.int32)
+
+
+def random_tree(seed: int, n: int, stream: int = 10) -> list:
+    """Parent pointers of a random n-node draft tree: node 0 is the root
+    (parent -1), node i > 0 hangs under a uniformly chosen earlier node."""
+    g = rng(seed, stream)
+    return [-1] + [int(g.integers(0, i)) for i in range(1, n)]

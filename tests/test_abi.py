@@ -96,3 +96,44 @@ def test_product_path_never_imports_the_oracle():
         if f.endswith(".py"):
             src = open(os.path.join(ROOT, "oracle", f)).read()
             assert "speculative_decoding_verification_pass_gb300" not in src, f
+
+
+def test_tree_masks_match_the_oracle(lib):
+    """spec_tree_masks (host only) gives the oracle's visibility matrix as
+    bit masks and its depths, for the pages' tree, chains and random trees;
+    malformed trees and trees above 64 nodes are refused."""
+    import numpy as np
+
+    from oracle import tree as Tr
+    from speculative_decoding_verification_pass_gb300 import workloads as wl
+
+    trees = [Tr.full_tree_parents(2, 2), Tr.full_tree_parents(3, 3), Tr.chain_parents(1),
+             Tr.chain_parents(64), [-1, 0, 0, 0, 1, 1, 3, 6, 2]]
+    trees += [wl.random_tree(s, n) for s, n in ((1, 5), (2, 33), (3, 64))]
+    for par in trees:
+        anc, depth = lib.spec_tree_masks(par)
+        d_ref, vis = Tr.tree_structure(par)
+        n = len(par)
+        bits = np.array([[(a >> j) & 1 for j in range(n)] for a in anc])
+        np.testing.assert_array_equal(bits, vis)
+        assert all(a >> n == 0 for a in anc)
+        assert depth == d_ref.tolist()
+    for bad in ([0, 0], [-1, 1], [-1, 0, 3, 1], [-1, -1]):
+        with pytest.raises(lib.SpecError):
+            lib.spec_tree_masks(bad)
+    with pytest.raises(lib.SpecError) as e:
+        lib.spec_tree_masks(Tr.chain_parents(65))
+    assert e.value.status == lib.SPEC_ESIZE
+    L = lib.lib()
+    fake = ctypes.c_void_p(4096)
+    # tree calls validate before touching the device
+    assert L.spec_tree_accept(None, None, None, None, None, 1, 4, 10, 1.0, 1.0, None, None, None,
+                              None, 0, None) == lib.SPEC_EINVAL
+    ws = lib.spec_tree_accept_workspace_bytes(1, 10)
+    assert L.spec_tree_accept(fake, fake, fake, fake, fake, 1, 65, 10, 1.0, 1.0, fake, fake, fake,
+                              fake, ws, None) == lib.SPEC_ESIZE
+    assert L.spec_tree_accept(fake, fake, fake, fake, fake, 1, 4, 10, 1.0, 1.0, fake, fake, fake,
+                              fake, ws - 1, None) == lib.SPEC_ESIZE
+    assert L.spec_kv_tree_commit(None, None, None, None, 4, None, None) == lib.SPEC_EINVAL
+    assert L.spec_verify_forward_tree(None, None, None, None, 1, 4, None, None, None, 0,
+                                      None) == lib.SPEC_EINVAL
