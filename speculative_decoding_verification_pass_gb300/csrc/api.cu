@@ -206,7 +206,7 @@ WsPlan plan_ws(const spec_model_config& c, int B, int gamma, int cap) {
   };
   const size_t d = c.d_model;
   const size_t qd = c.n_layers ? static_cast<size_t>(c.n_heads) * hd : 0;
-  p.status = take(4);
+  p.status = take(68);  // status word; the persistent kernel's launch epoch at +64
   p.pos_base = take(static_cast<size_t>(B) * 4);
   p.seq_ok = take(static_cast<size_t>(B) * 4);
   p.mk_bar = take(256);  // directly before the counters: one memset clears both
@@ -565,7 +565,8 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
     for (int l = 1; l < c.n_layers; ++l)
       uniform = uniform && static_cast<long long>(L.g_attn[l] - L.g_attn[0]) == stride * l &&
                 static_cast<long long>(L.g_mlp[l] - L.g_mlp[0]) == stride * l;
-    if (shape_ok && cps >= 1 && uniform) {
+    // the stream-K words (8 bytes each) of at most kMaxGrid / 2 CTAs fit the partials area
+    if (shape_ok && cps >= 1 && uniform && m->sm_count * cps <= kMaxGrid / 2) {
       MkParams* mp = new MkParams();
       MkParams& Q = *mp;
       const void* xs[6] = {hb, hb_lo, o, o_lo, act, act_lo};
@@ -633,6 +634,7 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       Q.partials = reinterpret_cast<float*>(W + P.gpart);
       Q.counters = counters;
       Q.bar = reinterpret_cast<unsigned*>(W + P.mk_bar);
+      Q.epoch = reinterpret_cast<unsigned*>(W + P.status + 64);  // outside the per-launch memset
       Q.status = status;
       Q.pos_base = pos_base;
       Q.seq_ok = seq_ok;

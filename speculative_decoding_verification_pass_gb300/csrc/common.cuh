@@ -20,6 +20,17 @@ SPEC_DEVINL void set_status(int32_t* status, int32_t bit) {
 }
 
 // Load with acquire semantics at GPU scope (grid-barrier counters).
+// 64-bit relaxed accesses at GPU scope: single-copy atomic, so a word that
+// carries a value and a tag is seen whole or not at all.
+SPEC_DEVINL void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+SPEC_DEVINL unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+
 SPEC_DEVINL uint32_t ld_acquire(const unsigned* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

@@ -220,11 +220,12 @@ struct MkSmem {
   float* red;
   int* slots;
   float* sq;        // [128] embedding partial sums
+  int* qpre;        // [3][128] QKV epilogue: KV slot, rotary position, fit flag per column
 };
 
 __host__ __device__ inline size_t mk_att_bytes(int hd) { return static_cast<size_t>(384) * hd; }
 constexpr size_t kMkBarBytes = 512;
-constexpr size_t kMkTail = kMkBarBytes + 256 * 4 + 64 * 4 + 64 * 4 + 128 * 4 + 64;
+constexpr size_t kMkTail = kMkBarBytes + 256 * 4 + 64 * 4 + 64 * 4 + 128 * 4 + 384 * 4 + 64;
 
 SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
   uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023);
@@ -244,7 +245,77 @@ SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
   s.red = s.rs + 256;
   s.slots = reinterpret_cast<int*>(s.red + 64);
   s.sq = reinterpret_cast<float*>(s.slots + 64);
+  s.qpre = reinterpret_cast<int*>(s.sq + 128);
   return s;
+}
+
+// Stream-K exchange of the persistent kernel.  A tile cut over several CTAs
+// is finished by the CTA holding its first unit (whose share of the tile is
+// the last segment of its range); the other contributors store their fp32
+// partial sums as 64-bit words (value, tag) with tag = (launch epoch << 9) |
+// phase, and the finisher polls those words until every tag is the current
+// one.  No fence, counter or second pass sits between a contributor's last
+// MMA and the finisher's read; the epoch (a workspace word advanced once per
+// launch) keeps words of an earlier launch, e.g. an earlier replay of a
+// captured graph, from being taken as current.
+SPEC_DEVINL unsigned long long tag_word(uint32_t tag, float v) {
+  return (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(v);
+}
+
+SPEC_DEVINL unsigned long long* part_word(unsigned long long* part, uint32_t c, int slot, int ntok,
+                                          int col, int r) {
+  return part + ((static_cast<long long>(c) * 2 + slot) * ntok + col) * kTileN + r;
+}
+
+// acc[j] (the finisher's own accumulators on entry; the finisher is the
+// tile's first contributor) += the other contributors' column c0 + j
+// (j < JN), added in CTA order.  CB contributors' words are in flight
+// together.  False when the wait gave up (abort set).
+template <int JN, int CB>
+SPEC_DEVINL bool fixup_tagged(unsigned long long* part, int ntok, int c0, int r, uint32_t c_first,
+                              int nc, const int* slots, float (&acc)[16], uint32_t tag,
+                              volatile int* abort, int32_t* status) {
+  for (int i0 = 1; i0 < nc; i0 += CB) {
+    unsigned long long w[CB][JN];
+    const unsigned long long* src[CB];
+#pragma unroll
+    for (int k = 0; k < CB; ++k) {
+      const int i = i0 + k;
+      const bool remote = i < nc;
+      src[k] = remote ? part_word(part, c_first + static_cast<uint32_t>(i), slots[i], ntok, c0, r)
+                      : nullptr;
+#pragma unroll
+      for (int j = 0; j < JN; ++j)
+        w[k][j] = remote ? ld_relaxed_u64(src[k] + j * kTileN) : tag_word(tag, 0.f);
+    }
+    unsigned long long t0 = 0;
+    for (;;) {
+      bool ready = true;
+#pragma unroll
+      for (int k = 0; k < CB; ++k)
+#pragma unroll
+        for (int j = 0; j < JN; ++j)
+          if (static_cast<uint32_t>(w[k][j] >> 32) != tag) {
+            w[k][j] = ld_relaxed_u64(src[k] + j * kTileN);
+            ready = false;
+          }
+      if (ready) break;
+      if (*abort) return false;
+      const unsigned long long now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        *abort = 1;
+        set_status(status, SPEC_DEV_TIMEOUT);
+        return false;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < CB; ++k)
+#pragma unroll
+      for (int j = 0; j < JN; ++j) acc[j] += __uint_as_float(static_cast<uint32_t>(w[k][j]));
+  }
+  return true;
 }
 
 // Every epilogue thread publishes its writes; one thread arrives.
@@ -373,51 +444,182 @@ SPEC_DEVINL int att_chunk_keys(int Tk, int nch) {
   return ((per + kAttUnitKeys - 1) / kAttUnitKeys) * kAttUnitKeys;
 }
 
+// Where a 64-key block of keys and values sits in shared memory: eight pieces
+// of 16 rows (piece q = slot * 4 + (value ? 2 : 0) + half, slot = key / 32,
+// half = key / 16 % 2), `pps` pieces per region and regions `stride` bytes
+// apart.  The attention stage holds one block contiguously; while the
+// attention phase runs, the ring stages' activation areas (idle between this
+// CTA's last QKV MMA and the O phase's activation loads) hold a second one.
+struct KVLayout {
+  uint32_t base, stride;
+  int pps;
+  template <int HD>
+  SPEC_DEVINL uint32_t piece(int q) const {
+    return base + static_cast<uint32_t>(q / pps) * stride + static_cast<uint32_t>(q % pps) * 16u * HD * 2u;
+  }
+};
+
 // Issue the cp.async copies of the 64-key block at kb (keys and values) into
-// the K/V stage: `what` = 0 every row (zero fill past kend), 1 the rows this
-// pass does not write (cached keys below Lb; zero fill past kend), 2 the rows
-// this pass writes (keys Lb .. kend-1).
+// `lay`: `what` = 0 every row (zero fill past kend), 1 the rows this pass
+// does not write (cached keys below Lb; zero fill past kend), 2 the rows this
+// pass writes (keys Lb .. kend-1).
 template <int HD>
-SPEC_DEVINL void att_load_block(uint8_t* sK, const uint16_t* kc, const uint16_t* vc, long long head_base,
-                                int kb, int kend, int Lb, int what, int e) {
-  constexpr int kRowB = HD * 2;
+SPEC_DEVINL void att_load_block(const KVLayout& lay, const uint16_t* kc, const uint16_t* vc,
+                                long long head_base, int kb, int kend, int Lb, int what, int e) {
   constexpr int kCPR = HD / 8;
   for (int idx = e; idx < kAttUnitKeys * kCPR; idx += kEpiThreads) {
     const int i = idx / kCPR, c = idx % kCPR;  // key kb + i
-    const int s = i >> 5, ii = i & 31;
     const int key = kb + i;
     const bool valid = key < kend;
     const bool fresh = valid && key >= Lb;
     if ((what == 1 && fresh) || (what == 2 && !fresh)) continue;
     const long long g = (head_base + (valid ? key : kb)) * HD + c * 8;
-    const uint32_t dk = smem_u32(sK + s * 64 * kRowB) + swz<HD>(ii, c);
-    cp_async16(dk, kc + g, valid ? 16 : 0);
-    cp_async16(dk + 32 * kRowB, vc + g, valid ? 16 : 0);
+    const int qk = (i >> 5) * 4 + ((i >> 4) & 1);
+    const uint32_t off = swz<HD>(i & 15, c);
+    cp_async16(lay.piece<HD>(qk) + off, kc + g, valid ? 16 : 0);
+    cp_async16(lay.piece<HD>(qk + 2) + off, vc + g, valid ? 16 : 0);
   }
 }
 
-// Before the QKV phase completes: start loading the cached keys / values of
-// the first 64-key block of this CTA's first attention unit of layer l (they
-// do not depend on the pass).
+// Attention unit of this CTA: (sequence, KV head, key chunk), or false.
+struct AttUnit {
+  int b, kvh, ch, Lb, kbeg, kend, nu;
+};
+SPEC_DEVINL bool att_unit(const MkParams& P, int unit, AttUnit& u) {
+  const int nch = P.att_nch;
+  if (unit >= P.B * P.Hkv * nch) return false;
+  u.b = unit / (P.Hkv * nch);
+  u.kvh = (unit / nch) % P.Hkv;
+  u.ch = unit % nch;
+  u.Lb = __ldcg(P.pos_base + u.b);
+  const int Tk = min(u.Lb + P.n, P.cap);
+  const int ck = att_chunk_keys(Tk, nch);
+  u.kbeg = u.ch * ck;
+  u.kend = min(u.kbeg + ck, Tk);
+  u.nu = (Tk + ck - 1) / ck;  // chunks holding keys
+  return u.kbeg < u.kend;
+}
+
+SPEC_DEVINL KVLayout att_stage_layout(const MkSmem& sm, int hd) {
+  // [q hi 32 rows | q lo 32 rows | block]
+  return KVLayout{smem_u32(sm.att) + 64u * hd * 2u, 0u, 8};
+}
+
+// Load the cached keys / values of the first 64-key block of this CTA's first
+// attention unit of layer l (they do not depend on the pass), early: the
+// attention stage is not used by the GEMM phases before the attention phase
+// beyond the epilogue exchange buffer and the QKV bookkeeping, which sit in
+// the q area.
 template <int HD>
 SPEC_DEVINL void att_prefetch(const MkParams& P, const MkSmem& sm, int l) {
   const int e = threadIdx.x - kEpiFirstThread;
-  const int nch = P.att_nch;
-  const int unit = blockIdx.x;
-  if (unit >= P.B * P.Hkv * nch) return;
-  const int b = unit / (P.Hkv * nch);
-  const int kvh = (unit / nch) % P.Hkv;
-  const int ch = unit % nch;
-  const int Lb = __ldcg(P.pos_base + b);
-  const int Tk = min(Lb + P.n, P.cap);
-  const int ck = att_chunk_keys(Tk, nch);
-  const int kbeg = ch * ck, kend = min(kbeg + ck, Tk);
-  if (kbeg >= kend) return;
-  const long long head_base = (static_cast<long long>(b) * P.Hkv + kvh) * P.cap;
-  uint8_t* sK = sm.att + 64 * HD * 2;
-  att_load_block<HD>(sK, P.kc + P.layer_kv * l, P.vc + P.layer_kv * l, head_base, kbeg, kend, Lb, 1, e);
+  AttUnit u;
+  if (!att_unit(P, blockIdx.x, u)) return;
+  const long long head_base = (static_cast<long long>(u.b) * P.Hkv + u.kvh) * P.cap;
+  att_load_block<HD>(att_stage_layout(sm, HD), P.kc + P.layer_kv * l, P.vc + P.layer_kv * l, head_base,
+                     u.kbeg, u.kend, u.Lb, 1, e);
 }
 
+// One 64-key block of a unit for this warp's 32 keys (slot) and 16 query rows
+// (qt): scores with q as bf16 hi/lo, the online softmax, P (hi/lo) times V.
+template <int HD>
+SPEC_DEVINL void att_block(const MkParams& P, const KVLayout& lay, uint32_t aQ, uint32_t aQlo, int kb,
+                           int kend, int Lb, int b, int R, int G, int slot, int qt, int lane,
+                           float (&mrow)[2], float (&lrow)[2], float (&oacc)[HD / 8][4]) {
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int k0 = kb + slot * kAttBlockKeys;
+  if (k0 >= kend) return;
+  const uint32_t kp[2] = {lay.piece<HD>(slot * 4), lay.piece<HD>(slot * 4 + 1)};
+  const uint32_t vp[2] = {lay.piece<HD>(slot * 4 + 2), lay.piece<HD>(slot * 4 + 3)};
+  float sacc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    uint32_t a0, a1, a2, a3, q0, q1, q2, q3;
+    const int qrow = qt * 16 + (lane & 15);
+    ldsm_x4(aQ + swz<HD>(qrow, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+    ldsm_x4(aQlo + swz<HD>(qrow, kk * 2 + (lane >> 4)), q0, q1, q2, q3);
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      const int key = (lane & 7) + ((lane >> 4) << 3);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kp[np] + swz<HD>(key, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
+      mma_bf16(sacc[np * 2], a0, a1, a2, a3, b0, b1);
+      mma_bf16(sacc[np * 2 + 1], a0, a1, a2, a3, b2, b3);
+      mma_bf16(sacc[np * 2], q0, q1, q2, q3, b0, b1);
+      mma_bf16(sacc[np * 2 + 1], q0, q1, q2, q3, b2, b3);
+    }
+  }
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int r = qt * 16 + g8 + hr * 8;
+    const bool rv = r < R;
+    const int jn = rv ? r / G : 0;
+    const uint64_t am = (P.anc && rv) ? __ldg(P.anc + static_cast<long long>(b) * P.n + jn) : 0ull;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int kabs = k0 + nt * 8 + t4 * 2 + x;
+        const bool ok = rv && kabs < kend && key_visible(kabs, Lb, jn, P.anc, am);
+        const float v = ok ? sacc[nt][hr * 2 + x] * P.scale_log2 : -INFINITY;
+        sacc[nt][hr * 2 + x] = v;
+        mx = fmaxf(mx, v);
+      }
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(mrow[hr], mx);
+    const float alpha = mrow[hr] == -INFINITY ? 0.f : exp2f(mrow[hr] - mn);
+    float sum = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const float pe = mn == -INFINITY ? 0.f : exp2f(sacc[nt][hr * 2 + x] - mn);
+        sacc[nt][hr * 2 + x] = pe;
+        sum += pe;
+      }
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    mrow[hr] = mn;
+    lrow[hr] = lrow[hr] * alpha + sum;
+#pragma unroll
+    for (int nd = 0; nd < HD / 8; ++nd) {
+      oacc[nd][hr * 2] *= alpha;
+      oacc[nd][hr * 2 + 1] *= alpha;
+    }
+  }
+#pragma unroll
+  for (int k2 = 0; k2 < 2; ++k2) {
+    const uint32_t a0 = pack_bf16x2(sacc[2 * k2][0], sacc[2 * k2][1]);
+    const uint32_t a1 = pack_bf16x2(sacc[2 * k2][2], sacc[2 * k2][3]);
+    const uint32_t a2 = pack_bf16x2(sacc[2 * k2 + 1][0], sacc[2 * k2 + 1][1]);
+    const uint32_t a3 = pack_bf16x2(sacc[2 * k2 + 1][2], sacc[2 * k2 + 1][3]);
+    const uint32_t p0 = pack_bf16x2(sacc[2 * k2][0] - bf16lo(a0), sacc[2 * k2][1] - bf16hi(a0));
+    const uint32_t p1 = pack_bf16x2(sacc[2 * k2][2] - bf16lo(a1), sacc[2 * k2][3] - bf16hi(a1));
+    const uint32_t p2 = pack_bf16x2(sacc[2 * k2 + 1][0] - bf16lo(a2), sacc[2 * k2 + 1][1] - bf16hi(a2));
+    const uint32_t p3 = pack_bf16x2(sacc[2 * k2 + 1][2] - bf16lo(a3), sacc[2 * k2 + 1][3] - bf16hi(a3));
+#pragma unroll
+    for (int dn = 0; dn < HD / 16; ++dn) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vp[k2] + swz<HD>(lane & 15, dn * 2 + (lane >> 4)), b0, b1, b2, b3);
+      mma_bf16(oacc[2 * dn], a0, a1, a2, a3, b0, b1);
+      mma_bf16(oacc[2 * dn + 1], a0, a1, a2, a3, b2, b3);
+      mma_bf16(oacc[2 * dn], p0, p1, p2, p3, b0, b1);
+      mma_bf16(oacc[2 * dn + 1], p0, p1, p2, p3, b2, b3);
+    }
+  }
+}
+
+// The attention phase: every unit (sequence b, KV head, key chunk) runs its
+// chunk for the n x G query rows of the KV head's group; its partial (max,
+// sum, O) goes to the chunk partials, merged by the next phase.  Block 0's
+// cached rows were loaded early; block 1 goes to the ring stages' activation
+// areas at once, so both blocks' copies are in flight with q's.
 // Merge the chunk partials of every query row by log-sum-exp into the
 // attention output (bf16 hi/lo).  One warp per (sequence, KV head, row,
 // 32-dimension group): each lane owns one dimension, so every partial load of
@@ -474,7 +676,7 @@ SPEC_DEVINL void cmb_phase(const MkParams& P) {
 }
 
 template <int HD>
-SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
+SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t sbytes) {
   const int e = threadIdx.x - kEpiFirstThread;
   const int w = e >> 5, lane = e & 31;
   const int slot = w >> 1, qt = w & 1;
@@ -482,38 +684,36 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
   const int R = P.n * G;
   const int qdim = P.H * HD;
   constexpr int kRowB = HD * 2;
-  uint8_t* sQ = sm.att;
-  uint8_t* sQlo = sQ + 32 * kRowB;
-  uint8_t* sK = sQlo + 32 * kRowB;  // [slot][K 32 rows | V 32 rows]
-  const uint32_t aQ = smem_u32(sQ), aQlo = smem_u32(sQlo);
-  const uint32_t aK = smem_u32(sK + slot * 64 * kRowB), aV = aK + 32 * kRowB;
-  float* merge = reinterpret_cast<float*>(sm.att);  // [2 tiles][16][HD], reuses the Q area
+  constexpr int kCPR = HD / 8;
+  const uint32_t aQ = smem_u32(sm.att), aQlo = aQ + 32 * kRowB;
+  const KVLayout stage_lay = att_stage_layout(sm, HD);
+  // the second block in the ring stages' activation areas, when they hold it
+  const int act_pps = (2 * P.ntok * 128) / (16 * kRowB);
+  const bool two = act_pps > 0 && P.stages * act_pps >= 8;
+  const KVLayout act_lay{smem_u32(sm.ring) + kATileBytes, sbytes, act_pps > 0 ? act_pps : 1};
+  float* merge = reinterpret_cast<float*>(sm.att);  // [2 tiles][16][HD], reuses the q area
   const uint16_t* kc = P.kc + P.layer_kv * l;
   const uint16_t* vc = P.vc + P.layer_kv * l;
   const int nch = P.att_nch;
   const int units = P.B * P.Hkv * nch;
   const int g8 = lane >> 2, t4 = lane & 3;
-  constexpr int kCPR = HD / 8;
   const bool active = qt * 16 < R;
   for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
-    const int b = unit / (P.Hkv * nch);
-    const int kvh = (unit / nch) % P.Hkv;
-    const int ch = unit % nch;
-    const int Lb = __ldcg(P.pos_base + b);
-    const int Tk = min(Lb + P.n, P.cap);
-    const int ck = att_chunk_keys(Tk, nch);
-    const int kbeg = ch * ck, kend = min(kbeg + ck, Tk);
-    if (kbeg >= kend) continue;  // uniform across the CTA
-    const long long head_base = (static_cast<long long>(b) * P.Hkv + kvh) * P.cap;
-    // the first block of the CTA's first unit was prefetched except the rows
-    // this pass wrote; they are in flight while q is staged
-    att_load_block<HD>(sK, kc, vc, head_base, kbeg, kend, Lb, unit == static_cast<int>(blockIdx.x) ? 2 : 0, e);
-    // ---- stage q (hi, lo) rows with async copies (zero rows past R)
+    AttUnit u;
+    if (!att_unit(P, unit, u)) continue;  // uniform across the CTA
+    const long long head_base = (static_cast<long long>(u.b) * P.Hkv + u.kvh) * P.cap;
+    const bool first = unit == static_cast<int>(blockIdx.x);
+    // block 0: the cached rows were prefetched for the first unit; block 1
+    // into the activation areas at once
+    att_load_block<HD>(stage_lay, kc, vc, head_base, u.kbeg, u.kend, u.Lb, first ? 2 : 0, e);
+    const bool staged1 = two && u.kbeg + kAttUnitKeys < u.kend;
+    if (staged1) att_load_block<HD>(act_lay, kc, vc, head_base, u.kbeg + kAttUnitKeys, u.kend, u.Lb, 0, e);
+    // q (hi, lo) rows with async copies (zero rows past R)
     for (int idx = e; idx < 32 * kCPR; idx += kEpiThreads) {
       const int r = idx / kCPR, c = idx % kCPR;
       const bool valid = r < R;
       const int j = valid ? r / G : 0, g = valid ? r % G : 0;
-      const long long off = (static_cast<long long>(b) * P.n + j) * qdim + (kvh * G + g) * HD + c * 8;
+      const long long off = (static_cast<long long>(u.b) * P.n + j) * qdim + (u.kvh * G + g) * HD + c * 8;
       cp_async16(aQ + swz<HD>(r, c), P.q + off, valid ? 16 : 0);
       cp_async16(aQlo + swz<HD>(r, c), P.q_lo + off, valid ? 16 : 0);
     }
@@ -521,103 +721,22 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
     float oacc[HD / 8][4];
 #pragma unroll
     for (int i = 0; i < HD / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-    for (int kb = kbeg; kb < kend; kb += kAttUnitKeys) {
-      if (kb > kbeg) {
-        named_bar(kArriveBar, kEpiThreads);  // previous block consumed
-        att_load_block<HD>(sK, kc, vc, head_base, kb, kend, Lb, 0, e);
+    cp_async_wait_all();
+    named_bar(kArriveBar, kEpiThreads);
+    for (int kb = u.kbeg, bi = 0; kb < u.kend; kb += kAttUnitKeys, ++bi) {
+      const bool in_act = staged1 && bi == 1;
+      if (bi > 0 && !in_act) {
+        named_bar(kArriveBar, kEpiThreads);  // the stage's previous block consumed
+        att_load_block<HD>(stage_lay, kc, vc, head_base, kb, u.kend, u.Lb, 0, e);
+        cp_async_wait_all();
+        named_bar(kArriveBar, kEpiThreads);
       }
-      cp_async_wait_all();
-      named_bar(kArriveBar, kEpiThreads);
-      const int k0 = kb + slot * kAttBlockKeys;
-      if (!active || k0 >= kend) continue;
-      float sacc[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        uint32_t a0, a1, a2, a3, q0, q1, q2, q3;
-        const int qrow = qt * 16 + (lane & 15);
-        ldsm_x4(aQ + swz<HD>(qrow, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
-        ldsm_x4(aQlo + swz<HD>(qrow, kk * 2 + (lane >> 4)), q0, q1, q2, q3);
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(aK + swz<HD>(key, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
-          mma_bf16(sacc[np * 2], a0, a1, a2, a3, b0, b1);
-          mma_bf16(sacc[np * 2 + 1], a0, a1, a2, a3, b2, b3);
-          mma_bf16(sacc[np * 2], q0, q1, q2, q3, b0, b1);
-          mma_bf16(sacc[np * 2 + 1], q0, q1, q2, q3, b2, b3);
-        }
-      }
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int r = qt * 16 + g8 + hr * 8;
-        const bool rv = r < R;
-        const int jn = rv ? r / G : 0;
-        const uint64_t am = (P.anc && rv) ? __ldg(P.anc + static_cast<long long>(b) * P.n + jn) : 0ull;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const int kabs = k0 + nt * 8 + t4 * 2 + x;
-            const bool ok = rv && kabs < kend && key_visible(kabs, Lb, jn, P.anc, am);
-            const float v = ok ? sacc[nt][hr * 2 + x] * P.scale_log2 : -INFINITY;
-            sacc[nt][hr * 2 + x] = v;
-            mx = fmaxf(mx, v);
-          }
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(mrow[hr], mx);
-        const float alpha = mrow[hr] == -INFINITY ? 0.f : exp2f(mrow[hr] - mn);
-        float sum = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const float pe = mn == -INFINITY ? 0.f : exp2f(sacc[nt][hr * 2 + x] - mn);
-            sacc[nt][hr * 2 + x] = pe;
-            sum += pe;
-          }
-        }
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        mrow[hr] = mn;
-        lrow[hr] = lrow[hr] * alpha + sum;
-#pragma unroll
-        for (int nd = 0; nd < HD / 8; ++nd) {
-          oacc[nd][hr * 2] *= alpha;
-          oacc[nd][hr * 2 + 1] *= alpha;
-        }
-      }
-#pragma unroll
-      for (int k2 = 0; k2 < 2; ++k2) {
-        const uint32_t a0 = pack_bf16x2(sacc[2 * k2][0], sacc[2 * k2][1]);
-        const uint32_t a1 = pack_bf16x2(sacc[2 * k2][2], sacc[2 * k2][3]);
-        const uint32_t a2 = pack_bf16x2(sacc[2 * k2 + 1][0], sacc[2 * k2 + 1][1]);
-        const uint32_t a3 = pack_bf16x2(sacc[2 * k2 + 1][2], sacc[2 * k2 + 1][3]);
-        const uint32_t p0 = pack_bf16x2(sacc[2 * k2][0] - bf16lo(a0), sacc[2 * k2][1] - bf16hi(a0));
-        const uint32_t p1 = pack_bf16x2(sacc[2 * k2][2] - bf16lo(a1), sacc[2 * k2][3] - bf16hi(a1));
-        const uint32_t p2 =
-            pack_bf16x2(sacc[2 * k2 + 1][0] - bf16lo(a2), sacc[2 * k2 + 1][1] - bf16hi(a2));
-        const uint32_t p3 =
-            pack_bf16x2(sacc[2 * k2 + 1][2] - bf16lo(a3), sacc[2 * k2 + 1][3] - bf16hi(a3));
-        const int key = k2 * 16 + (lane & 15);
-#pragma unroll
-        for (int dn = 0; dn < HD / 16; ++dn) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(aV + swz<HD>(key, dn * 2 + (lane >> 4)), b0, b1, b2, b3);
-          mma_bf16(oacc[2 * dn], a0, a1, a2, a3, b0, b1);
-          mma_bf16(oacc[2 * dn + 1], a0, a1, a2, a3, b2, b3);
-          mma_bf16(oacc[2 * dn], p0, p1, p2, p3, b0, b1);
-          mma_bf16(oacc[2 * dn + 1], p0, p1, p2, p3, b2, b3);
-        }
-      }
+      if (active)
+        att_block<HD>(P, in_act ? act_lay : stage_lay, aQ, aQlo, kb, u.kend, u.Lb, u.b, R, G, slot, qt,
+                      lane, mrow, lrow, oacc);
     }
     // ---- merge the two slots: slot 1 through shared memory
-    named_bar(kArriveBar, kEpiThreads);  // the Q area becomes the merge buffer
+    named_bar(kArriveBar, kEpiThreads);  // the q area becomes the merge buffer
     float* mb = merge + qt * 16 * HD;
     float* mm = sm.red + qt * 32;  // [16] max, [16] sum
     if (slot == 1 && active) {
@@ -637,7 +756,7 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
     }
     named_bar(kArriveBar, kEpiThreads);
     if (slot == 0 && active) {
-      const long long ubase = (static_cast<long long>(b) * P.Hkv + kvh) * nch + ch;
+      const long long ubase = (static_cast<long long>(u.b) * P.Hkv + u.kvh) * nch + u.ch;
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int rr = g8 + hr * 8;
@@ -667,6 +786,8 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l) {
     }
     named_bar(kArriveBar, kEpiThreads);  // shared memory free for the next unit
   }
+  // the activation areas go back to the TMA loads of the O phase
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // -------------------------------------------------------------- the kernel
@@ -839,19 +960,24 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
     gs.slots = sm.slots;
     gs.flag = sm.flag;
     int seg = 0;
+    unsigned long long* const part64 = reinterpret_cast<unsigned long long*>(P.partials);
+    // read before this CTA arrives on the embedding phase; advanced after it
+    const uint32_t epoch = *reinterpret_cast<volatile unsigned*>(P.epoch) & 0x7FFFFFu;
     for (int ph = 0; ph < nph; ++ph) {
       const int kind = ph_kind(ph, P.L);
+      const uint32_t tag = (epoch << 9) | static_cast<uint32_t>(ph);
       if (kind == PH_EMBED) {
         embed_phase(P, sm);
       } else if (kind == PH_ATT) {
-        att_prefetch<HD>(P, sm, (ph - 1) / kPhPerLayer);
         if (!epi_wait(P, sm, ph)) break;
-        att_phase<HD>(P, sm, (ph - 1) / kPhPerLayer);
+        att_phase<HD>(P, sm, (ph - 1) / kPhPerLayer, sbytes);
       } else if (kind == PH_CMB) {
         if (!epi_wait(P, sm, ph)) break;
         cmb_phase<HD>(P);
       } else {
         if (!epi_wait(P, sm, ph)) break;
+        // every CTA read the epoch before arriving on the embedding phase
+        if (ph == 1 && blockIdx.x == 0 && e == 0) *P.epoch = epoch + 1;
         const GPh g = gph(P, ph);
         const GemmParams p = phase_params(P, g);
         const uint32_t kc = g.K / 64;
@@ -866,6 +992,19 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
             sm.rs[c] = rsqrtf(s * p.inv_d + p.eps);
           }
         }
+        // QKV: per token column KV slot, rotary position and fit flag
+        int* const qpre = sm.qpre;
+        if (p.epi == EPI_QKV) {
+          att_prefetch<HD>(P, sm, g.l);  // this layer's first key block, early
+          for (int c = e; c < p.ntok; c += kEpiThreads) {
+            const int m = min(c, p.M - 1);
+            const int b = m / p.n_per_seq, node = m - b * p.n_per_seq;
+            const int base = __ldcg(p.pos_base + b);
+            qpre[c] = base + node;
+            qpre[128 + c] = base + (p.depth ? __ldg(p.depth + m) : node);
+            qpre[256 + c] = __ldcg(p.seq_ok + b);
+          }
+        }
         named_bar(kEpiBar, kEpiThreads);
         uint32_t u = u0;
         while (u < u1) {
@@ -875,11 +1014,22 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
           // the residual stream of this tile's rows, loaded while the MMAs run
           float hv[16];
           const bool pre_h = p.epi == EPI_RESID && p.ntok <= 16;
+          const int f = static_cast<int>(t) * kTileN + r;
           if (pre_h) {
-            const int f = static_cast<int>(t) * kTileN + r;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               hv[j] = (j < p.M && f < p.N) ? __ldcg(p.h + static_cast<long long>(j) * p.d + f) : 0.f;
+          }
+          // the epilogue's other inputs, also loaded while the MMAs run
+          EpiPre pre;
+          if (p.epi == EPI_RESID) {
+            pre.have_gn = true;
+            pre.gn = f < p.N ? __ldg(p.g_next + f) : 0.f;
+          } else if (p.epi == EPI_QKV) {
+            const int dim = f % p.hd, half = p.hd >> 1;
+            pre.have_fr = true;
+            pre.fr = __ldg(p.rope + (dim < half ? dim : dim - half));
+            pre.qkv = qpre;
           }
           mbar_wait(&sm.accfull[a], (seg >> 1) & 1, sm.abort);
           named_bar(kEpiBar, kEpiThreads);
@@ -889,40 +1039,35 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
           const uint32_t c_first = part.cta_of(t * kc);
           const uint32_t c_last = part.cta_of((t + 1) * kc - 1);
           const int nc = static_cast<int>(c_last - c_first + 1);
-          bool finisher = true;
-          if (nc > 1) {
+          const bool finisher = nc == 1 || me == c_first;
+          if (!finisher) {
             const int slot = part.slot(me, t);
-            float* dst = p.partials + (static_cast<long long>(me) * 2 + slot) * p.ntok * kTileN;
-            for (int c0 = 0; c0 < p.ntok; c0 += 16) {
+            for (int c0 = 0; c0 < p.M; c0 += 16) {
               float v[16];
               load_acc(tacc, c0, p.ntok, 1, v);
+              // the columns the finisher reads: 8 when at most 8 are valid, else 16
+              const int jn = p.M - c0 <= 8 ? 8 : 16;
+              unsigned long long* dst = part_word(part64, me, slot, p.ntok, c0, r);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) __stcg(dst + (c0 + j) * kTileN + r, v[j]);
+              for (int j = 0; j < 16; ++j)
+                if (j < jn) st_relaxed_u64(dst + j * kTileN, tag_word(tag, v[j]));
             }
-            if (e < nc) sm.slots[e] = part.slot(c_first + e, t);
-            __threadfence();
-            named_bar(kEpiBar, kEpiThreads);
-            if (e == 0) {
-              const int old = atomicAdd(&p.counters[t], 1);
-              const int last = old == nc - 1;
-              if (last) p.counters[t] = 0;
-              *sm.flag = last;
+          } else {
+            if (nc > 1) {
+              if (e < nc) sm.slots[e] = part.slot(c_first + e, t);
+              named_bar(kEpiBar, kEpiThreads);
             }
-            named_bar(kEpiBar, kEpiThreads);
-            finisher = *sm.flag != 0;
-            __threadfence();
-          }
-          if (finisher) {
             for (int c0 = 0; c0 < p.ntok; c0 += 16) {
-              float own[16], acc[16];
-              load_acc(tacc, c0, p.ntok, 1, own);
-              if (nc == 1) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] = own[j];
-              } else {
-                fixup_sum<4>(p.partials, p.ntok, c0, r, c_first, nc, me, sm.slots, own, acc);
+              float acc[16];
+              load_acc(tacc, c0, p.ntok, 1, acc);
+              if (nc > 1) {
+                const bool ok = p.M - c0 <= 8 ? fixup_tagged<8, 5>(part64, p.ntok, c0, r, c_first, nc,
+                                                                    sm.slots, acc, tag, sm.abort, P.status)
+                                              : fixup_tagged<16, 2>(part64, p.ntok, c0, r, c_first, nc,
+                                                                    sm.slots, acc, tag, sm.abort, P.status);
+                if (!ok) break;
               }
-              epilogue_chunk_h(p, gs, t, r, c0, acc, hv, pre_h);
+              epilogue_chunk_h(p, gs, t, r, c0, acc, hv, pre_h, pre);
             }
           }
           tc_fence_before();

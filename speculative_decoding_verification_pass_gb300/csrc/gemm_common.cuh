@@ -140,11 +140,23 @@ __device__ __forceinline__ void fixup_sum(const float* partials, int ntok, int c
 }
 
 // --------------------------------------------------------------- epilogues
+// Values an epilogue needs besides the accumulators, loaded ahead of it (while
+// the MMAs run) by callers that can; left unset, the epilogue loads them.
+struct EpiPre {
+  bool have_gn = false;
+  float gn = 0.f;           // EPI_RESID: the next norm's gain of this row's feature
+  bool have_fr = false;
+  float2 fr{};              // EPI_QKV: RoPE frequency of this row's dimension
+  const int* qkv = nullptr; // EPI_QKV: shared [3][128] per token column: KV slot, rotary
+                            // position, fit flag (persistent kernel, tok0 = 0)
+};
+
 // Apply the epilogue to 16 token columns [c0, c0+16) of this thread's row.
 // With have_h the residual-stream values of these columns were loaded
 // beforehand (hv); otherwise the residual epilogue loads them.
 __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t tile, int r, int c0,
-                                 const float (&acc)[16], const float (&hv_in)[16], bool have_h) {
+                                 const float (&acc)[16], const float (&hv_in)[16], bool have_h,
+                                 const EpiPre& pre) {
   const int f = static_cast<int>(tile) * kTileN + r;  // weight row = output feature
   const int e = threadIdx.x - kEpiFirstThread;
   float v[16];
@@ -168,7 +180,7 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
     // all 16 residual loads in flight before the first store (the residual
     // stream is rewritten by other CTAs between passes over it: L2 loads)
     const bool fok = f < p.N;
-    const float gn = fok ? p.g_next[f] : 0.f;
+    const float gn = pre.have_gn ? pre.gn : (fok ? p.g_next[f] : 0.f);
     float hv[16], sq[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -217,18 +229,27 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
     const int dim = f % hd;
     const bool rot = f < qdim + kdim;
     const int pr = dim < half ? r + half : r - half;
-    const float2 fr = p.rope[dim < half ? dim : dim - half];
+    const float2 fr = pre.have_fr ? pre.fr : p.rope[dim < half ? dim : dim - half];
     // slot = len + node index; rotary position = len + node depth (the node
     // index itself for a chain)
     int slotv[16], posv[16], okv[16];
+    if (pre.qkv) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {  // sequence bookkeeping, loads in flight together
-      const int m = min(p.tok0 + c0 + j, p.M - 1);
-      const int b = m / p.n_per_seq;
-      const int base = ldcg_i(p.pos_base + b), node = m - b * p.n_per_seq;
-      slotv[j] = base + node;
-      posv[j] = base + (p.depth ? __ldg(p.depth + m) : node);
-      okv[j] = ldcg_i(p.seq_ok + b);
+      for (int j = 0; j < 16; ++j) {
+        slotv[j] = pre.qkv[c0 + j];
+        posv[j] = pre.qkv[128 + c0 + j];
+        okv[j] = pre.qkv[256 + c0 + j];
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {  // sequence bookkeeping, loads in flight together
+        const int m = min(p.tok0 + c0 + j, p.M - 1);
+        const int b = m / p.n_per_seq;
+        const int base = ldcg_i(p.pos_base + b), node = m - b * p.n_per_seq;
+        slotv[j] = base + node;
+        posv[j] = base + (p.depth ? __ldg(p.depth + m) : node);
+        okv[j] = ldcg_i(p.seq_ok + b);
+      }
     }
 #pragma unroll 4
     for (int j = 0; j < 16; ++j) {
@@ -296,7 +317,7 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
 __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Smem& sm, uint32_t tile, int r,
                                                int c0, const float (&acc)[16]) {
   const float none[16] = {};
-  epilogue_chunk_h(p, sm, tile, r, c0, acc, none, false);
+  epilogue_chunk_h(p, sm, tile, r, c0, acc, none, false, EpiPre{});
 }
 
 }  // namespace

@@ -120,9 +120,10 @@ struct MkParams {
   float* h;
   uint16_t *hb, *hb_lo, *q, *q_lo, *o, *o_lo, *act, *act_lo;
   float* ssq;
-  float* partials;
+  float* partials;                        // stream-K words: [grid][2][ntok][128] x 8 bytes
   int32_t* counters;
   unsigned* bar;                          // grid-barrier arrivals, zero at launch
+  unsigned* epoch;                        // launch epoch (advanced by every launch; never cleared)
   int32_t* status;
   int32_t* pos_base;
   int32_t* seq_ok;
