@@ -37,24 +37,30 @@ METRIC = "verify-pass HBM GB/s (% of peak) and emitted tokens/s, 8B-shape γ=4, 
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from ncu
 # captures summarised under profiles/, keyed by the sha1 of the kernel's
-# source file: reported only while the source is the one that was measured.
+# source files (concatenated in the order listed): reported only while the
+# sources are the ones that were measured.
 TRAFFIC = {
     # one 8B-dims layer's four GEMMs x 32 + the LM head, / 129 launches
-    "gemm_tc_kernel": {"file": "gemm.cu", "source_sha1": "8e216fc32ca40f7636d65c01def4ef52f68a3a17",
+    "gemm_tc_kernel": {"files": ["gemm.cu", "gemm_common.cuh", "common.cuh", "internal.h"],
+                       "source_sha1": "8e216fc32ca40f7636d65c01def4ef52f68a3a17",
                        "bytes_per_launch": 118288036},
-    # 2-layer 8B-dims capture scaled to 32 layers by the algorithmic bytes
-    # (profiles/forward_kernel_8b_2layers.md)
-    "forward_kernel": {"file": "forward.cu", "source_sha1": "32656b28ccacbb51d79e6b575fd8320b1c3cafce",
-                       "bytes_per_launch": 15348201291},
+    # a 2-layer capture with the 8B dimensions, scaled to 32 layers by the
+    # algorithmic bytes (weights, KV and logits each move once)
+    "forward_kernel": {"files": ["forward.cu", "gemm_common.cuh", "attn_common.cuh", "common.cuh",
+                                 "internal.h"],
+                       "source_sha1": "8c8b97e7c7f62b1d7cd86e312f1efb7d12b3c9bc",
+                       "bytes_per_launch": 15345739312},
 }
 
 
 def kernel_traffic(kernel: str):
     import hashlib
     t = TRAFFIC[kernel]
-    src = os.path.join(ROOT, "speculative_decoding_verification_pass_gb300", "csrc", t["file"])
-    with open(src, "rb") as f:
-        ok = hashlib.sha1(f.read()).hexdigest() == t["source_sha1"]
+    h = hashlib.sha1()
+    for f in t["files"]:
+        with open(os.path.join(ROOT, "speculative_decoding_verification_pass_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    ok = h.hexdigest() == t["source_sha1"]
     return t["bytes_per_launch"] if ok else None
 
 
