@@ -395,6 +395,119 @@ def blas_threads():
     return os.cpu_count()
 
 
+# ----------------------------------------------------------- tree rounds
+TREE_PARENTS = [-1, 0, 0, 1, 1, 2, 2]   # root + full binary tree of depth 2 (6 drafted nodes)
+
+
+class TreeRound:
+    """Draft-tree verification on the same model and cache: the root is the
+    last emitted token, every node's children are two independent draws from
+    a noisy copy of the target's distribution at that node (drafted level by
+    level with untimed tree passes); the timed round is the tree forward,
+    the tree accept walk and the KV commit."""
+
+    def __init__(self, w: Workload):
+        self.w = w
+        B, V = w.B, w.cfg.vocab
+        self.par = TREE_PARENTS
+        self.n = len(self.par)
+        dev = "cuda"
+        self.tokens = torch.zeros(B, self.n, dtype=torch.int32, device=dev)
+        self.parents = torch.tensor([self.par] * B, dtype=torch.int32, device=dev)
+        anc, dep = [], []
+        for k in range(1, self.n + 1):
+            a, d = sb.spec_tree_masks(self.par[:k])
+            anc.append(a)
+            dep.append(d)
+        self.masks = []   # per prefix size: (anc, depth) on the device
+        for a, d in zip(anc, dep):
+            at = torch.from_numpy(np.array([a] * B, dtype=np.uint64).view(np.int64)).to(dev)
+            dt = torch.tensor([d] * B, dtype=torch.int32, device=dev)
+            self.masks.append((at, dt))
+        self.logits = torch.empty(B, self.n, V, device=dev)
+        self.q = torch.zeros(B, self.n, V, device=dev)
+        self.u = torch.zeros(B, self.n, device=dev)
+        self.out = torch.empty(B, self.n, dtype=torch.int32, device=dev)
+        self.path = torch.empty(B, self.n, dtype=torch.int32, device=dev)
+        self.nacc = torch.empty(B, dtype=torch.int32, device=dev)
+        self.tws = sb.workspace(sb.spec_tree_accept_workspace_bytes(B, V))
+        self.fws = sb.workspace(sb.spec_workspace_bytes(w.cfg, B, self.n - 1, w.cap))
+        self.qrows = torch.empty(2 * B, V, device=dev)
+        self.xrows = torch.empty(2 * B, dtype=torch.int32, device=dev)
+        self.emitted = 0
+
+    def draft(self):
+        w, B, V = self.w, self.w.B, self.w.cfg.vocab
+        self.tokens[:, 0] = w.t_last
+        # levels: nodes 0 | 1 2 | 3 4 5 6; node c's children are 2c + 1, 2c + 2
+        for k, level in ((1, [0]), (3, [1, 2])):
+            z = torch.empty(B, k, V, device="cuda")
+            a, d = self.masks[k - 1]
+            sb.spec_verify_forward_tree(w.model.handle, self.tokens[:, :k].contiguous(), a, d, B, k,
+                                        w.kv, z, self.fws)
+            w.kv.len.fill_(w.ctx)
+            for c in level:
+                zq = z[:, c] + w.sigma * torch.randn(B, V, device="cuda", generator=w.gen)
+                zq2 = zq.repeat_interleave(2, dim=0).contiguous()
+                ud = torch.rand(2 * B, device="cuda", generator=w.gen)
+                sb.spec_draft_sample(zq2, 2 * B, V, w.T, w.top_p, ud, self.qrows, self.xrows, w.aws)
+                self.q[:, c] = self.qrows.view(B, 2, V)[:, 0]
+                self.tokens[:, 2 * c + 1:2 * c + 3] = self.xrows.view(B, 2)
+        self.u.copy_(torch.rand(B, self.n, device="cuda", generator=w.gen))
+
+    def step(self):
+        w = self.w
+        a, d = self.masks[-1]
+        sb.spec_verify_forward_tree(w.model.handle, self.tokens, a, d, w.B, self.n, w.kv, self.logits,
+                                    self.fws)
+        sb.spec_tree_accept(self.logits, self.q, self.tokens, self.parents, self.u, w.B, self.n,
+                            w.cfg.vocab, w.T, w.top_p, self.out, self.path, self.nacc, self.tws)
+        sb.spec_kv_tree_commit(w.model.handle, w.kv, self.path, self.nacc, self.n, self.fws)
+
+    def finish(self):
+        w = self.w
+        n = self.nacc.cpu().numpy()
+        o = self.out.cpu().numpy()
+        self.emitted += int((n + 1).sum())
+        w.t_last = torch.from_numpy(o[np.arange(w.B), n].astype(np.int32)).cuda()
+        w.kv.len.fill_(w.ctx)
+
+
+def time_tree(w: Workload, K: int, warmup: int = 2):
+    tr = TreeRound(w)
+    times = []
+    for i in range(warmup + K):
+        tr.draft()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        tr.step()
+        b.record()
+        torch.cuda.synchronize()
+        if i == warmup - 1:
+            tr.emitted = 0
+        if i >= warmup:
+            times.append(a.elapsed_time(b))
+        tr.finish()
+    for ws in (tr.tws, tr.fws):
+        st, bits = sb.spec_device_status(ws)
+        if st != sb.SPEC_OK:
+            raise RuntimeError(f"tree device status {hex(bits)}")
+    w.check_status()
+    ms = sum(times) / len(times)
+    c = w.cfg
+    hd, d = c.head_dim, c.d_model
+    kv_tok = c.n_layers * c.n_kv_heads * hd * 2 * 2
+    fwd = w.gemm_bytes() + w.B * tr.n * d * 2 + w.B * ((w.ctx + tr.n) * kv_tok + tr.n * kv_tok) \
+        + w.B * tr.n * c.vocab * 4
+    return {"workload": f"draft tree: root + full binary tree of depth 2 ({tr.n - 1} drafted "
+                        f"nodes), batch {w.B}, context {w.ctx}, same model, draft and T",
+            "ms_per_round": ms, "emitted_per_round": tr.emitted / (K * w.B),
+            "emitted_tokens_per_s": tr.emitted / (sum(times) / 1e3),
+            "hbm_gbs": fwd / (ms / 1e3) / 1e9, "rounds": K}
+
+
 # ------------------------------------------------------------------ main
 def parse():
     ap = argparse.ArgumentParser()
@@ -491,6 +604,10 @@ def main():
     for ms, n, by in instrumented(w, k_inst):
         gm += ms[0]; gn += n[0]; gb += by[0]; am += ms[1]; an += n[1]; pm += ms[2]; pn += n[2]
     acc_ms = accept_time(w, 10)
+    try:
+        tree = time_tree(w, max(5, args.steps // 2)) if w.n <= 8 else None
+    except Exception as exc:
+        tree = {"unavailable": str(exc).splitlines()[0][:200]}
     hbm, _, src = peaks()
     # launches of this library's kernels per step: the forward's (one
     # persistent kernel, or embedding + per-step GEMM / attention kernels),
@@ -524,6 +641,8 @@ def main():
                      "launch_ms": k_ms / k_n if k_n else None},
         "clocks": clk.summary(),
     }
+    if tree is not None:
+        line["tree"] = tree
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         est, sample = oracle_step_estimate(cfg, args.batch, args.gamma, args.context,
                                            args.temperature, 3)
