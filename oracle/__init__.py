@@ -17,6 +17,10 @@ model    -- the Llama-style decoder forward over the gamma+1 new positions
 weights  -- the seeded synthetic weights: Philox4x64-10 counter-based
             generator + Box-Muller in fp64, rounded to bf16.
 bf16     -- round-to-nearest-even conversion of fp64 values to bf16.
+tree     -- draft-tree verification: ancestor masks and depths, the tree
+            forward, the per-node acceptance walk, the KV commit.
+constrain -- constrained acceptance: one allowed-token mask applied to the
+            target and draft logits alike.
 
 Every function cites the passage it follows.  Parity status per function:
 
@@ -31,4 +35,11 @@ Every function cites the passage it follows.  Parity status per function:
                                values are otherwise unpinned.
 * weights                      pinned by the published Philox4x64-10
                                known-answer vectors and normal moments.
+* tree.*                       pinned (the printed mask / depths and
+                               expected-depth values, simulated coins, chain
+                               equivalence, path-by-path chain passes,
+                               chi-square of the walk's output)
+* constrain.apply_mask         pinned (restricted-softmax closed form,
+                               chi-square and acceptance rate with the same
+                               mask on both sides, one-sided mask breaks it)
 """
