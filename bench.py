@@ -346,6 +346,34 @@ def accept_time(w: Workload, K: int):
     return statistics.median(ts)
 
 
+def mask_time(w: Workload, K: int, frac: float = 0.05):
+    """Constrained rows: spec_mask_logits on the step's target logits (a copy)
+    with one allowed-token set per row (a narrow, JSON-like set), then the
+    accept on the masked rows.  Median device microseconds of each."""
+    rows, V = w.B * w.n, w.cfg.vocab
+    allowed = torch.from_numpy(wl.pack_allowed(wl.allowed_sets(17, rows, V, frac))).cuda()
+    z = w.logits.clone()
+    st = torch.cuda.current_stream()
+    tm, ta = [], []
+    for _ in range(K):
+        z.copy_(w.logits)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        c = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        sb.spec_mask_logits(z, allowed, rows, V, w.aws)
+        b.record(st)
+        sb.spec_accept(z, w.q, w.x, w.u, w.B, w.gamma, V, w.T, w.top_p, w.out, w.nacc, w.aws)
+        c.record(st)
+        torch.cuda.synchronize()
+        tm.append(a.elapsed_time(b))
+        ta.append(b.elapsed_time(c))
+    stt, bits = sb.spec_device_status(w.aws)   # drafts outside the mask read as q(x) = 0
+    if stt not in (sb.SPEC_OK, sb.SPEC_EDEVICE) or (bits & ~sb.DEV_Q_ZERO):
+        raise RuntimeError(f"mask device status {hex(bits)}")
+    return statistics.median(tm) * 1e3, statistics.median(ta) * 1e3
+
+
 # ------------------------------------------------------------- CPU oracle
 def oracle_step_estimate(cfg: sb.ModelConfig, B: int, gamma: int, ctx: int, T: float, seed: int,
                          head_rows: int = 8192):
@@ -605,6 +633,14 @@ def main():
         gm += ms[0]; gn += n[0]; gb += by[0]; am += ms[1]; an += n[1]; pm += ms[2]; pn += n[2]
     acc_ms = accept_time(w, 10)
     try:
+        m_us, ma_us = mask_time(w, 10)
+        constrained = {"workload": f"one allowed-token set per target row ({w.B * w.n} rows x "
+                                   f"{w.cfg.vocab}, 5% of tokens allowed)",
+                       "mask_us": m_us, "masked_accept_us": ma_us,
+                       "mask_frac_of_step": m_us / (t_total / args.steps * 1e6)}
+    except Exception as exc:
+        constrained = {"unavailable": str(exc).splitlines()[0][:200]}
+    try:
         tree = time_tree(w, max(5, args.steps // 2)) if w.n <= 8 else None
     except Exception as exc:
         tree = {"unavailable": str(exc).splitlines()[0][:200]}
@@ -641,6 +677,7 @@ def main():
                      "launch_ms": k_ms / k_n if k_n else None},
         "clocks": clk.summary(),
     }
+    line["constrained"] = constrained
     if tree is not None:
         line["tree"] = tree
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -73,6 +73,7 @@ typedef enum {
 #define SPEC_DEV_TIMEOUT       0x8   /* a bounded wait in a kernel gave up */
 #define SPEC_DEV_BAD_NACC      0x10  /* truncate: n_accepted outside [0, gamma] */
 #define SPEC_DEV_BAD_TREE      0x20  /* tree accept / commit: bad parents, path or n_accepted */
+#define SPEC_DEV_EMPTY_MASK    0x40  /* mask_logits: a row's mask allows no token */
 
 /* Text for a spec_status value (static storage). */
 const char* spec_status_string(int status);
@@ -257,6 +258,29 @@ int spec_accept(const float* d_target_logits, const float* d_draft_probs,
 int spec_draft_sample(const float* d_logits, int rows, int vocab, float temperature, float top_p,
                       const float* d_uniforms, float* d_probs, int32_t* d_tokens, void* d_ws,
                       size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------ constrained rows */
+/* Constrained generation ([engine] the question on JSON mode / grammar
+ * constraints): the target and the draft apply the SAME allowed-token mask
+ * before their probabilities are formed, the caller's constraint automaton
+ * running in lockstep for both (a mask on one side only makes the acceptance
+ * ratios wrong).  This call applies one mask per logits row in place:
+ * d_logits[r][x] = -inf wherever bit (x % 32) of d_allowed[r][x / 32] is 0,
+ * so the softmax gives those tokens probability 0 and the allowed tokens
+ * keep their relative weights.  Apply it to the target rows before
+ * spec_accept and to the draft rows before spec_draft_sample (or before
+ * forming q): spec_accept, spec_draft_sample and spec_tree_accept handle
+ * -inf logits.  Under greedy decoding the argmax is over the allowed tokens.
+ *   d_logits   fp32 [rows][vocab], modified in place; rows <= 65535 (else
+ *              SPEC_ESIZE).
+ *   d_allowed  uint32 [rows][ceil(vocab / 32)]; bits at ids >= vocab are
+ *              ignored.
+ *   d_ws       any workspace of this library (its status word is used).
+ * A row whose mask allows no token is left unchanged and sets
+ * SPEC_DEV_EMPTY_MASK.  A drafted token outside the mask then has q(x) = 0
+ * and is a rejection (SPEC_DEV_Q_ZERO). */
+int spec_mask_logits(float* d_logits, const uint32_t* d_allowed, int rows, int vocab, void* d_ws,
+                     void* stream);
 
 /* --------------------------------------------------------------- rollback */
 /* KV rollback after a pass that appended gamma+1 slots ([engine] Rollback

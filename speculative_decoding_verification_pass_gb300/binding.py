@@ -20,6 +20,7 @@ SPEC_OK, SPEC_EINVAL, SPEC_ESIZE, SPEC_ECUDA, SPEC_EDEVICE, SPEC_ETIMEOUT, SPEC_
     0, -1, -2, -3, -4, -5, -6)
 DEV_BAD_TOKEN, DEV_KV_OVERFLOW, DEV_Q_ZERO, DEV_TIMEOUT, DEV_BAD_NACC, DEV_BAD_TREE = (
     0x1, 0x2, 0x4, 0x8, 0x10, 0x20)
+DEV_EMPTY_MASK = 0x40
 
 
 class SpecError(RuntimeError):
@@ -66,6 +67,7 @@ _SIGS = {
     "spec_accept": (_I, [_P, _P, _P, _P, _I, _I, _I, _F, _F, _P, _P, _P, _SZ, _P]),
     "spec_draft_sample": (_I, [_P, _I, _I, _F, _F, _P, _P, _P, _P, _SZ, _P]),
     "spec_kv_truncate": (_I, [ctypes.POINTER(spec_kv_cache), _P, _I, _P, _P]),
+    "spec_mask_logits": (_I, [_P, _P, _I, _I, _P, _P]),
     "spec_tree_masks": (_I, [ctypes.POINTER(ctypes.c_int32), _I, ctypes.POINTER(ctypes.c_uint64),
                              ctypes.POINTER(ctypes.c_int32)]),
     "spec_verify_forward_tree": (_I, [_P, _P, _P, _P, _I, _I, ctypes.POINTER(spec_kv_cache), _P, _P,
@@ -227,6 +229,12 @@ def spec_draft_sample(logits, rows: int, vocab: int, temperature: float, top_p: 
 def spec_kv_truncate(kv: "KVCache", n_accepted, gamma: int, ws, stream=None):
     _check(lib().spec_kv_truncate(ctypes.byref(kv.c()), _ptr(n_accepted), gamma, _ptr(ws),
                                   _stream(stream)), "spec_kv_truncate")
+
+
+def spec_mask_logits(logits, allowed, rows: int, vocab: int, ws, stream=None):
+    """logits[r][x] = -inf where bit x of row r's packed mask is clear (in place)."""
+    _check(lib().spec_mask_logits(_ptr(logits), _ptr(allowed), rows, vocab, _ptr(ws), _stream(stream)),
+           "spec_mask_logits")
 
 
 def spec_tree_masks(parents) -> tuple[list, list]:

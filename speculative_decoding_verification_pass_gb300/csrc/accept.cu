@@ -125,7 +125,7 @@ __device__ void row_stats(const float* z, int V, float c, Red& r, float& m_out, 
     if (v > m) {
       s = (m == -INFINITY ? 0.f : s * exp2f((m - v) * c)) + 1.0f;
       m = v;
-    } else {
+    } else if (v != -INFINITY) {  // masked-out logits (-inf) weigh nothing
       s += exp2f((v - m) * c);
     }
   }
@@ -517,7 +517,7 @@ __device__ float2 chunk_ms(const float* z, int x0, int x1, float c, ASmem& s) {
     if (v > m) {
       sum = (m == -INFINITY ? 0.f : sum * exp2f((m - v) * c)) + 1.0f;
       m = v;
-    } else {
+    } else if (v != -INFINITY) {  // masked-out logits (-inf) weigh nothing
       sum += exp2f((v - m) * c);
     }
   }
@@ -1068,6 +1068,72 @@ __global__ void __launch_bounds__(kT, 1) sample_kernel(const SampleParams p) {
   if (threadIdx.x == 0) p.tokens[row] = t < 0 ? 0 : t;
 }
 
+// ------------------------------------------------------- constrained rows
+// Constrained generation ("Build a Speculative Decoding Engine ...", the
+// question on JSON / grammar constraints): the target and the draft apply the
+// same allowed-token mask before their probabilities are formed.  A masked
+// logit becomes -inf, so its probability is 0 after the softmax and the rule
+// runs unchanged.  Grid (row, 256-word chunk); a thread owns one mask word
+// (32 ids) and rewrites only the float4 groups holding a disallowed id.  Every
+// CTA first counts its row's allowed ids (the whole mask row, from L2): a row
+// whose mask allows nothing is left as it is and flagged.
+constexpr int kMaskThreads = 256;
+
+__global__ void __launch_bounds__(kMaskThreads) mask_logits_kernel(float* logits, const uint32_t* allowed,
+                                                                   int V, int vec4, int32_t* status) {
+  __shared__ int s_cnt[kMaskThreads / 32];
+  const int row = blockIdx.y;
+  const int W = (V + 31) / 32;
+  const uint32_t* a = allowed + static_cast<long long>(row) * W;
+  float* z = logits + static_cast<long long>(row) * V;
+  int cnt = 0;
+  // 8 mask words per thread in flight at a time (the count is latency-bound)
+  for (int w0 = threadIdx.x; w0 < W; w0 += 8 * kMaskThreads) {
+    uint32_t bits[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int w = w0 + k * kMaskThreads;
+      bits[k] = w < W ? __ldg(a + w) : 0u;
+      if (w == W - 1 && (V & 31)) bits[k] &= (1u << (V & 31)) - 1u;  // ids past V are not tokens
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) cnt += __popc(bits[k]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if ((threadIdx.x & 31) == 0) s_cnt[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  int total = 0;
+#pragma unroll
+  for (int k = 0; k < kMaskThreads / 32; ++k) total += s_cnt[k];
+  if (total == 0) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, SPEC_DEV_EMPTY_MASK);
+    return;
+  }
+  const int w = blockIdx.x * kMaskThreads + threadIdx.x;
+  if (w >= W) return;
+  const uint32_t bits = __ldg(a + w);
+  const int x0 = w * 32, n = min(32, V - x0);
+  if (n == 32 && bits == 0xffffffffu) return;
+  if (vec4 && n == 32) {
+    float4* z4 = reinterpret_cast<float4*>(z + x0);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint32_t nib = (bits >> (4 * g)) & 0xFu;
+      if (nib == 0xFu) continue;
+      float4 v = z4[g];
+      if (!(nib & 1u)) v.x = -INFINITY;
+      if (!(nib & 2u)) v.y = -INFINITY;
+      if (!(nib & 4u)) v.z = -INFINITY;
+      if (!(nib & 8u)) v.w = -INFINITY;
+      z4[g] = v;
+    }
+  } else {
+    for (int k = 0; k < n; ++k)
+      if (!((bits >> k) & 1u)) z[x0 + k] = -INFINITY;
+  }
+}
+
 // ------------------------------------------------------------- tree accept
 // The acceptance walk over one sequence's draft tree ("Speculative Decoding:
 // Speeding Sequential Generation", Tree-Based Drafting: the accept/reject test
@@ -1384,6 +1450,16 @@ cudaError_t launch_truncate(int32_t* len, const int32_t* n_acc, int B, int gamma
   void* args[] = {&len, const_cast<int32_t**>(&n_acc), &B, &gamma, &status};
   return launch_pdl(reinterpret_cast<const void*>(truncate_kernel), dim3((B + 127) / 128),
                     dim3(128), args, stream, pdl);
+}
+
+cudaError_t launch_mask_logits(float* logits, const uint32_t* allowed, int rows, int V, int32_t* status,
+                               cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const int W = (V + 31) / 32;
+  const int vec4 = (V % 4 == 0 && reinterpret_cast<uintptr_t>(logits) % 16 == 0) ? 1 : 0;
+  const dim3 grid((W + kMaskThreads - 1) / kMaskThreads, rows);
+  mask_logits_kernel<<<grid, kMaskThreads, 0, stream>>>(logits, allowed, V, vec4, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tree_accept(const TreeAcceptParams& p, cudaStream_t stream) {

@@ -1036,6 +1036,15 @@ int spec_kv_truncate(const spec_kv_cache* kv, const int32_t* d_n_accepted, int g
   return SPEC_OK;
 }
 
+int spec_mask_logits(float* d_logits, const uint32_t* d_allowed, int rows, int vocab, void* d_ws,
+                     void* stream) {
+  if (!d_logits || !d_allowed || !d_ws || rows < 0 || vocab <= 0) return SPEC_EINVAL;
+  if (rows > 65535) return SPEC_ESIZE;
+  SPEC_CUDA(launch_mask_logits(d_logits, d_allowed, rows, vocab, static_cast<int32_t*>(d_ws),
+                               static_cast<cudaStream_t>(stream)));
+  return SPEC_OK;
+}
+
 size_t spec_tree_accept_workspace_bytes(int batch, int vocab) {
   if (batch < 0 || vocab <= 0) return 0;
   return 64 + align_up(static_cast<size_t>(batch) * static_cast<size_t>(vocab) * 4);

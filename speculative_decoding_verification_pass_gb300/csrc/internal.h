@@ -231,6 +231,10 @@ struct TreeAcceptParams {
 };
 cudaError_t launch_tree_accept(const TreeAcceptParams& p, cudaStream_t stream);
 
+// logits[r][x] = -inf where bit x % 32 of allowed[r][x / 32] is clear
+cudaError_t launch_mask_logits(float* logits, const uint32_t* allowed, int rows, int V, int32_t* status,
+                               cudaStream_t stream);
+
 struct TreeCommitParams {
   uint16_t* k;             // [L][B][Hkv][cap][hd]
   uint16_t* v;

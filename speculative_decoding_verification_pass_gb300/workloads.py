@@ -87,3 +87,23 @@ def random_tree(seed: int, n: int, stream: int = 10) -> list:
     (parent -1), node i > 0 hangs under a uniformly chosen earlier node."""
     g = rng(seed, stream)
     return [-1] + [int(g.integers(0, i)) for i in range(1, n)]
+
+
+def allowed_sets(seed: int, rows: int, vocab: int, frac: float, stream: int = 14) -> np.ndarray:
+    """A random allowed-token set per row (bool [rows][vocab]), each token
+    allowed with probability frac and at least one per row."""
+    a = rng(seed, stream).random((rows, vocab)) < frac
+    a[~a.any(axis=1), 0] = True
+    return a
+
+
+def pack_allowed(a) -> np.ndarray:
+    """Bool [rows][vocab] -> uint32 [rows][ceil(vocab / 32)], token x at bit
+    x % 32 of word x / 32."""
+    a = np.asarray(a, dtype=bool)
+    rows, V = a.shape
+    W = (V + 31) // 32
+    pad = np.zeros((rows, W * 32), dtype=bool)
+    pad[:, :V] = a
+    bits = pad.reshape(rows, W, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)
+    return bits.sum(axis=2).astype(np.uint32)
