@@ -21,6 +21,8 @@ tree     -- draft-tree verification: ancestor masks and depths, the tree
             forward, the per-node acceptance walk, the KV commit.
 constrain -- constrained acceptance: one allowed-token mask applied to the
             target and draft logits alike.
+gamma    -- the dynamic speculation-depth controller (rolling acceptance
+            window, depth maximising expected tokens per millisecond).
 
 Every function cites the passage it follows.  Parity status per function:
 
@@ -39,6 +41,10 @@ Every function cites the passage it follows.  Parity status per function:
                                expected-depth values, simulated coins, chain
                                equivalence, path-by-path chain passes,
                                chi-square of the walk's output)
+* gamma.*                      pinned (printed expected-token values,
+                               simulated coins, simulated throughput per
+                               depth, limits, the page's alpha < 0.65
+                               statement, window and warm-up)
 * constrain.apply_mask         pinned (restricted-softmax closed form,
                                chi-square and acceptance rate with the same
                                mask on both sides, one-sided mask breaks it)
