@@ -374,6 +374,41 @@ def mask_time(w: Workload, K: int, frac: float = 0.05):
     return statistics.median(tm) * 1e3, statistics.median(ta) * 1e3
 
 
+def gamma_ctl_probe(w: Workload, alpha: float, step_ms: float):
+    """The host-side depth controller: its cost per recorded step for 64
+    slots, and the depth it picks at the measured acceptance rate with the
+    page's costs (2.0 ms per draft token, 20.0 ms per target pass) and with
+    this run's own costs (one single-token pass of the drafting harness,
+    one verify step)."""
+    B = w.B
+    cur = w.t_last.view(B, 1).clone()
+    ts = []
+    for _ in range(5):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        sb.spec_verify_forward(w.model.handle, cur, B, 0, w.kv, w.zrow, w.ws)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+        w.kv.len.fill_(w.ctx)
+    draft_ms = statistics.median(ts)
+    ctl = sb.GammaController(64)
+    rng = np.random.default_rng(0)
+    slots = list(range(64))
+    used = [4] * 64
+    accs = [rng.integers(0, 5, size=64).tolist() for _ in range(200)]
+    t0 = time.perf_counter()
+    for a in accs:
+        used = ctl.step(slots, used, [min(x, u) for x, u in zip(a, used)])
+    host_us = (time.perf_counter() - t0) / len(accs) * 1e6
+    ctl.close()
+    return {"host_us_per_step_64_slots": host_us, "alpha_measured": alpha,
+            "gamma_page_costs": sb.spec_gamma_optimal(alpha, 2, 8, 2.0, 20.0),
+            "draft_pass_ms": draft_ms, "verify_step_ms": step_ms,
+            "gamma_measured_costs": sb.spec_gamma_optimal(alpha, 2, 8, draft_ms, step_ms)}
+
+
 # ------------------------------------------------------------- CPU oracle
 def oracle_step_estimate(cfg: sb.ModelConfig, B: int, gamma: int, ctx: int, T: float, seed: int,
                          head_rows: int = 8192):
@@ -641,6 +676,11 @@ def main():
     except Exception as exc:
         constrained = {"unavailable": str(exc).splitlines()[0][:200]}
     try:
+        gctl = gamma_ctl_probe(w, accepted / max(1, args.steps * args.batch * args.gamma),
+                               t_total / args.steps * 1e3)
+    except Exception as exc:
+        gctl = {"unavailable": str(exc).splitlines()[0][:200]}
+    try:
         tree = time_tree(w, max(5, args.steps // 2)) if w.n <= 8 else None
     except Exception as exc:
         tree = {"unavailable": str(exc).splitlines()[0][:200]}
@@ -678,6 +718,7 @@ def main():
         "clocks": clk.summary(),
     }
     line["constrained"] = constrained
+    line["gamma_ctl"] = gctl
     if tree is not None:
         line["tree"] = tree
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

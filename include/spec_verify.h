@@ -385,6 +385,48 @@ int spec_tree_accept(const float* d_target_logits, const float* d_draft_probs,
 int spec_kv_tree_commit(const spec_model* model, const spec_kv_cache* kv, const int32_t* d_path,
                         const int32_t* d_n_accepted, int n_nodes, void* d_ws, void* stream);
 
+/* ---------------------------------------------------------- dynamic gamma */
+/* The speculation-depth controller ([engine] Speculation Depth Tuning and
+ * Tree Drafting; Dynamic Gamma Controller).  Host only (no device access,
+ * no stream): after each pass the caller records, per slot, the depth it
+ * used and its n_accepted (spec_accept's output, copied to the host); each
+ * slot keeps its last `window` passes and, once `min_records` are in,
+ * chooses the depth in [gamma_min, gamma_max] that maximises expected
+ * tokens per millisecond,
+ *     E(alpha, g) / (g * draft_ms_per_token + target_ms_per_pass),
+ *     E(alpha, g) = (1 - alpha^(g+1)) / (1 - alpha)   (g + 1 at alpha >= 1),
+ * with alpha = accepted drafts / drafted tokens over the window
+ * (alpha_prior while the window is empty).  Ties go to the smaller depth.
+ * A slot is a sequence, or a group of sequences the caller pools (e.g. one
+ * content type, [engine] the multi-tenant question).  The page's setting:
+ * depths 2..8 starting at 4, window 20, decisions after 5 passes, 2.0 ms
+ * per draft token, 20.0 ms per target pass (calibrate both), prior 0.80.
+ * Not thread-safe per controller. */
+typedef struct spec_gamma_ctl spec_gamma_ctl;
+
+int spec_gamma_ctl_create(int slots, int gamma_min, int gamma_max, int gamma_init, int window,
+                          int min_records, double draft_ms_per_token, double target_ms_per_pass,
+                          double alpha_prior, spec_gamma_ctl** out);
+int spec_gamma_ctl_destroy(spec_gamma_ctl* ctl);
+/* Forget slot's passes (a new sequence in the slot); its depth returns to
+ * gamma_init. */
+int spec_gamma_ctl_reset(spec_gamma_ctl* ctl, int slot);
+/* Record n passes: h_slot[i] used depth h_gamma_used[i] and accepted
+ * h_n_accepted[i] drafts (host arrays of n entries; a slot may appear more
+ * than once, in order).  h_gamma_next[i] receives that slot's depth for its
+ * next pass.  An entry with a slot outside [0, slots) or n_accepted outside
+ * [0, gamma_used] returns SPEC_EINVAL and records nothing. */
+int spec_gamma_ctl_step(spec_gamma_ctl* ctl, int n, const int32_t* h_slot,
+                        const int32_t* h_gamma_used, const int32_t* h_n_accepted,
+                        int32_t* h_gamma_next);
+/* A slot's current alpha estimate, depth and number of passes in its window
+ * (any output pointer may be NULL). */
+int spec_gamma_ctl_state(const spec_gamma_ctl* ctl, int slot, double* out_alpha,
+                         int32_t* out_gamma, int32_t* out_records);
+/* The depth rule alone, for a given alpha (clamped to 1). */
+int spec_gamma_optimal(double alpha, int gamma_min, int gamma_max, double draft_ms_per_token,
+                       double target_ms_per_pass, int32_t* out_gamma);
+
 /* ----------------------------------------------------------------- status */
 /* Synchronise `stream`, read the device status word of workspace d_ws into
  * *out (a SPEC_DEV_* bit set), clear it, and return SPEC_OK if it was 0,

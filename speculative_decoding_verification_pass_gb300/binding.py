@@ -68,6 +68,15 @@ _SIGS = {
     "spec_draft_sample": (_I, [_P, _I, _I, _F, _F, _P, _P, _P, _P, _SZ, _P]),
     "spec_kv_truncate": (_I, [ctypes.POINTER(spec_kv_cache), _P, _I, _P, _P]),
     "spec_mask_logits": (_I, [_P, _P, _I, _I, _P, _P]),
+    "spec_gamma_ctl_create": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_double, ctypes.c_double,
+                                   ctypes.c_double, ctypes.POINTER(_P)]),
+    "spec_gamma_ctl_destroy": (_I, [_P]),
+    "spec_gamma_ctl_reset": (_I, [_P, _I]),
+    "spec_gamma_ctl_step": (_I, [_P, _I, _P, _P, _P, _P]),
+    "spec_gamma_ctl_state": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32),
+                                  ctypes.POINTER(ctypes.c_int32)]),
+    "spec_gamma_optimal": (_I, [ctypes.c_double, _I, _I, ctypes.c_double, ctypes.c_double,
+                                ctypes.POINTER(ctypes.c_int32)]),
     "spec_tree_masks": (_I, [ctypes.POINTER(ctypes.c_int32), _I, ctypes.POINTER(ctypes.c_uint64),
                              ctypes.POINTER(ctypes.c_int32)]),
     "spec_verify_forward_tree": (_I, [_P, _P, _P, _P, _I, _I, ctypes.POINTER(spec_kv_cache), _P, _P,
@@ -235,6 +244,57 @@ def spec_mask_logits(logits, allowed, rows: int, vocab: int, ws, stream=None):
     """logits[r][x] = -inf where bit x of row r's packed mask is clear (in place)."""
     _check(lib().spec_mask_logits(_ptr(logits), _ptr(allowed), rows, vocab, _ptr(ws), _stream(stream)),
            "spec_mask_logits")
+
+
+class GammaController:
+    """Host-side speculation-depth controller (spec_gamma_ctl_*): one rolling
+    acceptance window per slot, the depth maximising expected tokens/ms."""
+
+    def __init__(self, slots: int, gamma_min: int = 2, gamma_max: int = 8, gamma_init: int = 4,
+                 window: int = 20, min_records: int = 5, draft_ms_per_token: float = 2.0,
+                 target_ms_per_pass: float = 20.0, alpha_prior: float = 0.80):
+        h = ctypes.c_void_p()
+        _check(lib().spec_gamma_ctl_create(slots, gamma_min, gamma_max, gamma_init, window,
+                                           min_records, draft_ms_per_token, target_ms_per_pass,
+                                           alpha_prior, ctypes.byref(h)), "spec_gamma_ctl_create")
+        self.handle = h.value
+        self.slots = slots
+
+    def step(self, slots, gamma_used, n_accepted) -> list:
+        n = len(slots)
+        arr = lambda v: (ctypes.c_int32 * max(n, 1))(*[int(x) for x in v])
+        s, g, a = arr(slots), arr(gamma_used), arr(n_accepted)
+        out = (ctypes.c_int32 * max(n, 1))()
+        _check(lib().spec_gamma_ctl_step(self.handle, n, s, g, a, out), "spec_gamma_ctl_step")
+        return list(out)[:n]
+
+    def state(self, slot: int):
+        al, g, r = ctypes.c_double(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().spec_gamma_ctl_state(self.handle, slot, ctypes.byref(al), ctypes.byref(g),
+                                          ctypes.byref(r)), "spec_gamma_ctl_state")
+        return al.value, g.value, r.value
+
+    def reset(self, slot: int):
+        _check(lib().spec_gamma_ctl_reset(self.handle, slot), "spec_gamma_ctl_reset")
+
+    def close(self):
+        if self.handle:
+            lib().spec_gamma_ctl_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def spec_gamma_optimal(alpha: float, gamma_min: int, gamma_max: int, draft_ms_per_token: float,
+                       target_ms_per_pass: float) -> int:
+    out = ctypes.c_int32()
+    _check(lib().spec_gamma_optimal(alpha, gamma_min, gamma_max, draft_ms_per_token,
+                                    target_ms_per_pass, ctypes.byref(out)), "spec_gamma_optimal")
+    return out.value
 
 
 def spec_tree_masks(parents) -> tuple[list, list]:
