@@ -74,6 +74,7 @@ typedef enum {
 #define SPEC_DEV_BAD_NACC      0x10  /* truncate: n_accepted outside [0, gamma] */
 #define SPEC_DEV_BAD_TREE      0x20  /* tree accept / commit: bad parents, path or n_accepted */
 #define SPEC_DEV_EMPTY_MASK    0x40  /* mask_logits: a row's mask allows no token */
+#define SPEC_DEV_BAD_PAGE      0x80  /* paged cache: a page id outside [0, n_pages) */
 
 /* Text for a spec_status value (static storage). */
 const char* spec_status_string(int status);
@@ -291,6 +292,68 @@ int spec_mask_logits(float* d_logits, const uint32_t* d_allowed, int rows, int v
  * the forward's or the accept's workspace). */
 int spec_kv_truncate(const spec_kv_cache* kv, const int32_t* d_n_accepted, int gamma, void* d_ws,
                      void* stream);
+
+/* --------------------------------------------------------------- paged KV */
+/* A paged target cache ([engine] Rollback Protocol: a paged KV cache with a
+ * block pointer table; rollback updates the table and returns the pages of
+ * rejected positions to the free list, nothing is zeroed).  Pages hold
+ * SPEC_PAGE_SLOTS consecutive slots of one sequence for every KV head:
+ *   k, v   bf16 [n_layers][n_pages][n_kv_heads][SPEC_PAGE_SLOTS][head_dim]
+ *          (spec_paged_kv_bytes each), 16-byte aligned;
+ *   len    int32 [batch] device, the valid length of each sequence;
+ *   table  int32 [batch][max_pages] device: table[b][j] is the page holding
+ *          slots j*SPEC_PAGE_SLOTS .. j*SPEC_PAGE_SLOTS + SPEC_PAGE_SLOTS-1
+ *          of sequence b; only entries covering slots below len[b] + gamma
+ *          + 1 are read by a pass.
+ * The logical capacity of a sequence is max_pages * SPEC_PAGE_SLOTS <= 32768
+ * slots.  A pass whose slots reach a page id outside [0, n_pages) sets
+ * SPEC_DEV_BAD_PAGE and treats that sequence as overflowing (nothing written,
+ * len not advanced). */
+#define SPEC_PAGE_SLOTS 64
+typedef struct {
+  void* k;
+  void* v;
+  int32_t* len;
+  const int32_t* table;
+  int batch;
+  int n_pages;
+  int max_pages;
+} spec_paged_kv_cache;
+
+/* Bytes of the paged k array (and of v) for n_pages pages. */
+size_t spec_paged_kv_bytes(const spec_model_config* cfg, int n_pages);
+
+/* spec_verify_forward on a paged cache: the same pass (same kernels and
+ * schedules, same results bit for bit as the contiguous cache holding the
+ * same rows), every key / value row addressed through the page table.
+ * Workspace: spec_workspace_bytes(cfg, batch, gamma, max_pages *
+ * SPEC_PAGE_SLOTS). */
+int spec_verify_forward_paged(const spec_model* model, const int32_t* d_tokens, int batch, int gamma,
+                              const spec_paged_kv_cache* kv, float* d_logits, void* d_ws,
+                              size_t ws_bytes, void* stream);
+
+/* Rollback of a paged cache on the device: len[b] -= gamma - n_accepted[b]
+ * (as spec_kv_truncate).  The pages wholly past the new length are then
+ * returned by the host page pool (spec_page_pool_release). */
+int spec_paged_kv_truncate(const spec_paged_kv_cache* kv, const int32_t* d_n_accepted, int gamma,
+                           void* d_ws, void* stream);
+
+/* Host page pool (no device access): a free list of n_pages page ids and a
+ * host copy of the page table [batch][max_pages] (-1 = unmapped), to be
+ * copied to the device table before a pass. */
+typedef struct spec_page_pool spec_page_pool;
+int spec_page_pool_create(int n_pages, int batch, int max_pages, spec_page_pool** out);
+int spec_page_pool_destroy(spec_page_pool* pool);
+/* Map every page sequence b needs for `slots` slots, taking pages from the
+ * free list in order; SPEC_ESIZE (nothing taken) if the free list or
+ * max_pages is too short. */
+int spec_page_pool_reserve(spec_page_pool* pool, int b, int slots);
+/* Return sequence b's pages past the first ceil(slots / SPEC_PAGE_SLOTS) to
+ * the free list (after a rollback to `slots` slots; 0 frees the sequence). */
+int spec_page_pool_release(spec_page_pool* pool, int b, int slots);
+/* The host table [batch][max_pages] (valid until the pool is destroyed). */
+const int32_t* spec_page_pool_table(const spec_page_pool* pool);
+int spec_page_pool_free_pages(const spec_page_pool* pool);
 
 /* ------------------------------------------------------------ draft trees */
 /* Verification of a draft TREE instead of a chain ([aci] Tree-Based Drafting;

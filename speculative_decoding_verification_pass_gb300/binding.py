@@ -12,6 +12,7 @@ import ctypes
 import os
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 from . import _build
@@ -21,6 +22,7 @@ SPEC_OK, SPEC_EINVAL, SPEC_ESIZE, SPEC_ECUDA, SPEC_EDEVICE, SPEC_ETIMEOUT, SPEC_
 DEV_BAD_TOKEN, DEV_KV_OVERFLOW, DEV_Q_ZERO, DEV_TIMEOUT, DEV_BAD_NACC, DEV_BAD_TREE = (
     0x1, 0x2, 0x4, 0x8, 0x10, 0x20)
 DEV_EMPTY_MASK = 0x40
+DEV_BAD_PAGE = 0x80
 
 
 class SpecError(RuntimeError):
@@ -43,6 +45,13 @@ class spec_kv_cache(ctypes.Structure):
                 ("batch", ctypes.c_int), ("capacity", ctypes.c_int)]
 
 
+class spec_paged_kv_cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("len", ctypes.c_void_p),
+                ("table", ctypes.c_void_p), ("batch", ctypes.c_int), ("n_pages", ctypes.c_int),
+                ("max_pages", ctypes.c_int)]
+
+
+PAGE_SLOTS = 64
 _LIB = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -68,6 +77,16 @@ _SIGS = {
     "spec_draft_sample": (_I, [_P, _I, _I, _F, _F, _P, _P, _P, _P, _SZ, _P]),
     "spec_kv_truncate": (_I, [ctypes.POINTER(spec_kv_cache), _P, _I, _P, _P]),
     "spec_mask_logits": (_I, [_P, _P, _I, _I, _P, _P]),
+    "spec_paged_kv_bytes": (_SZ, [ctypes.POINTER(spec_model_config), _I]),
+    "spec_verify_forward_paged": (_I, [_P, _P, _I, _I, ctypes.POINTER(spec_paged_kv_cache), _P, _P,
+                                       _SZ, _P]),
+    "spec_paged_kv_truncate": (_I, [ctypes.POINTER(spec_paged_kv_cache), _P, _I, _P, _P]),
+    "spec_page_pool_create": (_I, [_I, _I, _I, ctypes.POINTER(_P)]),
+    "spec_page_pool_destroy": (_I, [_P]),
+    "spec_page_pool_reserve": (_I, [_P, _I, _I]),
+    "spec_page_pool_release": (_I, [_P, _I, _I]),
+    "spec_page_pool_table": (ctypes.POINTER(ctypes.c_int32), [_P]),
+    "spec_page_pool_free_pages": (_I, [_P]),
     "spec_gamma_ctl_create": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_double, ctypes.c_double,
                                    ctypes.c_double, ctypes.POINTER(_P)]),
     "spec_gamma_ctl_destroy": (_I, [_P]),
@@ -244,6 +263,74 @@ def spec_mask_logits(logits, allowed, rows: int, vocab: int, ws, stream=None):
     """logits[r][x] = -inf where bit x of row r's packed mask is clear (in place)."""
     _check(lib().spec_mask_logits(_ptr(logits), _ptr(allowed), rows, vocab, _ptr(ws), _stream(stream)),
            "spec_mask_logits")
+
+
+class PagedKVCache:
+    """Paged target cache: k, v bf16 [layers][n_pages][Hkv][64][hd], len int32
+    [B], the device page table int32 [B][max_pages], and a host page pool
+    (free list + host table) that `sync()` copies to the device."""
+
+    def __init__(self, cfg: ModelConfig, batch: int, n_pages: int, max_pages: int, device="cuda"):
+        self.cfg, self.batch, self.n_pages, self.max_pages = cfg, batch, n_pages, max_pages
+        shape = (cfg.n_layers, n_pages, cfg.n_kv_heads, PAGE_SLOTS, cfg.head_dim)
+        self.k = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        self.v = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        assert self.k.numel() * 2 == int(lib().spec_paged_kv_bytes(ctypes.byref(cfg.c()), n_pages))
+        self.len = torch.zeros(batch, dtype=torch.int32, device=device)
+        self.table = torch.full((batch, max_pages), -1, dtype=torch.int32, device=device)
+        h = ctypes.c_void_p()
+        _check(lib().spec_page_pool_create(n_pages, batch, max_pages, ctypes.byref(h)),
+               "spec_page_pool_create")
+        self.pool = h.value
+
+    @property
+    def capacity(self) -> int:
+        return self.max_pages * PAGE_SLOTS
+
+    def c(self) -> spec_paged_kv_cache:
+        return spec_paged_kv_cache(self.k.data_ptr(), self.v.data_ptr(), self.len.data_ptr(),
+                                   self.table.data_ptr(), self.batch, self.n_pages, self.max_pages)
+
+    def reserve(self, b: int, slots: int):
+        _check(lib().spec_page_pool_reserve(self.pool, b, slots), "spec_page_pool_reserve")
+
+    def release(self, b: int, slots: int):
+        _check(lib().spec_page_pool_release(self.pool, b, slots), "spec_page_pool_release")
+
+    def host_table(self) -> np.ndarray:
+        ptr = lib().spec_page_pool_table(self.pool)
+        return np.ctypeslib.as_array(ptr, shape=(self.batch * self.max_pages,)).reshape(
+            self.batch, self.max_pages).copy()
+
+    def free_pages(self) -> int:
+        return int(lib().spec_page_pool_free_pages(self.pool))
+
+    def sync(self):
+        """Copy the host page table to the device table."""
+        self.table.copy_(torch.from_numpy(self.host_table()))
+
+    def close(self):
+        if self.pool:
+            lib().spec_page_pool_destroy(self.pool)
+            self.pool = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def spec_verify_forward_paged(handle: int, tokens, batch: int, gamma: int, kv: "PagedKVCache", logits,
+                              ws, stream=None):
+    _check(lib().spec_verify_forward_paged(handle, _ptr(tokens), batch, gamma, ctypes.byref(kv.c()),
+                                           _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)),
+           "spec_verify_forward_paged")
+
+
+def spec_paged_kv_truncate(kv: "PagedKVCache", n_accepted, gamma: int, ws, stream=None):
+    _check(lib().spec_paged_kv_truncate(ctypes.byref(kv.c()), _ptr(n_accepted), gamma, _ptr(ws),
+                                        _stream(stream)), "spec_paged_kv_truncate")
 
 
 class GammaController:

@@ -509,12 +509,20 @@ size_t spec_workspace_bytes(const spec_model_config* cfg, int batch, int gamma, 
   return plan_ws(*cfg, batch, gamma, capacity).total;
 }
 
+// Page table of a paged cache (table == nullptr: the contiguous layout).
+struct PageDesc {
+  const int32_t* table = nullptr;
+  int max_pages = 0, n_pages = 0;
+};
+
 // The verification forward; d_anc / d_depth describe a draft tree per
 // sequence (nullptr: the chain, node j at position len + j seeing new slots
-// 0..j).
+// 0..j); pg the page table of a paged cache (kv->capacity = its logical
+// capacity).
 static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, const uint64_t* d_anc,
                                const int32_t* d_depth, int batch, int gamma, const spec_kv_cache* kv,
-                               float* d_logits, void* d_ws, size_t ws_bytes, void* stream) {
+                               float* d_logits, void* d_ws, size_t ws_bytes, void* stream,
+                               const PageDesc& pg = PageDesc{}) {
   if (!m || !d_tokens || !kv || !d_logits || !d_ws) return SPEC_EINVAL;
   if (batch < 0 || gamma < 0) return SPEC_EINVAL;
   const spec_model_config& c = m->cfg;
@@ -617,7 +625,11 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       Q.layer_stride = stride;
       Q.kc = static_cast<uint16_t*>(kv->k);
       Q.vc = static_cast<uint16_t*>(kv->v);
-      Q.layer_kv = static_cast<long long>(batch) * Hkv * kv->capacity * hd;
+      Q.layer_kv = pg.table ? static_cast<long long>(pg.n_pages) * Hkv * SPEC_PAGE_SLOTS * hd
+                            : static_cast<long long>(batch) * Hkv * kv->capacity * hd;
+      Q.kv_table = pg.table;
+      Q.kv_max_pages = pg.max_pages;
+      Q.kv_n_pages = pg.n_pages;
       Q.len = kv->len;
       Q.tokens = d_tokens;
       Q.logits = d_logits;
@@ -684,6 +696,9 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
   ep.d = d;
   ep.V = c.vocab;
   ep.cap = kv->capacity;
+  ep.kv_table = pg.table;
+  ep.kv_max_pages = pg.max_pages;
+  ep.kv_n_pages = pg.n_pages;
   SPEC_CUDA(launch_embed(ep, st, pdl));
 
   GemmParams g0{};
@@ -696,7 +711,8 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
   g0.counters = counters;
   g0.status = status;
 
-  const size_t layer_kv = static_cast<size_t>(batch) * Hkv * kv->capacity * hd;
+  const size_t layer_kv = pg.table ? static_cast<size_t>(pg.n_pages) * Hkv * SPEC_PAGE_SLOTS * hd
+                                   : static_cast<size_t>(batch) * Hkv * kv->capacity * hd;
   for (int l = 0; l < c.n_layers; ++l) {
     uint16_t* kc = static_cast<uint16_t*>(kv->k) + l * layer_kv;
     uint16_t* vc = static_cast<uint16_t*>(kv->v) + l * layer_kv;
@@ -712,6 +728,9 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       p.seq_ok = seq_ok;
       p.rope = reinterpret_cast<const float2*>(B + L.rope);
       p.depth = d_depth;
+      p.kv_table = pg.table;
+      p.kv_max_pages = pg.max_pages;
+      p.kv_n_pages = pg.n_pages;
       p.n_per_seq = n;
       p.H = H;
       p.Hkv = Hkv;
@@ -730,6 +749,9 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       a.o_lo = o_lo;
       a.pos_base = pos_base;
       a.anc = d_anc;
+      a.kv_table = pg.table;
+      a.kv_max_pages = pg.max_pages;
+      a.kv_n_pages = pg.n_pages;
       a.part_o = reinterpret_cast<float*>(W + P.apart_o);
       a.part_ml = reinterpret_cast<float*>(W + P.apart_ml);
       a.counters = counters + P.attn_counter0;
@@ -809,6 +831,47 @@ int spec_verify_forward(const spec_model* m, const int32_t* d_tokens, int batch,
                         void* stream) {
   return verify_forward_impl(m, d_tokens, nullptr, nullptr, batch, gamma, kv, d_logits, d_ws, ws_bytes,
                              stream);
+}
+
+size_t spec_paged_kv_bytes(const spec_model_config* cfg, int n_pages) {
+  if (!cfg_ok(cfg) || n_pages < 0 || cfg->n_layers == 0) return 0;
+  const size_t hd = static_cast<size_t>(cfg->d_model / cfg->n_heads);
+  return static_cast<size_t>(cfg->n_layers) * n_pages * cfg->n_kv_heads * SPEC_PAGE_SLOTS * hd * 2;
+}
+
+static int paged_view(const spec_paged_kv_cache* kv, spec_kv_cache* view, PageDesc* pg) {
+  if (!kv || !kv->k || !kv->v || !kv->len || !kv->table) return SPEC_EINVAL;
+  if (kv->batch < 0 || kv->n_pages <= 0 || kv->max_pages <= 0) return SPEC_EINVAL;
+  if (static_cast<long long>(kv->max_pages) * SPEC_PAGE_SLOTS > kAttnChunk * kAttnMaxChunks) return SPEC_ESIZE;
+  view->k = kv->k;
+  view->v = kv->v;
+  view->len = kv->len;
+  view->batch = kv->batch;
+  view->capacity = kv->max_pages * SPEC_PAGE_SLOTS;
+  pg->table = kv->table;
+  pg->max_pages = kv->max_pages;
+  pg->n_pages = kv->n_pages;
+  return SPEC_OK;
+}
+
+int spec_verify_forward_paged(const spec_model* m, const int32_t* d_tokens, int batch, int gamma,
+                              const spec_paged_kv_cache* kv, float* d_logits, void* d_ws,
+                              size_t ws_bytes, void* stream) {
+  spec_kv_cache view{};
+  PageDesc pg;
+  const int r = paged_view(kv, &view, &pg);
+  if (r) return r;
+  return verify_forward_impl(m, d_tokens, nullptr, nullptr, batch, gamma, &view, d_logits, d_ws, ws_bytes,
+                             stream, pg);
+}
+
+int spec_paged_kv_truncate(const spec_paged_kv_cache* kv, const int32_t* d_n_accepted, int gamma,
+                           void* d_ws, void* stream) {
+  spec_kv_cache view{};
+  PageDesc pg;
+  const int r = paged_view(kv, &view, &pg);
+  if (r) return r;
+  return spec_kv_truncate(&view, d_n_accepted, gamma, d_ws, stream);
 }
 
 int spec_tree_masks(const int32_t* parents, int n_nodes, uint64_t* out_anc, int32_t* out_depth) {

@@ -76,12 +76,12 @@ __global__ void __launch_bounds__(kThreads) attn_splitkv_kernel(const AttnParams
   int* flag = reinterpret_cast<int*>(smem + L::kFlag);
 
   // ---- stage this chunk's keys and values (rows past the end are zero)
-  const long long head_base = (static_cast<long long>(b) * p.Hkv + kvh) * p.cap;
+  const KVMap map{p.kv_table, p.kv_max_pages, p.kv_n_pages, p.Hkv, p.cap, HD};
   constexpr int kCPR = HD / 8;  // 16-byte chunks per row
   for (int idx = tid; idx < kChunk * kCPR; idx += kThreads) {
     const int i = idx / kCPR, c = idx % kCPR;
     const int row = i < nk ? i : 0;
-    const long long g = (head_base + k0 + row) * HD + c * 8;
+    const long long g = map.row(b, kvh, k0 + row) + c * 8;
     const int bytes = i < nk ? 16 : 0;
     cp_async16(sK + swz<HD>(i, c), p.kcache + g, bytes);
     cp_async16(sV + swz<HD>(i, c), p.vcache + g, bytes);
@@ -430,13 +430,13 @@ __global__ void __launch_bounds__(kClusterThreads)
   const bool lo = p.q_lo != nullptr;
 
   // ---- stage this rank's keys/values and the query rows (hi, lo)
-  const long long head_base = (static_cast<long long>(b) * p.Hkv + kvh) * p.cap;
+  const KVMap map{p.kv_table, p.kv_max_pages, p.kv_n_pages, p.Hkv, p.cap, HD};
   constexpr int kCPR = HD / 8;
   const int nk_pad = (nk + 31) & ~31;
   for (int idx = tid; idx < nk_pad * kCPR; idx += kClusterThreads) {
     const int i = idx / kCPR, c = idx % kCPR;
     const int row = i < nk ? i : 0;
-    const long long g = (head_base + k_lo + row) * HD + c * 8;
+    const long long g = map.row(b, kvh, k_lo + row) + c * 8;
     const int bytes = i < nk ? 16 : 0;
     cp_async16(sK + swz<HD>(i, c), p.kcache + g, bytes);
     cp_async16(sV + swz<HD>(i, c), p.vcache + g, bytes);

@@ -41,6 +41,42 @@ SPEC_DEVINL uint32_t ld_acquire(const unsigned* p) {
 // slot Lb: cached keys always; a new slot Lb + s by the causal order (s <= j)
 // for a chain, or, with a draft tree (anc != nullptr), iff bit s of the
 // node's ancestor mask `am` is set (the node itself or one of its ancestors).
+// Where (sequence b, KV head h, slot t)'s key / value row starts within one
+// layer's cache, in elements: contiguous [B][Hkv][cap][hd], or paged through a
+// block table (page = table[b][t / kPageSlots], rows [page][Hkv][kPageSlots][hd];
+// a page id outside [0, n_pages) is clamped, the pass flags it beforehand).
+constexpr int kPageSlots = SPEC_PAGE_SLOTS;
+
+// The pass's slot check: len + n within the capacity and, for a paged cache,
+// every page covering slots [0, len + n) a valid page id.  0 when it fits,
+// else the status bit to raise.
+SPEC_DEVINL int32_t seq_fit(int L, int n, int cap, const int32_t* table, int max_pages, int n_pages,
+                            int b) {
+  if (L < 0 || L + n > cap) return SPEC_DEV_KV_OVERFLOW;
+  if (table) {
+    const int np = (L + n + kPageSlots - 1) / kPageSlots;
+    for (int j = 0; j < np; ++j) {
+      const int pg = __ldg(table + static_cast<long long>(b) * max_pages + j);
+      if (pg < 0 || pg >= n_pages) return SPEC_DEV_BAD_PAGE;
+    }
+  }
+  return 0;
+}
+struct KVMap {
+  const int32_t* table;  // [B][max_pages] physical page ids, or nullptr (contiguous)
+  int max_pages, n_pages;
+  int Hkv, cap, hd;
+  // kLayout: 0 decided by `table` at run time, 1 contiguous, 2 paged
+  template <int kLayout = 0>
+  SPEC_DEVINL long long row(int b, int h, int t) const {
+    if (kLayout == 1 || (kLayout == 0 && !table))
+      return ((static_cast<long long>(b) * Hkv + h) * cap + t) * hd;
+    int page = __ldg(table + static_cast<long long>(b) * max_pages + t / kPageSlots);
+    page = page < 0 ? 0 : (page >= n_pages ? n_pages - 1 : page);
+    return ((static_cast<long long>(page) * Hkv + h) * kPageSlots + (t % kPageSlots)) * hd;
+  }
+};
+
 SPEC_DEVINL bool key_visible(int kabs, int Lb, int j, const uint64_t* anc, uint64_t am) {
   if (kabs < Lb) return true;
   const int s = kabs - Lb;

@@ -160,6 +160,9 @@ SPEC_DEVINL GemmParams phase_params(const MkParams& P, const GPh& g) {
     p.seq_ok = P.seq_ok;
     p.rope = P.rope;
     p.depth = P.depth;
+    p.kv_table = P.kv_table;
+    p.kv_max_pages = P.kv_max_pages;
+    p.kv_n_pages = P.kv_n_pages;
     p.n_per_seq = P.n;
     p.H = P.H;
     p.Hkv = P.Hkv;
@@ -341,13 +344,13 @@ SPEC_DEVINL void embed_phase(const MkParams& P, const MkSmem& sm) {
   if (blockIdx.x == 0) {
     for (int b = e; b < P.B; b += kEpiThreads) {
       const int L = P.len[b];
-      const bool ok = L >= 0 && L + P.n <= P.cap;
+      const int32_t bad = seq_fit(L, P.n, P.cap, P.kv_table, P.kv_max_pages, P.kv_n_pages, b);
       P.pos_base[b] = L < 0 ? 0 : L;
-      P.seq_ok[b] = ok ? 1 : 0;
-      if (ok)
+      P.seq_ok[b] = bad ? 0 : 1;
+      if (!bad)
         P.len[b] = L + P.n;
       else
-        set_status(P.status, SPEC_DEV_KV_OVERFLOW);
+        set_status(P.status, bad);
     }
   }
   const int fpt = P.d / 128;  // features per thread (a tile of 128 = 128/fpt threads)
@@ -463,9 +466,10 @@ struct KVLayout {
 // `lay`: `what` = 0 every row (zero fill past kend), 1 the rows this pass
 // does not write (cached keys below Lb; zero fill past kend), 2 the rows this
 // pass writes (keys Lb .. kend-1).
-template <int HD>
+template <int HD, bool kPaged>
 SPEC_DEVINL void att_load_block(const KVLayout& lay, const uint16_t* kc, const uint16_t* vc,
-                                long long head_base, int kb, int kend, int Lb, int what, int e) {
+                                const KVMap& map, int b, int kvh, int kb, int kend, int Lb, int what,
+                                int e) {
   constexpr int kCPR = HD / 8;
   for (int idx = e; idx < kAttUnitKeys * kCPR; idx += kEpiThreads) {
     const int i = idx / kCPR, c = idx % kCPR;  // key kb + i
@@ -473,7 +477,7 @@ SPEC_DEVINL void att_load_block(const KVLayout& lay, const uint16_t* kc, const u
     const bool valid = key < kend;
     const bool fresh = valid && key >= Lb;
     if ((what == 1 && fresh) || (what == 2 && !fresh)) continue;
-    const long long g = (head_base + (valid ? key : kb)) * HD + c * 8;
+    const long long g = map.row<kPaged ? 2 : 1>(b, kvh, valid ? key : kb) + c * 8;
     const int qk = (i >> 5) * 4 + ((i >> 4) & 1);
     const uint32_t off = swz<HD>(i & 15, c);
     cp_async16(lay.piece<HD>(qk) + off, kc + g, valid ? 16 : 0);
@@ -510,14 +514,14 @@ SPEC_DEVINL KVLayout att_stage_layout(const MkSmem& sm, int hd) {
 // attention stage is not used by the GEMM phases before the attention phase
 // beyond the epilogue exchange buffer and the QKV bookkeeping, which sit in
 // the q area.
-template <int HD>
+template <int HD, bool kPaged>
 SPEC_DEVINL void att_prefetch(const MkParams& P, const MkSmem& sm, int l) {
   const int e = threadIdx.x - kEpiFirstThread;
   AttUnit u;
   if (!att_unit(P, blockIdx.x, u)) return;
-  const long long head_base = (static_cast<long long>(u.b) * P.Hkv + u.kvh) * P.cap;
-  att_load_block<HD>(att_stage_layout(sm, HD), P.kc + P.layer_kv * l, P.vc + P.layer_kv * l, head_base,
-                     u.kbeg, u.kend, u.Lb, 1, e);
+  const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, HD};
+  att_load_block<HD, kPaged>(att_stage_layout(sm, HD), P.kc + P.layer_kv * l, P.vc + P.layer_kv * l, map, u.b,
+                     u.kvh, u.kbeg, u.kend, u.Lb, 1, e);
 }
 
 // One 64-key block of a unit for this warp's 32 keys (slot) and 16 query rows
@@ -675,7 +679,7 @@ SPEC_DEVINL void cmb_phase(const MkParams& P) {
   }
 }
 
-template <int HD>
+template <int HD, bool kPaged>
 SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t sbytes) {
   const int e = threadIdx.x - kEpiFirstThread;
   const int w = e >> 5, lane = e & 31;
@@ -694,6 +698,7 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
   float* merge = reinterpret_cast<float*>(sm.att);  // [2 tiles][16][HD], reuses the q area
   const uint16_t* kc = P.kc + P.layer_kv * l;
   const uint16_t* vc = P.vc + P.layer_kv * l;
+  const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, HD};
   const int nch = P.att_nch;
   const int units = P.B * P.Hkv * nch;
   const int g8 = lane >> 2, t4 = lane & 3;
@@ -701,13 +706,13 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
   for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
     AttUnit u;
     if (!att_unit(P, unit, u)) continue;  // uniform across the CTA
-    const long long head_base = (static_cast<long long>(u.b) * P.Hkv + u.kvh) * P.cap;
     const bool first = unit == static_cast<int>(blockIdx.x);
     // block 0: the cached rows were prefetched for the first unit; block 1
     // into the activation areas at once
-    att_load_block<HD>(stage_lay, kc, vc, head_base, u.kbeg, u.kend, u.Lb, first ? 2 : 0, e);
+    att_load_block<HD, kPaged>(stage_lay, kc, vc, map, u.b, u.kvh, u.kbeg, u.kend, u.Lb, first ? 2 : 0, e);
     const bool staged1 = two && u.kbeg + kAttUnitKeys < u.kend;
-    if (staged1) att_load_block<HD>(act_lay, kc, vc, head_base, u.kbeg + kAttUnitKeys, u.kend, u.Lb, 0, e);
+    if (staged1)
+      att_load_block<HD, kPaged>(act_lay, kc, vc, map, u.b, u.kvh, u.kbeg + kAttUnitKeys, u.kend, u.Lb, 0, e);
     // q (hi, lo) rows with async copies (zero rows past R)
     for (int idx = e; idx < 32 * kCPR; idx += kEpiThreads) {
       const int r = idx / kCPR, c = idx % kCPR;
@@ -727,7 +732,7 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
       const bool in_act = staged1 && bi == 1;
       if (bi > 0 && !in_act) {
         named_bar(kArriveBar, kEpiThreads);  // the stage's previous block consumed
-        att_load_block<HD>(stage_lay, kc, vc, head_base, kb, u.kend, u.Lb, 0, e);
+        att_load_block<HD, kPaged>(stage_lay, kc, vc, map, u.b, u.kvh, kb, u.kend, u.Lb, 0, e);
         cp_async_wait_all();
         named_bar(kArriveBar, kEpiThreads);
       }
@@ -791,7 +796,7 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
 }
 
 // -------------------------------------------------------------- the kernel
-template <int HD>
+template <int HD, bool kPaged>
 __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_constant__ MkParams P) {
   extern __shared__ uint8_t smem_raw[];
   const int nb = 2 * P.ntok;  // B rows per stage: hi rows then lo rows
@@ -970,7 +975,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         embed_phase(P, sm);
       } else if (kind == PH_ATT) {
         if (!epi_wait(P, sm, ph)) break;
-        att_phase<HD>(P, sm, (ph - 1) / kPhPerLayer, sbytes);
+        att_phase<HD, kPaged>(P, sm, (ph - 1) / kPhPerLayer, sbytes);
       } else if (kind == PH_CMB) {
         if (!epi_wait(P, sm, ph)) break;
         cmb_phase<HD>(P);
@@ -995,7 +1000,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         // QKV: per token column KV slot, rotary position and fit flag
         int* const qpre = sm.qpre;
         if (p.epi == EPI_QKV) {
-          att_prefetch<HD>(P, sm, g.l);  // this layer's first key block, early
+          att_prefetch<HD, kPaged>(P, sm, g.l);  // this layer's first key block, early
           for (int c = e; c < p.ntok; c += kEpiThreads) {
             const int m = min(c, p.M - 1);
             const int b = m / p.n_per_seq, node = m - b * p.n_per_seq;
@@ -1067,7 +1072,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
                                                                     sm.slots, acc, tag, sm.abort, P.status);
                 if (!ok) break;
               }
-              epilogue_chunk_h(p, gs, t, r, c0, acc, hv, pre_h, pre);
+              epilogue_chunk_h<kPaged ? 2 : 1>(p, gs, t, r, c0, acc, hv, pre_h, pre);
             }
           }
           tc_fence_before();
@@ -1107,11 +1112,15 @@ int forward_max_stages(int ntok, int hd, size_t budget) {
 // CTAs per SM the persistent forward can keep resident (0: not launchable).
 int forward_ctas_per_sm(int ntok, int stages, int hd) {
   const size_t smem = forward_smem_bytes(ntok, stages, hd);
-  const void* fn = hd == 128 ? reinterpret_cast<const void*>(forward_kernel<128>)
-                             : reinterpret_cast<const void*>(forward_kernel<64>);
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
-    return 0;
+  const void* fns[2] = {hd == 128 ? reinterpret_cast<const void*>(forward_kernel<128, false>)
+                                  : reinterpret_cast<const void*>(forward_kernel<64, false>),
+                        hd == 128 ? reinterpret_cast<const void*>(forward_kernel<128, true>)
+                                  : reinterpret_cast<const void*>(forward_kernel<64, true>)};
+  const void* fn = fns[0];
+  for (const void* f : fns)  // both cache layouts take the same shared memory
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+      return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kMkThreads, smem) != cudaSuccess) return 0;
   // every resident CTA holds its accumulators in TMEM (512 columns per SM)
@@ -1133,8 +1142,12 @@ cudaError_t launch_forward(const MkParams& P, int grid, int hd, cudaStream_t str
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (hd == 128) return cudaLaunchKernelEx(&cfg, forward_kernel<128>, P);
-  return cudaLaunchKernelEx(&cfg, forward_kernel<64>, P);
+  const bool paged = P.kv_table != nullptr;
+  if (hd == 128)
+    return paged ? cudaLaunchKernelEx(&cfg, forward_kernel<128, true>, P)
+                 : cudaLaunchKernelEx(&cfg, forward_kernel<128, false>, P);
+  return paged ? cudaLaunchKernelEx(&cfg, forward_kernel<64, true>, P)
+               : cudaLaunchKernelEx(&cfg, forward_kernel<64, false>, P);
 }
 
 }  // namespace spec

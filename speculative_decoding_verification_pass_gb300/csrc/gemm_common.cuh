@@ -154,6 +154,8 @@ struct EpiPre {
 // Apply the epilogue to 16 token columns [c0, c0+16) of this thread's row.
 // With have_h the residual-stream values of these columns were loaded
 // beforehand (hv); otherwise the residual epilogue loads them.
+// kKV: the KV cache layout of the QKV epilogue's appends (KVMap::row).
+template <int kKV = 0>
 __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t tile, int r, int c0,
                                  const float (&acc)[16], const float (&hv_in)[16], bool have_h,
                                  const EpiPre& pre) {
@@ -278,8 +280,8 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
       } else if (okv[j] && slotv[j] < p.cap) {
         const int kf = f < qdim + kdim ? f - qdim : f - qdim - kdim;
         const int kvh = kf / hd;
-        const long long idx =
-            ((static_cast<long long>(b) * p.Hkv + kvh) * p.cap + slotv[j]) * hd + (kf % hd);
+        const KVMap map{p.kv_table, p.kv_max_pages, p.kv_n_pages, p.Hkv, p.cap, hd};
+        const long long idx = map.row<kKV>(b, kvh, slotv[j]) + (kf % hd);
         if (f < qdim + kdim)
           p.kcache[idx] = f32_to_bf16(out);
         else

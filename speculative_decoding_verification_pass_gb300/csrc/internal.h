@@ -53,6 +53,8 @@ struct GemmParams {
   const int32_t* seq_ok;  // per sequence: 1 if its slots fit in the cache
   const float2* rope;     // [hd/2] frequency (hi, lo)
   const int32_t* depth;   // [M] draft-tree node depths (position = base + depth), or nullptr
+  const int32_t* kv_table;  // [B][kv_max_pages] page table of a paged cache, or nullptr
+  int kv_max_pages, kv_n_pages;
   int n_per_seq, H, Hkv, hd, cap;
   // EPI_SWIGLU: rows 0-63 of a tile are gate features, 64-127 up features
   uint16_t* act;  // [M][ffn]
@@ -81,6 +83,8 @@ struct AttnParams {
   uint16_t* o_lo;         // bf16 residual of o, or nullptr
   const int32_t* pos_base;
   const uint64_t* anc;    // [B][n] draft-tree ancestor masks, or nullptr (chain)
+  const int32_t* kv_table;  // [B][kv_max_pages] page table of a paged cache, or nullptr
+  int kv_max_pages, kv_n_pages;
   float* part_o;          // [B][Hkv][splits][R][hd]
   float* part_ml;         // [B][Hkv][splits][R][2]
   int32_t* counters;      // [B*Hkv], zero on entry, left zero
@@ -114,6 +118,8 @@ struct MkParams {
   uint16_t* kc;                           // KV cache base; layer l is + l * layer_kv elements
   uint16_t* vc;
   long long layer_kv;
+  const int32_t* kv_table;                // [B][kv_max_pages] page table, or nullptr (contiguous)
+  int kv_max_pages, kv_n_pages;
   int32_t* len;
   const int32_t* tokens;
   float* logits;
@@ -153,6 +159,8 @@ struct EmbedParams {
   int32_t* counters;      // zeroed here
   int n_counters;
   int32_t* status;
+  const int32_t* kv_table;  // page table to validate, or nullptr
+  int kv_max_pages, kv_n_pages;
   int B, n, d, V, cap;
 };
 cudaError_t launch_embed(const EmbedParams& p, cudaStream_t stream, bool pdl);

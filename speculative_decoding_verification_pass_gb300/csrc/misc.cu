@@ -23,13 +23,13 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedParams p) {
     for (int i = threadIdx.x; i < p.n_counters; i += blockDim.x) p.counters[i] = 0;
     for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
       const int L = p.len[b];
-      const bool ok = L >= 0 && L + p.n <= p.cap;
+      const int32_t bad = seq_fit(L, p.n, p.cap, p.kv_table, p.kv_max_pages, p.kv_n_pages, b);
       p.pos_base[b] = L < 0 ? 0 : L;
-      p.seq_ok[b] = ok ? 1 : 0;
-      if (ok)
+      p.seq_ok[b] = bad ? 0 : 1;
+      if (!bad)
         p.len[b] = L + p.n;
       else
-        set_status(p.status, SPEC_DEV_KV_OVERFLOW);
+        set_status(p.status, bad);
     }
   }
   int tok = p.tokens[m];
