@@ -571,6 +571,61 @@ def time_tree(w: Workload, K: int, warmup: int = 2):
             "hbm_gbs": fwd / (ms / 1e3) / 1e9, "rounds": K}
 
 
+# ------------------------------------------------------------- paged KV
+def time_paged(w: Workload, K: int):
+    """The same step on a paged copy of the cache (64-slot pages through a
+    page table, pages taken from the host pool's free list): forward +
+    accept + device rollback timed; the pool's release of the pages past the
+    new length, and its reservation for the next pass, happen between steps."""
+    B, c = w.B, w.cfg
+    max_pages = -(-w.cap // sb.PAGE_SLOTS)
+    pk = sb.PagedKVCache(c, B, n_pages=B * max_pages + 4, max_pages=max_pages)
+    for b in range(B):
+        pk.reserve(b, w.ctx)
+    t = pk.host_table()
+    for b in range(B):
+        for j in range(-(-w.ctx // sb.PAGE_SLOTS)):
+            lo, hi = j * sb.PAGE_SLOTS, min(w.ctx, (j + 1) * sb.PAGE_SLOTS)
+            pk.k[:, t[b, j], :, :hi - lo] = w.kv.k[:, b, :, lo:hi]
+            pk.v[:, t[b, j], :, :hi - lo] = w.kv.v[:, b, :, lo:hi]
+    pk.len.fill_(w.ctx)
+    st = torch.cuda.current_stream()
+    times = []
+    free_before = pk.free_pages()
+    for i in range(K + 2):
+        w.draft()
+        for b in range(B):
+            pk.reserve(b, w.ctx + w.n)
+        pk.sync()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        sb.spec_verify_forward_paged(w.model.handle, w.tokens, B, w.gamma, pk, w.logits, w.ws)
+        sb.spec_accept(w.logits, w.q, w.x, w.u, B, w.gamma, c.vocab, w.T, w.top_p, w.out, w.nacc,
+                       w.aws)
+        sb.spec_paged_kv_truncate(pk, w.nacc, w.gamma, w.ws)
+        e.record(st)
+        torch.cuda.synchronize()
+        if i >= 2:
+            times.append(a.elapsed_time(e))
+        lens = pk.len.cpu().numpy()
+        for b in range(B):
+            pk.release(b, int(lens[b]))
+        w.finish()
+        pk.len.fill_(w.ctx)
+        for b in range(B):
+            pk.release(b, w.ctx)
+    w.check_status()
+    ms = sum(times) / len(times)
+    out = {"workload": f"the verify step on a paged cache ({sb.PAGE_SLOTS}-slot pages, "
+                       f"{max_pages} pages per sequence), same model, context and draft",
+           "ms_per_step": ms, "value": w.bytes_per_step() / (ms / 1e3) / 1e9, "unit": "GB/s",
+           "steps": K, "pages_returned": pk.free_pages() == free_before}
+    pk.close()
+    return out
+
+
 # ------------------------------------------------------------------ main
 def parse():
     ap = argparse.ArgumentParser()
@@ -681,6 +736,10 @@ def main():
     except Exception as exc:
         gctl = {"unavailable": str(exc).splitlines()[0][:200]}
     try:
+        paged = time_paged(w, max(5, args.steps // 2))
+    except Exception as exc:
+        paged = {"unavailable": str(exc).splitlines()[0][:200]}
+    try:
         tree = time_tree(w, max(5, args.steps // 2)) if w.n <= 8 else None
     except Exception as exc:
         tree = {"unavailable": str(exc).splitlines()[0][:200]}
@@ -719,6 +778,7 @@ def main():
     }
     line["constrained"] = constrained
     line["gamma_ctl"] = gctl
+    line["paged"] = paged
     if tree is not None:
         line["tree"] = tree
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
