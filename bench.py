@@ -553,6 +553,23 @@ def time_tree(w: Workload, K: int, warmup: int = 2):
         if i >= warmup:
             times.append(a.elapsed_time(b))
         tr.finish()
+    # the tree accept and the commit alone (last round's inputs; the commit on
+    # a cache reset to the context + the round's slots each time)
+    stream = torch.cuda.current_stream()
+    ta, tc = [], []
+    for _ in range(5):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        w.kv.len.fill_(w.ctx + tr.n)
+        e0.record(stream)
+        sb.spec_tree_accept(tr.logits, tr.q, tr.tokens, tr.parents, tr.u, w.B, tr.n, w.cfg.vocab, w.T,
+                            w.top_p, tr.out, tr.path, tr.nacc, tr.tws)
+        e1.record(stream)
+        sb.spec_kv_tree_commit(w.model.handle, w.kv, tr.path, tr.nacc, tr.n, tr.fws)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        ta.append(e0.elapsed_time(e1))
+        tc.append(e1.elapsed_time(e2))
+    w.kv.len.fill_(w.ctx)
     for ws in (tr.tws, tr.fws):
         st, bits = sb.spec_device_status(ws)
         if st != sb.SPEC_OK:
@@ -568,7 +585,8 @@ def time_tree(w: Workload, K: int, warmup: int = 2):
                         f"nodes), batch {w.B}, context {w.ctx}, same model, draft and T",
             "ms_per_round": ms, "emitted_per_round": tr.emitted / (K * w.B),
             "emitted_tokens_per_s": tr.emitted / (sum(times) / 1e3),
-            "hbm_gbs": fwd / (ms / 1e3) / 1e9, "rounds": K}
+            "hbm_gbs": fwd / (ms / 1e3) / 1e9, "rounds": K,
+            "tree_accept_us": statistics.median(ta) * 1e3, "commit_us": statistics.median(tc) * 1e3}
 
 
 # ------------------------------------------------------------- paged KV

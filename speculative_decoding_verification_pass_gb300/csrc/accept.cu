@@ -120,6 +120,7 @@ SPEC_DEVINL void ms_merge(float& m, float& s, float m2, float s2, float c) {
 // Row statistics of softmax(z / T): block max and sum of exp2((z-max)*c).
 __device__ void row_stats(const float* z, int V, float c, Red& r, float& m_out, float& s_out) {
   float m = -INFINITY, s = 0.f;
+  #pragma unroll 4
   for (int x = threadIdx.x; x < V; x += kT) {
     const float v = __ldcg(z + x);
     if (v > m) {
@@ -165,6 +166,7 @@ __device__ void row_stats(const float* z, int V, float c, Red& r, float& m_out, 
 __device__ int row_argmax(const float* z, int V, Red& r) {
   float best = -INFINITY;
   int bi = 0x7fffffff;
+  #pragma unroll 4
   for (int x = threadIdx.x; x < V; x += kT) {
     const float v = __ldcg(z + x);
     if (v > best || (v == best && x < bi)) {
@@ -231,6 +233,7 @@ __device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r
   // mass-weighted radix select over the bit patterns of e(x) (all >= 0):
   // tau = the largest value v with sum_{e >= v} e >= top_p * sum e.
   unsigned long long tot = 0;
+  #pragma unroll 4
   for (int x = threadIdx.x; x < V; x += kT) tot += static_cast<unsigned long long>(d.e(x) * kFix40);
   tot = block_sum_u64(tot, r);
   const double target = static_cast<double>(top_p) * static_cast<double>(tot);
@@ -241,6 +244,7 @@ __device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r
     const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
     for (int i = threadIdx.x; i < 256; i += kT) r.hist[i] = 0ull;
     __syncthreads();
+    #pragma unroll 4
     for (int x = threadIdx.x; x < V; x += kT) {
       const float v = d.e(x);
       const uint32_t bits = __float_as_uint(v);
@@ -272,6 +276,7 @@ __device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r
   }
   d.tau = __uint_as_float(prefix);
   float z_kept = 0.f;
+  #pragma unroll 4
   for (int x = threadIdx.x; x < V; x += kT) {
     const float v = d.e(x);
     z_kept += v >= d.tau ? v : 0.f;
@@ -305,19 +310,48 @@ SPEC_DEVINL unsigned long long warp_incl_scan_u64(unsigned long long v) {
 
 // Inverse-CDF draw: the smallest id t with sum_{x<=t} fx(x) > floor(u * total).
 // `total` is the exact fixed-point sum; `last_pos` the last id with fx > 0.
+// Two levels: every warp sums a contiguous chunk of ids exactly (independent
+// loads in flight), an exclusive scan of the chunk totals finds the chunk
+// where the cumulative weight crosses the threshold, and that chunk alone is
+// scanned id by id in tiles of 4 ids per thread.  The integer sums are exact,
+// so the id is the one a single scan in id order finds.
 template <class DW>
 __device__ int draw(const DW& dw, int V, float u, unsigned long long total, int last_pos, Red& r) {
   const unsigned long long thr =
       static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(total));
-  unsigned long long run = 0;  // exact prefix before the current tile
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  for (int base = 0; base < V; base += 4 * kT) {
+  const int chunk = ((V + kWarps - 1) / kWarps + 31) & ~31;
+  {
+    const int c0 = w * chunk, c1 = min(V, c0 + chunk);
+    unsigned long long s = 0;
+#pragma unroll 4
+    for (int x = c0 + l; x < c1; x += 32) s += dw.fx(x);
+    s = warp_sum_u64(s);
+    __syncthreads();  // the reduction area may still be read by a previous step
+    if (l == 0) r.u[w] = s;
+    __syncthreads();
+    if (w == 0) {
+      const unsigned long long t = l < kWarps ? r.u[l] : 0ull;
+      const unsigned long long ti = warp_incl_scan_u64(t);
+      const bool hit = l < kWarps && ti - t <= thr && thr < ti;
+      const unsigned ball = __ballot_sync(0xffffffffu, hit);
+      if (hit) r.bu[2] = ti - t;  // one lane at most: the prefix before the crossing chunk
+      if (l == 0) r.bi[3] = ball ? __ffs(ball) - 1 : -1;
+    }
+    __syncthreads();
+  }
+  const int cw = r.bi[3];
+  if (cw < 0) return last_pos;  // u * total rounded up to total
+  unsigned long long run = r.bu[2];  // exact prefix before the current tile
+  const int b0 = cw * chunk, b1 = min(V, b0 + chunk);
+  __syncthreads();
+  for (int base = b0; base < b1; base += 4 * kT) {
     const int x0 = base + threadIdx.x * 4;
     unsigned long long f[4];
     unsigned long long mine = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      f[k] = (x0 + k < V) ? dw.fx(x0 + k) : 0ull;
+      f[k] = (x0 + k < b1) ? dw.fx(x0 + k) : 0ull;
       mine += f[k];
     }
     const unsigned long long incl_w = warp_incl_scan_u64(mine);
@@ -360,6 +394,7 @@ __device__ void weights_total(const DW& dw, int V, Red& r, unsigned long long& t
                               int& last_pos) {
   unsigned long long s = 0;
   int lp = -1;
+  #pragma unroll 4
   for (int x = threadIdx.x; x < V; x += kT) {
     const unsigned long long f = dw.fx(x);
     s += f;
@@ -1057,6 +1092,7 @@ __global__ void __launch_bounds__(kT, 1) sample_kernel(const SampleParams p) {
   }
   RowDist dist = make_dist(z, V, p.T, p.top_p, red);
   if (probs)
+    #pragma unroll 4
     for (int x = threadIdx.x; x < V; x += kT) probs[x] = dist.p(x);
   DrawWeights dw;
   dw.p = dist;
@@ -1256,6 +1292,7 @@ __global__ void __launch_bounds__(kT, 1) tree_accept_kernel(const TreeAcceptPara
       weights_total(tw, V, red, total, last_pos);
       if (static_cast<double>(total) > kResidualFallback * 4503599627370496.0) {
         const float inv = static_cast<float>(4503599627370496.0 / static_cast<double>(total));
+        #pragma unroll 4
         for (int x = threadIdx.x; x < V; x += kT) pb[x] = tw.w(x) * inv;
         __syncthreads();
         tw.pb = pb;

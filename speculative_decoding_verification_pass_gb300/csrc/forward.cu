@@ -626,8 +626,10 @@ SPEC_DEVINL void att_block(const MkParams& P, const KVLayout& lay, uint32_t aQ, 
 // areas at once, so both blocks' copies are in flight with q's.
 // Merge the chunk partials of every query row by log-sum-exp into the
 // attention output (bf16 hi/lo).  One warp per (sequence, KV head, row,
-// 32-dimension group): each lane owns one dimension, so every partial load of
-// a lane is in flight at once.
+// 64-dimension group): each lane owns two adjacent dimensions (float2
+// loads), so every partial load of a lane is in flight at once and a decode
+// batch needs at most one item per warp (8 KV heads x 20 rows x 2 groups at
+// batch 1, against 608 warps).
 template <int HD>
 SPEC_DEVINL void cmb_phase(const MkParams& P) {
   const int e = threadIdx.x - kEpiFirstThread;
@@ -636,7 +638,7 @@ SPEC_DEVINL void cmb_phase(const MkParams& P) {
   const int R = P.n * G;
   const int qdim = P.H * HD;
   const int nch = P.att_nch;
-  constexpr int kDG = HD / 32;
+  constexpr int kDG = HD / 64;
   const int items = P.B * P.Hkv * R * kDG;
   const float2* mlp = reinterpret_cast<const float2*>(P.att_ml);
   for (int it = blockIdx.x * 4 + w; it < items; it += gridDim.x * 4) {
@@ -648,34 +650,42 @@ SPEC_DEVINL void cmb_phase(const MkParams& P) {
     const int ck = att_chunk_keys(Tk, nch);
     const int nu = (Tk + ck - 1) / ck;
     const long long ubase = (static_cast<long long>(b) * P.Hkv + kvh) * nch;
-    const float* ob = P.att_o + (ubase * 32 + r) * HD + dg * 32 + lane;
-    float acc = 0.f, lsum = 0.f, m = -INFINITY;
+    const float2* ob = reinterpret_cast<const float2*>(P.att_o + (ubase * 32 + r) * HD + dg * 64) + lane;
+    float2 acc = make_float2(0.f, 0.f);
+    float lsum = 0.f, m = -INFINITY;
     for (int u0 = 0; u0 < nu; u0 += 32) {
       // lane k holds unit u0 + k's (max, sum); the o loads of the 32 units
       // below do not depend on them
       const int cnt = min(32, nu - u0);
       const float2 mv = lane < cnt ? __ldcg(&mlp[(ubase + u0 + lane) * 32 + r]) : make_float2(-INFINITY, 0.f);
-      float ov[32];
+      float2 ov[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) ov[k] = k < cnt ? __ldcg(ob + static_cast<long long>(u0 + k) * 32 * HD) : 0.f;
+      for (int k = 0; k < 32; ++k)
+        ov[k] = k < cnt ? __ldcg(ob + static_cast<long long>(u0 + k) * 32 * HD / 2) : make_float2(0.f, 0.f);
       const float mb = warp_max(mv.x);
       const float mn = fmaxf(m, mb);
       const float scale = m == -INFINITY ? 0.f : exp2f(m - mn);
       const float wgt = mv.x == -INFINITY ? 0.f : exp2f(mv.x - mn);
-      float a2 = 0.f;
+      float ax = 0.f, ay = 0.f;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) a2 += __shfl_sync(0xffffffffu, wgt, k) * ov[k];
-      acc = acc * scale + a2;
+      for (int k = 0; k < 32; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, wgt, k);
+        ax += wk * ov[k].x;
+        ay += wk * ov[k].y;
+      }
+      acc.x = acc.x * scale + ax;
+      acc.y = acc.y * scale + ay;
       lsum = lsum * scale + warp_sum(wgt * mv.y);
       m = mn;
     }
-    const float o = acc / lsum;
     const int j = r / G, g = r % G;
     const long long off =
-        (static_cast<long long>(b) * P.n + j) * qdim + (kvh * G + g) * HD + dg * 32 + lane;
-    const uint16_t hi = f32_to_bf16(o);
-    P.o[off] = hi;
-    P.o_lo[off] = f32_to_bf16(o - bf16_to_f32(hi));
+        (static_cast<long long>(b) * P.n + j) * qdim + (kvh * G + g) * HD + dg * 64 + 2 * lane;
+    const float o0 = acc.x / lsum, o1 = acc.y / lsum;
+    const uint16_t h0 = f32_to_bf16(o0), h1 = f32_to_bf16(o1);
+    *reinterpret_cast<uint32_t*>(P.o + off) = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+    const uint16_t l0 = f32_to_bf16(o0 - bf16_to_f32(h0)), l1 = f32_to_bf16(o1 - bf16_to_f32(h1));
+    *reinterpret_cast<uint32_t*>(P.o_lo + off) = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
   }
 }
 
