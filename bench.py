@@ -48,8 +48,8 @@ TRAFFIC = {
     # algorithmic bytes (weights, KV and logits each move once)
     "forward_kernel": {"files": ["forward.cu", "gemm_common.cuh", "attn_common.cuh", "common.cuh",
                                  "internal.h"],
-                       "source_sha1": "8c8b97e7c7f62b1d7cd86e312f1efb7d12b3c9bc",
-                       "bytes_per_launch": 15345739312},
+                       "source_sha1": "7210126e44c39f46cb351f2c0aecbdb3498f9dbf",
+                       "bytes_per_launch": 15346274946},
 }
 
 

@@ -220,8 +220,14 @@ struct RowDist {
   }
 };
 
+// Per-warp histograms of the nucleus radix select (dynamic shared memory of
+// the per-sequence kernels): each warp adds into its own 256 bins, so lanes
+// contend only within their warp, then the warps' bins are summed.
+constexpr size_t kHistBytes = static_cast<size_t>(kWarps) * 256 * sizeof(unsigned long long);
+
 // Softmax statistics and (top_p < 1) the nucleus threshold of one row.
-__device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r) {
+__device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r,
+                             unsigned long long* whist) {
   RowDist d;
   d.z = z;
   d.c = kLog2e / T;
@@ -242,14 +248,21 @@ __device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r
   for (int level = 0; level < 4; ++level) {
     const int shift = 24 - 8 * level;
     const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
-    for (int i = threadIdx.x; i < 256; i += kT) r.hist[i] = 0ull;
-    __syncthreads();
+    unsigned long long* wh = whist + (threadIdx.x >> 5) * 256;
+    for (int i = threadIdx.x & 31; i < 256; i += 32) wh[i] = 0ull;
+    __syncwarp();
     #pragma unroll 4
     for (int x = threadIdx.x; x < V; x += kT) {
       const float v = d.e(x);
       const uint32_t bits = __float_as_uint(v);
       if ((bits & hi_mask) == prefix)
-        atomicAdd(&r.hist[(bits >> shift) & 0xFFu], static_cast<unsigned long long>(v * kFix40));
+        atomicAdd(&wh[(bits >> shift) & 0xFFu], static_cast<unsigned long long>(v * kFix40));
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 256; i += kT) {
+      unsigned long long t = 0;
+      for (int w = 0; w < kWarps; ++w) t += whist[w * 256 + i];
+      r.hist[i] = t;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -409,6 +422,7 @@ __device__ void weights_total(const DW& dw, int V, Red& r, unsigned long long& t
 // visited lazily up to the first rejection.
 __global__ void __launch_bounds__(kT, 1) accept_seq_kernel(const AcceptParams p) {
   __shared__ Red red;
+  extern __shared__ unsigned long long dyn_hist[];  // kHistBytes
   __shared__ int s_flag;
   const int b = blockIdx.x;
   const int gamma = p.gamma, V = p.V, n = gamma + 1;
@@ -438,7 +452,7 @@ __global__ void __launch_bounds__(kT, 1) accept_seq_kernel(const AcceptParams p)
   int j = gamma;
   RowDist dist;
   for (int i = 0; i < gamma; ++i) {
-    dist = make_dist(zb + static_cast<long long>(i) * V, V, p.T, p.top_p, red);
+    dist = make_dist(zb + static_cast<long long>(i) * V, V, p.T, p.top_p, red, dyn_hist);
     if (threadIdx.x == 0) {
       int x = __ldg(xb + i);
       bool accept = false;
@@ -464,7 +478,7 @@ __global__ void __launch_bounds__(kT, 1) accept_seq_kernel(const AcceptParams p)
   }
   DrawWeights dw;
   if (j == gamma) {
-    dist = make_dist(zb + static_cast<long long>(gamma) * V, V, p.T, p.top_p, red);
+    dist = make_dist(zb + static_cast<long long>(gamma) * V, V, p.T, p.top_p, red, dyn_hist);
     dw.p = dist;
     dw.q = nullptr;
   } else {
@@ -1079,6 +1093,7 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
 
 __global__ void __launch_bounds__(kT, 1) sample_kernel(const SampleParams p) {
   __shared__ Red red;
+  extern __shared__ unsigned long long dyn_hist[];  // kHistBytes
   const int row = blockIdx.x;
   const int V = p.V;
   const float* z = p.logits + static_cast<long long>(row) * V;
@@ -1090,7 +1105,7 @@ __global__ void __launch_bounds__(kT, 1) sample_kernel(const SampleParams p) {
     if (threadIdx.x == 0) p.tokens[row] = a;
     return;
   }
-  RowDist dist = make_dist(z, V, p.T, p.top_p, red);
+  RowDist dist = make_dist(z, V, p.T, p.top_p, red, dyn_hist);
   if (probs)
     #pragma unroll 4
     for (int x = threadIdx.x; x < V; x += kT) probs[x] = dist.p(x);
@@ -1205,6 +1220,7 @@ struct TreeWeights {
 
 __global__ void __launch_bounds__(kT, 1) tree_accept_kernel(const TreeAcceptParams p) {
   __shared__ Red red;
+  extern __shared__ unsigned long long dyn_hist[];  // kHistBytes
   __shared__ int s_flag;
   const int b = blockIdx.x;
   const int n = p.n, V = p.V;
@@ -1258,7 +1274,7 @@ __global__ void __launch_bounds__(kT, 1) tree_accept_kernel(const TreeAcceptPara
   for (;;) {
     const float* qrow = p.q + (row0 + cur) * V;
     TreeWeights tw;
-    tw.p = make_dist(zb + static_cast<long long>(cur) * V, V, p.T, p.top_p, red);
+    tw.p = make_dist(zb + static_cast<long long>(cur) * V, V, p.T, p.top_p, red, dyn_hist);
     tw.pb = nullptr;
     tw.q = nullptr;
     int nxt = -1;
@@ -1438,6 +1454,23 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, cudaS
 
 }  // namespace
 
+// The per-sequence kernels take kHistBytes of dynamic shared memory (above
+// the 48 KB default): set once per process.
+cudaError_t per_seq_smem_attrs() {
+  static cudaError_t e = [] {
+    const void* fns[3] = {reinterpret_cast<const void*>(accept_seq_kernel),
+                          reinterpret_cast<const void*>(sample_kernel),
+                          reinterpret_cast<const void*>(tree_accept_kernel)};
+    for (const void* f : fns) {
+      const cudaError_t r = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(kHistBytes));
+      if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
+  }();
+  return e;
+}
+
 int accept_grid_capacity() {
   static int cap = [] {
     int dev = 0, sms = 0, per = 0;
@@ -1455,8 +1488,10 @@ cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * (p.gamma + 1);
   const int cap = accept_grid_capacity();
   if (!p.grid || rows > kAcceptGridRows || cap <= 0) {
+    const cudaError_t e = per_seq_smem_attrs();
+    if (e != cudaSuccess) return e;
     AcceptParams a = p;
-    accept_seq_kernel<<<p.B, kT, 0, stream>>>(a);
+    accept_seq_kernel<<<p.B, kT, kHistBytes, stream>>>(a);
     return cudaGetLastError();
   }
   const long long units = rows * p.S;
@@ -1477,7 +1512,9 @@ cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream) {
 
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t stream) {
   if (p.R == 0) return cudaSuccess;
-  sample_kernel<<<p.R, kT, 0, stream>>>(p);
+  const cudaError_t e = per_seq_smem_attrs();
+  if (e != cudaSuccess) return e;
+  sample_kernel<<<p.R, kT, kHistBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1501,7 +1538,9 @@ cudaError_t launch_mask_logits(float* logits, const uint32_t* allowed, int rows,
 
 cudaError_t launch_tree_accept(const TreeAcceptParams& p, cudaStream_t stream) {
   if (p.B == 0) return cudaSuccess;
-  tree_accept_kernel<<<p.B, kT, 0, stream>>>(p);
+  const cudaError_t e = per_seq_smem_attrs();
+  if (e != cudaSuccess) return e;
+  tree_accept_kernel<<<p.B, kT, kHistBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
