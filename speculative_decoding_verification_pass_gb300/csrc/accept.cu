@@ -117,19 +117,43 @@ SPEC_DEVINL void ms_merge(float& m, float& s, float m2, float s2, float c) {
   m = mn;
 }
 
+// f(x, a[x], b[x]) for every id x of a row (b may be nullptr: f gets 0).
+// When both rows allow it, each thread takes groups of 4 consecutive ids
+// with 16-byte loads, several groups in flight; else one id at a time.
+template <class F>
+SPEC_DEVINL void visit_row(const float* a, const float* b, int V, F&& f) {
+  const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(a) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(b) & 15) == 0;
+  if (vec) {
+    const float4* a4 = reinterpret_cast<const float4*>(a);
+    const float4* b4 = reinterpret_cast<const float4*>(b);
+    const int V4 = V >> 2;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < V4; i += kT) {
+      const float4 va = __ldcg(a4 + i);
+      const float4 vb = b ? __ldcg(b4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      f(4 * i, va.x, vb.x);
+      f(4 * i + 1, va.y, vb.y);
+      f(4 * i + 2, va.z, vb.z);
+      f(4 * i + 3, va.w, vb.w);
+    }
+  } else {
+#pragma unroll 4
+    for (int x = threadIdx.x; x < V; x += kT) f(x, __ldcg(a + x), b ? __ldcg(b + x) : 0.f);
+  }
+}
+
 // Row statistics of softmax(z / T): block max and sum of exp2((z-max)*c).
 __device__ void row_stats(const float* z, int V, float c, Red& r, float& m_out, float& s_out) {
   float m = -INFINITY, s = 0.f;
-  #pragma unroll 4
-  for (int x = threadIdx.x; x < V; x += kT) {
-    const float v = __ldcg(z + x);
+  visit_row(z, nullptr, V, [&](int, float v, float) {
     if (v > m) {
       s = (m == -INFINITY ? 0.f : s * exp2f((m - v) * c)) + 1.0f;
       m = v;
     } else if (v != -INFINITY) {  // masked-out logits (-inf) weigh nothing
       s += exp2f((v - m) * c);
     }
-  }
+  });
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -166,14 +190,12 @@ __device__ void row_stats(const float* z, int V, float c, Red& r, float& m_out, 
 __device__ int row_argmax(const float* z, int V, Red& r) {
   float best = -INFINITY;
   int bi = 0x7fffffff;
-  #pragma unroll 4
-  for (int x = threadIdx.x; x < V; x += kT) {
-    const float v = __ldcg(z + x);
+  visit_row(z, nullptr, V, [&](int x, float v, float) {
     if (v > best || (v == best && x < bi)) {
       best = v;
       bi = x;
     }
-  }
+  });
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
@@ -213,11 +235,12 @@ __device__ int row_argmax(const float* z, int V, Red& r) {
 struct RowDist {
   const float* z;
   float m, c, tau, Z;
-  SPEC_DEVINL float e(int x) const { return exp2f((__ldcg(z + x) - m) * c); }
-  SPEC_DEVINL float p(int x) const {
-    const float v = e(x);
+  SPEC_DEVINL float e_of(float zv) const { return exp2f((zv - m) * c); }
+  SPEC_DEVINL float p_of(float zv) const {
+    const float v = e_of(zv);
     return v >= tau ? v / Z : 0.f;
   }
+  SPEC_DEVINL float p(int x) const { return p_of(__ldcg(z + x)); }
 };
 
 // Per-warp histograms of the nucleus radix select (dynamic shared memory of
@@ -239,8 +262,9 @@ __device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r
   // mass-weighted radix select over the bit patterns of e(x) (all >= 0):
   // tau = the largest value v with sum_{e >= v} e >= top_p * sum e.
   unsigned long long tot = 0;
-  #pragma unroll 4
-  for (int x = threadIdx.x; x < V; x += kT) tot += static_cast<unsigned long long>(d.e(x) * kFix40);
+  visit_row(z, nullptr, V, [&](int, float zv, float) {
+    tot += static_cast<unsigned long long>(d.e_of(zv) * kFix40);
+  });
   tot = block_sum_u64(tot, r);
   const double target = static_cast<double>(top_p) * static_cast<double>(tot);
   uint32_t prefix = 0;
@@ -251,13 +275,12 @@ __device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r
     unsigned long long* wh = whist + (threadIdx.x >> 5) * 256;
     for (int i = threadIdx.x & 31; i < 256; i += 32) wh[i] = 0ull;
     __syncwarp();
-    #pragma unroll 4
-    for (int x = threadIdx.x; x < V; x += kT) {
-      const float v = d.e(x);
+    visit_row(z, nullptr, V, [&](int, float zv, float) {
+      const float v = d.e_of(zv);
       const uint32_t bits = __float_as_uint(v);
       if ((bits & hi_mask) == prefix)
         atomicAdd(&wh[(bits >> shift) & 0xFFu], static_cast<unsigned long long>(v * kFix40));
-    }
+    });
     __syncthreads();
     for (int i = threadIdx.x; i < 256; i += kT) {
       unsigned long long t = 0;
@@ -289,25 +312,31 @@ __device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r
   }
   d.tau = __uint_as_float(prefix);
   float z_kept = 0.f;
-  #pragma unroll 4
-  for (int x = threadIdx.x; x < V; x += kT) {
-    const float v = d.e(x);
+  visit_row(z, nullptr, V, [&](int, float zv, float) {
+    const float v = d.e_of(zv);
     z_kept += v >= d.tau ? v : 0.f;
-  }
+  });
   d.Z = block_sum_f(z_kept, r);
   return d;
 }
 
 // Weight of id x for the final draw: the residual max(0, p - q) or p itself.
+// (The weight types expose the rows they read -- src() and q -- and the
+// weight of one id from those rows' values, so passes can load them in
+// vector groups.)
 struct DrawWeights {
   RowDist p;
   const float* q;  // nullptr: draw from p
-  SPEC_DEVINL float w(int x) const {
-    const float pv = p.p(x);
-    return q ? fmaxf(pv - __ldcg(q + x), 0.f) : pv;
+  SPEC_DEVINL const float* src() const { return p.z; }
+  SPEC_DEVINL float w_of(float zv, float qv) const {
+    const float pv = p.p_of(zv);
+    return q ? fmaxf(pv - qv, 0.f) : pv;
+  }
+  SPEC_DEVINL unsigned long long fx_of(float zv, float qv) const {
+    return static_cast<unsigned long long>(w_of(zv, qv) * kFix52);
   }
   SPEC_DEVINL unsigned long long fx(int x) const {
-    return static_cast<unsigned long long>(w(x) * kFix52);
+    return fx_of(__ldcg(p.z + x), q ? __ldcg(q + x) : 0.f);
   }
 };
 
@@ -333,12 +362,26 @@ __device__ int draw(const DW& dw, int V, float u, unsigned long long total, int 
   const unsigned long long thr =
       static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(total));
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  const int chunk = ((V + kWarps - 1) / kWarps + 31) & ~31;
+  const int chunk = ((V + kWarps - 1) / kWarps + 127) & ~127;
+  const float* src = dw.src();
+  const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(dw.q) & 15) == 0;
   {
     const int c0 = w * chunk, c1 = min(V, c0 + chunk);
     unsigned long long s = 0;
+    if (vec) {  // c0 and c1 are multiples of 4
+      const float4* a4 = reinterpret_cast<const float4*>(src);
+      const float4* b4 = reinterpret_cast<const float4*>(dw.q);
 #pragma unroll 4
-    for (int x = c0 + l; x < c1; x += 32) s += dw.fx(x);
+      for (int i = c0 / 4 + l; i < c1 / 4; i += 32) {
+        const float4 va = __ldcg(a4 + i);
+        const float4 vb = dw.q ? __ldcg(b4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        s += dw.fx_of(va.x, vb.x) + dw.fx_of(va.y, vb.y) + dw.fx_of(va.z, vb.z) + dw.fx_of(va.w, vb.w);
+      }
+    } else {
+#pragma unroll 4
+      for (int x = c0 + l; x < c1; x += 32) s += dw.fx(x);
+    }
     s = warp_sum_u64(s);
     __syncthreads();  // the reduction area may still be read by a previous step
     if (l == 0) r.u[w] = s;
@@ -362,11 +405,19 @@ __device__ int draw(const DW& dw, int V, float u, unsigned long long total, int 
     const int x0 = base + threadIdx.x * 4;
     unsigned long long f[4];
     unsigned long long mine = 0;
+    if (vec && x0 + 3 < b1) {
+      const float4 va = __ldcg(reinterpret_cast<const float4*>(src + x0));
+      const float4 vb = dw.q ? __ldcg(reinterpret_cast<const float4*>(dw.q + x0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      f[0] = dw.fx_of(va.x, vb.x);
+      f[1] = dw.fx_of(va.y, vb.y);
+      f[2] = dw.fx_of(va.z, vb.z);
+      f[3] = dw.fx_of(va.w, vb.w);
+    } else {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      f[k] = (x0 + k < b1) ? dw.fx(x0 + k) : 0ull;
-      mine += f[k];
+      for (int k = 0; k < 4; ++k) f[k] = (x0 + k < b1) ? dw.fx(x0 + k) : 0ull;
     }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mine += f[k];
     const unsigned long long incl_w = warp_incl_scan_u64(mine);
     __syncthreads();
     if (l == 31) r.u[w] = incl_w;
@@ -407,12 +458,11 @@ __device__ void weights_total(const DW& dw, int V, Red& r, unsigned long long& t
                               int& last_pos) {
   unsigned long long s = 0;
   int lp = -1;
-  #pragma unroll 4
-  for (int x = threadIdx.x; x < V; x += kT) {
-    const unsigned long long f = dw.fx(x);
+  visit_row(dw.src(), dw.q, V, [&](int x, float sv, float qv) {
+    const unsigned long long f = dw.fx_of(sv, qv);
     s += f;
-    if (f) lp = x;
-  }
+    if (f) lp = max(lp, x);
+  });
   total = block_sum_u64(s, r);
   last_pos = block_max_i(lp, r);
 }
@@ -1107,8 +1157,7 @@ __global__ void __launch_bounds__(kT, 1) sample_kernel(const SampleParams p) {
   }
   RowDist dist = make_dist(z, V, p.T, p.top_p, red, dyn_hist);
   if (probs)
-    #pragma unroll 4
-    for (int x = threadIdx.x; x < V; x += kT) probs[x] = dist.p(x);
+        visit_row(z, nullptr, V, [&](int x, float zv, float) { probs[x] = dist.p_of(zv); });
   DrawWeights dw;
   dw.p = dist;
   dw.q = nullptr;
@@ -1208,13 +1257,17 @@ struct TreeWeights {
   RowDist p;
   const float* pb;  // materialised p', or nullptr
   const float* q;   // residual against q, or nullptr
+  SPEC_DEVINL const float* src() const { return pb ? pb : p.z; }
   SPEC_DEVINL float base(int x) const { return pb ? __ldcg(pb + x) : p.p(x); }
-  SPEC_DEVINL float w(int x) const {
-    const float v = base(x);
-    return q ? fmaxf(v - __ldcg(q + x), 0.f) : v;
+  SPEC_DEVINL float w_of(float sv, float qv) const {
+    const float v = pb ? sv : p.p_of(sv);
+    return q ? fmaxf(v - qv, 0.f) : v;
+  }
+  SPEC_DEVINL unsigned long long fx_of(float sv, float qv) const {
+    return static_cast<unsigned long long>(w_of(sv, qv) * kFix52);
   }
   SPEC_DEVINL unsigned long long fx(int x) const {
-    return static_cast<unsigned long long>(w(x) * kFix52);
+    return fx_of(__ldcg(src() + x), q ? __ldcg(q + x) : 0.f);
   }
 };
 
@@ -1308,8 +1361,7 @@ __global__ void __launch_bounds__(kT, 1) tree_accept_kernel(const TreeAcceptPara
       weights_total(tw, V, red, total, last_pos);
       if (static_cast<double>(total) > kResidualFallback * 4503599627370496.0) {
         const float inv = static_cast<float>(4503599627370496.0 / static_cast<double>(total));
-        #pragma unroll 4
-        for (int x = threadIdx.x; x < V; x += kT) pb[x] = tw.w(x) * inv;
+                visit_row(tw.src(), tw.q, V, [&](int x, float sv, float qv) { pb[x] = tw.w_of(sv, qv) * inv; });
         __syncthreads();
         tw.pb = pb;
       }
