@@ -267,3 +267,41 @@ def test_persistent_and_per_step_schedules_agree(cfg, monkeypatch):
     _close(zp, zs, tol=1e-3)
     _close(kp, ks, tol=8e-3)
     _close(vp, vs, tol=8e-3)
+
+
+def test_graph_replays_recompute_every_pass():
+    """The persistent kernel tags its stream-K words with a launch epoch kept
+    in the workspace, so replays of one captured graph (frozen parameters)
+    never take an earlier replay's words as current: every replay with new
+    tokens in place must give the eager pass's logits exactly."""
+    cfg = SMALL[1]
+    B, cap, n = 2, 96, 5
+    m = sb.Model(cfg, 12)
+    kv_g = sb.KVCache(cfg, B, cap)
+    kv_e = sb.KVCache(cfg, B, cap)
+    ws_g = sb.workspace(sb.spec_workspace_bytes(cfg, B, n - 1, cap))
+    ws_e = sb.workspace(sb.spec_workspace_bytes(cfg, B, n - 1, cap))
+    toks = torch.zeros(B, n, dtype=torch.int32, device="cuda")
+    out_g = torch.empty(B, n, cfg.vocab, device="cuda")
+    out_e = torch.empty_like(out_g)
+    for kv in (kv_g, kv_e):
+        kv.len.fill_(20)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        sb.spec_verify_forward(m.handle, toks, B, n - 1, kv_g, out_g, ws_g, st)   # warm-up
+        kv_g.len.fill_(20)
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            sb.spec_verify_forward(m.handle, toks, B, n - 1, kv_g, out_g, ws_g, st)
+    for it in range(4):
+        toks.copy_(torch.from_numpy(wl.tokens(100 + it, B, n, cfg.vocab).astype(np.int32)))
+        kv_g.len.fill_(20 + it)
+        kv_e.len.fill_(20 + it)
+        g.replay()
+        sb.spec_verify_forward(m.handle, toks, B, n - 1, kv_e, out_e, ws_e)
+        torch.cuda.synchronize()
+        assert torch.equal(out_g, out_e), it
+    for ws in (ws_g, ws_e):
+        stt, bits = sb.spec_device_status(ws)
+        assert stt == sb.SPEC_OK, hex(bits)
