@@ -321,20 +321,28 @@ SPEC_DEVINL bool fixup_tagged(unsigned long long* part, int ntok, int c0, int r,
   return true;
 }
 
-// Every epilogue thread publishes its writes; one thread arrives.
+// The epilogue threads' writes of a phase are published by one release: the
+// CTA barrier orders every thread's writes before the arriving thread's
+// fence, and that fence before its arrival (the grid-barrier pattern of
+// cooperative groups).  Each thread orders its own generic-proxy writes before
+// the next phase's TMA reads.
 SPEC_DEVINL void phase_arrive(const MkParams& P) {
-  __threadfence();
   fence_proxy_async();
   named_bar(kArriveBar, kEpiThreads);
-  if (threadIdx.x == kEpiFirstThread) atomicAdd(P.bar, 1u);
+  if (threadIdx.x == kEpiFirstThread) {
+    __threadfence();
+    atomicAdd(P.bar, 1u);
+  }
 }
 
-// All epilogue threads wait for phase `ph - 1` to be complete.
+// All epilogue threads wait for phase `ph - 1` to be complete: one thread
+// acquires the barrier count, the CTA barrier orders the others after it.
 SPEC_DEVINL bool epi_wait(const MkParams& P, const MkSmem& sm, int ph) {
-  if (threadIdx.x == kEpiFirstThread)
+  if (threadIdx.x == kEpiFirstThread) {
     grid_wait(P.bar, static_cast<unsigned>(ph) * gridDim.x, sm.abort, P.status);
+    __threadfence();
+  }
   named_bar(kArriveBar, kEpiThreads);
-  __threadfence();
   return *sm.abort == 0;
 }
 
