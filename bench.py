@@ -48,8 +48,8 @@ TRAFFIC = {
     # algorithmic bytes (weights, KV and logits each move once)
     "forward_kernel": {"files": ["forward.cu", "gemm_common.cuh", "attn_common.cuh", "common.cuh",
                                  "internal.h"],
-                       "source_sha1": "7210126e44c39f46cb351f2c0aecbdb3498f9dbf",
-                       "bytes_per_launch": 15346274946},
+                       "source_sha1": "3c0171fd5b2c1dac3c636144c8d9e93be337c3d6",
+                       "bytes_per_launch": 15347362447},
 }
 
 
