@@ -575,7 +575,7 @@ struct ASmem {
   float g[kAW];
   int i[kAW];
   unsigned long long u[kAW];
-  unsigned long long hist[256];
+  unsigned long long hist[kAW][256];  // one nucleus histogram per warp
   float rm[kMaxRows];   // row max (greedy: argmax value)
   float rz[kMaxRows];   // row normaliser (kept mass with a nucleus)
   float rtau[kMaxRows]; // nucleus threshold on e(x) (0: none)
@@ -611,8 +611,15 @@ SPEC_DEVINL bool agrid_sync(const AcceptParams& p, unsigned target, ASmem& s) {
 // Block (max, sum exp2((z - max) c)) over ids [x0, x1), fixed merge order.
 __device__ float2 chunk_ms(const float* z, int x0, int x1, float c, ASmem& s) {
   float m = -INFINITY, sum = 0.f;
-  for (int x = x0 + threadIdx.x; x < x1; x += kAT) {
-    const float v = __ldcg(z + x);
+  float zv[kAPer];  // this thread's ids x0 + threadIdx.x + k kAT, loaded together
+#pragma unroll
+  for (int k = 0; k < kAPer; ++k) {
+    const int x = x0 + threadIdx.x + k * kAT;
+    zv[k] = x < x1 ? __ldcg(z + x) : -INFINITY;
+  }
+#pragma unroll
+  for (int k = 0; k < kAPer; ++k) {
+    const float v = zv[k];
     if (v > m) {
       sum = (m == -INFINITY ? 0.f : sum * exp2f((m - v) * c)) + 1.0f;
       m = v;
@@ -809,10 +816,11 @@ SPEC_DEVINL int warp_select(const unsigned long long* hist, double target,
 struct ARow {  // the distribution of one row: e = exp2((z - m) c), kept iff e >= tau
   const float* z;
   float m, c, tau, Z;
-  SPEC_DEVINL float p(int x) const {
-    const float e = exp2f((__ldcg(z + x) - m) * c);
+  SPEC_DEVINL float p_of(float zx) const {
+    const float e = exp2f((zx - m) * c);
     return e >= tau ? e / Z : 0.f;
   }
+  SPEC_DEVINL float p(int x) const { return p_of(__ldcg(z + x)); }
 };
 
 // Statistics of every row of sequence b into shared memory (all warps).
@@ -846,34 +854,52 @@ SPEC_DEVINL ARow arow(const AcceptParams& p, int b, int i, float c, const ASmem&
   return r;
 }
 
-// Thread 0: the first rejected draft of sequence b (gamma if none), with the
-// device status flags when `flag`.
-__device__ int decide(const AcceptParams& p, int b, float c, const ASmem& s, bool flag) {
+// Warp 0 (every lane): the first rejected draft of sequence b (gamma if
+// none), with the device status flag of that draft when `flag`.  Each lane
+// tests one draft (its token, q and p loads in flight together); the answer
+// is the first draft that is rejected or invalid, as in the sequential rule.
+__device__ int decide_warp(const AcceptParams& p, int b, float c, const ASmem& s, bool flag) {
+  const int l = threadIdx.x & 31;
   const int32_t* xb = p.draft + static_cast<long long>(b) * p.gamma;
   const float* qb = p.q + static_cast<long long>(b) * p.gamma * p.V;
   const float* ub = p.u + static_cast<long long>(b) * (p.gamma + 1);
-  for (int i = 0; i < p.gamma; ++i) {
-    const int x = __ldg(xb + i);
-    if (x < 0 || x >= p.V) {
-      if (flag) set_status(p.status, SPEC_DEV_BAD_TOKEN);
-      return i;
+  for (int i0 = 0; i0 < p.gamma; i0 += 32) {
+    const int i = i0 + l;
+    int why = 0;  // 0 accepted, 1 rejected, 2 token out of range, 3 q(x) = 0
+    if (i < p.gamma) {
+      const int x = __ldg(xb + i);
+      if (x < 0 || x >= p.V) {
+        why = 2;
+      } else {
+        const float qx = __ldg(qb + static_cast<long long>(i) * p.V + x);
+        const float px = arow(p, b, i, c, s).p(x);
+        const float ui = __ldg(ub + i);
+        if (!(qx > 0.f))
+          why = 3;
+        else if (!(ui < fminf(1.0f, px / qx)))
+          why = 1;
+      }
     }
-    const float qx = __ldg(qb + static_cast<long long>(i) * p.V + x);
-    if (!(qx > 0.f)) {
-      if (flag) set_status(p.status, SPEC_DEV_Q_ZERO);
-      return i;
+    const unsigned stop = __ballot_sync(0xffffffffu, why != 0);
+    if (stop) {
+      const int first = __ffs(stop) - 1;
+      const int w = __shfl_sync(0xffffffffu, why, first);
+      if (flag && l == 0 && w >= 2) set_status(p.status, w == 2 ? SPEC_DEV_BAD_TOKEN : SPEC_DEV_Q_ZERO);
+      return i0 + first;
     }
-    const float a = fminf(1.0f, arow(p, b, i, c, s).p(x) / qx);
-    if (!(__ldg(ub + i) < a)) return i;
   }
   return p.gamma;
 }
 
-// Fixed-point draw weights of id x: k = 0 residual max(0, p_j - q_j), k = 1 p_r.
+// Fixed-point draw weights of an id with p = pv, q = qv: k = 0 residual
+// max(0, p_j - q_j), k = 1 p_r.
+SPEC_DEVINL unsigned long long fx_of(float pv, float qv, int k) {
+  const float w = k == 0 ? fmaxf(pv - qv, 0.f) : pv;
+  return static_cast<unsigned long long>(w * kFix52);
+}
 SPEC_DEVINL unsigned long long fx_weight(const ARow& r, const float* qrow, int x, int k) {
   const float pv = r.p(x);
-  const float w = k == 0 ? fmaxf(pv - __ldcg(qrow + x), 0.f) : pv;
-  return static_cast<unsigned long long>(w * kFix52);
+  return fx_of(pv, k == 0 ? __ldcg(qrow + x) : 0.f, k);
 }
 
 __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) {
@@ -975,7 +1001,7 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
             s.prefix = prefix;
           }
         }
-        for (int k = threadIdx.x; k < 256; k += kAT) s.hist[k] = 0ull;
+        for (int k = threadIdx.x; k < kAW * 256; k += kAT) (&s.hist[0][0])[k] = 0ull;
         __syncthreads();
         const float m = s.bf[0];
         const uint32_t prefix = s.prefix;
@@ -983,25 +1009,47 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
           const int shift = 24 - 8 * level;
           const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
           unsigned long long mass = 0;
-          for (int x = x0 + threadIdx.x; x < x1; x += kAT) {
-            const float e = exp2f((__ldcg(z + x) - m) * c);
+          // this warp's histogram: same-bucket atomics contend within the warp only
+          unsigned long long* wh = s.hist[threadIdx.x >> 5];
+          float zv[kAPer];
+#pragma unroll
+          for (int k = 0; k < kAPer; ++k) {
+            const int x = x0 + threadIdx.x + k * kAT;
+            zv[k] = x < x1 ? __ldcg(z + x) : 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < kAPer; ++k) {
+            if (x0 + threadIdx.x + k * kAT >= x1) break;
+            const float e = exp2f((zv[k] - m) * c);
             const uint32_t bits = __float_as_uint(e);
             const unsigned long long fx = static_cast<unsigned long long>(e * kFix40);
             mass += fx;
-            if ((bits & hi_mask) == prefix) atomicAdd(&s.hist[(bits >> shift) & 0xFFu], fx);
+            if ((bits & hi_mask) == prefix) atomicAdd(&wh[(bits >> shift) & 0xFFu], fx);
           }
           if (level == 0) {
             mass = ablock_sum_u64(mass, s);
             if (threadIdx.x == 0) atomicAdd(p.tot40 + row, mass);
           }
           __syncthreads();
-          for (int k = threadIdx.x; k < 256; k += kAT)
-            if (s.hist[k]) atomicAdd(p.hist + (row * 4 + level) * 256 + k, s.hist[k]);
+          for (int k = threadIdx.x; k < 256; k += kAT) {
+            unsigned long long t = 0;  // integer sums: exact in any order
+#pragma unroll
+            for (int w = 0; w < kAW; ++w) t += s.hist[w][k];
+            if (t) atomicAdd(p.hist + (row * 4 + level) * 256 + k, t);
+          }
         } else {
           const float tau = __uint_as_float(prefix);
           float kept = 0.f;
-          for (int x = x0 + threadIdx.x; x < x1; x += kAT) {
-            const float e = exp2f((__ldcg(z + x) - m) * c);
+          float zv[kAPer];
+#pragma unroll
+          for (int k = 0; k < kAPer; ++k) {
+            const int x = x0 + threadIdx.x + k * kAT;
+            zv[k] = x < x1 ? __ldcg(z + x) : 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < kAPer; ++k) {
+            if (x0 + threadIdx.x + k * kAT >= x1) break;
+            const float e = exp2f((zv[k] - m) * c);
             kept += e >= tau ? e : 0.f;
           }
           kept = ablock_sum_f(kept, s);
@@ -1018,7 +1066,10 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
   for (long long u = blockIdx.x; u < units2; u += G) {
     const int b = static_cast<int>(u / S), ch = static_cast<int>(u % S);
     seq_stats(p, b, c, nucleus, s);
-    if (threadIdx.x == 0) s.j = decide(p, b, c, s, ch == 0);
+    if (threadIdx.x < 32) {
+      const int jd = decide_warp(p, b, c, s, ch == 0);
+      if (threadIdx.x == 0) s.j = jd;
+    }
     __syncthreads();
     const int j = s.j;
     const ARow r = arow(p, b, j, c, s);
@@ -1026,12 +1077,23 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
     const int x0 = ch * C, x1 = min(x0 + C, V);
     unsigned long long tr = 0, tp = 0;
     int lr = -1, lp = -1;
-    for (int x = x0 + threadIdx.x; x < x1; x += kAT) {
-      const unsigned long long fp = fx_weight(r, qrow, x, 1);
+    float zv[kAPer], qv[kAPer];  // this thread's ids, loaded together
+#pragma unroll
+    for (int k = 0; k < kAPer; ++k) {
+      const int x = x0 + threadIdx.x + k * kAT;
+      zv[k] = x < x1 ? __ldcg(r.z + x) : -INFINITY;
+      qv[k] = x < x1 && j < p.gamma ? __ldcg(qrow + x) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kAPer; ++k) {
+      const int x = x0 + threadIdx.x + k * kAT;
+      if (x >= x1) break;
+      const float pv = r.p_of(zv[k]);
+      const unsigned long long fp = fx_of(pv, 0.f, 1);
       tp += fp;
       if (fp) lp = x;
       if (j < p.gamma) {
-        const unsigned long long fr = fx_weight(r, qrow, x, 0);
+        const unsigned long long fr = fx_of(pv, qv[k], 0);
         tr += fr;
         if (fr) lr = x;
       }
@@ -1053,15 +1115,19 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
   // ---- P3: the draw
   for (int b = blockIdx.x; b < B; b += G) {
     seq_stats(p, b, c, nucleus, s);
-    if (threadIdx.x == 0) {
-      const int j = decide(p, b, c, s, false);
+    if (threadIdx.x < 32) {
+      // warp 0: the decision, the totals and the chunk holding the draw
+      const int l = threadIdx.x;
+      const int j = decide_warp(p, b, c, s, false);
       const unsigned long long* tot = p.part_tot + static_cast<long long>(b) * S * 2;
       const int* last = p.part_last + static_cast<long long>(b) * S * 2;
       unsigned long long total_r = 0, total_p = 0;
-      for (int k = 0; k < S; ++k) {
+      for (int k = l; k < S; k += 32) {
         total_r += __ldcg(tot + 2 * k);
         total_p += __ldcg(tot + 2 * k + 1);
       }
+      total_r = warp_sum_u64(total_r);  // integer sums: exact in any order
+      total_p = warp_sum_u64(total_p);
       int kind = 1;
       if (j < p.gamma && !(static_cast<double>(total_r) <= kResidualFallback * 4503599627370496.0))
         kind = 0;
@@ -1069,25 +1135,40 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
       const float uu = __ldg(p.u + static_cast<long long>(b) * n + p.gamma);
       const unsigned long long thr =
           static_cast<unsigned long long>(static_cast<double>(uu) * static_cast<double>(total));
-      unsigned long long run = 0;
+      // the first chunk k with thr < (sum of chunks 0..k): 32 chunks a round
+      unsigned long long run = 0, base = 0;
       int found = -1, lastpos = -1;
-      for (int k = 0; k < S; ++k) {
-        const unsigned long long t = __ldcg(tot + 2 * k + kind);
-        lastpos = max(lastpos, __ldcg(last + 2 * k + kind));
-        if (found < 0) {
-          if (thr < run + t)
-            found = k;
-          else
-            run += t;
+      for (int k0 = 0; k0 < S; k0 += 32) {
+        const int k = k0 + l;
+        const unsigned long long t = k < S ? __ldcg(tot + 2 * k + kind) : 0ull;
+        if (k < S) lastpos = max(lastpos, __ldcg(last + 2 * k + kind));
+        unsigned long long incl = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (l >= o) incl += v;
         }
+        if (found < 0) {
+          const unsigned hit = __ballot_sync(0xffffffffu, k < S && thr < base + incl);
+          if (hit) {
+            const int f = __ffs(hit) - 1;
+            found = k0 + f;
+            run = base + __shfl_sync(0xffffffffu, incl - t, f);
+          }
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
       }
-      s.j = j;
-      s.bi[0] = found;
-      s.bi[1] = kind;
-      s.bi[2] = lastpos;
-      s.bu[1] = run;
-      s.bu[2] = thr;
-      s.tok = -1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, o));
+      if (l == 0) {
+        s.j = j;
+        s.bi[0] = found;
+        s.bi[1] = kind;
+        s.bi[2] = lastpos;
+        s.bu[1] = run;
+        s.bu[2] = thr;
+        s.tok = -1;
+      }
     }
     __syncthreads();
     const int j = s.j, found = s.bi[0], kind = s.bi[1];
