@@ -48,7 +48,7 @@ TRAFFIC = {
     # algorithmic bytes (weights, KV and logits each move once)
     "forward_kernel": {"files": ["forward.cu", "gemm_common.cuh", "attn_common.cuh", "common.cuh",
                                  "internal.h"],
-                       "source_sha1": "3c0171fd5b2c1dac3c636144c8d9e93be337c3d6",
+                       "source_sha1": "508a9578f247b9104e67d8934e6c216273cf3683",
                        "bytes_per_launch": 15347362447},
 }
 

@@ -879,7 +879,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
     if (elect_lane0()) {
       // ------------------------------------------------- weight producer
       // Streams every GEMM phase's weight tiles of this CTA into the ring,
-      // running ahead across phases (only the ring's free stages limit it).
+      // running ahead across phases: the ring's free stages limit it, and
+      // before a phase's grid barrier has passed it issues at most all but
+      // kPreFree stages' worth of that phase's tiles.
       const uint64_t pol_w = l2_policy_evict_first();
       uint32_t issued[kMaxStages];
       for (int s = 0; s < S; ++s) issued[s] = 0;
