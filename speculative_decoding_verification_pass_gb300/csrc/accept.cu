@@ -823,6 +823,14 @@ struct ARow {  // the distribution of one row: e = exp2((z - m) c), kept iff e >
   SPEC_DEVINL float p(int x) const { return p_of(__ldcg(z + x)); }
 };
 
+// Id ranges per row of the nucleus select's work units: about one unit per
+// CTA, so that a unit's fixed costs (the row's statistics and the digits
+// chosen so far, read by one warp; block barriers) are paid once per range.
+SPEC_DEVINL int nucleus_split(const AcceptParams& p) {
+  const int rows = p.B * (p.gamma + 1);
+  return max(1, min(p.S, static_cast<int>(gridDim.x) / max(rows, 1)));
+}
+
 // Statistics of every row of sequence b into shared memory (all warps).
 __device__ void seq_stats(const AcceptParams& p, int b, float c, bool nucleus, ASmem& s) {
   const int n = p.gamma + 1;
@@ -832,7 +840,8 @@ __device__ void seq_stats(const AcceptParams& p, int b, float c, bool nucleus, A
     const float2 ms = warp_row_ms(p.part_ms + row * p.S, p.S, c);
     float Z = ms.y, tau = 0.f;
     if (nucleus) {
-      Z = warp_sum_parts(p.part_z + row * p.S, p.S);
+      const int SL = nucleus_split(p);
+      Z = warp_sum_parts(p.part_z + row * SL, SL);
       tau = __uint_as_float(static_cast<uint32_t>(__ldcg(p.sel + (row * 4 + 3) * 2)));
     }
     if (l == 0) {
@@ -973,12 +982,15 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
 
   // ---- N0..N3, NZ: the nucleus threshold of every row
   if (nucleus) {
+    const int SL = nucleus_split(p);
+    const long long units_l = static_cast<long long>(B) * n * SL;
     for (int level = 0; level <= 4; ++level) {
-      for (long long u = blockIdx.x; u < units1; u += G) {
-        const int ch = static_cast<int>(u % S);
-        const long long row = u / S;
+      for (long long u = blockIdx.x; u < units_l; u += G) {
+        const int kr = static_cast<int>(u % SL);
+        const long long row = u / SL;
         const float* z = p.logits + row * V;
-        const int x0 = ch * C, x1 = min(x0 + C, V);
+        const int x0 = static_cast<int>(static_cast<long long>(kr) * V / SL);
+        const int x1 = static_cast<int>(static_cast<long long>(kr + 1) * V / SL);
         if (threadIdx.x < 32) {
           const float2 ms = warp_row_ms(p.part_ms + row * S, S, c);
           uint32_t prefix = 0;
@@ -991,7 +1003,7 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
             const double target = static_cast<double>(p.top_p) * static_cast<double>(__ldcg(p.tot40 + row));
             const int chosen = warp_select(p.hist + (row * 4 + level - 1) * 256, target, above);
             prefix |= static_cast<uint32_t>(chosen) << (24 - 8 * (level - 1));
-            if (threadIdx.x == 0 && ch == 0) {
+            if (threadIdx.x == 0 && kr == 0) {
               p.sel[(row * 4 + level - 1) * 2] = prefix;
               p.sel[(row * 4 + level - 1) * 2 + 1] = above;
             }
@@ -1011,20 +1023,22 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
           unsigned long long mass = 0;
           // this warp's histogram: same-bucket atomics contend within the warp only
           unsigned long long* wh = s.hist[threadIdx.x >> 5];
-          float zv[kAPer];
+          for (int xs = x0; xs < x1; xs += kAPer * kAT) {
+            float zv[kAPer];  // this thread's ids of the block, loaded together
 #pragma unroll
-          for (int k = 0; k < kAPer; ++k) {
-            const int x = x0 + threadIdx.x + k * kAT;
-            zv[k] = x < x1 ? __ldcg(z + x) : 0.f;
-          }
+            for (int k = 0; k < kAPer; ++k) {
+              const int x = xs + threadIdx.x + k * kAT;
+              zv[k] = x < x1 ? __ldcg(z + x) : 0.f;
+            }
 #pragma unroll
-          for (int k = 0; k < kAPer; ++k) {
-            if (x0 + threadIdx.x + k * kAT >= x1) break;
-            const float e = exp2f((zv[k] - m) * c);
-            const uint32_t bits = __float_as_uint(e);
-            const unsigned long long fx = static_cast<unsigned long long>(e * kFix40);
-            mass += fx;
-            if ((bits & hi_mask) == prefix) atomicAdd(&wh[(bits >> shift) & 0xFFu], fx);
+            for (int k = 0; k < kAPer; ++k) {
+              if (xs + threadIdx.x + k * kAT >= x1) break;
+              const float e = exp2f((zv[k] - m) * c);
+              const uint32_t bits = __float_as_uint(e);
+              const unsigned long long fx = static_cast<unsigned long long>(e * kFix40);
+              mass += fx;
+              if ((bits & hi_mask) == prefix) atomicAdd(&wh[(bits >> shift) & 0xFFu], fx);
+            }
           }
           if (level == 0) {
             mass = ablock_sum_u64(mass, s);
@@ -1040,17 +1054,19 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
         } else {
           const float tau = __uint_as_float(prefix);
           float kept = 0.f;
-          float zv[kAPer];
+          for (int xs = x0; xs < x1; xs += kAPer * kAT) {
+            float zv[kAPer];
 #pragma unroll
-          for (int k = 0; k < kAPer; ++k) {
-            const int x = x0 + threadIdx.x + k * kAT;
-            zv[k] = x < x1 ? __ldcg(z + x) : 0.f;
-          }
+            for (int k = 0; k < kAPer; ++k) {
+              const int x = xs + threadIdx.x + k * kAT;
+              zv[k] = x < x1 ? __ldcg(z + x) : 0.f;
+            }
 #pragma unroll
-          for (int k = 0; k < kAPer; ++k) {
-            if (x0 + threadIdx.x + k * kAT >= x1) break;
-            const float e = exp2f((zv[k] - m) * c);
-            kept += e >= tau ? e : 0.f;
+            for (int k = 0; k < kAPer; ++k) {
+              if (xs + threadIdx.x + k * kAT >= x1) break;
+              const float e = exp2f((zv[k] - m) * c);
+              kept += e >= tau ? e : 0.f;
+            }
           }
           kept = ablock_sum_f(kept, s);
           if (threadIdx.x == 0) p.part_z[u] = kept;
