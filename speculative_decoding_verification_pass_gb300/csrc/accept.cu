@@ -823,6 +823,16 @@ struct ARow {  // the distribution of one row: e = exp2((z - m) c), kept iff e >
   SPEC_DEVINL float p(int x) const { return p_of(__ldcg(z + x)); }
 };
 
+// This thread's ids xs + threadIdx.x + k kAT (k < kAPer) below x1, loaded
+// together (0 past x1).
+SPEC_DEVINL void load_block(const float* z, int xs, int x1, float (&zv)[kAPer]) {
+#pragma unroll
+  for (int k = 0; k < kAPer; ++k) {
+    const int x = xs + threadIdx.x + k * kAT;
+    zv[k] = x < x1 ? __ldcg(z + x) : 0.f;
+  }
+}
+
 // Id ranges per row of the nucleus select's work units: about one unit per
 // CTA, so that a unit's fixed costs (the row's statistics and the digits
 // chosen so far, read by one warp; block barriers) are paid once per range.
@@ -1023,13 +1033,11 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
           unsigned long long mass = 0;
           // this warp's histogram: same-bucket atomics contend within the warp only
           unsigned long long* wh = s.hist[threadIdx.x >> 5];
+          float zv[kAPer];
+          load_block(z, x0, x1, zv);
           for (int xs = x0; xs < x1; xs += kAPer * kAT) {
-            float zv[kAPer];  // this thread's ids of the block, loaded together
-#pragma unroll
-            for (int k = 0; k < kAPer; ++k) {
-              const int x = xs + threadIdx.x + k * kAT;
-              zv[k] = x < x1 ? __ldcg(z + x) : 0.f;
-            }
+            float zn[kAPer];  // the next block's loads in flight during this one
+            load_block(z, xs + kAPer * kAT, x1, zn);
 #pragma unroll
             for (int k = 0; k < kAPer; ++k) {
               if (xs + threadIdx.x + k * kAT >= x1) break;
@@ -1039,6 +1047,8 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
               mass += fx;
               if ((bits & hi_mask) == prefix) atomicAdd(&wh[(bits >> shift) & 0xFFu], fx);
             }
+#pragma unroll
+            for (int k = 0; k < kAPer; ++k) zv[k] = zn[k];
           }
           if (level == 0) {
             mass = ablock_sum_u64(mass, s);
@@ -1054,19 +1064,19 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
         } else {
           const float tau = __uint_as_float(prefix);
           float kept = 0.f;
+          float zv[kAPer];
+          load_block(z, x0, x1, zv);
           for (int xs = x0; xs < x1; xs += kAPer * kAT) {
-            float zv[kAPer];
-#pragma unroll
-            for (int k = 0; k < kAPer; ++k) {
-              const int x = xs + threadIdx.x + k * kAT;
-              zv[k] = x < x1 ? __ldcg(z + x) : 0.f;
-            }
+            float zn[kAPer];
+            load_block(z, xs + kAPer * kAT, x1, zn);
 #pragma unroll
             for (int k = 0; k < kAPer; ++k) {
               if (xs + threadIdx.x + k * kAT >= x1) break;
               const float e = exp2f((zv[k] - m) * c);
               kept += e >= tau ? e : 0.f;
             }
+#pragma unroll
+            for (int k = 0; k < kAPer; ++k) zv[k] = zn[k];
           }
           kept = ablock_sum_f(kept, s);
           if (threadIdx.x == 0) p.part_z[u] = kept;
