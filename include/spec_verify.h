@@ -496,6 +496,19 @@ int spec_gamma_optimal(double alpha, int gamma_min, int gamma_max, double draft_
  * SPEC_ETIMEOUT if the timeout bit was set, else SPEC_EDEVICE. */
 int spec_device_status(void* d_ws, void* stream, int32_t* out);
 
+/* Self-test of the bounded waits.  One thread of one CTA waits until the
+ * uint32 counter at d_counter (device, 4-byte aligned, caller-owned) is >=
+ * target, with the wait function every grid barrier of the persistent
+ * forward uses, but bounded by limit_ms (0 < limit_ms <= 2000) instead of the
+ * barrier's 2 s.  If the counter does not reach target in time the wait
+ * gives up, sets SPEC_DEV_TIMEOUT in the status word of workspace d_ws (at
+ * least 4 bytes, 4-byte aligned; any workspace of this library) and the
+ * kernel returns: spec_device_status then reports SPEC_ETIMEOUT and the CUDA
+ * context stays usable.  Errors: SPEC_EINVAL for NULL or misaligned pointers,
+ * ws_bytes < 4 or limit_ms outside (0, 2000]; SPEC_ECUDA on a launch error. */
+int spec_wait_selftest(const uint32_t* d_counter, uint32_t target, double limit_ms, void* d_ws,
+                       size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------ diagnostics */
 /* Per-kernel-kind timing for benchmarks.  When enabled on a model, every
  * subsequent forward records CUDA events around each launch of the GEMM,

@@ -104,6 +104,7 @@ _SIGS = {
     "spec_tree_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _F, _P, _P, _P, _P, _SZ, _P]),
     "spec_kv_tree_commit": (_I, [_P, ctypes.POINTER(spec_kv_cache), _P, _P, _I, _P, _P]),
     "spec_device_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    "spec_wait_selftest": (_I, [_P, ctypes.c_uint32, ctypes.c_double, _P, _SZ, _P]),
     "spec_timing_enable": (_I, [_P, _I]),
     "spec_timing_read": (_I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
                               ctypes.POINTER(ctypes.c_double)]),
@@ -420,6 +421,14 @@ def spec_kv_tree_commit(handle: int, kv: "KVCache", path, n_accepted, n_nodes: i
                         stream=None):
     _check(lib().spec_kv_tree_commit(handle, ctypes.byref(kv.c()), _ptr(path), _ptr(n_accepted),
                                      n_nodes, _ptr(ws), _stream(stream)), "spec_kv_tree_commit")
+
+
+def spec_wait_selftest(counter, target: int, limit_ms: float, ws, stream=None) -> None:
+    """One bounded wait (the persistent forward's grid-barrier wait) on the
+    uint32 device counter `counter` until it reaches `target`, giving up after
+    `limit_ms`; a wait that gives up sets the timeout bit in `ws`'s status."""
+    _check(lib().spec_wait_selftest(_ptr(counter), target, limit_ms, _ptr(ws), ws.numel(),
+                                    _stream(stream)), "spec_wait_selftest")
 
 
 def spec_device_status(ws, stream=None) -> tuple[int, int]:

@@ -1187,6 +1187,16 @@ int spec_device_status(void* d_ws, void* stream, int32_t* out) {
   return (v & SPEC_DEV_TIMEOUT) ? SPEC_ETIMEOUT : SPEC_EDEVICE;
 }
 
+int spec_wait_selftest(const uint32_t* d_counter, uint32_t target, double limit_ms, void* d_ws,
+                       size_t ws_bytes, void* stream) {
+  if (!d_counter || !d_ws || ws_bytes < 4 || !(limit_ms > 0.0) || limit_ms > 2000.0) return SPEC_EINVAL;
+  if (reinterpret_cast<uintptr_t>(d_counter) % 4 || reinterpret_cast<uintptr_t>(d_ws) % 4) return SPEC_EINVAL;
+  const auto ns = static_cast<unsigned long long>(limit_ms * 1e6);
+  SPEC_CUDA(launch_wait_probe(d_counter, target, ns, static_cast<int32_t*>(d_ws),
+                              static_cast<cudaStream_t>(stream)));
+  return SPEC_OK;
+}
+
 int spec_timing_enable(spec_model* m, int enable) {
   if (!m) return SPEC_EINVAL;
   m->timing = enable != 0;

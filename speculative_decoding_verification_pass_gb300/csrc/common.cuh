@@ -92,6 +92,26 @@ SPEC_DEVINL unsigned long long globaltimer() {
   return t;
 }
 
+// Wait (one thread) until *ctr >= target, reading it with acquire semantics.
+// Bounded: after limit_ns of wall-clock time it sets *abort and the timeout
+// bit of *status and returns false; it also returns false once *abort is set
+// by another thread.  The persistent forward's grid barrier waits through it.
+SPEC_DEVINL bool wait_count(const unsigned* ctr, unsigned target, volatile int* abort,
+                            int32_t* status, unsigned long long limit_ns = kWaitLimitNs) {
+  if (ld_acquire(ctr) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    if (ld_acquire(ctr) >= target) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *abort = 1;
+      set_status(status, SPEC_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(32);
+  }
+}
+
 // ------------------------------------------------------- dependent launches
 // Wait until the previous kernel in the stream has completed and its writes
 // are visible (no-op when the launch had no programmatic dependency).

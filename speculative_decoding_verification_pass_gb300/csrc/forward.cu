@@ -194,18 +194,7 @@ SPEC_DEVINL void fence_proxy_async() { asm volatile("fence.proxy.async.global;" 
 // Wait (one thread) until `target` arrivals; bounded.
 SPEC_DEVINL bool grid_wait(const unsigned* bar, unsigned target, volatile int* abort,
                            int32_t* status) {
-  if (ld_acquire(bar) >= target) return true;
-  const unsigned long long t0 = globaltimer();
-  for (;;) {
-    if (ld_acquire(bar) >= target) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      set_status(status, SPEC_DEV_TIMEOUT);
-      return false;
-    }
-    __nanosleep(32);
-  }
+  return wait_count(bar, target, abort, status);
 }
 
 struct MkSmem {

@@ -170,6 +170,8 @@ cudaError_t launch_init_weights(uint16_t* dst, long long rows, long long cols, i
                                 cudaStream_t stream);
 cudaError_t launch_fill_f32(float* dst, long long n, float v, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* dst, int hd, double theta, cudaStream_t stream);
+cudaError_t launch_wait_probe(const unsigned* ctr, unsigned target, unsigned long long limit_ns,
+                              int32_t* status, cudaStream_t stream);
 
 // ------------------------------------------------------------------ accept
 constexpr int kAcceptMaxChunk = 4096;  // vocabulary ids per accept work unit

@@ -168,7 +168,25 @@ __global__ void rope_table_kernel(float2* dst, int hd, double theta) {
   dst[i] = make_float2(hi, static_cast<float>(f - static_cast<double>(hi)));
 }
 
+// One bounded wait of the persistent forward's grid barrier on a caller's
+// counter: the self-test of the timeout path (a counter that nothing
+// advances ends the wait with the timeout bit set, and the kernel returns).
+__global__ void wait_probe_kernel(const unsigned* ctr, unsigned target, unsigned long long limit_ns,
+                                  int32_t* status) {
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    abort = 0;
+    wait_count(ctr, target, &abort, status, limit_ns);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(const unsigned* ctr, unsigned target, unsigned long long limit_ns,
+                              int32_t* status, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(ctr, target, limit_ns, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_embed(const EmbedParams& p, cudaStream_t stream, bool pdl) {
   const int M = p.B * p.n;

@@ -83,6 +83,13 @@ def test_argument_validation_without_gpu(lib):
     cfg = lib.LLAMA_1B.c()
     assert L.spec_model_create(ctypes.byref(cfg), 1, None, 0, None, ctypes.byref(out)) == lib.SPEC_EINVAL
     assert L.spec_model_destroy(None) == lib.SPEC_OK
+    # the bounded-wait self-test: a limit outside (0, 2000] ms, a NULL or
+    # misaligned pointer, or a workspace below one status word
+    assert L.spec_wait_selftest(fake, 1, 0.0, fake, 256, None) == lib.SPEC_EINVAL
+    assert L.spec_wait_selftest(fake, 1, 2500.0, fake, 256, None) == lib.SPEC_EINVAL
+    assert L.spec_wait_selftest(None, 1, 50.0, fake, 256, None) == lib.SPEC_EINVAL
+    assert L.spec_wait_selftest(P(4098), 1, 50.0, fake, 256, None) == lib.SPEC_EINVAL
+    assert L.spec_wait_selftest(fake, 1, 50.0, fake, 2, None) == lib.SPEC_EINVAL
 
 
 def test_product_path_never_imports_the_oracle():

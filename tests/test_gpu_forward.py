@@ -305,3 +305,40 @@ def test_graph_replays_recompute_every_pass():
     for ws in (ws_g, ws_e):
         stt, bits = sb.spec_device_status(ws)
         assert stt == sb.SPEC_OK, hex(bits)
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """The persistent forward's grid-barrier wait on a counter that nothing
+    advances: it gives up after its limit, sets the timeout bit, the kernel
+    returns, and afterwards a verify pass gives the same logits as before."""
+    import time
+    cfg = SMALL[1]
+    B, cap, n = 1, 64, 5
+    m = sb.Model(cfg, 21)
+    ws = sb.workspace(sb.spec_workspace_bytes(cfg, B, n - 1, cap))
+    toks = torch.from_numpy(wl.tokens(31, B, n, cfg.vocab).astype(np.int32)).cuda()
+
+    def verify():
+        kv = sb.KVCache(cfg, B, cap)
+        kv.len.fill_(7)
+        out = torch.empty(B, n, cfg.vocab, device="cuda")
+        sb.spec_verify_forward(m.handle, toks, B, n - 1, kv, out, ws)
+        assert sb.spec_device_status(ws) == (sb.SPEC_OK, 0)
+        return out
+
+    before = verify()
+    ctr = torch.full((1,), 3, dtype=torch.int32, device="cuda")
+    sb.spec_wait_selftest(ctr, 3, 50.0, ws)            # already reached: no timeout
+    assert sb.spec_device_status(ws) == (sb.SPEC_OK, 0)
+    ctr.zero_()                                        # nothing advances it
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    sb.spec_wait_selftest(ctr, 1, 50.0, ws)
+    st, bits = sb.spec_device_status(ws)
+    waited = time.perf_counter() - t0
+    assert st == sb.SPEC_ETIMEOUT and bits == sb.DEV_TIMEOUT, (st, hex(bits))
+    assert waited >= 0.045, waited
+    assert sb.spec_device_status(ws) == (sb.SPEC_OK, 0)   # read and cleared
+    assert torch.equal(verify(), before)
+    with pytest.raises(sb.SpecError):
+        sb.spec_wait_selftest(ctr, 1, 0.0, ws)
