@@ -664,6 +664,22 @@ def parse():
     return ap.parse_args()
 
 
+def job_seconds(t_local: float, world: int, device) -> float:
+    """The job's time for the timed region: the maximum over the ranks (each
+    rank's replica runs the same steps; the slowest one ends the job)."""
+    if world == 1:
+        return t_local
+    import torch.distributed as dist
+    tt = torch.tensor([t_local], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt)
+
+
+def job_value(step_bytes: float, steps: int, world: int, seconds: float) -> float:
+    """Whole-job algorithmic GB/s: the bytes all replicas moved over the job's time."""
+    return step_bytes * steps * world / seconds / 1e9
+
+
 def main():
     args = parse()
     if args.warmup < 3:
@@ -717,14 +733,9 @@ def main():
         times = time_steps(w, args.steps)
     w.check_status()
     emitted, accepted = w.emitted, w.accepted
-    t_total = sum(times) / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t_total], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_total = float(tt)
+    t_total = job_seconds(sum(times) / 1e3, world, "cuda")
     step_bytes = w.bytes_per_step()
-    value = step_bytes * args.steps * world / t_total / 1e9
+    value = job_value(step_bytes, args.steps, world, t_total)
     try:
         gt = time_graph(w, max(3, args.steps // 2))
         w.check_status()
