@@ -144,3 +144,14 @@ def test_tree_masks_match_the_oracle(lib):
     assert L.spec_kv_tree_commit(None, None, None, None, 4, None, None) == lib.SPEC_EINVAL
     assert L.spec_verify_forward_tree(None, None, None, None, 1, 4, None, None, None, 0,
                                       None) == lib.SPEC_EINVAL
+
+
+def test_missing_library_fails_loudly(lib, monkeypatch, tmp_path):
+    """Without the built library the binding raises: there is no fallback."""
+    from speculative_decoding_verification_pass_gb300 import _build
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "libspec_missing.so"))
+    monkeypatch.setattr(lib, "_LIB", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        lib.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        lib.spec_workspace_bytes(lib.LLAMA_8B, 1, 4, 4096)
