@@ -18,7 +18,7 @@ Sources (page title, section):
   correction, n_accepted) and the numerical fallback to p when the residual
   mass is below 1e-8.
 
-Readings where the pages leave a step open (each is listed in the design doc):
+Readings where the pages leave a step open:
 
 * Uniforms are inputs: u[i] (i < gamma) is the coin of the i-th ratio test and
   u[gamma] drives the single residual or bonus draw.

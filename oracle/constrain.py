@@ -13,7 +13,7 @@ Source (page title, section):
   lockstep for both models); a mask applied on one side only, or in a
   different automaton state, makes the acceptance ratios wrong.
 
-Readings where the page leaves a step open (each is listed in the design doc):
+Readings where the page leaves a step open:
 
 * A mask is one allowed-token set per logits row; the target row i and the
   draft row it is paired with carry the same set (the caller's automaton

@@ -20,7 +20,7 @@ LLM Latency by 3x":
 * *The Accept/Reject Mechanism* (the result record): a pass that accepts
   n of its gamma drafts records n accepted and gamma - n rejected.
 
-Readings where the page leaves a step open (each is listed in the design doc):
+Readings where the page leaves a step open:
 
 * alpha over the window = (sum of accepted) / (sum of accepted + rejected),
   i.e. accepted drafts over drafted tokens (the page's estimator).

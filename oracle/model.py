@@ -16,7 +16,7 @@ What the pages fix:
   *KV Cache Management for Dual Models* and *Rollback Protocol*).
 
 The decoder itself is the "Llama-style" model the workloads name; the pages
-say nothing of its layers, so these readings are used (listed in the design doc):
+say nothing of its layers, so these readings are used:
 RMSNorm with eps 1e-5 and unit gains; rotate-half RoPE over pairs
 (i, i + hd/2) with frequency theta^(-2i/hd), theta = 500000, positions from 0;
 grouped-query attention with group n_heads / n_kv_heads and scale

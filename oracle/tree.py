@@ -24,7 +24,7 @@ Sources (page title, section):
 * "Speculative Decoding: How to Make an LLM 3x Faster..." (kishorek): verify
   the whole tree in one pass and accept the longest valid root-to-node path.
 
-Readings where the pages leave a step open (each is listed in the design doc):
+Readings where the pages leave a step open:
 
 * Node 0 is the root: the previous pass's emitted token t_last, not yet in
   the cache, at position L_b (depth 0).  Node i > 0 has a parent p(i) < i, so
