@@ -155,3 +155,23 @@ def test_missing_library_fails_loudly(lib, monkeypatch, tmp_path):
         lib.lib()
     with pytest.raises(RuntimeError, match="not built"):
         lib.spec_workspace_bytes(lib.LLAMA_8B, 1, 4, 4096)
+
+
+def test_header_and_library_from_plain_c(lib, tmp_path):
+    """include/spec_verify.h compiles as C99 (no C++), the library links from
+    C, and the host-only calls behave as documented (tests/c/abi_from_c.c)."""
+    import shutil
+    import subprocess
+    from speculative_decoding_verification_pass_gb300 import _build
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    so = _build.LIB
+    exe = str(tmp_path / "abi_from_c")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c", "abi_from_c.c"),
+                        so, "-Wl,-rpath," + os.path.dirname(so), "-o", exe],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
