@@ -125,3 +125,37 @@ def test_outcome_is_a_function_of_the_uniforms():
 
     assert run(5) == run(5)
     assert run(5) != run(6)
+
+
+def _tree_first_tokens(trials, seed):
+    from oracle import tree as Tr
+    rng = np.random.default_rng(seed)
+    V = 6
+    parents = [-1, 0, 0, 0, 1, 1, 2, 2, 3, 3]
+    n = len(parents)
+    P = rng.dirichlet(np.ones(V), size=n)
+    Q = np.clip(P + rng.normal(0, 0.12, size=(n, V)), 0.02, None)
+    Q /= Q.sum(1, keepdims=True)
+    z = np.log(P)
+    first = np.zeros(V)
+    for _ in range(trials):
+        toks = [0] * n
+        for c in range(1, n):
+            toks[c] = int(rng.choice(V, p=Q[parents[c]]))
+        first[Tr.tree_accept(z, Q, toks, parents, rng.random(n), 1.0).tokens[0]] += 1
+    return first, P[0]
+
+
+def test_tree_siblings_without_the_carried_residual_is_caught(monkeypatch):
+    """Aci, *Tree-Based Drafting* (the per-node test): after a rejected child
+    the next sibling is tested against norm(max(0, p' - q)), not against p.
+    Planted by raising the tree oracle's residual-fallback threshold above any
+    mass, so p' never changes: the root's first emitted token no longer
+    follows p and the chi-square pin fails."""
+    from oracle import tree as Tr
+    trials = 20_000
+    first, p0 = _tree_first_tokens(trials, seed=21)
+    assert stats.chisquare(first, p0 * trials).pvalue > 1e-3
+    monkeypatch.setattr(Tr, "RESIDUAL_FALLBACK", np.inf)
+    first, p0 = _tree_first_tokens(trials, seed=21)
+    assert stats.chisquare(first, p0 * trials).pvalue < 1e-9
