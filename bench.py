@@ -48,7 +48,7 @@ TRAFFIC = {
     # algorithmic bytes (weights, KV and logits each move once)
     "forward_kernel": {"files": ["forward.cu", "gemm_common.cuh", "attn_common.cuh", "common.cuh",
                                  "internal.h"],
-                       "source_sha1": "d0ff7f7edf0736417f9171af5f0684ed720e2c44",
+                       "source_sha1": "0498182cf4892512931c22315edd222c5792a713",
                        "bytes_per_launch": 15347362447},
 }
 

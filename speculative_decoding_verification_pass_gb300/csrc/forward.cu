@@ -247,8 +247,9 @@ SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
 // barrier has passed: it streams at most S - kPreFree tiles of the phase
 // ahead.  A full ring of early tiles (the refill of every CTA at once) slows
 // the stream-K exchange and barrier round trips that end the phase before;
-// two free stages measured best at 8 stages (3.49 ms a pass against 3.58 for
-// none, 3.52 for three, 3.81 for all eight).
+// with 8 stages, two free measured best (3.54 ms a pass against 3.57 with
+// none free and 3.81 with all eight free on one GB300; on another, three
+// free ran 0.03 ms slower than two and one free the same as two).
 constexpr int kPreFree = 2;
 
 // The weight producer waits (bounded) until the activation producer has
