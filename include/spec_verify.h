@@ -202,13 +202,18 @@ int spec_lm_head(const spec_model* model, const uint16_t* d_hidden, int rows, fl
  *             SPEC_ESIZE); a model vocabulary above 262144 gives SPEC_ESIZE.
  *   d_logits  fp32 [rows][vocab].
  * It allocates and frees nothing.  The first call on a device looks up the
- * array's device address on that device (the current device at the call);
- * make that first call before any stream capture.  All calls share the one
+ * array's device address on that device (the current device at the call)
+ * and keeps it for the life of the process; make that first call before any
+ * stream capture.  cudaDeviceReset() unloads the array with the rest of the
+ * context, so after a reset of a device this entry point must not be called
+ * on that device again in the same process (the kept address is stale).  All calls share the one
  * array and leave their contents in it: calls whose work overlaps on the GPU
  * (two streams, two host threads) race and produce wrong logits -- serialise
  * them.  The tile counters are cleared on `stream` at the start of every
  * call.  A device-side bounded-wait timeout is recorded in the library's own
- * scratch, not in a caller workspace, and is not reported. */
+ * scratch, not in a caller workspace, and is not reported: a caller of this
+ * entry point has no way to learn that a call timed out (spec_lm_head, with
+ * a workspace, reports it through spec_device_status). */
 int spec_lm_head_noalloc(const spec_model* model, const uint16_t* d_hidden, int rows,
                          float* d_logits, void* stream);
 

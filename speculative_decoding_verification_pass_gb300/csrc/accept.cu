@@ -1614,32 +1614,45 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, cudaS
 }  // namespace
 
 // The per-sequence kernels take kHistBytes of dynamic shared memory (above
-// the 48 KB default): set once per process.
+// the 48 KB default): set once per device.
 cudaError_t per_seq_smem_attrs() {
-  static cudaError_t e = [] {
-    const void* fns[3] = {reinterpret_cast<const void*>(accept_seq_kernel),
-                          reinterpret_cast<const void*>(sample_kernel),
-                          reinterpret_cast<const void*>(tree_accept_kernel)};
-    for (const void* f : fns) {
-      const cudaError_t r = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(kHistBytes));
-      if (r != cudaSuccess) return r;
-    }
-    return cudaSuccess;
-  }();
+  static PerDevice<cudaError_t> done;
+  cudaError_t e = cudaErrorInvalidDevice;
+  if (!done.get(
+          [] {
+            const void* fns[3] = {reinterpret_cast<const void*>(accept_seq_kernel),
+                                  reinterpret_cast<const void*>(sample_kernel),
+                                  reinterpret_cast<const void*>(tree_accept_kernel)};
+            for (const void* f : fns) {
+              const cudaError_t r = cudaFuncSetAttribute(
+                  f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kHistBytes));
+              if (r != cudaSuccess) return r;
+            }
+            return cudaSuccess;
+          },
+          &e))
+    return cudaErrorInvalidDevice;
   return e;
 }
 
+// CTAs of the cooperative accept grid the current device keeps resident.
 int accept_grid_capacity() {
-  static int cap = [] {
-    int dev = 0, sms = 0, per = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, accept_grid_kernel, kAT, 0) != cudaSuccess)
-      return 0;
-    return sms * per;
-  }();
-  return cap;
+  static PerDevice<int> cap;
+  int v = 0;
+  if (!cap.get(
+          [] {
+            int dev = 0, sms = 0, per = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+              return 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, accept_grid_kernel, kAT, 0) !=
+                cudaSuccess)
+              return 0;
+            return sms * per;
+          },
+          &v))
+    return 0;
+  return v;
 }
 
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream) {

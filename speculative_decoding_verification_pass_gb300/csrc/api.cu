@@ -992,12 +992,18 @@ AcceptWs plan_accept(int B, int gamma, int V) {
 }
 
 int device_sm_count() {
-  static int v = [] {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-  }();
+  static PerDevice<int> sms;
+  int v = 0;
+  if (!sms.get(
+          [] {
+            int dev = 0, n = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+            if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+              return 0;
+            return n;
+          },
+          &v))
+    return 0;
   return v;
 }
 

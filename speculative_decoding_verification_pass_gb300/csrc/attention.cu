@@ -638,20 +638,27 @@ __global__ void __launch_bounds__(kClusterThreads)
   cluster_sync();  // peers' shared memory stays alive until every rank has read it
 }
 
+// Dynamic shared memory up to the per-CTA maximum and clusters above the
+// portable size, set once per device.
+constexpr int kMaxDynSmem = 227 * 1024;
+
 template <int HD>
 cudaError_t configure_cluster(size_t smem) {
-  static int configured_smem = 0;
-  if (static_cast<int>(smem) > configured_smem) {
-    cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<HD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_cluster_kernel<HD>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    configured_smem = static_cast<int>(smem);
-  }
-  return cudaSuccess;
+  if (smem > static_cast<size_t>(kMaxDynSmem)) return cudaErrorInvalidValue;
+  static PerDevice<cudaError_t> done;
+  cudaError_t e = cudaErrorInvalidDevice;
+  if (!done.get(
+          [] {
+            cudaError_t r = cudaFuncSetAttribute(attn_cluster_kernel<HD>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kMaxDynSmem);
+            if (r != cudaSuccess) return r;
+            return cudaFuncSetAttribute(attn_cluster_kernel<HD>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+          },
+          &e))
+    return cudaErrorInvalidDevice;
+  return e;
 }
 
 // Can clusters of `cs` CTAs with this much shared memory be placed at all?
@@ -699,15 +706,14 @@ cudaError_t launch_cluster(const AttnParams& p, cudaStream_t stream, bool pdl) {
 
 template <int HD>
 cudaError_t launch_hd(const AttnParams& p, cudaStream_t stream, bool pdl) {
-  static bool configured = false;
+  static PerDevice<cudaError_t> configured;
   const size_t smem = AttnSmem<HD>::kBytes;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_splitkv_kernel<HD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t ce = cudaErrorInvalidDevice;
+  if (!configured.get([smem] { return cudaFuncSetAttribute(attn_splitkv_kernel<HD>,
+                                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                           static_cast<int>(smem)); },
+                      &ce) || ce != cudaSuccess)
+    return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, p.Hkv, p.B);
   cfg.blockDim = dim3(kThreads);
@@ -724,9 +730,21 @@ cudaError_t launch_hd(const AttnParams& p, cudaStream_t stream, bool pdl) {
 }  // namespace
 
 int attention_cluster_size(int hd, int cap, size_t smem_limit) {
-  static int cache_key[3] = {-1, -1, -1}, cache_val = 0;
-  if (cache_key[0] == hd && cache_key[1] == cap && cache_key[2] == static_cast<int>(smem_limit))
-    return cache_val;
+  // the last answer per device, keyed by the arguments
+  struct Entry {
+    int hd = -1, cap = -1;
+    size_t lim = 0;
+    int val = 0;
+  };
+  static std::mutex mu;
+  static Entry cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const Entry& c = cache[dev];
+    if (c.hd == hd && c.cap == cap && c.lim == smem_limit) return c.val;
+  }
   int best = 0;
   int cs = (cap + 127) / 128;
   cs = cs < 1 ? 1 : (cs > 16 ? 16 : cs);
@@ -737,10 +755,8 @@ int attention_cluster_size(int hd, int cap, size_t smem_limit) {
     const bool ok = hd == 128 ? cluster_fits<128>(cs, smem) : cluster_fits<64>(cs, smem);
     if (ok) best = cs;
   }
-  cache_key[0] = hd;
-  cache_key[1] = cap;
-  cache_key[2] = static_cast<int>(smem_limit);
-  cache_val = best;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[dev] = Entry{hd, cap, smem_limit, best};
   return best;
 }
 

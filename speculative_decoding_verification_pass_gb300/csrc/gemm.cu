@@ -305,13 +305,13 @@ int gemm_max_stages(int rows_b, size_t budget, int ksub) {
 cudaError_t launch_gemm(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmXlo,
                         const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
   const size_t smem = gemm_smem_bytes(p.split ? 2 * p.ntok : p.ntok, p.stages, p.ksub);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDevice<cudaError_t> configured;
+  cudaError_t ce = cudaErrorInvalidDevice;
+  if (!configured.get([] { return cudaFuncSetAttribute(gemm_tc_kernel,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       227 * 1024); },
+                      &ce) || ce != cudaSuccess)
+    return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

@@ -261,14 +261,17 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
       float out = v[j];
       const int pos = posv[j];
       if (rot) {
-        // angle = pos * freq with the product kept to ~fp64 accuracy:
-        // freq = hi + lo, pos*hi = a + err exactly (fma), angle ~ a + (err + pos*lo)
+        // rotation in turns = pos * (hi + lo): pos * hi = t + terr exactly
+        // (fma), whole turns are removed exactly (t - rint(t) is representable),
+        // and sin / cos of 2 pi * frac come from sincospif on [-1, 1], so the
+        // angle keeps ~1e-7 rad absolute accuracy at any cached position
+        // (fast-math does not replace sincospif)
         const float fp = static_cast<float>(pos);
-        const float a = fp * fr.x;
-        const float err = fmaf(fp, fr.x, -a) + fp * fr.y;
-        float s, c;
-        sincosf(a, &s, &c);
-        const float sn = s + err * c, cs = c - err * s;
+        const float t = fp * fr.x;
+        const float terr = fmaf(fp, fr.x, -t) + fp * fr.y;
+        const float frac = (t - rintf(t)) + terr;
+        float sn, cs;
+        sincospif(2.0f * frac, &sn, &cs);
         const float partner = sm.xbuf[j * kTileN + pr];
         out = dim < half ? v[j] * cs - partner * sn : v[j] * cs + partner * sn;
       }

@@ -7,9 +7,34 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "spec_verify.h"
 
 namespace spec {
+
+// One value per device, made once per device by the first call with that
+// device current.  CUDA keeps function attributes (e.g. the dynamic shared
+// memory limit) and occupancy per device, so a process that drives several
+// GPUs needs every such set-up on each of them.  Thread-safe.
+constexpr int kMaxDevices = 64;
+template <typename T>
+class PerDevice {
+ public:
+  // false when the current device cannot be read or is out of range
+  template <typename F>
+  bool get(F make, T* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::call_once(once_[dev], [&] { val_[dev] = make(); });
+    *out = val_[dev];
+    return true;
+  }
+
+ private:
+  std::once_flag once_[kMaxDevices];
+  T val_[kMaxDevices] = {};
+};
 
 // ------------------------------------------------------------------ GEMM
 // Y[m][n] = sum_k X[m][k] * W[n][k]; W bf16 [N][K] (TMA map tmW), X bf16

@@ -159,11 +159,14 @@ __global__ void fill_f32_kernel(float* dst, long long n, float v) {
     dst[i] = v;
 }
 
-// freq_i = theta^(-2i/hd) split as hi + lo floats.
+// Rotary frequency of pair i in turns per position, theta^(-2i/hd) / (2 pi),
+// split as hi + lo floats (the QKV epilogue removes whole turns exactly, so
+// the sine is evaluated on a reduced argument at any position).
 __global__ void rope_table_kernel(float2* dst, int hd, double theta) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= hd / 2) return;
-  const double f = pow(theta, -2.0 * i / hd);
+  const double two_pi = 6.283185307179586;
+  const double f = pow(theta, -2.0 * i / hd) / two_pi;
   const float hi = static_cast<float>(f);
   dst[i] = make_float2(hi, static_cast<float>(f - static_cast<double>(hi)));
 }

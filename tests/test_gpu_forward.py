@@ -133,6 +133,54 @@ def test_forward_matches_oracle_ragged_batch(cfg):
     pr.model.close()
 
 
+def _bf16_ulp(x):
+    """Spacing of bf16 values at |x| (8 significant bits)."""
+    a = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+@pytest.mark.parametrize("L0", [4091, 32003])
+def test_rope_cache_rows_at_large_positions(L0):
+    """Keys written at cached positions L0 .. L0+4 (up to 32007 of a
+    32768-slot cache) agree with the oracle's bf16 keys to within one bf16
+    ulp, and all but a small fraction agree exactly: the rotation angle is
+    reduced by whole turns before the sine is taken, so its error stays near
+    1e-7 rad at any position (an unreduced fast sine loses ~|angle| * 2^-22).
+    Layer 0's keys depend only on the token, its position and the weights,
+    so the cache below L0 can stay empty."""
+    cfg = sb.ModelConfig(1, 512, 4, 2, 256, 1000)   # hd 128
+    B, cap, n = 1, 32768, 5
+    m = sb.Model(cfg, 77)
+    kv = sb.KVCache(cfg, B, cap)
+    ws = sb.workspace(sb.spec_workspace_bytes(cfg, B, n - 1, cap))
+    kv.len.fill_(L0)
+    toks = wl.tokens(78 + L0, B, n, cfg.vocab)
+    out = torch.empty(B, n, cfg.vocab, device="cuda")
+    sb.spec_verify_forward(m.handle, torch.from_numpy(toks).cuda(), B, n - 1, kv, out, ws)
+    st, bits = sb.spec_device_status(ws)
+    assert st == sb.SPEC_OK, hex(bits)
+    ocfg = _ocfg(cfg)
+    W = OW.Weights(ocfg, 77)
+    w = W.layer(0)
+    x = OM.rmsnorm(W.embed_rows(toks[0]).astype(np.float64), W.norm_gain(), ocfg.rms_eps)
+    hd = ocfg.head_dim
+    k = (x @ w[OW.WK].astype(np.float64).T).reshape(n, ocfg.n_kv_heads, hd).transpose(1, 0, 2)
+    v = (x @ w[OW.WV].astype(np.float64).T).reshape(n, ocfg.n_kv_heads, hd).transpose(1, 0, 2)
+    pos = L0 + np.arange(n)
+    from oracle.bf16 import round_bf16
+    kref = round_bf16(OM.rope(k, pos, ocfg.rope_theta))
+    vref = round_bf16(v)
+    kd = kv.k[0, 0, :, L0:L0 + n].double().cpu().numpy()
+    vd = kv.v[0, 0, :, L0:L0 + n].double().cpu().numpy()
+    for got, ref in ((kd, kref), (vd, vref)):
+        diff = np.abs(got - ref)
+        assert (diff <= _bf16_ulp(ref) * (1 + 1e-9)).all(), diff.max()
+        frac = float((diff > 0).mean())
+        print("bf16 rows differing by one ulp: %.4f" % frac)
+        assert frac < 0.02, frac
+    m.close()
+
+
 def test_one_pass_equals_sequential_passes_on_device():
     cfg = SMALL[1]
     B, cap, gamma = 2, 200, 4
