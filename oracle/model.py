@@ -128,13 +128,56 @@ class KVState:
             self.V[l][:, :, :L] = V_prefix[l]
         self.lens[:] = lens
 
+    def seq(self, l: int, b: int):
+        """Layer l's keys and values of sequence b, [Hkv][cap][hd] (views)."""
+        return self.K[l][b], self.V[l][b]
 
-def forward(cfg: Config, W: "wts.Weights", tokens, kv: KVState,
+    def keep(self, l: int, b: int, K, V, start: int, n: int) -> None:
+        """Slots start..start+n-1 were written into the views: nothing to do."""
+
+
+class PrefixKV:
+    """A cache for long batched contexts whose full fp64 copy would not fit
+    in host memory.  The cached prefix of each (layer, sequence) is not
+    stored: ``prefix(l, b)`` returns it, [Hkv][lens[b]][hd] fp64, whenever
+    a pass needs it; only the slots that passes write after the prefix
+    (at most ``extra`` per sequence) are kept.  The same cache contents as a
+    KVState loaded with the same prefix, in another storage."""
+
+    def __init__(self, lens, prefix, extra: int = 64):
+        self.base = np.array(lens, dtype=np.int64)
+        self.lens = self.base.copy()
+        self.capacity = self.base + extra
+        self.prefix = prefix
+        self.extra = extra
+        self.new = {}
+
+    def seq(self, l: int, b: int):
+        K0, V0 = self.prefix(l, b)
+        Hkv, L, hd = K0.shape
+        if L != self.base[b]:
+            raise ValueError("prefix length differs from the cached length")
+        K = np.zeros((Hkv, L + self.extra, hd))
+        V = np.zeros_like(K)
+        K[:, :L], V[:, :L] = K0, V0
+        if (l, b) in self.new:
+            K[:, L:], V[:, L:] = self.new[(l, b)]
+        return K, V
+
+    def keep(self, l: int, b: int, K, V, start: int, n: int) -> None:
+        L = int(self.base[b])
+        if start < L:
+            raise ValueError("a pass may not rewrite the stored prefix")
+        self.new[(l, b)] = (K[:, L:].copy(), V[:, L:].copy())
+
+
+def forward(cfg: Config, W: "wts.Weights", tokens, kv,
             round_kv: bool = True) -> np.ndarray:
     """One verification pass: tokens [B][n] -> logits [B][n][V] (fp64).
 
     Writes keys/values of the n new positions at slots len_b .. len_b+n-1 and
-    advances len_b by n (the rollback afterwards is ``truncate``)."""
+    advances len_b by n (the rollback afterwards is ``truncate``).  ``kv`` is
+    a KVState or a PrefixKV."""
     toks = np.asarray(tokens, dtype=np.int64)
     B, n = toks.shape
     d, H, Hkv, hd = cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
@@ -157,9 +200,11 @@ def forward(cfg: Config, W: "wts.Weights", tokens, kv: KVState,
             pos = L0[b] + np.arange(n)
             qb = rope(q[b].transpose(1, 0, 2), pos, cfg.rope_theta).transpose(1, 0, 2)
             kb = rope(k[b].transpose(1, 0, 2), pos, cfg.rope_theta)       # [Hkv][n][hd]
-            kv.K[l][b, :, pos[0]:pos[0] + n] = store(kb)
-            kv.V[l][b, :, pos[0]:pos[0] + n] = store(v[b].transpose(1, 0, 2))
-            o[b] = attention(qb, kv.K[l][b], kv.V[l][b], pos)
+            Kb, Vb = kv.seq(l, b)
+            Kb[:, pos[0]:pos[0] + n] = store(kb)
+            Vb[:, pos[0]:pos[0] + n] = store(v[b].transpose(1, 0, 2))
+            kv.keep(l, b, Kb, Vb, int(pos[0]), n)
+            o[b] = attention(qb, Kb, Vb, pos)
         h = h + o.reshape(B, n, H * hd) @ w[wts.WO].astype(np.float64).T
         x = rmsnorm(h, g, cfg.rms_eps)
         h = h + swiglu(x, w[wts.WG], w[wts.WU], w[wts.WD])

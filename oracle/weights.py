@@ -130,20 +130,36 @@ def layer_shapes(cfg):
     }
 
 
-class Weights:
-    """Lazily generated weights of one seeded model (fp32 holding bf16)."""
+def _bits(a) -> np.ndarray:
+    """uint16 bit patterns of fp32 arrays holding bf16-exact values."""
+    return (np.ascontiguousarray(a, dtype=np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
 
-    def __init__(self, cfg, seed: int, cache_layers: bool = True):
+
+def _unbits(b) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+class Weights:
+    """Lazily generated weights of one seeded model (fp32 holding bf16).
+
+    cache_layers: True keeps generated layers as fp32, "bf16" keeps them as
+    bf16 bit patterns (half the memory; the values are bf16 already), False
+    regenerates a layer whenever it is asked for."""
+
+    def __init__(self, cfg, seed: int, cache_layers=True):
         self.cfg, self.seed, self.cache = cfg, seed, cache_layers
         self._layers = {}
         self._head = None
 
     def layer(self, l: int) -> dict:
         if l in self._layers:
-            return self._layers[l]
+            w = self._layers[l]
+            return {k: _unbits(v) for k, v in w.items()} if self.cache == "bf16" else w
         w = {k: tensor(self.seed, tensor_id(l, k), *shape)
              for k, shape in layer_shapes(self.cfg).items()}
-        if self.cache:
+        if self.cache == "bf16":
+            self._layers[l] = {k: _bits(v) for k, v in w.items()}
+        elif self.cache:
             self._layers[l] = w
         return w
 

@@ -14,6 +14,8 @@ Recipes (numbers are the workloads' own):
 * ``tokens``: token ids uniform over the vocabulary.
 * ``kv_prefix``: cache contents ~ N(0, 1) rounded to bf16 (bit patterns).
 * ``context_lengths``: per-sequence lengths uniform in [lo, hi].
+* ``kv_pool`` / ``kv_pool_index``: cache rows ~ N(0, 1) in bf16 drawn from a
+  seeded pool, for contexts too long to draw row by row.
 * ``gauss``: plain N(0, sigma^2) fp32 noise.
 """
 from __future__ import annotations
@@ -76,6 +78,24 @@ def kv_prefix(seed: int, n_layers: int, batch: int, n_kv_heads: int,
     K = f32_to_bf16_bits(g.standard_normal(shape, dtype=np.float32))
     V = f32_to_bf16_bits(g.standard_normal(shape, dtype=np.float32))
     return K, V
+
+
+def kv_pool(seed: int, rows: int, head_dim: int, stream: int = 15):
+    """(K, V) pools of cache rows: bf16 bit patterns [rows][hd] ~ N(0, 1).
+    Long batched contexts take their cached rows from these pools (see
+    kv_pool_index) instead of drawing every row: the contents keep the same
+    distribution, and each side can rebuild any (layer, sequence) slice."""
+    g = rng(seed, stream)
+    K = f32_to_bf16_bits(g.standard_normal((rows, head_dim), dtype=np.float32))
+    V = f32_to_bf16_bits(g.standard_normal((rows, head_dim), dtype=np.float32))
+    return K, V
+
+
+def kv_pool_index(seed: int, layer: int, seq: int, n_kv_heads: int, length: int,
+                  pool_rows: int, stream: int = 16) -> np.ndarray:
+    """Pool rows of the cached keys and values of one (layer, sequence):
+    int64 [2][Hkv][length], [0] for K and [1] for V, uniform over the pool."""
+    return rng(seed, stream, layer, seq).integers(0, pool_rows, size=(2, n_kv_heads, length))
 
 
 def context_lengths(seed: int, batch: int, lo: int, hi: int, stream: int = 7) -> np.ndarray:

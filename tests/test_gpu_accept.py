@@ -5,7 +5,8 @@ draft tokens, uniforms); the draft side (q and x) is produced by the oracle.
 Emitted tokens and n_accepted must match exactly except where the oracle
 flags a decision within its fp32/fp64 margin (|u - min(1,p/q)| < 1e-4, an
 inverse-CDF point within 1e-5 of u*S, a nucleus threshold within 1e-5);
-such excused disagreements are counted and must stay below 0.1%.  Probabilities from
+such excused disagreements are counted and must stay below 0.1% of the
+cases, which allows none below 1000 cases (tests/parity.py).  Probabilities from
 spec_draft_sample must match the oracle within relative error 1e-5.
 """
 import numpy as np
@@ -13,6 +14,7 @@ import pytest
 import torch
 from scipy import stats
 
+import parity
 from oracle import accept as OA
 from speculative_decoding_verification_pass_gb300 import binding as sb
 from speculative_decoding_verification_pass_gb300 import workloads as wl
@@ -90,7 +92,7 @@ def test_accept_matches_oracle(B, gamma, V, T, top_p):
         x = np.where(agree, zp[:, :gamma].argmax(-1), x).astype(np.int32)
     out, nacc = _run_accept(zp, q, x, u, T, top_p)
     excused, near = _compare(zp, q, x, u, T, top_p, out, nacc)
-    assert excused <= 0.001 * B, (excused, near)
+    parity.check(f"accept B={B} gamma={gamma} V={V} T={T} top_p={top_p}", B, near, excused)
     if T > 0 and gamma > 0:
         assert (nacc > 0).any()
 
@@ -125,8 +127,10 @@ def test_draft_sample_probs_and_tokens(R, V, T, top_p):
     rel = np.abs(P[mask] - qs[mask]) / qs[mask]
     assert rel.max() <= 1e-5, rel.max()
     assert (P[~mask] <= 1e-30).all()
-    ok = (t == ts) | bnd
-    assert ok.all(), np.flatnonzero(~ok)
+    differ = t != ts
+    assert (bnd[differ]).all(), np.flatnonzero(differ & ~bnd)
+    parity.check(f"draft sample R={R} V={V} T={T} top_p={top_p}", R, int(bnd.sum()),
+                 int(differ.sum()))
 
 
 def test_worked_example_on_device():
@@ -176,8 +180,8 @@ def test_chi_square_v8_million_trials():
 def test_accept_grid_and_per_sequence_schedules_agree(T, top_p, monkeypatch):
     """The cooperative grid (batches up to 1024 rows) and the per-sequence
     kernel take the same decisions and draws: each matches the oracle under
-    the boundary rule, and they differ on at most 0.1% of the sequences
-    (only where fp32 summation order crosses a boundary)."""
+    the boundary rule with no excused disagreement (96 sequences: the 0.1%
+    bar allows none), so the two schedules agree on every sequence."""
     B, gamma, V = 96, 4, 32000
     seed = 77 + int(10 * T) + int(100 * top_p)
     zq, zp = wl.accept_logits(seed, B, gamma, V)
@@ -192,9 +196,9 @@ def test_accept_grid_and_per_sequence_schedules_agree(T, top_p, monkeypatch):
         monkeypatch.setenv("SPEC_ACCEPT_GRID", mode)
         res[mode] = _run_accept(zp, q, x, u, T, top_p)
         excused, near = _compare(zp, q, x, u, T, top_p, *res[mode])
-        assert excused <= max(1, 0.001 * B), (mode, excused, near)
+        parity.check(f"accept schedule grid={mode} T={T} top_p={top_p}", B, near, excused)
     diff = (res["1"][0] != res["0"][0]).any(1) | (res["1"][1] != res["0"][1])
-    assert diff.sum() <= max(1, 0.001 * B), np.nonzero(diff)
+    assert diff.sum() == 0, np.nonzero(diff)
 
 
 @pytest.mark.parametrize("top_p", [1.0, 0.9])
@@ -202,7 +206,7 @@ def test_accept_llama3_vocabulary_batch_one(top_p):
     """The verify step's own shape: one sequence, gamma 4, V = 128256 (the
     grid schedule spreads each row over the SMs), 40 independent steps."""
     gamma, V, steps = 4, 128256, 40
-    excused = 0
+    excused = near = 0
     for k in range(steps):
         seed = 5000 + k
         zq, zp = wl.accept_logits(seed, 1, gamma, V)
@@ -210,6 +214,7 @@ def test_accept_llama3_vocabulary_batch_one(top_p):
         u = wl.uniforms(seed, 1, gamma + 1)
         q, x = _draft(zq[:, :gamma], ud, 1.0, top_p)
         out, nacc = _run_accept(zp, q, x, u, 1.0, top_p)
-        e, _ = _compare(zp, q, x, u, 1.0, top_p, out, nacc)
+        e, nr = _compare(zp, q, x, u, 1.0, top_p, out, nacc)
         excused += e
-    assert excused <= 1, excused
+        near += nr
+    parity.check(f"accept B=1 gamma=4 V=128256 top_p={top_p}", steps, near, excused)

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import parity
 from oracle import accept as OA
 from oracle import constrain as OC
 from oracle import tree as Tr
@@ -109,10 +110,11 @@ def test_masked_accept_matches_oracle(B, gamma, V, T, top_p, frac, grid, monkeyp
     st, bits = sb.spec_device_status(ws)
     assert st == sb.SPEC_OK, hex(bits)
     out, nacc = out.cpu().numpy(), nacc.cpu().numpy()
-    excused = 0
+    excused = near = 0
     for b in range(B):
         r = OA.accept(OC.apply_mask(zp[b], a[b]), q[b] if T > 0 else None, x[b],
                       u[b] if T > 0 else None, T, top_p)
+        near += r.boundary
         m = int(nacc[b])
         emitted = out[b, :m + 1]
         assert all(a[b, i, t] for i, t in enumerate(emitted)), (b, emitted.tolist())
@@ -120,7 +122,7 @@ def test_masked_accept_matches_oracle(B, gamma, V, T, top_p, frac, grid, monkeyp
         if not same:
             assert r.boundary, (b, out[b].tolist(), r.tokens)
             excused += 1
-    assert excused <= 0.001 * B + 1, excused
+    parity.check(f"masked accept B={B} V={V} T={T} top_p={top_p}", B, near, excused)
     assert (nacc > 0).any()
 
 
@@ -137,12 +139,16 @@ def test_masked_draft_sample_probs():
     p = probs.cpu().numpy()
     t = toks.cpu().numpy()
     assert (p[~a] == 0).all()
+    excused = near = 0
     for r in range(R):
         qs, ts, bnd = OA.draft_sample(OC.apply_mask(z[r:r + 1], a[r:r + 1]), u[r:r + 1], T, top_p)
-        if not bnd[0]:
-            assert t[r] == ts[0]
-            np.testing.assert_allclose(p[r], qs[0], rtol=1e-5, atol=1e-9)
+        near += bool(bnd[0])
+        np.testing.assert_allclose(p[r], qs[0], rtol=1e-5, atol=1e-9)
+        if t[r] != ts[0]:
+            assert bnd[0], r
+            excused += 1
         assert a[r, t[r]]
+    parity.check("masked draft sample", R, int(near), excused)
 
 
 def test_masked_tree_accept_matches_oracle():
@@ -172,9 +178,10 @@ def test_masked_tree_accept_matches_oracle():
     st, bits = sb.spec_device_status(ws)
     assert st == sb.SPEC_OK, hex(bits)
     out, path, nacc = out.cpu().numpy(), path.cpu().numpy(), nacc.cpu().numpy()
-    excused = 0
+    excused = near = 0
     for b in range(B):
         r = Tr.tree_accept(OC.apply_mask(zp[b], a[b]), q[b], toks[b], parents, u[b], 1.0)
+        near += r.boundary
         m = int(nacc[b])
         same = m == r.n_accepted and out[b, :m + 1].tolist() == r.tokens and path[b, :m].tolist() == r.path
         # the emitted token is allowed at the node it follows
@@ -183,4 +190,4 @@ def test_masked_tree_accept_matches_oracle():
         if not same:
             assert r.boundary, (b, out[b].tolist(), r.tokens)
             excused += 1
-    assert excused <= 1, excused
+    parity.check("masked tree accept", B, near, excused)

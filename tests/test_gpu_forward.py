@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import parity
 from oracle import accept as OA
 from oracle import model as OM
 from oracle import weights as OW
@@ -256,15 +257,25 @@ def test_lm_head_workload_and_accept():
     out = torch.empty(1, 5, dtype=torch.int32, device="cuda")
     nacc = torch.empty(1, dtype=torch.int32, device="cuda")
     aws = sb.workspace(sb.spec_accept_workspace_bytes(1, 4, cfg.vocab))
-    sb.spec_accept(z.view(1, 5, -1), torch.from_numpy(q.astype(np.float32)[None]).cuda(),
-                   torch.from_numpy(x.astype(np.int32)[None]).cuda(), torch.from_numpy(u).cuda(),
-                   1, 4, cfg.vocab, 1.0, 1.0, out, nacc, aws)
-    # the oracle decides on its own logits; decisions closer to a boundary
-    # than the logits tolerance allows are not graded
-    r = OA.accept(ref.astype(np.float32), q.astype(np.float32), x, u[0], 1.0,
-                  margins=(5e-3, 5e-3, 5e-3))
-    if not r.boundary:
-        assert int(nacc[0]) == r.n_accepted and out[0].tolist() == r.tokens
+    q32 = q.astype(np.float32)
+    dq = torch.from_numpy(q32[None]).cuda()
+    dx = torch.from_numpy(x.astype(np.int32)[None]).cuda()
+    du = torch.from_numpy(u).cuda()
+    ref32 = ref.astype(np.float32)
+    # identical (oracle) fp32 logits on both sides: exact outside the margins
+    sb.spec_accept(torch.from_numpy(ref32[None]).cuda(), dq, dx, du, 1, 4, cfg.vocab, 1.0, 1.0,
+                   out, nacc, aws)
+    r = OA.accept(ref32, q32, x, u[0], 1.0)
+    same = int(nacc[0]) == r.n_accepted and out[0].tolist() == r.tokens
+    assert same or r.boundary
+    # end to end: the device decides on its own logits, the oracle on its
+    # own; decisions closer to a boundary than the logits tolerance are
+    # counted, not graded
+    sb.spec_accept(z.view(1, 5, -1), dq, dx, du, 1, 4, cfg.vocab, 1.0, 1.0, out, nacc, aws)
+    re = OA.accept(ref32, q32, x, u[0], 1.0, margins=(5e-3, 5e-3, 5e-3))
+    if not re.boundary:
+        assert int(nacc[0]) == re.n_accepted and out[0].tolist() == re.tokens
+    parity.check("LM-head workload accept", 1, int(r.boundary), int(not same), int(re.boundary))
     m.close()
 
 

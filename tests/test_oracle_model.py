@@ -197,3 +197,51 @@ def test_forward_rejects_bad_inputs():
         Mo.forward(cfg, Wt, np.array([[1, 2, 3, 4, 5]]), kv)
     with pytest.raises(ValueError):
         Mo.forward(cfg, Wt, np.array([[cfg.vocab]]), kv)
+
+
+def test_prefix_cache_equals_stored_cache():
+    """The streamed cache (prefix rebuilt from the row pool on demand, only
+    the written slots kept) gives the stored cache's logits and new cache
+    rows, over a pass, a rollback and a second pass, with ragged lengths."""
+    from speculative_decoding_verification_pass_gb300 import workloads as wl
+    B, n, gamma = 3, 5, 4
+    lens = np.array([17, 40, 9])
+    Kp, Vp = wl.kv_pool(4, 64, TINY.head_dim)
+
+    def prefix(l, b):
+        idx = wl.kv_pool_index(4, l, b, TINY.n_kv_heads, int(lens[b]), 64)
+        return from_bits(Kp[idx[0]]), from_bits(Vp[idx[1]])
+
+    Wt = W.Weights(TINY, 3)
+    stored = Mo.KVState(TINY, B, 64)
+    for l in range(TINY.n_layers):
+        for b in range(B):
+            K0, V0 = prefix(l, b)
+            stored.K[l][b, :, :lens[b]] = K0
+            stored.V[l][b, :, :lens[b]] = V0
+    stored.lens[:] = lens
+    streamed = Mo.PrefixKV(lens, prefix, extra=16)
+    t1 = np.random.default_rng(0).integers(0, TINY.vocab, (B, n))
+    t2 = np.random.default_rng(1).integers(0, TINY.vocab, (B, n))
+    np.testing.assert_array_equal(Mo.forward(TINY, Wt, t1, stored), Mo.forward(TINY, Wt, t1, streamed))
+    n_acc = np.array([0, 4, 2])
+    stored.lens = Mo.truncate(stored.lens, n_acc, gamma)
+    streamed.lens = Mo.truncate(streamed.lens, n_acc, gamma)
+    np.testing.assert_array_equal(Mo.forward(TINY, Wt, t2, stored), Mo.forward(TINY, Wt, t2, streamed))
+    for l in range(TINY.n_layers):
+        for b in range(B):
+            K, V = streamed.seq(l, b)
+            L = int(streamed.lens[b])
+            np.testing.assert_array_equal(K[:, :L], stored.K[l][b, :, :L])
+            np.testing.assert_array_equal(V[:, :L], stored.V[l][b, :, :L])
+    with pytest.raises(ValueError):             # passes beyond the kept slots
+        streamed.lens = streamed.base + 14
+        Mo.forward(TINY, Wt, t1, streamed)
+
+
+def test_bf16_layer_cache_returns_the_generated_values():
+    a = W.Weights(TINY, 8, cache_layers="bf16")
+    b = W.Weights(TINY, 8, cache_layers=False)
+    for k, v in b.layer(1).items():
+        np.testing.assert_array_equal(a.layer(1)[k], v)
+        np.testing.assert_array_equal(a.layer(1)[k], v)   # from the cache
