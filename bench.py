@@ -116,23 +116,55 @@ class ClockSampler:
 
 
 class Workload:
-    def __init__(self, cfg: sb.ModelConfig, B: int, gamma: int, ctx: int, T: float,
-                 top_p: float, sigma: float, seed: int, steps_cap: int):
-        self.cfg, self.B, self.gamma, self.ctx = cfg, B, gamma, ctx
+    """One verify-step workload on the device: model, cache, drafts, outputs.
+
+    ctx is one cached length for every sequence or an array of per-sequence
+    lengths.  kv_init: "prefix" draws the cache contents on the host
+    (N(0, 1) in bf16, seeded), "device" draws them on the device with a
+    seeded torch generator (for caches too large to draw on the host),
+    "prefill" runs spec_verify_forward over uniform random tokens (untimed).
+    model / kv: share an existing Model / KVCache instead of creating one.""" 
+
+    def __init__(self, cfg: sb.ModelConfig, B: int, gamma: int, ctx, T: float,
+                 top_p: float, sigma: float, seed: int, steps_cap: int = 0,
+                 model: "sb.Model | None" = None, kv_init: str = "prefix", cap: int = 0,
+                 kv: "sb.KVCache | None" = None):
+        self.cfg, self.B, self.gamma = cfg, B, gamma
         self.T, self.top_p, self.sigma = T, top_p, sigma
         self.n = gamma + 1
-        self.cap = ctx + self.n + 16
+        self.lens = np.full(B, int(ctx), np.int64) if np.ndim(ctx) == 0 else np.asarray(ctx, np.int64)
+        self.ctx = int(self.lens.max())
+        self.cap = cap or self.ctx + self.n + 16
         dev = "cuda"
-        self.model = sb.Model(cfg, 1000 + seed)
-        self.kv = sb.KVCache(cfg, B, self.cap)
-        hd = cfg.head_dim
-        K, V = wl.kv_prefix(seed, cfg.n_layers, B, cfg.n_kv_heads, ctx, hd)
-        self.kv.k[:, :, :, :ctx].copy_(torch.from_numpy(K.view(np.int16)).view(torch.bfloat16))
-        self.kv.v[:, :, :, :ctx].copy_(torch.from_numpy(V.view(np.int16)).view(torch.bfloat16))
-        del K, V
-        self.kv.len.fill_(ctx)
-        self.ws = sb.workspace(sb.spec_workspace_bytes(cfg, B, gamma, self.cap))
+        self.own_model = model is None
+        self.model = model if model is not None else sb.Model(cfg, 1000 + seed)
+        if kv is not None:              # share a cache whose contents are already drawn
+            self.cap = kv.capacity
+            kv_init = "shared"
+        self.kv = kv if kv is not None else sb.KVCache(cfg, B, self.cap)
+        self.lens_dev = torch.from_numpy(self.lens.astype(np.int32)).to(dev)
+        self.ws = sb.workspace(sb.spec_workspace_bytes(cfg, B, max(gamma, 127), self.cap))
         self.aws = sb.workspace(sb.spec_accept_workspace_bytes(B, gamma, cfg.vocab))
+        hd = cfg.head_dim
+        if kv_init == "prefix":
+            ctx0 = self.ctx
+            K, V = wl.kv_prefix(seed, cfg.n_layers, B, cfg.n_kv_heads, ctx0, hd)
+            self.kv.k[:, :, :, :ctx0].copy_(torch.from_numpy(K.view(np.int16)).view(torch.bfloat16))
+            self.kv.v[:, :, :, :ctx0].copy_(torch.from_numpy(V.view(np.int16)).view(torch.bfloat16))
+            del K, V
+        elif kv_init == "device":
+            g = torch.Generator(device=dev)
+            g.manual_seed(seed)
+            self.kv.k.normal_(generator=g)
+            self.kv.v.normal_(generator=g)
+        elif kv_init == "prefill":
+            toks = torch.from_numpy(wl.tokens(seed, B, self.ctx, cfg.vocab)).to(dev)
+            for c0 in range(0, self.ctx, 128):
+                blk = toks[:, c0:c0 + 128].contiguous()
+                z = torch.empty(B, blk.shape[1], cfg.vocab, device=dev)
+                sb.spec_verify_forward(self.model.handle, blk, B, blk.shape[1] - 1, self.kv, z, self.ws)
+            torch.cuda.synchronize()
+        self.kv.len.copy_(self.lens_dev)
         Vv = cfg.vocab
         self.tokens = torch.zeros(B, self.n, dtype=torch.int32, device=dev)
         self.logits = torch.empty(B, self.n, Vv, device=dev)
@@ -144,7 +176,6 @@ class Workload:
         self.zrow = torch.empty(B, 1, Vv, device=dev)
         self.qrow = torch.empty(B, Vv, device=dev)
         self.xrow = torch.empty(B, dtype=torch.int32, device=dev)
-        self.zeros = torch.zeros(B, dtype=torch.int32, device=dev)
         self.gen = torch.Generator(device=dev)
         self.gen.manual_seed(seed)
         self.t_last = torch.from_numpy(wl.tokens(seed, B, 1, Vv)).to(dev).view(B)
@@ -170,7 +201,7 @@ class Workload:
             self.x[:, i] = self.xrow
             self.tokens[:, i + 1] = self.xrow
             cur = self.xrow.view(B, 1).clone()
-        sb.spec_kv_truncate(self.kv, self.zeros, g, self.ws)      # back to the context
+        self.kv.len.copy_(self.lens_dev)                          # back to the context
         self.u.copy_(torch.rand(B, self.n, device="cuda", generator=self.gen))
 
     def step(self, stream=None):
@@ -189,7 +220,11 @@ class Workload:
         self.emitted += int((n + 1).sum())
         self.accepted += int(n.sum())
         self.t_last = torch.from_numpy(o[np.arange(self.B), n].astype(np.int32)).cuda()
-        self.kv.len.fill_(self.ctx)
+        self.kv.len.copy_(self.lens_dev)
+
+    def close(self):
+        if self.own_model:
+            self.model.close()
 
     def check_status(self):
         for ws in (self.ws, self.aws):
@@ -205,11 +240,26 @@ class Workload:
         per_layer = (qkv * d + d * c.n_heads * hd + 2 * c.d_ffn * d + d * c.d_ffn) * 2
         M = self.B * self.n
         w = c.n_layers * per_layer + c.vocab * d * 2 + M * d * 2
-        kv_tok = c.n_layers * c.n_kv_heads * hd * 2 * 2
-        kv = self.B * ((self.ctx + self.n) * kv_tok + self.n * kv_tok)
         logits = M * c.vocab * 4 * 2
         q = self.B * self.gamma * c.vocab * 4
-        return float(w + kv + logits + q)
+        return float(w + self.kv_bytes() + logits + q)
+
+    def kv_bytes(self) -> float:
+        """Keys/values read (each sequence's context + the new slots) and
+        the new slots written, every layer."""
+        c = self.cfg
+        kv_tok = c.n_layers * c.n_kv_heads * c.head_dim * 2 * 2
+        return float(sum((int(L) + self.n) * kv_tok + self.n * kv_tok for L in self.lens))
+
+    def flops_per_step(self) -> float:
+        """2 * M * weight parameters + the attention (scores and values,
+        4 * keys * H * hd per new position and layer)."""
+        c = self.cfg
+        hd, d = c.head_dim, c.d_model
+        qkv = (c.n_heads + 2 * c.n_kv_heads) * hd
+        params = c.n_layers * (qkv * d + d * c.n_heads * hd + 3 * c.d_ffn * d) + c.vocab * d
+        att = sum(4 * (int(L) + j + 1) * c.n_heads * hd for L in self.lens for j in range(self.n))
+        return float(2 * self.B * self.n * params + c.n_layers * att)
 
     def gemm_bytes(self) -> float:
         c = self.cfg
@@ -223,11 +273,8 @@ class Workload:
         new tokens' embedding rows, the attended keys/values (context + the
         gamma+1 new slots, every layer), the appended slots and the logits."""
         c = self.cfg
-        hd, d = c.head_dim, c.d_model
         M = self.B * self.n
-        kv_tok = c.n_layers * c.n_kv_heads * hd * 2 * 2
-        kv = self.B * ((self.ctx + self.n) * kv_tok + self.n * kv_tok)
-        return float(self.gemm_bytes() + M * d * 2 + kv + M * c.vocab * 4)
+        return float(self.gemm_bytes() + M * c.d_model * 2 + self.kv_bytes() + M * c.vocab * 4)
 
 
 def time_steps(w: Workload, K: int):
@@ -410,45 +457,72 @@ def gamma_ctl_probe(w: Workload, alpha: float, step_ms: float):
 
 
 # ------------------------------------------------------------- CPU oracle
-def oracle_step_estimate(cfg: sb.ModelConfig, B: int, gamma: int, ctx: int, T: float, seed: int,
-                         head_rows: int = 8192):
-    """The oracle timed on this host on a bounded sample of the same step:
-    one decoder layer of the 8B shape over the gamma+1 new positions at the
-    same context (cache contents from the same generator), an LM-head slice
-    of head_rows rows, and the accept rule on a full-vocabulary step; scaled
-    to a whole step as n_layers * layer + (V / head_rows) * head + accept."""
-    from oracle import accept as OA
-    from oracle import model as OM
-    from oracle import weights as OW
-    one = OM.Config(1, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn, head_rows,
-                    cfg.rms_eps, cfg.rope_theta)
-    W = OW.Weights(one, 1000 + seed)
-    W.layer(0)
-    W.head()
-    kvs = OM.KVState(one, B, ctx + gamma + 1)
-    K, V = wl.kv_prefix(seed, 1, B, cfg.n_kv_heads, ctx, cfg.head_dim)
-    from oracle.bf16 import from_bits
-    kvs.load_prefix([from_bits(K[0])], [from_bits(V[0])], [ctx] * B)
-    toks = wl.tokens(seed, B, gamma + 1, head_rows)
-    t0 = time.perf_counter()
-    OM.forward(one, W, toks, kvs)
-    t_fwd = time.perf_counter() - t0
-    x = np.random.default_rng(seed).standard_normal((B * (gamma + 1), cfg.d_model))
-    t0 = time.perf_counter()
-    OM.lm_head(x, W.head())
-    t_head = time.perf_counter() - t0
-    zq, zp = wl.accept_logits(seed, 1, gamma, cfg.vocab)
-    ud = wl.uniforms(seed, 1, gamma, stream=8)
-    q, xs, _ = OA.draft_sample(zq[0, :gamma], ud[0], T)
-    u = wl.uniforms(seed, 1, gamma + 1)[0]
-    t0 = time.perf_counter()
-    OA.accept(zp[0], q, xs, u, T)
-    t_acc = (time.perf_counter() - t0) * B
-    est = cfg.n_layers * max(t_fwd - t_head, 1e-9) + (cfg.vocab / head_rows) * t_head + t_acc
-    sample = (f"1 of {cfg.n_layers} decoder layers (M={B * (gamma + 1)}, context {ctx}), "
-              f"LM head {head_rows} of {cfg.vocab} rows, accept on one full-vocabulary step; "
-              f"scaled to a full step ({t_fwd + t_acc:.1f} s measured)")
-    return est, sample
+class OracleSample:
+    """The oracle on this host, on a bounded sample of the verify step: one
+    decoder layer of the model's shape over the M = B(gamma+1) new positions
+    at the same cached length (cache contents from the same generator), an
+    LM-head slice of head_rows rows, and the acceptance rule on one
+    full-vocabulary step per sequence.  Every run() is a fresh step (new
+    tokens, the cache reset to the context); its algorithmic bytes are the
+    sample's own (that layer's weights and KV traffic, the head slice, the
+    accept's logits and draft probabilities), so bytes / time is the oracle's
+    rate on this workload, with no extrapolation.  The set-up (weights of the
+    one layer and the head slice) is not timed."""
+
+    def __init__(self, cfg: sb.ModelConfig, B: int, gamma: int, ctx: int, T: float, seed: int,
+                 head_rows: int = 8192):
+        from oracle import accept as OA
+        from oracle import model as OM
+        from oracle import weights as OW
+        from oracle.bf16 import from_bits
+        self.OA, self.OM = OA, OM
+        self.cfg, self.B, self.gamma, self.ctx, self.T, self.seed = cfg, B, gamma, ctx, T, seed
+        self.head_rows = min(head_rows, cfg.vocab)
+        self.one = OM.Config(1, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.d_ffn,
+                             self.head_rows, cfg.rms_eps, cfg.rope_theta)
+        self.W = OW.Weights(self.one, 1000 + seed)
+        self.W.layer(0)
+        self.W.head()
+        self.kvs = OM.KVState(self.one, B, ctx + gamma + 1)
+        K, V = wl.kv_prefix(seed, 1, B, cfg.n_kv_heads, ctx, cfg.head_dim)
+        self.kvs.load_prefix([from_bits(K[0])], [from_bits(V[0])], [ctx] * B)
+        self.it = 0
+        c = cfg
+        hd, d = c.head_dim, c.d_model
+        qkv = (c.n_heads + 2 * c.n_kv_heads) * hd
+        layer_w = (qkv * d + d * c.n_heads * hd + 3 * c.d_ffn * d) * 2
+        kv_tok = c.n_kv_heads * hd * 2 * 2
+        n = gamma + 1
+        self.bytes = float(layer_w + B * ((ctx + n) * kv_tok + n * kv_tok)
+                           + self.head_rows * d * 2 + B * (2 * n + gamma) * c.vocab * 4)
+        self.desc = (f"one step of: 1 of {c.n_layers} decoder layers (M={B * n}, context {ctx}), "
+                     f"LM head {self.head_rows} of {c.vocab} rows, accept on {B} full-vocabulary "
+                     f"step(s); GB/s of that sample's own algorithmic bytes")
+
+    def run(self) -> float:
+        OA, OM = self.OA, self.OM
+        self.it += 1
+        s = self.seed + 7 * self.it
+        B, g, V = self.B, self.gamma, self.cfg.vocab
+        toks = wl.tokens(s, B, g + 1, self.head_rows)
+        zq, zp = wl.accept_logits(s, B, g, V)
+        ud = wl.uniforms(s, B, g, stream=8)
+        u = wl.uniforms(s, B, g + 1)
+        qx = [OA.draft_sample(zq[b, :g], ud[b], self.T if self.T > 0 else 1.0)[:2] for b in range(B)]
+        self.kvs.lens[:] = self.ctx
+        t0 = time.perf_counter()
+        OM.forward(self.one, self.W, toks, self.kvs)
+        for b in range(B):
+            OA.accept(zp[b], qx[b][0], qx[b][1], u[b], self.T)
+        return time.perf_counter() - t0
+
+
+def oracle_rate(sample: OracleSample, steps: int, warmup: int = 1):
+    """(GB/s, mean seconds per sample step, steps timed)."""
+    for _ in range(warmup):
+        sample.run()
+    ts = [sample.run() for _ in range(steps)]
+    return sample.bytes * len(ts) / sum(ts) / 1e9, sum(ts) / len(ts), len(ts)
 
 
 def blas_threads():
@@ -644,6 +718,318 @@ def time_paged(w: Workload, K: int):
     return out
 
 
+# ------------------------------------------------------- per-config lines
+def _ev():
+    return torch.cuda.Event(enable_timing=True)
+
+
+class L2Flush:
+    """Writes a 512 MB buffer (about four times the L2) before a timed
+    iteration whose working set would otherwise stay in L2; untimed."""
+
+    def __init__(self):
+        self.buf = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        self.i = 0
+
+    def __call__(self):
+        self.i += 1
+        self.buf.fill_(self.i & 0xFF)
+        torch.cuda.synchronize()
+
+
+def _parity(name, cases, near, excused):
+    return {"sample": name, "cases": cases, "in_margin": near, "excused": excused,
+            "in_margin_frac": near / max(1, cases), "boundary_frac": excused / max(1, cases)}
+
+
+def launch_floor_us(K: int = 200) -> float:
+    """Median device time of this library's smallest launch (the rollback
+    kernel on one sequence): the latency floor of a one-launch call."""
+    cfg = sb.ModelConfig(1, 256, 4, 2, 256, 1000)
+    kv = sb.KVCache(cfg, 1, 64)
+    kv.len.fill_(10)
+    ws = sb.workspace(sb.spec_workspace_bytes(cfg, 1, 4, 64))
+    nacc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ts = []
+    for _ in range(K):
+        a, b = _ev(), _ev()
+        a.record()
+        sb.spec_kv_truncate(kv, nacc, 0, ws)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts) * 1e3
+
+
+def config_accept_only(steps: int = 1000):
+    """Accept-only workload: batch 1, gamma 4, V 4096, z_q ~ N(0, 2^2),
+    z_p = z_q + N(0, 0.5^2), q = softmax(z_q) in fp64 on the host, drafts
+    drawn from q, T = 1; `steps` independent steps, L2 flushed before each.
+    Its bytes (147 KB) are far below anything HBM-bound: the bound is the
+    launch latency of one kernel, reported as the floor."""
+    from oracle import accept as OA
+    B, g, V, T = 1, 4, 4096, 1.0
+    seed = wl.BASE_SEED
+    zq, zp = wl.accept_logits(seed, steps, g, V)
+    ud = wl.uniforms(seed, steps, g, stream=8)
+    u = wl.uniforms(seed, steps, g + 1)
+    q = np.zeros((steps, g, V), np.float32)
+    x = np.zeros((steps, g), np.int32)
+    for i in range(steps):
+        qs, ts, _ = OA.draft_sample(zq[i, :g], ud[i], T)
+        q[i], x[i] = qs.astype(np.float32), ts
+    dz, dq = torch.from_numpy(zp).cuda(), torch.from_numpy(q).cuda()
+    dx, du = torch.from_numpy(x).cuda(), torch.from_numpy(u).cuda()
+    out = torch.empty(steps, g + 1, dtype=torch.int32, device="cuda")
+    nacc = torch.empty(steps, dtype=torch.int32, device="cuda")
+    ws = sb.workspace(sb.spec_accept_workspace_bytes(B, g, V))
+    flush = L2Flush()
+    ts = []
+    for i in range(steps):
+        flush()
+        a, b = _ev(), _ev()
+        a.record()
+        sb.spec_accept(dz[i:i + 1], dq[i:i + 1], dx[i:i + 1], du[i:i + 1], B, g, V, T, 1.0,
+                       out[i:i + 1], nacc[i:i + 1], ws)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    if sb.spec_device_status(ws)[0] != sb.SPEC_OK:
+        raise RuntimeError("accept-only device status")
+    o, na = out.cpu().numpy(), nacc.cpu().numpy()
+    near = excused = 0
+    t0 = time.perf_counter()
+    for i in range(steps):
+        r = OA.accept(zp[i], q[i], x[i], u[i], T)
+        near += r.boundary
+        if not (int(na[i]) == r.n_accepted and o[i].tolist() == r.tokens):
+            excused += 1
+            if not r.boundary:
+                raise RuntimeError(f"accept-only step {i} differs from the oracle")
+    oracle_us = (time.perf_counter() - t0) / steps * 1e6
+    med = statistics.median(ts)
+    floor = launch_floor_us()
+    nbytes = (2 * (g + 1) + g) * V * 4
+    return {"workload": f"spec_accept only: batch 1, gamma 4, V 4096, T 1, {steps} steps, "
+                        f"L2 flushed before each", "us_per_call": med,
+            "p90_us": float(np.percentile(ts, 90)), "bytes_per_call": nbytes,
+            "roofline": {"bound": "latency", "achieved_us": med, "floor_us": floor,
+                         "frac": floor / med,
+                         "note": "one launch of the smallest kernel of this library"},
+            "acceptance": float(na.mean()) / g,
+            "parity": _parity("every step vs the oracle on identical inputs", steps, near, excused),
+            "cpu_baseline": {"us_per_call": oracle_us, "kind": "oracle", "cores": 1,
+                             "sample": f"the oracle's accept on the same {steps} steps"}}
+
+
+def config_lm_head(hbm: float, steps: int = 40):
+    """LM-head verify + accept: activations ~ N(0, 1) in bf16 for 5
+    positions, LM head 4096 x 32000 ~ N(0, 0.02^2); draft probabilities from
+    the same head on the activations + N(0, 0.3^2) (fp64, host), T = 1; the
+    timed step is the M = 5 skinny GEMM then the fused accept, L2 flushed
+    before each step."""
+    from oracle import accept as OA
+    from oracle import model as OM
+    from oracle import weights as OW
+    cfg = sb.ModelConfig(0, 4096, 32, 8, 128, 32000)
+    seed = wl.BASE_SEED + 1
+    m = sb.Model(cfg, seed)
+    head = OW.tensor(seed, OW.HEAD, cfg.vocab, cfg.d_model)
+    ws = sb.workspace(sb.spec_workspace_bytes(cfg, 5, 0, 1))
+    aws = sb.workspace(sb.spec_accept_workspace_bytes(1, 4, cfg.vocab))
+    z = torch.empty(1, 5, cfg.vocab, device="cuda")
+    out = torch.empty(1, 5, dtype=torch.int32, device="cuda")
+    nacc = torch.empty(1, dtype=torch.int32, device="cuda")
+    flush = L2Flush()
+    ts, t_or = [], []
+    near = excused = 0
+    err = 0.0
+    accepted = 0
+    for i in range(steps):
+        hb = wl.hidden_bf16(seed + i, 5, cfg.d_model)
+        h = wl.bf16_bits_to_f32(hb).astype(np.float64)
+        t0 = time.perf_counter()
+        ref = OM.lm_head(h, head)
+        noisy = h[:4] + wl.gauss(seed + i, (4, cfg.d_model), 0.3)
+        q, x, _ = OA.draft_sample(OM.lm_head(noisy, head), wl.uniforms(seed + i, 4, stream=8), 1.0)
+        u = wl.uniforms(seed + i, 1, 5)
+        r = OA.accept(ref.astype(np.float32), q.astype(np.float32), x, u[0], 1.0)
+        t_or.append(time.perf_counter() - t0)
+        dh = torch.from_numpy(hb.view(np.int16)).cuda()
+        dq = torch.from_numpy(q.astype(np.float32)[None]).cuda()
+        dx = torch.from_numpy(x.astype(np.int32)[None]).cuda()
+        du = torch.from_numpy(u).cuda()
+        flush()
+        a, b = _ev(), _ev()
+        a.record()
+        sb.spec_lm_head(m.handle, dh, 5, z, ws)
+        sb.spec_accept(z, dq, dx, du, 1, 4, cfg.vocab, 1.0, 1.0, out, nacc, aws)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+        accepted += int(nacc[0])
+        err = max(err, float((np.abs(z[0].double().cpu().numpy() - ref) / (1 + np.abs(ref))).max()))
+        # parity sample: the device accept on the oracle's logits
+        sb.spec_accept(torch.from_numpy(ref.astype(np.float32)[None]).cuda(), dq, dx, du, 1, 4,
+                       cfg.vocab, 1.0, 1.0, out, nacc, aws)
+        near += r.boundary
+        if not (int(nacc[0]) == r.n_accepted and out[0].tolist() == r.tokens):
+            excused += 1
+            if not r.boundary:
+                raise RuntimeError(f"LM-head step {i} accept differs from the oracle")
+    for w_ in (ws, aws):
+        if sb.spec_device_status(w_)[0] != sb.SPEC_OK:
+            raise RuntimeError("LM-head workload device status")
+    m.close()
+    ms = statistics.median(ts)
+    nbytes = cfg.vocab * cfg.d_model * 2 + 5 * cfg.d_model * 2 + 5 * cfg.vocab * 4 * 2 \
+        + 4 * cfg.vocab * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": "LM head 4096 x 32000 on 5 positions + fused accept, batch 1, gamma 4, "
+                        f"T 1, {steps} steps, L2 flushed before each",
+            "ms_per_step": ms, "value": gbs, "unit": "GB/s", "bytes_per_step": nbytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "peak_source": "measured (burst copy)"},
+            "logits_max_rel_err": err, "acceptance": accepted / (4 * steps),
+            "parity": _parity("device accept on the oracle's logits, every step", steps, near,
+                              excused),
+            "cpu_baseline": {"ms_per_step": statistics.median(t_or) * 1e3, "kind": "oracle",
+                             "cores": blas_threads(),
+                             "value": nbytes / statistics.median(t_or) / 1e9, "unit": "GB/s",
+                             "sample": "the oracle's LM head + accept on the same steps"}}
+
+
+def run_workload(w: Workload, steps: int, warmup: int, hbm: float, inst: bool = True):
+    """ms/step, GB/s, fractions, tokens/s and acceptance of a workload's
+    verify step (forward + accept + rollback), plus the forward kernel's own
+    launch time when inst."""
+    time_steps(w, warmup)
+    w.check_status()
+    w.emitted = w.accepted = 0
+    times = time_steps(w, steps)
+    w.check_status()
+    ms = sum(times) / len(times)
+    nbytes = w.bytes_per_step()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    fl = w.flops_per_step()
+    tf = fl / (ms / 1e3) / 1e12
+    res = {"batch": w.B, "gamma": w.gamma, "temperature": w.T, "top_p": w.top_p,
+           "sigma": w.sigma, "context_mean": float(w.lens.mean()),
+           "ms_per_step": ms, "value": gbs, "unit": "GB/s", "bytes_per_step": nbytes,
+           "hbm_frac_of_measured": gbs / hbm, "hbm_frac_of_8tbs": gbs / 8000.0,
+           "tflops": tf, "flops_per_step": fl,
+           "emitted_tokens_per_s": w.emitted / (sum(times) / 1e3),
+           "acceptance": w.accepted / max(1, steps * w.B * w.gamma),
+           "accept_us": accept_time(w, 5) * 1e3}
+    if inst:
+        gm = gn = am = an = pm = pn = 0.0
+        for ms_, n_, _ in instrumented(w, 2):
+            gm += ms_[0]; gn += n_[0]; am += ms_[1]; an += n_[1]; pm += ms_[2]; pn += n_[2]
+        if pn:
+            kms = pm / pn
+            res["forward_kernel"] = {"kernel": "forward_kernel", "launch_ms": kms,
+                                     "achieved_gbs": w.forward_bytes() / (kms / 1e3) / 1e9,
+                                     "frac": w.forward_bytes() / (kms / 1e3) / 1e9 / hbm}
+        elif gn:
+            res["forward_kernel"] = {"kernel": "gemm_tc_kernel + attention (per-step schedule)",
+                                     "gemm_ms_per_step": gm / 2, "attention_ms_per_step": am / 2,
+                                     "gemm_gbs": w.gemm_bytes() / (gm / 2 / 1e3) / 1e9}
+    return res
+
+
+def config_1b(hbm: float, steps: int, warmup: int):
+    """The 1B-shaped decoder: batch 1, 512 prefix tokens uniform over the
+    vocabulary prefilled through spec_verify_forward (untimed), gamma 4,
+    T 1, noisy-target draft sigma 0.5; 2.1 GB of weights per step."""
+    w = Workload(sb.LLAMA_1B, 1, 4, 512, 1.0, 1.0, 0.5, seed=5, kv_init="prefill")
+    res = run_workload(w, steps, warmup, hbm)
+    w.close()
+    smp = OracleSample(sb.LLAMA_1B, 1, 4, 512, 1.0, 5)
+    val, sec, k = oracle_rate(smp, 2)
+    res.update({"workload": "1B-shaped synthetic Llama decoder, batch 1, 512 prefilled tokens, "
+                            "gamma 4, T 1, noisy-target draft sigma 0.5",
+                "roofline": {"bound": "hbm", "achieved": res["value"], "peak": hbm, "unit": "GB/s",
+                             "frac": res["value"] / hbm, "peak_source": "measured (burst copy)"},
+                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": blas_threads(),
+                                 "kind": "oracle", "sample": f"{k} x {smp.desc}"}})
+    return res
+
+
+def config_8b_variants(w: Workload, hbm: float, steps: int, warmup: int):
+    """The 8B headline workload at the other draft lengths and at greedy
+    decoding: same model and 2048-token context; gamma 2 and 8 at T 1, and
+    gamma 2, 4 and 8 at T 0."""
+    out = []
+    for gamma, T in ((2, 1.0), (8, 1.0), (2, 0.0), (4, 0.0), (8, 0.0)):
+        v = Workload(w.cfg, 1, gamma, w.ctx, T, 1.0, w.sigma, seed=3, model=w.model, kv=w.kv)
+        r = run_workload(v, steps, warmup, hbm)
+        r["workload"] = (f"8B-shaped decoder, batch 1, context {w.ctx}, gamma {gamma}, T {T}, "
+                         f"noisy-target draft sigma {w.sigma}")
+        out.append(r)
+    w.kv.len.copy_(w.lens_dev)
+    return out
+
+
+def config_batched(model: sb.Model, hbm: float, tflops: float, steps: int, warmup: int):
+    """The batched 8B workload: batch 16 and 64, per-sequence cached lengths
+    uniform in [512, 4096] (cache contents N(0, 1) drawn on the device),
+    gamma 4, T 0.8 and top-p 0.9 on p and q, drafts from noisy copies of
+    the target with sigma 0.3 and 1.0; bytes and FLOPs from the drawn
+    lengths, against the HBM and the bf16 tensor bounds."""
+    out = []
+    for B in (16, 64):
+        lens = wl.context_lengths(wl.BASE_SEED + B, B, 512, 4096)
+        w = Workload(sb.LLAMA_8B, B, 4, lens, 0.8, 0.9, 0.3, seed=40 + B, model=model,
+                     kv_init="device", cap=4096 + 16)
+        for sigma in (0.3, 1.0):
+            w.sigma = sigma
+            r = run_workload(w, steps, warmup, hbm, inst=(sigma == 0.3))
+            t_hbm = r["bytes_per_step"] / (hbm * 1e9) * 1e3
+            t_tc = r["flops_per_step"] / (tflops * 1e12) * 1e3
+            r["workload"] = (f"8B-shaped decoder, batch {B}, contexts U[512, 4096] (mean "
+                             f"{lens.mean():.0f}), gamma 4, T 0.8, top-p 0.9, draft sigma {sigma}")
+            r["roofline"] = {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+                             "hbm_ms": t_hbm, "tensor_ms": t_tc,
+                             "frac": max(t_hbm, t_tc) / r["ms_per_step"],
+                             "tensor_frac": r["tflops"] / tflops,
+                             "hbm_frac": r["hbm_frac_of_measured"],
+                             "peaks": {"hbm_gbs": hbm, "bf16_tflops": tflops,
+                                       "source": "measured (burst)"}}
+            out.append(r)
+        del w
+        torch.cuda.empty_cache()
+    return out
+
+
+def headline_parity(T: float, top_p: float, steps: int = 100):
+    """Parity sample at the headline's accept shape (batch 1, gamma 4,
+    V 128256): the device accept against the oracle on identical seeded
+    inputs (accept-only recipe), counted under the boundary rule."""
+    from oracle import accept as OA
+    g, V = 4, 128256
+    ws = sb.workspace(sb.spec_accept_workspace_bytes(1, g, V))
+    out = torch.empty(1, g + 1, dtype=torch.int32, device="cuda")
+    nacc = torch.empty(1, dtype=torch.int32, device="cuda")
+    near = excused = 0
+    for i in range(steps):
+        seed = wl.BASE_SEED + 500 + i
+        zq, zp = wl.accept_logits(seed, 1, g, V)
+        q, x, _ = OA.draft_sample(zq[0, :g], wl.uniforms(seed, g, stream=8), T if T > 0 else 1.0,
+                                  top_p)
+        u = wl.uniforms(seed, 1, g + 1)
+        sb.spec_accept(torch.from_numpy(zp).cuda(), torch.from_numpy(q.astype(np.float32)[None]).cuda(),
+                       torch.from_numpy(x.astype(np.int32)[None]).cuda(), torch.from_numpy(u).cuda(),
+                       1, g, V, T, top_p, out, nacc, ws)
+        r = OA.accept(zp[0], q.astype(np.float32), x, u[0], T, top_p)
+        near += r.boundary
+        if not (int(nacc[0]) == r.n_accepted and out[0].tolist() == r.tokens):
+            excused += 1
+            if not r.boundary:
+                raise RuntimeError(f"headline parity step {i} differs from the oracle")
+    return _parity(f"{steps} accept steps at batch 1, gamma 4, V 128256, T {T}, top-p {top_p} "
+                   "(accept-only recipe), identical inputs", steps, near, excused)
+
+
 # ------------------------------------------------------------------ main
 def parse():
     ap = argparse.ArgumentParser()
@@ -661,6 +1047,9 @@ def parse():
     ap.add_argument("--layers", type=int, default=0,
                     help="override the decoder depth (profiling a smaller model)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config sub-lines (accept-only, LM head, 1B, 8B variants, "
+                         "batched)")
     return ap.parse_args()
 
 
@@ -701,18 +1090,18 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        est, sample = oracle_step_estimate(cfg, args.batch, args.gamma, args.context,
-                                           args.temperature, 3)
-        w_bytes = Workload.bytes_per_step.__get__(type("W", (), {
-            "cfg": cfg, "B": args.batch, "n": args.gamma + 1, "gamma": args.gamma,
-            "ctx": args.context}))()
-        val = w_bytes / est / 1e9
+        # the oracle as it stands on this host's cores: every step is one
+        # timed bounded sample of the workload (OracleSample), W untimed
+        # then K timed, so the line's steps are the steps that ran
+        smp = OracleSample(cfg, args.batch, args.gamma, args.context, args.temperature, 3)
+        val, sec, k = oracle_rate(smp, args.steps, args.warmup)
         line = {"metric": METRIC, "value": val, "unit": "GB/s", "impl": "reference",
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
+                "n_gpus": args.gpus, "steps": k, "warmup": args.warmup,
+                "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "step_is": smp.desc, "bytes_per_step": smp.bytes,
                 "cpu_baseline": {"value": val, "unit": "GB/s", "cores": blas_threads(),
-                                 "kind": "oracle", "sample": sample},
+                                 "kind": "oracle", "sample": smp.desc},
                 "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -810,11 +1199,32 @@ def main():
     line["paged"] = paged
     if tree is not None:
         line["tree"] = tree
+    if world == 1 and not args.no_configs and args.shape == "8b" and not args.layers:
+        _, tflops, _ = peaks()
+        configs = {}
+        steps_c = max(5, args.steps // 2)
+        for name, fn in (("accept_only_v4096", lambda: config_accept_only()),
+                         ("lm_head_accept", lambda: config_lm_head(hbm)),
+                         ("decoder_1b", lambda: config_1b(hbm, steps_c, args.warmup)),
+                         ("decoder_8b_variants", lambda: config_8b_variants(w, hbm, steps_c,
+                                                                            args.warmup)),
+                         ("batched_8b", lambda: config_batched(w.model, hbm, tflops or 1892.2,
+                                                               steps_c, args.warmup))):
+            try:
+                configs[name] = fn()
+            except Exception as exc:
+                configs[name] = {"unavailable": str(exc).splitlines()[0][:200]}
+        line["configs"] = configs
+        try:
+            line["parity"] = headline_parity(args.temperature, args.top_p)
+        except Exception as exc:
+            line["parity"] = {"unavailable": str(exc).splitlines()[0][:200]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        est, sample = oracle_step_estimate(cfg, args.batch, args.gamma, args.context,
-                                           args.temperature, 3)
-        line["cpu_baseline"] = {"value": step_bytes / est / 1e9, "unit": "GB/s",
-                                "cores": blas_threads(), "kind": "oracle", "sample": sample}
+        smp = OracleSample(cfg, args.batch, args.gamma, args.context, args.temperature, 3)
+        val, sec, k = oracle_rate(smp, 3)
+        line["cpu_baseline"] = {"value": val, "unit": "GB/s", "cores": blas_threads(),
+                                "kind": "oracle", "sample": f"{k} x {smp.desc}",
+                                "ms_per_sample_step": sec * 1e3}
     if rank == 0:
         print(json.dumps(line))
     w.model.close()

@@ -399,8 +399,9 @@ int spec_verify_forward_tree(const spec_model* model, const int32_t* d_tokens,
                              int n_nodes, const spec_kv_cache* kv, float* d_logits, void* d_ws,
                              size_t ws_bytes, void* stream);
 
-/* Workspace bytes for spec_tree_accept: the status word and one fp32
- * vocabulary row per sequence (the current residual distribution). */
+/* Workspace bytes for spec_tree_accept: the status word (256 bytes; the walk
+ * keeps each node's residual distribution in closed form, as a coefficient of
+ * q and a normaliser, so it needs no vocabulary-sized scratch). */
 size_t spec_tree_accept_workspace_bytes(int batch, int vocab);
 
 /* The acceptance walk over each sequence's tree ([aci] Tree-Based Drafting:

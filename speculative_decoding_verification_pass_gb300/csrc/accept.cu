@@ -243,6 +243,22 @@ struct RowDist {
   SPEC_DEVINL float p(int x) const { return p_of(__ldcg(z + x)); }
 };
 
+// Add fx into bin `bkt` of a warp's histogram (bkt < 0: nothing), the lanes
+// that hold the same bin summed first: one shared-memory atomic per distinct
+// bin instead of one per lane (the first digit of e(x) = 2^((z - m) / T)
+// falls into a handful of exponent bins, so per-lane atomics serialise).
+// fx <= 2^40 (a probability in 2^-40 fixed point): the 20-bit halves of up
+// to 32 such values sum exactly in 32 bits.  Called by every lane of
+// `lanes` together (the lanes converged at the call).
+SPEC_DEVINL void hist_add_peers(unsigned long long* wh, int bkt, unsigned long long fx,
+                                unsigned lanes) {
+  const unsigned peers = __match_any_sync(lanes, bkt);
+  const unsigned lo = __reduce_add_sync(peers, static_cast<unsigned>(fx & 0xFFFFFull));
+  const unsigned hi = __reduce_add_sync(peers, static_cast<unsigned>(fx >> 20));
+  if (bkt >= 0 && static_cast<int>(threadIdx.x & 31) == __ffs(peers) - 1)
+    atomicAdd(&wh[bkt], (static_cast<unsigned long long>(hi) << 20) + lo);
+}
+
 // Per-warp histograms of the nucleus radix select (dynamic shared memory of
 // the per-sequence kernels): each warp adds into its own 256 bins, so lanes
 // contend only within their warp, then the warps' bins are summed.
@@ -278,8 +294,8 @@ __device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r
     visit_row(z, nullptr, V, [&](int, float zv, float) {
       const float v = d.e_of(zv);
       const uint32_t bits = __float_as_uint(v);
-      if ((bits & hi_mask) == prefix)
-        atomicAdd(&wh[(bits >> shift) & 0xFFu], static_cast<unsigned long long>(v * kFix40));
+      const int bkt = (bits & hi_mask) == prefix ? static_cast<int>((bits >> shift) & 0xFFu) : -1;
+      hist_add_peers(wh, bkt, static_cast<unsigned long long>(v * kFix40), __activemask());
     });
     __syncthreads();
     for (int i = threadIdx.x; i < 256; i += kT) {
@@ -350,17 +366,30 @@ SPEC_DEVINL unsigned long long warp_incl_scan_u64(unsigned long long v) {
   return v;
 }
 
+// Arguments of draw(): the total is the sum of the first level's chunk
+// totals; the last positive id is found only if the threshold is not crossed
+// (u * total rounded up to the total); a residual whose total is numerically
+// zero returns kDrawFallback instead of drawing.
+constexpr unsigned long long kTotalFromChunks = ~0ull;
+constexpr int kLastPosLazy = -2;
+constexpr int kDrawFallback = -3;
+
+template <class DW>
+__device__ int last_positive(const DW& dw, int V, Red& r);
+
 // Inverse-CDF draw: the smallest id t with sum_{x<=t} fx(x) > floor(u * total).
-// `total` is the exact fixed-point sum; `last_pos` the last id with fx > 0.
+// `total` is the exact fixed-point sum (or kTotalFromChunks); `last_pos` the
+// last id with fx > 0 (or kLastPosLazy).
 // Two levels: every warp sums a contiguous chunk of ids exactly (independent
 // loads in flight), an exclusive scan of the chunk totals finds the chunk
 // where the cumulative weight crosses the threshold, and that chunk alone is
 // scanned id by id in tiles of 4 ids per thread.  The integer sums are exact,
-// so the id is the one a single scan in id order finds.
+// so the id is the one a single scan in id order finds.  With fallback set
+// and dw.q given, a total at or below the residual fallback returns
+// kDrawFallback (the caller draws from p instead).
 template <class DW>
-__device__ int draw(const DW& dw, int V, float u, unsigned long long total, int last_pos, Red& r) {
-  const unsigned long long thr =
-      static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(total));
+__device__ int draw(const DW& dw, int V, float u, unsigned long long total, int last_pos, Red& r,
+                    bool fallback = false) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int chunk = ((V + kWarps - 1) / kWarps + 127) & ~127;
   const float* src = dw.src();
@@ -389,15 +418,29 @@ __device__ int draw(const DW& dw, int V, float u, unsigned long long total, int 
     if (w == 0) {
       const unsigned long long t = l < kWarps ? r.u[l] : 0ull;
       const unsigned long long ti = warp_incl_scan_u64(t);
-      const bool hit = l < kWarps && ti - t <= thr && thr < ti;
+      const unsigned long long tot =
+          total == kTotalFromChunks ? __shfl_sync(0xffffffffu, ti, 31) : total;
+      const unsigned long long th =
+          static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(tot));
+      const bool fb = fallback && dw.q && static_cast<double>(tot) <= kResidualFallback * 4503599627370496.0;
+      const bool hit = !fb && l < kWarps && ti - t <= th && th < ti;
       const unsigned ball = __ballot_sync(0xffffffffu, hit);
       if (hit) r.bu[2] = ti - t;  // one lane at most: the prefix before the crossing chunk
-      if (l == 0) r.bi[3] = ball ? __ffs(ball) - 1 : -1;
+      if (l == 0) {
+        r.bi[3] = fb ? kDrawFallback : (ball ? __ffs(ball) - 1 : -1);
+        r.bu[3] = th;
+      }
     }
     __syncthreads();
   }
   const int cw = r.bi[3];
-  if (cw < 0) return last_pos;  // u * total rounded up to total
+  const unsigned long long thr = r.bu[3];
+  if (cw == kDrawFallback) {
+    __syncthreads();
+    return kDrawFallback;
+  }
+  if (cw < 0)  // u * total rounded up to total
+    return last_pos == kLastPosLazy ? last_positive(dw, V, r) : last_pos;
   unsigned long long run = r.bu[2];  // exact prefix before the current tile
   const int b0 = cw * chunk, b1 = min(V, b0 + chunk);
   __syncthreads();
@@ -450,6 +493,17 @@ __device__ int draw(const DW& dw, int V, float u, unsigned long long total, int 
     __syncthreads();
   }
   return last_pos;
+}
+
+// The last id with a positive draw weight (-1: none).
+template <class DW>
+__device__ int last_positive(const DW& dw, int V, Red& r) {
+  int lp = -1;
+  visit_row(dw.src(), dw.q, V, [&](int x, float sv, float qv) {
+    if (dw.fx_of(sv, qv)) lp = max(lp, x);
+  });
+  __syncthreads();
+  return block_max_i(lp, r);
 }
 
 // Exact fixed-point total and last positive id of the draw weights.
@@ -535,14 +589,12 @@ __global__ void __launch_bounds__(kT, 1) accept_seq_kernel(const AcceptParams p)
     dw.p = dist;
     dw.q = qb + static_cast<long long>(j) * V;
   }
-  unsigned long long total;
-  int last_pos;
-  weights_total(dw, V, red, total, last_pos);
-  if (dw.q && static_cast<double>(total) <= kResidualFallback * 4503599627370496.0) {
+  const float ug = __ldg(ub + gamma);
+  int t = draw(dw, V, ug, kTotalFromChunks, kLastPosLazy, red, true);
+  if (t == kDrawFallback) {
     dw.q = nullptr;  // residual mass numerically zero: draw from p
-    weights_total(dw, V, red, total, last_pos);
+    t = draw(dw, V, ug, kTotalFromChunks, kLastPosLazy, red);
   }
-  const int t = draw(dw, V, __ldg(ub + gamma), total, last_pos, red);
   if (threadIdx.x == 0) {
     out[j] = t < 0 ? 0 : t;
     p.n_acc[b] = j;
@@ -1040,12 +1092,15 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
             load_block(z, xs + kAPer * kAT, x1, zn);
 #pragma unroll
             for (int k = 0; k < kAPer; ++k) {
-              if (xs + threadIdx.x + k * kAT >= x1) break;
-              const float e = exp2f((zv[k] - m) * c);
+              // every lane takes part in each step (the peer sums below)
+              const bool valid = xs + static_cast<int>(threadIdx.x) + k * kAT < x1;
+              const float e = valid ? exp2f((zv[k] - m) * c) : 0.f;
               const uint32_t bits = __float_as_uint(e);
               const unsigned long long fx = static_cast<unsigned long long>(e * kFix40);
               mass += fx;
-              if ((bits & hi_mask) == prefix) atomicAdd(&wh[(bits >> shift) & 0xFFu], fx);
+              const int bkt =
+                  valid && (bits & hi_mask) == prefix ? static_cast<int>((bits >> shift) & 0xFFu) : -1;
+              hist_add_peers(wh, bkt, fx, 0xffffffffu);
             }
 #pragma unroll
             for (int k = 0; k < kAPer; ++k) zv[k] = zn[k];
@@ -1268,10 +1323,7 @@ __global__ void __launch_bounds__(kT, 1) sample_kernel(const SampleParams p) {
   DrawWeights dw;
   dw.p = dist;
   dw.q = nullptr;
-  unsigned long long total;
-  int last_pos;
-  weights_total(dw, V, red, total, last_pos);
-  const int t = draw(dw, V, __ldg(p.u + row), total, last_pos, red);
+  const int t = draw(dw, V, __ldg(p.u + row), kTotalFromChunks, kLastPosLazy, red);
   if (threadIdx.x == 0) p.tokens[row] = t < 0 ? 0 : t;
 }
 
@@ -1353,28 +1405,36 @@ __global__ void __launch_bounds__(kMaskThreads) mask_logits_kernel(float* logits
 // a leaf) one token is drawn from p' with u[0] and the walk ends.  T = 0: move
 // to the first child whose token is the argmax, else emit the argmax.
 //
-// p' starts as the softmax row itself (recomputed from the logits); the first
-// residual is materialised in pbuf (fp32) and later residuals replace it in
-// place.  Sums and the draw use the same 2^-52 fixed-point weights as the
-// chain rule.
+// p' starts as the softmax row itself (recomputed from the logits); the
+// residuals after rejected siblings are kept in closed form (below).  Sums
+// and the draw use the same 2^-52 fixed-point weights as the chain rule.
 
-// Draw weights of the tree walk: p' (the row, or pbuf once materialised),
-// minus q for a residual.
+// The current node's target distribution during the walk.  After k rejected
+// siblings (all drawn from the node's draft distribution q) the residual
+// p_k = norm(max(0, p_{k-1} - q)) has the closed form
+//   p_k = max(0, p - C_k q) / T_k,  C_k = C_{k-1} + T_{k-1},
+//   T_k = sum_x max(0, p - C_k q),  C_0 = 0, T_0 = 1,
+// (max(0, max(0, p - C q) / T - q) = max(0, p - (C + T) q) / T), so the walk
+// carries two scalars instead of materialising a row per rejection.
+// Weights: max(0, p - c q) with q set (unnormalised), p itself without.
 struct TreeWeights {
   RowDist p;
-  const float* pb;  // materialised p', or nullptr
-  const float* q;   // residual against q, or nullptr
-  SPEC_DEVINL const float* src() const { return pb ? pb : p.z; }
-  SPEC_DEVINL float base(int x) const { return pb ? __ldcg(pb + x) : p.p(x); }
+  const float* q;   // the node's draft distribution, or nullptr: p itself
+  float c;          // coefficient of q
+  float inv_t;      // 1 / sum of the weights (base() is a distribution)
+  SPEC_DEVINL const float* src() const { return p.z; }
   SPEC_DEVINL float w_of(float sv, float qv) const {
-    const float v = pb ? sv : p.p_of(sv);
-    return q ? fmaxf(v - qv, 0.f) : v;
+    const float v = p.p_of(sv);
+    return q ? fmaxf(v - c * qv, 0.f) : v;
+  }
+  SPEC_DEVINL float base(int x) const {
+    return q ? w_of(__ldcg(p.z + x), __ldcg(q + x)) * inv_t : p.p(x);
   }
   SPEC_DEVINL unsigned long long fx_of(float sv, float qv) const {
     return static_cast<unsigned long long>(w_of(sv, qv) * kFix52);
   }
   SPEC_DEVINL unsigned long long fx(int x) const {
-    return fx_of(__ldcg(src() + x), q ? __ldcg(q + x) : 0.f);
+    return fx_of(__ldcg(p.z + x), q ? __ldcg(q + x) : 0.f);
   }
 };
 
@@ -1430,13 +1490,13 @@ __global__ void __launch_bounds__(kT, 1) tree_accept_kernel(const TreeAcceptPara
   }
 
   const float* ub = p.u + row0;
-  float* pb = p.pbuf + static_cast<long long>(b) * V;
   for (;;) {
     const float* qrow = p.q + (row0 + cur) * V;
     TreeWeights tw;
     tw.p = make_dist(zb + static_cast<long long>(cur) * V, V, p.T, p.top_p, red, dyn_hist);
-    tw.pb = nullptr;
     tw.q = nullptr;
+    tw.c = 0.f;
+    tw.inv_t = 1.f;
     int nxt = -1;
     for (int c = cur + 1; c < n; ++c) {
       if (__ldg(par + c) != cur) continue;
@@ -1462,17 +1522,18 @@ __global__ void __launch_bounds__(kT, 1) tree_accept_kernel(const TreeAcceptPara
         break;
       }
       // rejected: p' <- norm(max(0, p' - q)) unless that mass is ~0
-      tw.q = qrow;
+      TreeWeights nx = tw;
+      const float t_cur = tw.q ? 1.f / tw.inv_t : 1.f;
+      nx.q = qrow;
+      nx.c = (tw.q ? tw.c : 0.f) + t_cur;
       unsigned long long total;
       int last_pos;
-      weights_total(tw, V, red, total, last_pos);
-      if (static_cast<double>(total) > kResidualFallback * 4503599627370496.0) {
-        const float inv = static_cast<float>(4503599627370496.0 / static_cast<double>(total));
-                visit_row(tw.src(), tw.q, V, [&](int x, float sv, float qv) { pb[x] = tw.w_of(sv, qv) * inv; });
-        __syncthreads();
-        tw.pb = pb;
+      weights_total(nx, V, red, total, last_pos);
+      const double t_new = static_cast<double>(total) / 4503599627370496.0;
+      if (t_new > kResidualFallback * static_cast<double>(t_cur)) {
+        nx.inv_t = static_cast<float>(1.0 / t_new);
+        tw = nx;
       }
-      tw.q = nullptr;
     }
     if (nxt >= 0) {
       if (threadIdx.x == 0) {
@@ -1483,10 +1544,7 @@ __global__ void __launch_bounds__(kT, 1) tree_accept_kernel(const TreeAcceptPara
       ++m;
       continue;
     }
-    unsigned long long total;
-    int last_pos;
-    weights_total(tw, V, red, total, last_pos);
-    const int t = draw(tw, V, __ldg(ub), total, last_pos, red);
+    const int t = draw(tw, V, __ldg(ub), kTotalFromChunks, kLastPosLazy, red);
     if (threadIdx.x == 0) {
       out[m] = t < 0 ? 0 : t;
       p.n_acc[b] = m;

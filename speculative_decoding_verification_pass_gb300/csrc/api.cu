@@ -1116,7 +1116,7 @@ int spec_mask_logits(float* d_logits, const uint32_t* d_allowed, int rows, int v
 
 size_t spec_tree_accept_workspace_bytes(int batch, int vocab) {
   if (batch < 0 || vocab <= 0) return 0;
-  return 64 + align_up(static_cast<size_t>(batch) * static_cast<size_t>(vocab) * 4);
+  return kAlign;  // the status word: the walk keeps its residuals in closed form
 }
 
 int spec_tree_accept(const float* d_target_logits, const float* d_draft_probs,
@@ -1141,7 +1141,6 @@ int spec_tree_accept(const float* d_target_logits, const float* d_draft_probs,
   p.tokens = d_node_tokens;
   p.parents = d_parents;
   p.u = d_uniforms;
-  p.pbuf = reinterpret_cast<float*>(static_cast<uint8_t*>(d_ws) + 64);
   p.out = d_out_tokens;
   p.path = d_out_path;
   p.n_acc = d_n_accepted;

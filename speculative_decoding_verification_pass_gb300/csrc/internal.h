@@ -256,7 +256,6 @@ struct TreeAcceptParams {
   const int32_t* tokens;   // [B][n] node tokens (node 0: the root)
   const int32_t* parents;  // [B][n] parent index, -1 for node 0
   const float* u;          // [B][n]: u[c] coin of child c, u[0] the final draw
-  float* pbuf;             // [B][V] the current node's residual target distribution
   int32_t* out;            // [B][n] accepted tokens, then the emitted token, -1 padding
   int32_t* path;           // [B][n] accepted nodes in depth order, -1 padding
   int32_t* n_acc;          // [B]
