@@ -611,7 +611,13 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       Q.ssq_ld = P.ssq_ld;
       const int grid = std::min(m->sm_count * cps, kMaxGrid);
       // key chunks per (sequence, KV head): about one attention unit per CTA
-      Q.att_nch = std::max(1, std::min(P.att_pairs, grid / std::max(1, batch * Hkv)));
+      // when that leaves at least 4 chunks per pair; a batch with fewer (its
+      // pairs alone fill the grid) takes about 4 units per CTA instead, so
+      // that one CTA does not walk a whole long sequence while others idle
+      const int pairs = std::max(1, batch * Hkv);
+      int nch = grid / pairs;
+      if (nch < 4) nch = (4 * grid + pairs - 1) / pairs;
+      Q.att_nch = std::max(1, std::min(P.att_pairs, nch));
       Q.eps = c.rms_eps;
       Q.inv_d = 1.0f / d;
       Q.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));

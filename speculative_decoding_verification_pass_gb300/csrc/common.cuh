@@ -31,6 +31,12 @@ SPEC_DEVINL unsigned long long ld_relaxed_u64(const unsigned long long* p) {
   return v;
 }
 
+// *p += v at GPU scope with release semantics: writes this thread has made
+// or observed (through a CTA barrier) are visible before the addition is.
+SPEC_DEVINL void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 SPEC_DEVINL uint32_t ld_acquire(const unsigned* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

@@ -338,16 +338,13 @@ SPEC_DEVINL bool fixup_tagged(unsigned long long* part, int ntok, int c0, int r,
 
 // The epilogue threads' writes of a phase are published by one release: the
 // CTA barrier orders every thread's writes before the arriving thread's
-// fence, and that fence before its arrival (the grid-barrier pattern of
-// cooperative groups).  Each thread orders its own generic-proxy writes before
+// release reduction (cumulative: it publishes what that thread has
+// observed through the barrier).  Each thread orders its own generic-proxy writes before
 // the next phase's TMA reads.
 SPEC_DEVINL void phase_arrive(const MkParams& P) {
   fence_proxy_async();
   named_bar(kArriveBar, kEpiThreads);
-  if (threadIdx.x == kEpiFirstThread) {
-    __threadfence();
-    atomicAdd(P.bar, 1u);
-  }
+  if (threadIdx.x == kEpiFirstThread) red_release_add(P.bar, 1u);
 }
 
 // All epilogue threads wait for phase `ph - 1` to be complete: one thread
@@ -1111,6 +1108,14 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
             }
             for (int c0 = 0; c0 < p.ntok; c0 += 16) {
               float acc[16];
+              // wide batches: this chunk's residual values requested before
+              // the contributors' words, so the two round trips overlap
+              if (p.epi == EPI_RESID && !pre_h) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  hv[j] = (c0 + j < p.M && f < p.N) ? __ldcg(p.h + static_cast<long long>(c0 + j) * p.d + f)
+                                                    : 0.f;
+              }
               load_acc(tacc, c0, p.ntok, 1, acc);
               if (nc > 1) {
                 const bool ok = p.M - c0 <= 8 ? fixup_tagged<8, 5>(part64, p.ntok, c0, r, c_first, nc,
@@ -1119,7 +1124,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
                                                                     sm.slots, acc, tag, sm.abort, P.status);
                 if (!ok) break;
               }
-              epilogue_chunk_h<kPaged ? 2 : 1>(p, gs, t, r, c0, acc, hv, pre_h, pre);
+              epilogue_chunk_h<kPaged ? 2 : 1>(p, gs, t, r, c0, acc, hv, p.epi == EPI_RESID, pre);
             }
           }
           tc_fence_before();

@@ -207,6 +207,7 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
     const int warp = (threadIdx.x >> 5) & 3;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
+      if (p.tok0 + c0 + j >= p.M) break;  // uniform: no valid column left
       const float s = warp_sum(sq[j]);
       if ((threadIdx.x & 31) == 0) sm.red[warp * 16 + j] = s;
     }
