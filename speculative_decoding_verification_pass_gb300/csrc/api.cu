@@ -86,6 +86,23 @@ bool mk_enabled() {
   return !(e && e[0] == '0');
 }
 
+// Key chunks per (sequence, KV head) of the persistent forward's attention:
+// about one unit per CTA when that leaves at least 4 chunks per pair; a batch
+// with fewer (its pairs alone nearly fill the grid) takes about 4 units per
+// CTA instead, so that one CTA does not walk a whole long sequence while
+// others idle.  Monotonic in the grid size.
+int mk_att_chunks(int grid, int pairs) {
+  pairs = std::max(1, pairs);
+  const int nch = grid / pairs;
+  return std::max(1, nch >= 4 ? nch : (4 * grid + pairs - 1) / pairs);
+}
+// The most chunks any grid up to kMaxGrid uses (the workspace's partials),
+// at most one per 64 cache slots.
+int mk_att_chunks_max(int pairs, int slot_chunks) {
+  const int p = std::max(1, pairs);
+  return std::max(1, std::min(slot_chunks, std::max(kMaxGrid / p, (4 * kMaxGrid + p - 1) / p)));
+}
+
 size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -225,8 +242,8 @@ WsPlan plan_ws(const spec_model_config& c, int B, int gamma, int cap) {
   const size_t rows = c.n_layers ? static_cast<size_t>(B) * Hkv * p.splits * p.R : 0;
   p.apart_o = take(rows * hd * 4);
   p.apart_ml = take(rows * 2 * 4);
-  p.att_pairs = (std::max(cap, 1) + 63) / 64;
-  const size_t urows = c.n_layers ? static_cast<size_t>(B) * Hkv * p.att_pairs * 32 : 0;
+  p.att_pairs = mk_att_chunks_max(B * Hkv, (std::max(cap, 1) + 63) / 64);
+  const size_t urows = c.n_layers ? static_cast<size_t>(B) * Hkv * p.att_pairs * kMkAttRows : 0;
   p.mk_att_o = take(urows * hd * 4);
   p.mk_att_ml = take(urows * 2 * 4);
   p.total = o;
@@ -563,7 +580,7 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
   {
     const int ntok = round_up(M, 16);
     const int fpt = d / 128;
-    const bool shape_ok = mk_enabled() && M <= 128 && P.R <= 32 && c.n_layers <= kMkMaxLayers &&
+    const bool shape_ok = mk_enabled() && M <= 128 && P.R <= kMkAttRows && c.n_layers <= kMkMaxLayers &&
                           (fpt & (fpt - 1)) == 0 && fpt <= 128;
     // one CTA per SM with a deep ring (the ring also absorbs grid barriers)
     int stages = shape_ok ? forward_max_stages(ntok, hd, static_cast<size_t>(mk_smem_kb()) * 1024) : 0;
@@ -610,14 +627,7 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       Q.stages = stages;
       Q.ssq_ld = P.ssq_ld;
       const int grid = std::min(m->sm_count * cps, kMaxGrid);
-      // key chunks per (sequence, KV head): about one attention unit per CTA
-      // when that leaves at least 4 chunks per pair; a batch with fewer (its
-      // pairs alone fill the grid) takes about 4 units per CTA instead, so
-      // that one CTA does not walk a whole long sequence while others idle
-      const int pairs = std::max(1, batch * Hkv);
-      int nch = grid / pairs;
-      if (nch < 4) nch = (4 * grid + pairs - 1) / pairs;
-      Q.att_nch = std::max(1, std::min(P.att_pairs, nch));
+      Q.att_nch = std::min(P.att_pairs, mk_att_chunks(grid, batch * Hkv));
       Q.eps = c.rms_eps;
       Q.inv_d = 1.0f / d;
       Q.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));

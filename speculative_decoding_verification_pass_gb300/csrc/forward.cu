@@ -548,7 +548,7 @@ SPEC_DEVINL void att_prefetch(const MkParams& P, const MkSmem& sm, int l) {
 // (qt): scores with q as bf16 hi/lo, the online softmax, P (hi/lo) times V.
 template <int HD>
 SPEC_DEVINL void att_block(const MkParams& P, const KVLayout& lay, uint32_t aQ, uint32_t aQlo, int kb,
-                           int kend, int Lb, int b, int R, int G, int slot, int qt, int lane,
+                           int kend, int Lb, int b, int R, int G, int rbase, int slot, int qt, int lane,
                            float (&mrow)[2], float (&lrow)[2], float (&oacc)[HD / 8][4]) {
   const int g8 = lane >> 2, t4 = lane & 3;
   const int k0 = kb + slot * kAttBlockKeys;
@@ -577,7 +577,7 @@ SPEC_DEVINL void att_block(const MkParams& P, const KVLayout& lay, uint32_t aQ, 
   }
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
-    const int r = qt * 16 + g8 + hr * 8;
+    const int r = rbase + qt * 16 + g8 + hr * 8;  // the query row of the unit
     const bool rv = r < R;
     const int jn = rv ? r / G : 0;
     const uint64_t am = (P.anc && rv) ? __ldg(P.anc + static_cast<long long>(b) * P.n + jn) : 0ull;
@@ -670,18 +670,18 @@ SPEC_DEVINL void cmb_phase(const MkParams& P) {
     const int ck = att_chunk_keys(Tk, nch);
     const int nu = (Tk + ck - 1) / ck;
     const long long ubase = (static_cast<long long>(b) * P.Hkv + kvh) * nch;
-    const float2* ob = reinterpret_cast<const float2*>(P.att_o + (ubase * 32 + r) * HD + dg * 64) + lane;
+    const float2* ob = reinterpret_cast<const float2*>(P.att_o + (ubase * kMkAttRows + r) * HD + dg * 64) + lane;
     float2 acc = make_float2(0.f, 0.f);
     float lsum = 0.f, m = -INFINITY;
     for (int u0 = 0; u0 < nu; u0 += 32) {
       // lane k holds unit u0 + k's (max, sum); the o loads of the 32 units
       // below do not depend on them
       const int cnt = min(32, nu - u0);
-      const float2 mv = lane < cnt ? __ldcg(&mlp[(ubase + u0 + lane) * 32 + r]) : make_float2(-INFINITY, 0.f);
+      const float2 mv = lane < cnt ? __ldcg(&mlp[(ubase + u0 + lane) * kMkAttRows + r]) : make_float2(-INFINITY, 0.f);
       float2 ov[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k)
-        ov[k] = k < cnt ? __ldcg(ob + static_cast<long long>(u0 + k) * 32 * HD / 2) : make_float2(0.f, 0.f);
+        ov[k] = k < cnt ? __ldcg(ob + static_cast<long long>(u0 + k) * kMkAttRows * HD / 2) : make_float2(0.f, 0.f);
       const float mb = warp_max(mv.x);
       const float mn = fmaxf(m, mb);
       const float scale = m == -INFINITY ? 0.f : exp2f(m - mn);
@@ -732,26 +732,30 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
   const int nch = P.att_nch;
   const int units = P.B * P.Hkv * nch;
   const int g8 = lane >> 2, t4 = lane & 3;
-  const bool active = qt * 16 < R;
   for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
     AttUnit u;
     if (!att_unit(P, unit, u)) continue;  // uniform across the CTA
-    const bool first = unit == static_cast<int>(blockIdx.x);
+    // query rows in passes of 32 (two tiles of 16); the unit's key blocks
+    // are loaded again for each pass
+    for (int rbase = 0; rbase < R; rbase += 32) {
+    const bool first = unit == static_cast<int>(blockIdx.x) && rbase == 0;
     // block 0: the cached rows were prefetched for the first unit; block 1
     // into the activation areas at once
     att_load_block<HD, kPaged>(stage_lay, kc, vc, map, u.b, u.kvh, u.kbeg, u.kend, u.Lb, first ? 2 : 0, e);
     const bool staged1 = two && u.kbeg + kAttUnitKeys < u.kend;
     if (staged1)
       att_load_block<HD, kPaged>(act_lay, kc, vc, map, u.b, u.kvh, u.kbeg + kAttUnitKeys, u.kend, u.Lb, 0, e);
-    // q (hi, lo) rows with async copies (zero rows past R)
+    // q (hi, lo) rows rbase .. rbase + 31 with async copies (zero rows past R)
     for (int idx = e; idx < 32 * kCPR; idx += kEpiThreads) {
       const int r = idx / kCPR, c = idx % kCPR;
-      const bool valid = r < R;
-      const int j = valid ? r / G : 0, g = valid ? r % G : 0;
+      const int rr = rbase + r;
+      const bool valid = rr < R;
+      const int j = valid ? rr / G : 0, g = valid ? rr % G : 0;
       const long long off = (static_cast<long long>(u.b) * P.n + j) * qdim + (u.kvh * G + g) * HD + c * 8;
       cp_async16(aQ + swz<HD>(r, c), P.q + off, valid ? 16 : 0);
       cp_async16(aQlo + swz<HD>(r, c), P.q_lo + off, valid ? 16 : 0);
     }
+    const bool active = rbase + qt * 16 < R;
     float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
     float oacc[HD / 8][4];
 #pragma unroll
@@ -767,8 +771,8 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
         named_bar(kArriveBar, kEpiThreads);
       }
       if (active)
-        att_block<HD>(P, in_act ? act_lay : stage_lay, aQ, aQlo, kb, u.kend, u.Lb, u.b, R, G, slot, qt,
-                      lane, mrow, lrow, oacc);
+        att_block<HD>(P, in_act ? act_lay : stage_lay, aQ, aQlo, kb, u.kend, u.Lb, u.b, R, G, rbase, slot,
+                      qt, lane, mrow, lrow, oacc);
     }
     // ---- merge the two slots: slot 1 through shared memory
     named_bar(kArriveBar, kEpiThreads);  // the q area becomes the merge buffer
@@ -795,13 +799,13 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int rr = g8 + hr * 8;
-        const int r = qt * 16 + rr;
+        const int r = rbase + qt * 16 + rr;
         const float m1 = mm[rr], l1 = mm[16 + rr];
         const float mn = fmaxf(mrow[hr], m1);
         const float s0 = mrow[hr] == -INFINITY ? 0.f : exp2f(mrow[hr] - mn);
         const float s1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mn);
         if (r < R) {
-          float* dst = P.att_o + (ubase * 32 + r) * HD;
+          float* dst = P.att_o + (ubase * kMkAttRows + r) * HD;
 #pragma unroll
           for (int nd = 0; nd < HD / 8; ++nd) {
             const int c = nd * 8 + t4 * 2;
@@ -814,12 +818,13 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
             float2 ml;
             ml.x = mn;
             ml.y = lrow[hr] * s0 + l1 * s1;
-            __stcg(reinterpret_cast<float2*>(P.att_ml + (ubase * 32 + r) * 2), ml);
+            __stcg(reinterpret_cast<float2*>(P.att_ml + (ubase * kMkAttRows + r) * 2), ml);
           }
         }
       }
     }
-    named_bar(kArriveBar, kEpiThreads);  // shared memory free for the next unit
+    named_bar(kArriveBar, kEpiThreads);  // shared memory free for the next pass
+    }
   }
   // the activation areas go back to the TMA loads of the O phase
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -127,6 +127,7 @@ int attention_cluster_size(int hd, int cap, size_t smem_limit);
 
 // --------------------------------------------------- persistent decode forward
 constexpr int kMkMaxLayers = 48;
+constexpr int kMkAttRows = 64;  // query rows per (sequence, KV head) of the persistent forward
 struct MkParams {
   CUtensorMap xmap[6];                    // hb, hb_lo, o, o_lo, act, act_lo (box rows = ntok)
   CUtensorMap wmap[4 * kMkMaxLayers + 1]; // per layer W_qkv, W_o, W_gu, W_d; then the LM head
@@ -160,8 +161,8 @@ struct MkParams {
   int32_t* seq_ok;
   const uint64_t* anc;                    // [B][n] draft-tree ancestor masks, or nullptr (chain)
   const int32_t* depth;                   // [B][n] draft-tree node depths, or nullptr (chain)
-  float* att_o;                           // [B][Hkv][att_nch][32][hd] chunk partials
-  float* att_ml;                          // [B][Hkv][att_nch][32][2] (max, sum)
+  float* att_o;                           // [B][Hkv][att_nch][kMkAttRows][hd] chunk partials
+  float* att_ml;                          // [B][Hkv][att_nch][kMkAttRows][2] (max, sum)
 };
 size_t forward_smem_bytes(int ntok, int stages, int hd);
 int forward_max_stages(int ntok, int hd, size_t budget);
