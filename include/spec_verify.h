@@ -244,7 +244,9 @@ size_t spec_accept_workspace_bytes(int batch, int gamma, int vocab);
  *                   ties), emit the argmax at the first mismatch or the bonus.
  *   top_p           in (0, 1]; 1 disables the nucleus.  The nucleus keeps every
  *                   token whose probability is >= that of the token where the
- *                   descending cumulative mass first reaches top_p.
+ *                   descending cumulative mass first reaches top_p.  With
+ *                   top_p < 1 the vocabulary is limited to 2^21 ids (else
+ *                   SPEC_ESIZE; also for spec_draft_sample and spec_tree_accept).
  *   d_out_tokens    int32 [batch][gamma+1]: x_1..x_n, then the correction or
  *                   bonus token, then -1 padding.
  *   d_n_accepted    int32 [batch].

@@ -243,30 +243,34 @@ struct RowDist {
   SPEC_DEVINL float p(int x) const { return p_of(__ldcg(z + x)); }
 };
 
-// Add fx into bin `bkt` of a warp's histogram (bkt < 0: nothing), the lanes
-// that hold the same bin summed first: one shared-memory atomic per distinct
-// bin instead of one per lane (the first digit of e(x) = 2^((z - m) / T)
-// falls into a handful of exponent bins, so per-lane atomics serialise).
-// fx <= 2^40 (a probability in 2^-40 fixed point): the 20-bit halves of up
-// to 32 such values sum exactly in 32 bits.  Called by every lane of
-// `lanes` together (the lanes converged at the call).
-SPEC_DEVINL void hist_add_peers(unsigned long long* wh, int bkt, unsigned long long fx,
-                                unsigned lanes) {
-  const unsigned peers = __match_any_sync(lanes, bkt);
-  const unsigned lo = __reduce_add_sync(peers, static_cast<unsigned>(fx & 0xFFFFFull));
-  const unsigned hi = __reduce_add_sync(peers, static_cast<unsigned>(fx >> 20));
-  if (bkt >= 0 && static_cast<int>(threadIdx.x & 31) == __ffs(peers) - 1)
-    atomicAdd(&wh[bkt], (static_cast<unsigned long long>(hi) << 20) + lo);
+// Nucleus histogram bins of 2^-40 fixed-point masses (fx <= 2^40), kept as
+// three 14-bit limbs in 32-bit counters: 32-bit shared-memory atomics are
+// native, 64-bit ones several times slower.  A bin set is [3][256] counters
+// shared by a pair of warps; the limb sums stay below 2^32 while a bin set
+// takes at most 2^18 ids per pass, and reassemble exactly.
+constexpr int kLimbBits = 14;
+constexpr unsigned kLimbMask = (1u << kLimbBits) - 1u;
+constexpr int kMaxIdsPerBins = 1 << 18;  // a bin set serves 1/8 (grid) or 1/16 of a row
+static_assert(kNucleusMaxVocab / 8 <= kMaxIdsPerBins, "nucleus bin limbs would overflow");
+SPEC_DEVINL void bins_add(unsigned* bins, int bkt, unsigned long long fx) {
+  atomicAdd(bins + bkt, static_cast<unsigned>(fx) & kLimbMask);
+  atomicAdd(bins + 256 + bkt, static_cast<unsigned>(fx >> kLimbBits) & kLimbMask);
+  atomicAdd(bins + 512 + bkt, static_cast<unsigned>(fx >> (2 * kLimbBits)));
+}
+SPEC_DEVINL unsigned long long bins_get(const unsigned* bins, int bkt) {
+  return static_cast<unsigned long long>(bins[bkt]) +
+         (static_cast<unsigned long long>(bins[256 + bkt]) << kLimbBits) +
+         (static_cast<unsigned long long>(bins[512 + bkt]) << (2 * kLimbBits));
 }
 
-// Per-warp histograms of the nucleus radix select (dynamic shared memory of
-// the per-sequence kernels): each warp adds into its own 256 bins, so lanes
-// contend only within their warp, then the warps' bins are summed.
-constexpr size_t kHistBytes = static_cast<size_t>(kWarps) * 256 * sizeof(unsigned long long);
+// Histograms of the nucleus radix select (dynamic shared memory of the
+// per-sequence kernels): one bin set per pair of warps, summed afterwards.
+constexpr int kBinSets = kWarps / 2;
+constexpr size_t kHistBytes = static_cast<size_t>(kBinSets) * 3 * 256 * sizeof(unsigned);
 
 // Softmax statistics and (top_p < 1) the nucleus threshold of one row.
 __device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r,
-                             unsigned long long* whist) {
+                             unsigned* whist) {
   RowDist d;
   d.z = z;
   d.c = kLog2e / T;
@@ -288,19 +292,19 @@ __device__ RowDist make_dist(const float* z, int V, float T, float top_p, Red& r
   for (int level = 0; level < 4; ++level) {
     const int shift = 24 - 8 * level;
     const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
-    unsigned long long* wh = whist + (threadIdx.x >> 5) * 256;
-    for (int i = threadIdx.x & 31; i < 256; i += 32) wh[i] = 0ull;
-    __syncwarp();
+    unsigned* wh = whist + (threadIdx.x >> 6) * 3 * 256;
+    for (int i = threadIdx.x; i < kBinSets * 3 * 256; i += kT) whist[i] = 0u;
+    __syncthreads();
     visit_row(z, nullptr, V, [&](int, float zv, float) {
       const float v = d.e_of(zv);
       const uint32_t bits = __float_as_uint(v);
-      const int bkt = (bits & hi_mask) == prefix ? static_cast<int>((bits >> shift) & 0xFFu) : -1;
-      hist_add_peers(wh, bkt, static_cast<unsigned long long>(v * kFix40), __activemask());
+      if ((bits & hi_mask) == prefix)
+        bins_add(wh, static_cast<int>((bits >> shift) & 0xFFu), static_cast<unsigned long long>(v * kFix40));
     });
     __syncthreads();
     for (int i = threadIdx.x; i < 256; i += kT) {
       unsigned long long t = 0;
-      for (int w = 0; w < kWarps; ++w) t += whist[w * 256 + i];
+      for (int w = 0; w < kBinSets; ++w) t += bins_get(whist + w * 3 * 256, i);
       r.hist[i] = t;
     }
     __syncthreads();
@@ -526,7 +530,7 @@ __device__ void weights_total(const DW& dw, int V, Red& r, unsigned long long& t
 // visited lazily up to the first rejection.
 __global__ void __launch_bounds__(kT, 1) accept_seq_kernel(const AcceptParams p) {
   __shared__ Red red;
-  extern __shared__ unsigned long long dyn_hist[];  // kHistBytes
+  extern __shared__ unsigned dyn_hist[];  // kHistBytes
   __shared__ int s_flag;
   const int b = blockIdx.x;
   const int gamma = p.gamma, V = p.V, n = gamma + 1;
@@ -606,9 +610,10 @@ __global__ void __launch_bounds__(kT, 1) accept_seq_kernel(const AcceptParams p)
 // chunk) units, phases separated by grid-wide barriers:
 //   P1  per chunk: online (max, sum exp2) of z / T, or (greedy) the chunk's
 //       argmax; with top_p < 1 the nucleus histograms and totals are cleared.
-//   N0..N3, NZ (top_p < 1 only)  the mass-weighted radix select of the
-//       nucleus threshold over global integer histograms (one 8-bit digit per
-//       phase), then each chunk's kept mass.
+//   N0..N3 (top_p < 1 only)  the mass-weighted radix select of the nucleus
+//       threshold over global integer histograms (one 8-bit digit per phase;
+//       the last digit is chosen where the row statistics are merged, and the
+//       kept mass is the mass above the threshold plus its own bin).
 //   P2  per (sequence, chunk): every unit takes the same accept decisions
 //       (they only need the merged row statistics and one id per row) and
 //       sums the chunk's 2^-52 fixed-point draw weights (residual and p).
@@ -627,7 +632,7 @@ struct ASmem {
   float g[kAW];
   int i[kAW];
   unsigned long long u[kAW];
-  unsigned long long hist[kAW][256];  // one nucleus histogram per warp
+  unsigned hist[kAW / 2][3 * 256];  // nucleus bins: one set per pair of warps
   float rm[kMaxRows];   // row max (greedy: argmax value)
   float rz[kMaxRows];   // row normaliser (kept mass with a nucleus)
   float rtau[kMaxRows]; // nucleus threshold on e(x) (0: none)
@@ -807,13 +812,6 @@ SPEC_DEVINL float2 warp_row_ms(const float2* part, int S, float c) {
   return make_float2(m, sum);
 }
 
-// One warp: fixed-order sum of S floats.
-SPEC_DEVINL float warp_sum_parts(const float* part, int S) {
-  float t = 0.f;
-  for (int k = threadIdx.x & 31; k < S; k += 32) t += __ldcg(part + k);
-  return warp_sum(t);
-}
-
 // One warp: one digit of the mass-weighted radix select.  Among the 256
 // buckets of `hist` (values sharing the digits chosen so far), scanning from
 // the top with `above` = the mass strictly above them, pick the first bucket
@@ -902,9 +900,16 @@ __device__ void seq_stats(const AcceptParams& p, int b, float c, bool nucleus, A
     const float2 ms = warp_row_ms(p.part_ms + row * p.S, p.S, c);
     float Z = ms.y, tau = 0.f;
     if (nucleus) {
-      const int SL = nucleus_split(p);
-      Z = warp_sum_parts(p.part_z + row * SL, SL);
-      tau = __uint_as_float(static_cast<uint32_t>(__ldcg(p.sel + (row * 4 + 3) * 2)));
+      // the last digit of the threshold, and the kept mass: everything
+      // strictly above it plus its own bin, from the exact histograms
+      unsigned long long above = __ldcg(p.sel + (row * 4 + 2) * 2 + 1);
+      const uint32_t prefix = static_cast<uint32_t>(__ldcg(p.sel + (row * 4 + 2) * 2));
+      const unsigned long long tot = __ldcg(p.tot40 + row);
+      const double target = static_cast<double>(p.top_p) * static_cast<double>(tot);
+      const int chosen = warp_select(p.hist + (row * 4 + 3) * 256, target, above);
+      const unsigned long long kept = above + __ldcg(p.hist + (row * 4 + 3) * 256 + chosen);
+      Z = static_cast<float>(static_cast<double>(kept < tot ? kept : tot) / 1099511627776.0);
+      tau = __uint_as_float(prefix | static_cast<uint32_t>(chosen));
     }
     if (l == 0) {
       s.rm[i] = ms.x;
@@ -1042,11 +1047,11 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
     return;
   }
 
-  // ---- N0..N3, NZ: the nucleus threshold of every row
+  // ---- N0..N3: the digits of the nucleus threshold of every row
   if (nucleus) {
     const int SL = nucleus_split(p);
     const long long units_l = static_cast<long long>(B) * n * SL;
-    for (int level = 0; level <= 4; ++level) {
+    for (int level = 0; level <= 3; ++level) {
       for (long long u = blockIdx.x; u < units_l; u += G) {
         const int kr = static_cast<int>(u % SL);
         const long long row = u / SL;
@@ -1075,16 +1080,16 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
             s.prefix = prefix;
           }
         }
-        for (int k = threadIdx.x; k < kAW * 256; k += kAT) (&s.hist[0][0])[k] = 0ull;
+        for (int k = threadIdx.x; k < kAW / 2 * 3 * 256; k += kAT) (&s.hist[0][0])[k] = 0u;
         __syncthreads();
         const float m = s.bf[0];
         const uint32_t prefix = s.prefix;
-        if (level < 4) {
+        {
           const int shift = 24 - 8 * level;
           const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
           unsigned long long mass = 0;
-          // this warp's histogram: same-bucket atomics contend within the warp only
-          unsigned long long* wh = s.hist[threadIdx.x >> 5];
+          // this warp pair's bins: same-bin atomics contend within the pair only
+          unsigned* wh = s.hist[threadIdx.x >> 6];
           float zv[kAPer];
           load_block(z, x0, x1, zv);
           for (int xs = x0; xs < x1; xs += kAPer * kAT) {
@@ -1098,9 +1103,7 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
               const uint32_t bits = __float_as_uint(e);
               const unsigned long long fx = static_cast<unsigned long long>(e * kFix40);
               mass += fx;
-              const int bkt =
-                  valid && (bits & hi_mask) == prefix ? static_cast<int>((bits >> shift) & 0xFFu) : -1;
-              hist_add_peers(wh, bkt, fx, 0xffffffffu);
+              if (valid && (bits & hi_mask) == prefix) bins_add(wh, static_cast<int>((bits >> shift) & 0xFFu), fx);
             }
 #pragma unroll
             for (int k = 0; k < kAPer; ++k) zv[k] = zn[k];
@@ -1113,28 +1116,9 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
           for (int k = threadIdx.x; k < 256; k += kAT) {
             unsigned long long t = 0;  // integer sums: exact in any order
 #pragma unroll
-            for (int w = 0; w < kAW; ++w) t += s.hist[w][k];
+            for (int w = 0; w < kAW / 2; ++w) t += bins_get(s.hist[w], k);
             if (t) atomicAdd(p.hist + (row * 4 + level) * 256 + k, t);
           }
-        } else {
-          const float tau = __uint_as_float(prefix);
-          float kept = 0.f;
-          float zv[kAPer];
-          load_block(z, x0, x1, zv);
-          for (int xs = x0; xs < x1; xs += kAPer * kAT) {
-            float zn[kAPer];
-            load_block(z, xs + kAPer * kAT, x1, zn);
-#pragma unroll
-            for (int k = 0; k < kAPer; ++k) {
-              if (xs + threadIdx.x + k * kAT >= x1) break;
-              const float e = exp2f((zv[k] - m) * c);
-              kept += e >= tau ? e : 0.f;
-            }
-#pragma unroll
-            for (int k = 0; k < kAPer; ++k) zv[k] = zn[k];
-          }
-          kept = ablock_sum_f(kept, s);
-          if (threadIdx.x == 0) p.part_z[u] = kept;
         }
         __syncthreads();
       }
@@ -1305,7 +1289,7 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
 
 __global__ void __launch_bounds__(kT, 1) sample_kernel(const SampleParams p) {
   __shared__ Red red;
-  extern __shared__ unsigned long long dyn_hist[];  // kHistBytes
+  extern __shared__ unsigned dyn_hist[];  // kHistBytes
   const int row = blockIdx.x;
   const int V = p.V;
   const float* z = p.logits + static_cast<long long>(row) * V;
@@ -1440,7 +1424,7 @@ struct TreeWeights {
 
 __global__ void __launch_bounds__(kT, 1) tree_accept_kernel(const TreeAcceptParams p) {
   __shared__ Red red;
-  extern __shared__ unsigned long long dyn_hist[];  // kHistBytes
+  extern __shared__ unsigned dyn_hist[];  // kHistBytes
   __shared__ int s_flag;
   const int b = blockIdx.x;
   const int n = p.n, V = p.V;

@@ -971,7 +971,7 @@ namespace {
 // partials of the cooperative accept grid, sized for the largest chunk count
 // a launch may choose.
 struct AcceptWs {
-  size_t bar, part_ms, tot40, hist, sel, part_z, part_tot, part_last, total;
+  size_t bar, part_ms, tot40, hist, sel, part_tot, part_last, total;
   int s_max;
 };
 
@@ -1000,7 +1000,6 @@ AcceptWs plan_accept(int B, int gamma, int V) {
   w.tot40 = take(B * n * 8);
   w.hist = take(B * n * 4 * 256 * 8);
   w.sel = take(B * n * 4 * 2 * 8);
-  w.part_z = take(B * n * S * 4);
   w.part_tot = take(B * S * 2 * 8);
   w.part_last = take(B * S * 2 * 4);
   w.total = off;
@@ -1036,6 +1035,8 @@ static int accept_common_checks(int batch, int gamma, int vocab, float T, float 
   if (batch < 0 || gamma < 0 || vocab <= 0) return SPEC_EINVAL;
   if (!(T >= 0.f) || std::isinf(T)) return SPEC_EINVAL;
   if (!(top_p > 0.f && top_p <= 1.f)) return SPEC_EINVAL;
+  // the nucleus select's exact 32-bit bin limbs hold up to 2^21 ids a row
+  if (top_p < 1.f && vocab > kNucleusMaxVocab) return SPEC_ESIZE;
   return SPEC_OK;
 }
 
@@ -1070,7 +1071,6 @@ int spec_accept(const float* d_target_logits, const float* d_draft_probs,
   p.tot40 = reinterpret_cast<unsigned long long*>(W + A.tot40);
   p.hist = reinterpret_cast<unsigned long long*>(W + A.hist);
   p.sel = reinterpret_cast<unsigned long long*>(W + A.sel);
-  p.part_z = reinterpret_cast<float*>(W + A.part_z);
   p.part_tot = reinterpret_cast<unsigned long long*>(W + A.part_tot);
   p.part_last = reinterpret_cast<int*>(W + A.part_last);
   p.logits = d_target_logits;

@@ -203,6 +203,7 @@ cudaError_t launch_wait_probe(const unsigned* ctr, unsigned target, unsigned lon
 constexpr int kAcceptMaxChunk = 4096;  // vocabulary ids per accept work unit
 constexpr int kAcceptMaxRows = 128;    // gamma + 1 per sequence
 constexpr int kAcceptGridRows = 1024;  // batch * (gamma + 1) of the grid schedule
+constexpr int kNucleusMaxVocab = 1 << 21;  // vocabulary limit of top_p < 1
 struct AcceptParams {
   const float* logits;   // [B][gamma+1][V]
   const float* q;        // [B][gamma][V]
@@ -216,7 +217,6 @@ struct AcceptParams {
   unsigned long long* tot40;     // [B][n] nucleus mass (2^-40 fixed point)
   unsigned long long* hist;      // [B][n][4][256] radix-select histograms
   unsigned long long* sel;       // [B][n][4][2] (prefix, mass above) per digit
-  float* part_z;                 // [B][n][S] kept mass per chunk
   unsigned long long* part_tot;  // [B][S][2] draw-weight sums (residual, p)
   int* part_last;                // [B][S][2] last id with positive weight
   int B, gamma, V, S, C;         // S chunks of C ids (C <= kAcceptMaxChunk)
