@@ -668,20 +668,22 @@ SPEC_DEVINL bool agrid_sync(const AcceptParams& p, unsigned target, ASmem& s) {
 // Block (max, sum exp2((z - max) c)) over ids [x0, x1), fixed merge order.
 __device__ float2 chunk_ms(const float* z, int x0, int x1, float c, ASmem& s) {
   float m = -INFINITY, sum = 0.f;
-  float zv[kAPer];  // this thread's ids x0 + threadIdx.x + k kAT, loaded together
+  for (int xs = x0; xs < x1; xs += kAPer * kAT) {
+    float zv[kAPer];  // this thread's ids xs + threadIdx.x + k kAT, loaded together
 #pragma unroll
-  for (int k = 0; k < kAPer; ++k) {
-    const int x = x0 + threadIdx.x + k * kAT;
-    zv[k] = x < x1 ? __ldcg(z + x) : -INFINITY;
-  }
+    for (int k = 0; k < kAPer; ++k) {
+      const int x = xs + threadIdx.x + k * kAT;
+      zv[k] = x < x1 ? __ldcg(z + x) : -INFINITY;
+    }
 #pragma unroll
-  for (int k = 0; k < kAPer; ++k) {
-    const float v = zv[k];
-    if (v > m) {
-      sum = (m == -INFINITY ? 0.f : sum * exp2f((m - v) * c)) + 1.0f;
-      m = v;
-    } else if (v != -INFINITY) {  // masked-out logits (-inf) weigh nothing
-      sum += exp2f((v - m) * c);
+    for (int k = 0; k < kAPer; ++k) {
+      const float v = zv[k];
+      if (v > m) {
+        sum = (m == -INFINITY ? 0.f : sum * exp2f((m - v) * c)) + 1.0f;
+        m = v;
+      } else if (v != -INFINITY) {  // masked-out logits (-inf) weigh nothing
+        sum += exp2f((v - m) * c);
+      }
     }
   }
 #pragma unroll
@@ -886,10 +888,10 @@ SPEC_DEVINL void load_block(const float* z, int xs, int x1, float (&zv)[kAPer]) 
 // Id ranges per row of the nucleus select's work units: about one unit per
 // CTA, so that a unit's fixed costs (the row's statistics and the digits
 // chosen so far, read by one warp; block barriers) are paid once per range.
-SPEC_DEVINL int nucleus_split(const AcceptParams& p) {
-  const int rows = p.B * (p.gamma + 1);
-  return max(1, min(p.S, static_cast<int>(gridDim.x) / max(rows, 1)));
-}
+// Units per row of the chunk statistics (P1) and of the nucleus select,
+// chosen by the launcher for the grid it launches.
+SPEC_DEVINL int stats_split(const AcceptParams& p) { return p.S1; }
+SPEC_DEVINL int nucleus_split(const AcceptParams& p) { return p.SL; }
 
 // Statistics of every row of sequence b into shared memory (all warps).
 __device__ void seq_stats(const AcceptParams& p, int b, float c, bool nucleus, ASmem& s) {
@@ -897,7 +899,7 @@ __device__ void seq_stats(const AcceptParams& p, int b, float c, bool nucleus, A
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   for (int i = w; i < n; i += kAW) {
     const long long row = static_cast<long long>(b) * n + i;
-    const float2 ms = warp_row_ms(p.part_ms + row * p.S, p.S, c);
+    const float2 ms = warp_row_ms(p.part_ms + row * p.S, stats_split(p), c);
     float Z = ms.y, tau = 0.f;
     if (nucleus) {
       // the last digit of the threshold, and the kept mass: everything
@@ -999,13 +1001,15 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
          k < static_cast<long long>(B) * n; k += static_cast<long long>(G) * kAT)
       p.tot40[k] = 0ull;
   }
-  const long long units1 = static_cast<long long>(B) * n * S;
+  const int S1 = stats_split(p);  // P1 units per row
+  const long long units1 = static_cast<long long>(B) * n * S1;
   for (long long u = blockIdx.x; u < units1; u += G) {
-    const int ch = static_cast<int>(u % S);
-    const long long row = u / S;
+    const int k = static_cast<int>(u % S1);
+    const long long row = u / S1;
     const float* z = p.logits + row * V;
-    const int x0 = ch * C, x1 = min(x0 + C, V);
-    p.part_ms[u] = greedy ? chunk_argmax(z, x0, x1, s) : chunk_ms(z, x0, x1, c, s);
+    const int x0 = static_cast<int>(static_cast<long long>(k) * V / S1);
+    const int x1 = static_cast<int>(static_cast<long long>(k + 1) * V / S1);
+    p.part_ms[row * S + k] = greedy ? chunk_argmax(z, x0, x1, s) : chunk_ms(z, x0, x1, c, s);
   }
   if (!agrid_sync(p, ++nbar * G, s)) return;
 
@@ -1016,7 +1020,7 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
         const float2* part = p.part_ms + (static_cast<long long>(b) * n + i) * S;
         float best = -INFINITY;
         int bi = 0x7fffffff;
-        for (int k = l; k < S; k += 32) {
+        for (int k = l; k < S1; k += 32) {
           const float2 v = __ldcg(part + k);
           arg_merge(best, bi, v.x, __float_as_int(v.y));
         }
@@ -1059,7 +1063,7 @@ __global__ void __launch_bounds__(kAT) accept_grid_kernel(const AcceptParams p) 
         const int x0 = static_cast<int>(static_cast<long long>(kr) * V / SL);
         const int x1 = static_cast<int>(static_cast<long long>(kr + 1) * V / SL);
         if (threadIdx.x < 32) {
-          const float2 ms = warp_row_ms(p.part_ms + row * S, S, c);
+          const float2 ms = warp_row_ms(p.part_ms + row * S, S1, c);
           uint32_t prefix = 0;
           if (level >= 1) {
             unsigned long long above = 0;
@@ -1697,6 +1701,24 @@ int accept_grid_capacity() {
   return v;
 }
 
+// Work units per row of a grid pass over every row: the count (at most
+// max_units) that minimises the busiest CTA's share -- rounds of units over
+// the grid times the ids of a unit plus a fixed cost per unit (its
+// reductions, row statistics and bin flush), in ids.
+int accept_row_split(long long rows, int V, int max_units, int grid, long long fixed) {
+  int best = 1;
+  long long best_cost = -1;
+  for (int sl = 1; sl <= max_units; ++sl) {
+    const long long rounds = (rows * sl + grid - 1) / grid;
+    const long long cost = rounds * ((V + sl - 1) / sl + fixed);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = sl;
+    }
+  }
+  return best;
+}
+
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream) {
   if (p.B == 0) return cudaSuccess;
   const long long rows = static_cast<long long>(p.B) * (p.gamma + 1);
@@ -1710,6 +1732,9 @@ cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream) {
   }
   const long long units = rows * p.S;
   const int grid = static_cast<int>(std::min<long long>(cap, std::max<long long>(units, 1)));
+  AcceptParams a = p;
+  a.S1 = accept_row_split(rows, p.V, p.S, grid, 2048);
+  a.SL = accept_row_split(rows, p.V, p.S, grid, 4096);
   cudaError_t e = cudaMemsetAsync(p.bar, 0, sizeof(unsigned), stream);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1721,7 +1746,7 @@ cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, accept_grid_kernel, p);
+  return cudaLaunchKernelEx(&cfg, accept_grid_kernel, a);
 }
 
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t stream) {

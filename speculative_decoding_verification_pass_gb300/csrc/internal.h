@@ -220,6 +220,8 @@ struct AcceptParams {
   unsigned long long* part_tot;  // [B][S][2] draw-weight sums (residual, p)
   int* part_last;                // [B][S][2] last id with positive weight
   int B, gamma, V, S, C;         // S chunks of C ids (C <= kAcceptMaxChunk)
+  int S1, SL;                    // grid schedule: units per row of the chunk statistics
+                                 // and of the nucleus select (<= S; set by the launcher)
   int grid;                      // 1: the cooperative grid schedule when it fits
   float T, top_p;
 };
