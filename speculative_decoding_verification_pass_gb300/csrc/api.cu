@@ -85,6 +85,12 @@ bool mk_enabled() {
   const char* e = getenv("SPEC_FORWARD_PERSISTENT");
   return !(e && e[0] == '0');
 }
+// Its attention runs on the tensor cores where the shape allows, unless the
+// environment sets SPEC_ATTENTION_TC=0 (read per call, for comparison).
+bool mk_att_tc_enabled() {
+  const char* e = getenv("SPEC_ATTENTION_TC");
+  return !(e && e[0] == '0');
+}
 
 // Key chunks per (sequence, KV head) of the persistent forward's attention:
 // about one unit per CTA when that leaves at least 4 chunks per pair; a batch
@@ -628,6 +634,7 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       Q.ssq_ld = P.ssq_ld;
       const int grid = std::min(m->sm_count * cps, kMaxGrid);
       Q.att_nch = std::min(P.att_pairs, mk_att_chunks(grid, batch * Hkv));
+      Q.att_tc = mk_att_tc_enabled() && forward_att_tc(ntok, stages, hd) ? 1 : 0;
       Q.eps = c.rms_eps;
       Q.inv_d = 1.0f / d;
       Q.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));

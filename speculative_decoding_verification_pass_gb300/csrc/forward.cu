@@ -204,6 +204,7 @@ struct MkSmem {
   uint64_t* empty;
   uint64_t* accfull;
   uint64_t* accempty;
+  uint64_t* attbar;  // tensor-core attention MMAs done
   uint32_t* tmem_slot;
   int* abort;
   int* flag;
@@ -230,7 +231,8 @@ SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
   s.empty = s.full + kMaxStages;
   s.accfull = s.empty + kMaxStages;
   s.accempty = s.accfull + 2;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.accempty + 2);
+  s.attbar = s.accempty + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.attbar + 1);
   s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
   s.flag = s.abort + 1;
   s.aseq = reinterpret_cast<unsigned*>(s.flag + 1);
@@ -462,10 +464,12 @@ SPEC_DEVINL void embed_phase(const MkParams& P, const MkSmem& sm) {
 // (slot s, query tile qt) takes keys [32 s, 32 s + 32) of every block for the
 // 16 query rows of tile qt and keeps its own online softmax state; the two
 // slots merge in shared memory into the unit's partial (max, sum, O).
-SPEC_DEVINL int att_chunk_keys(int Tk, int nch) {
+SPEC_DEVINL int att_chunk_keys(int Tk, int nch, int unit_keys) {
   const int per = (Tk + nch - 1) / nch;
-  return ((per + kAttUnitKeys - 1) / kAttUnitKeys) * kAttUnitKeys;
+  return ((per + unit_keys - 1) / unit_keys) * unit_keys;
 }
+// Keys per attention block of the phase: 128 on the tensor cores, else 64.
+SPEC_DEVINL int att_unit_keys(const MkParams& P) { return P.att_tc ? 128 : kAttUnitKeys; }
 
 // Where a 64-key block of keys and values sits in shared memory: eight pieces
 // of 16 rows (piece q = slot * 4 + (value ? 2 : 0) + half, slot = key / 32,
@@ -517,7 +521,7 @@ SPEC_DEVINL bool att_unit(const MkParams& P, int unit, AttUnit& u) {
   u.ch = unit % nch;
   u.Lb = __ldcg(P.pos_base + u.b);
   const int Tk = min(u.Lb + P.n, P.cap);
-  const int ck = att_chunk_keys(Tk, nch);
+  const int ck = att_chunk_keys(Tk, nch, att_unit_keys(P));
   u.kbeg = u.ch * ck;
   u.kend = min(u.kbeg + ck, Tk);
   u.nu = (Tk + ck - 1) / ck;  // chunks holding keys
@@ -667,7 +671,7 @@ SPEC_DEVINL void cmb_phase(const MkParams& P) {
     const int kvh = (it / (kDG * R)) % P.Hkv;
     const int b = it / (kDG * R * P.Hkv);
     const int Tk = min(__ldcg(P.pos_base + b) + P.n, P.cap);
-    const int ck = att_chunk_keys(Tk, nch);
+    const int ck = att_chunk_keys(Tk, nch, att_unit_keys(P));
     const int nu = (Tk + ck - 1) / ck;
     const long long ubase = (static_cast<long long>(b) * P.Hkv + kvh) * nch;
     const float2* ob = reinterpret_cast<const float2*>(P.att_o + (ubase * kMkAttRows + r) * HD + dg * 64) + lane;
@@ -830,6 +834,341 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------- attention on tcgen05
+// The attention phase on the tensor cores (head dim 128).  Per 128-key block
+// of a unit (sequence b, KV head, key chunk) and per pass of 32 query rows:
+//   S^T[key][r] = K[key] . q[r]     one UMMA chain, M = 128 keys, N = 64 (the
+//                                   32 rows' q as bf16 hi rows, then lo rows)
+//   P[r][key]   = 2^(s - m_r)       written as bf16 hi / lo columns of the
+//                                   next B operand, MN-major: one 128-byte
+//                                   row of 64 values per key
+//   O^T[d][r]   = sum_key V[key][d] P[r][key]
+//                                   M = 128 dims: A = V^T, read MN-major
+//                                   from the V tile as stored ([key][dim])
+// with an online softmax over the unit's blocks.  Each epilogue thread owns
+// TMEM lane t (t = its warp quarter * 32 + lane): key t of S^T, then
+// dimension t of O^T; the per-row max and sum over the 128 keys are warp
+// transpose-reductions (31 shuffles for 32 rows) and a 4-warp merge in
+// shared memory; each thread stores its key's 64 P values as eight 16-byte
+// words.  The first epilogue thread issues the MMAs (the GEMM issuer
+// is idle between GEMM phases) and commits them to the attention barrier.
+// Shared memory: q [64][128] and K [128][128] in the attention stage; V and
+// P in F ring stages that the weight producer leaves free until the O
+// phase's grid barrier has passed (it issues at most S - F of that phase's
+// tiles before it, and nothing of a later phase): F = 3 (V's two halves, P)
+// when a stage is under 32 KB, else 2 (V whole, P).  The cached rows of a
+// CTA's first block come early: K's during the QKV phase (the attention
+// stage's K area is not used by the GEMM phases), V's once the CTA's last QKV
+// accumulator has been read (its F stages are then free).
+constexpr int kTcKeys = 128;
+constexpr int kTcRows = 32;
+
+// Ring stages of sbytes bytes kept free for the attention phase.
+__host__ __device__ inline int tc_free_stages(uint32_t sbytes) { return sbytes >= 2u * 16384u ? 2 : 3; }
+
+// Byte offset of 16-byte chunk c (of 8 in a 128-byte row) of row i in a
+// K-major tile with 128-byte swizzling: 8-row groups of 1024 bytes.
+SPEC_DEVINL uint32_t sw128_off(int i, int c) {
+  return static_cast<uint32_t>((i >> 3) * 1024 + (i & 7) * 128 + ((c ^ (i & 7)) << 4));
+}
+
+// Reduce 32 values per lane over the warp's lanes with op; afterwards lane l
+// holds the result for value l (recursive halving: 31 shuffles).
+template <class Op>
+SPEC_DEVINL float warp_transpose_reduce(float (&v)[32], Op op) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+  }
+  return v[0];
+}
+
+SPEC_DEVINL void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,"
+      "%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory descriptor with explicit leading / stride byte offsets
+// (128-byte swizzle).  K-major tiles use (16, 1024); the MN-major V^T view
+// uses (distance between its two 64-dimension sub-tiles, 1024).
+SPEC_DEVINL uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Where the attention phase keeps its operands (shared addresses).
+struct TcLayout {
+  uint32_t q;       // [64 rows][128] as 2 sub-tiles [64][64] (8 KB apart)
+  uint32_t k;       // [128 keys][128] as 2 sub-tiles [128][64] (16 KB apart)
+  uint32_t v0, v1;  // the V tile's two [128 keys][64 dims] sub-tiles
+  uint32_t p;       // P [128 keys][64 rows]: one 128-byte swizzled row per key
+};
+
+// n_issued: weight tiles this CTA streamed before the O phase of this layer
+// (the O phase's first tile goes to ring stage n_issued % S).
+SPEC_DEVINL TcLayout tc_layout(const MkSmem& sm, uint32_t sbytes, int S, uint32_t n_issued) {
+  const int F = tc_free_stages(sbytes);
+  const int f0 = static_cast<int>((n_issued + static_cast<uint32_t>(S - F)) % static_cast<uint32_t>(S));
+  int va, pa;
+  if (F == 2) {  // V in one stage, P in the other
+    va = f0;
+    pa = (f0 + 1) % S;
+  } else {  // the V sub-tiles in two stages adjacent in memory, P in the third
+    va = f0 + 1 < S ? f0 : (f0 + 1) % S;
+    pa = f0 + 1 < S ? (f0 + 2) % S : f0;
+  }
+  TcLayout t;
+  t.q = smem_u32(sm.att);
+  t.k = t.q + 16384;
+  t.v0 = smem_u32(sm.ring) + static_cast<uint32_t>(va) * sbytes;
+  t.v1 = t.v0 + (F == 2 ? 16384u : sbytes);
+  t.p = smem_u32(sm.ring) + static_cast<uint32_t>(pa) * sbytes;
+  return t;
+}
+
+// cp.async of 128 keys x 128 dims of one cache into [key][dim] sub-tiles
+// (sub0, sub0 + stride): `what` as in att_load_block (0 every row, zero
+// fill past kend; 1 the rows this pass does not write; 2 the rows it writes).
+template <bool kPaged>
+SPEC_DEVINL void tc_load_rows(uint32_t sub0, uint32_t stride, const uint16_t* cache, const KVMap& map,
+                              int b, int kvh, int kb, int kend, int Lb, int what, int e) {
+  for (int idx = e; idx < kTcKeys * 16; idx += kEpiThreads) {
+    const int i = idx >> 4, c = idx & 15;  // key kb + i, dims 8c .. 8c + 7
+    const int key = kb + i;
+    const bool valid = key < kend;
+    const bool fresh = valid && key >= Lb;
+    if ((what == 1 && fresh) || (what == 2 && !fresh)) continue;
+    const long long g = map.row<kPaged ? 2 : 1>(b, kvh, valid ? key : kb) + c * 8;
+    cp_async16(sub0 + static_cast<uint32_t>(c >> 3) * stride + sw128_off(i, c & 7), cache + g, valid ? 16 : 0);
+  }
+}
+
+// The cached keys of this CTA's first attention block of layer l, early
+// (during the QKV phase; the attention stage's K area is not used by the
+// GEMM phases).
+template <bool kPaged>
+SPEC_DEVINL void tc_prefetch(const MkParams& P, const MkSmem& sm, int l) {
+  const int e = threadIdx.x - kEpiFirstThread;
+  AttUnit u;
+  if (!att_unit(P, blockIdx.x, u)) return;
+  const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, 128};
+  tc_load_rows<kPaged>(smem_u32(sm.att) + 16384, 16384, P.kc + P.layer_kv * l, map, u.b, u.kvh, u.kbeg,
+                       u.kend, u.Lb, 1, e);
+}
+
+// The cached rows of the same block's V, once this CTA has read its last QKV
+// accumulator: every MMA of the phase has then completed, and the weight
+// producer writes none of the three stages that the attention phase uses.
+template <bool kPaged>
+SPEC_DEVINL void tc_prefetch_v(const MkParams& P, const MkSmem& sm, int l, uint32_t sbytes, uint32_t n_issued) {
+  const int e = threadIdx.x - kEpiFirstThread;
+  AttUnit u;
+  if (!att_unit(P, blockIdx.x, u)) return;
+  const TcLayout L = tc_layout(sm, sbytes, P.stages, n_issued);
+  const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, 128};
+  tc_load_rows<kPaged>(L.v0, L.v1 - L.v0, P.vc + P.layer_kv * l, map, u.b, u.kvh, u.kbeg, u.kend, u.Lb, 1, e);
+}
+
+SPEC_DEVINL void tc_wait(uint64_t* bar, uint32_t& parity, volatile int* abort) {
+  mbar_wait(bar, parity, abort);
+  parity ^= 1u;
+  tc_fence_after();
+}
+
+template <bool kPaged>
+SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32_t sbytes,
+                              uint32_t n_issued, uint32_t tmem_att, uint32_t& att_par) {
+  constexpr int HD = 128;
+  const int e = threadIdx.x - kEpiFirstThread;
+  const int quarter = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const int t = quarter * 32 + lane;  // this thread's TMEM lane: a key of S^T, a dim of O^T
+  const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+  const int G = P.H / P.Hkv;
+  const int R = P.n * G;
+  const int qdim = P.H * HD;
+  const TcLayout L = tc_layout(sm, sbytes, P.stages, n_issued);
+  const uint16_t* kc = P.kc + P.layer_kv * l;
+  const uint16_t* vc = P.vc + P.layer_kv * l;
+  const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, HD};
+  const int nch = P.att_nch;
+  const int units = P.B * P.Hkv * nch;
+  float* rowm = sm.rs;         // [32] running max of each row (log2 units)
+  float* rowl = sm.rs + 32;    // [32] running sum
+  float* alpha = sm.rs + 64;   // [32] rescale of this block
+  float* red = sm.rs + 128;    // [4][32] per-warp partials
+  unsigned long long* am = reinterpret_cast<unsigned long long*>(sm.qpre);  // [32] tree masks
+  const uint32_t id_s = idesc_bf16(kTcKeys, 2 * kTcRows);
+  // A (V^T) and B (P) both MN-major
+  const uint32_t id_o = idesc_bf16(HD, 2 * kTcRows) | (1u << 15) | (1u << 16);
+  for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    AttUnit u;
+    if (!att_unit(P, unit, u)) continue;  // uniform across the CTA
+    for (int rbase = 0; rbase < R; rbase += kTcRows) {
+      const bool first_unit = unit == static_cast<int>(blockIdx.x) && rbase == 0;
+      // q rows rbase .. rbase + 31: hi in tile rows 0..31, lo in 32..63 (zero past R)
+      for (int idx = e; idx < 2 * kTcRows * 16; idx += kEpiThreads) {
+        const int r = idx >> 4, c = idx & 15;
+        const int rr = rbase + (r & (kTcRows - 1));
+        const bool valid = rr < R;
+        const int j = valid ? rr / G : 0, g = valid ? rr % G : 0;
+        const long long off = (static_cast<long long>(u.b) * P.n + j) * qdim + (u.kvh * G + g) * HD + c * 8;
+        cp_async16(L.q + static_cast<uint32_t>(c >> 3) * 8192 + sw128_off(r, c & 7),
+                   (r < kTcRows ? P.q : P.q_lo) + off, valid ? 16 : 0);
+      }
+      if (e < kTcRows) {
+        const int rr = rbase + e;
+        rowm[e] = -INFINITY;
+        rowl[e] = 0.f;
+        am[e] = (P.anc && rr < R) ? __ldg(P.anc + static_cast<long long>(u.b) * P.n + rr / G) : 0ull;
+      }
+      float acc[kTcRows];
+#pragma unroll
+      for (int r = 0; r < kTcRows; ++r) acc[r] = 0.f;
+      for (int kb = u.kbeg; kb < u.kend; kb += kTcKeys) {
+        const bool first_block = first_unit && kb == u.kbeg;
+        tc_load_rows<kPaged>(L.k, 16384, kc, map, u.b, u.kvh, kb, u.kend, u.Lb, first_block ? 2 : 0, e);
+        tc_load_rows<kPaged>(L.v0, L.v1 - L.v0, vc, map, u.b, u.kvh, kb, u.kend, u.Lb, first_block ? 2 : 0, e);
+        cp_async_wait_all();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        named_bar(kArriveBar, kEpiThreads);
+        if (e == 0) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16(tmem_att, sdesc_sw128(L.k + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                      sdesc_sw128(L.q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          umma_commit(sm.attbar);
+        }
+        tc_wait(sm.attbar, att_par, sm.abort);
+        // ---- scores of key kb + t for the 32 rows (hi + lo halves)
+        float sv[kTcRows], hv2[kTcRows];
+        tmem_ld32(tmem_att + lane_addr, sv);
+        tmem_ld32(tmem_att + lane_addr + kTcRows, hv2);
+        // bit r: row rbase + r may see key kb + t (a cached key, or a key of
+        // this step that the row's token attends to)
+        const int key = kb + t;
+        uint32_t vis = 0u;
+        if (key < u.kend) {
+          const int nr = min(R - rbase, kTcRows);
+          vis = nr >= 32 ? 0xFFFFFFFFu : (1u << nr) - 1u;
+          if (key >= u.Lb) {
+            const int s = key - u.Lb;  // the key's token index within the step
+            if (P.anc) {
+              uint32_t m = 0u;
+              if (s < 64)
+                for (int r = 0; r < nr; ++r) m |= static_cast<uint32_t>((am[r] >> s) & 1ull) << r;
+              vis &= m;
+            } else {
+              // chain: row rr (token rr / G) sees token s iff rr >= s * G
+              const int first = s * G - rbase;
+              vis &= first <= 0 ? 0xFFFFFFFFu : (first >= 32 ? 0u : 0xFFFFFFFFu << first);
+            }
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kTcRows; ++r)
+          sv[r] = ((vis >> r) & 1u) ? (sv[r] + hv2[r]) * P.scale_log2 : -INFINITY;
+        // ---- row maxima over the 128 keys
+        float tv[kTcRows];
+#pragma unroll
+        for (int r = 0; r < kTcRows; ++r) tv[r] = sv[r];
+        red[quarter * kTcRows + lane] = warp_transpose_reduce(tv, [](float a, float b) { return fmaxf(a, b); });
+        named_bar(kArriveBar, kEpiThreads);
+        if (e < kTcRows) {
+          const float mb = fmaxf(fmaxf(red[e], red[kTcRows + e]), fmaxf(red[2 * kTcRows + e], red[3 * kTcRows + e]));
+          const float mo = rowm[e];
+          const float mn = fmaxf(mo, mb);
+          alpha[e] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+          rowm[e] = mn;
+        }
+        named_bar(kArriveBar, kEpiThreads);
+#pragma unroll
+        for (int r = 0; r < kTcRows; ++r) {
+          const float m = rowm[r];
+          sv[r] = sv[r] == -INFINITY ? 0.f : exp2f(sv[r] - m);
+          tv[r] = sv[r];
+        }
+        red[quarter * kTcRows + lane] = warp_transpose_reduce(tv, [](float a, float b) { return a + b; });
+        // ---- P row of key t: rows 0..31 as bf16 hi, then their lo parts
+        {
+          uint32_t w[kTcRows];
+#pragma unroll
+          for (int i = 0; i < kTcRows / 2; ++i) {
+            w[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+            w[kTcRows / 2 + i] = pack_bf16x2(sv[2 * i] - bf16lo(w[i]), sv[2 * i + 1] - bf16hi(w[i]));
+          }
+          const uint32_t prow = L.p + static_cast<uint32_t>(t) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((c ^ (t & 7)) << 4)),
+                         "r"(w[4 * c]), "r"(w[4 * c + 1]), "r"(w[4 * c + 2]), "r"(w[4 * c + 3])
+                         : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        named_bar(kArriveBar, kEpiThreads);
+        if (e < kTcRows)
+          rowl[e] = rowl[e] * alpha[e] + ((red[e] + red[kTcRows + e]) + (red[2 * kTcRows + e] + red[3 * kTcRows + e]));
+        if (e == 0) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTcKeys / 16; ++kk)
+            umma_bf16(tmem_att + 2 * kTcRows, sdesc_sw128(L.v0 + kk * 2048, L.v1 - L.v0, 1024),
+                      sdesc_sw128(L.p + kk * 2048, 8192, 1024), id_o, kk > 0 ? 1u : 0u);
+          umma_commit(sm.attbar);
+        }
+        tc_wait(sm.attbar, att_par, sm.abort);
+        // ---- O^T: dimension t of the 32 rows
+        float ov[kTcRows], ol[kTcRows];
+        tmem_ld32(tmem_att + lane_addr + 2 * kTcRows, ov);
+        tmem_ld32(tmem_att + lane_addr + 3 * kTcRows, ol);
+#pragma unroll
+        for (int r = 0; r < kTcRows; ++r) acc[r] = acc[r] * alpha[r] + (ov[r] + ol[r]);
+        tc_fence_before();
+        named_bar(kArriveBar, kEpiThreads);  // operands and TMEM free for the next block
+        if (*sm.abort) break;
+      }
+      // ---- this unit's partial for rows rbase .. rbase + 31
+      const long long ubase = (static_cast<long long>(u.b) * P.Hkv + u.kvh) * nch + u.ch;
+#pragma unroll
+      for (int r = 0; r < kTcRows; ++r)
+        if (rbase + r < R) __stcg(P.att_o + (ubase * kMkAttRows + rbase + r) * HD + t, acc[r]);
+      if (e < kTcRows && rbase + e < R)
+        __stcg(reinterpret_cast<float2*>(P.att_ml + (ubase * kMkAttRows + rbase + e) * 2),
+               make_float2(rowm[e], rowl[e]));
+      named_bar(kArriveBar, kEpiThreads);  // the row statistics free for the next pass
+      if (*sm.abort) return;
+    }
+  }
+  // the ring stages go back to the TMA loads of the O phase
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // -------------------------------------------------------------- the kernel
 template <int HD, bool kPaged>
 __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_constant__ MkParams P) {
@@ -842,7 +1181,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
   const int warp = threadIdx.x >> 5;
   const uint32_t me = blockIdx.x, GR = gridDim.x;
   const int nph = 2 + kPhPerLayer * P.L;
-  const uint32_t tcols = tmem_cols_for(ncols);
+  // GEMM accumulators in [0, 2 ncols); the attention's S^T and O^T after them
+  const uint32_t tcols = P.att_tc ? tmem_cols_pow2(2u * static_cast<uint32_t>(ncols) + 4u * kTcRows)
+                                  : tmem_cols_for(ncols);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -853,6 +1194,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
       mbar_init(&sm.accfull[a], 1);
       mbar_init(&sm.accempty[a], 4);
     }
+    mbar_init(sm.attbar, 1);
     *sm.abort = 0;
     *sm.aseq = 0;
     *sm.open = 0;
@@ -888,9 +1230,14 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         if (cur.ph != cur_ph) {
           cur_ph = cur.ph;
           in_ph = 0;
+          // the tensor-core attention borrows ring stages until the O phase
+          // has opened: nothing of the phase after it goes out before that
+          if (P.att_tc && ph_kind(cur.ph, P.L) == PH_GU && !open_wait(sm, cur.ph - 1)) break;
         }
         // at most `pre` tiles of a phase before its grid barrier has passed
-        if (in_ph == pre && !open_wait(sm, cur.ph)) break;
+        // (of the O phase, tc_free_stages fewer when the attention borrows them)
+        const int lim = (P.att_tc && ph_kind(cur.ph, P.L) == PH_O) ? S - tc_free_stages(sbytes) : pre;
+        if (in_ph == lim && !open_wait(sm, cur.ph)) break;
         ++in_ph;
         if (n >= static_cast<uint32_t>(S) && !mbar_wait(&sm.empty[stage], phase ^ 1u, sm.abort)) break;
         uint8_t* st = sm.ring + static_cast<size_t>(stage) * sbytes;
@@ -1014,17 +1361,30 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
     gs.slots = sm.slots;
     gs.flag = sm.flag;
     int seg = 0;
+    uint32_t n_issued = 0;  // weight tiles of the GEMM phases so far (this CTA)
+    uint32_t att_par = 0;   // parity of the attention barrier
+    const uint32_t tmem_att = tmem_base + 2u * static_cast<uint32_t>(ncols);
     unsigned long long* const part64 = reinterpret_cast<unsigned long long*>(P.partials);
     // read before this CTA arrives on the embedding phase; advanced after it
     const uint32_t epoch = *reinterpret_cast<volatile unsigned*>(P.epoch) & 0x7FFFFFu;
     for (int ph = 0; ph < nph; ++ph) {
       const int kind = ph_kind(ph, P.L);
       const uint32_t tag = (epoch << 9) | static_cast<uint32_t>(ph);
+      int v_layer = -1;  // QKV phase of this layer done here: its first V block next
       if (kind == PH_EMBED) {
         embed_phase(P, sm);
       } else if (kind == PH_ATT) {
         if (!epi_wait(P, sm, ph)) break;
-        att_phase<HD, kPaged>(P, sm, (ph - 1) / kPhPerLayer, sbytes);
+        if constexpr (HD == 128) {
+          if (P.att_tc) {
+            att_phase_tc<kPaged>(P, sm, (ph - 1) / kPhPerLayer, sbytes, n_issued, tmem_att, att_par);
+            if (*sm.abort) break;
+          } else {
+            att_phase<HD, kPaged>(P, sm, (ph - 1) / kPhPerLayer, sbytes);
+          }
+        } else {
+          att_phase<HD, kPaged>(P, sm, (ph - 1) / kPhPerLayer, sbytes);
+        }
       } else if (kind == PH_CMB) {
         if (!epi_wait(P, sm, ph)) break;
         cmb_phase<HD>(P);
@@ -1038,6 +1398,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         const PhaseSplit ps = phase_split(g, me, GR);
         const Partition& part = ps.part;
         const uint32_t u0 = ps.u0, u1 = ps.u1;
+        n_issued += u1 - u0;
         if (p.ssq_in) {
           for (int c = e; c < p.ntok; c += kEpiThreads) {
             float s = 0.f;
@@ -1049,7 +1410,15 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         // QKV: per token column KV slot, rotary position and fit flag
         int* const qpre = sm.qpre;
         if (p.epi == EPI_QKV) {
-          att_prefetch<HD, kPaged>(P, sm, g.l);  // this layer's first key block, early
+          // this layer's first key block, early
+          if constexpr (HD == 128) {
+            if (P.att_tc)
+              tc_prefetch<kPaged>(P, sm, g.l);
+            else
+              att_prefetch<HD, kPaged>(P, sm, g.l);
+          } else {
+            att_prefetch<HD, kPaged>(P, sm, g.l);
+          }
           for (int c = e; c < p.ntok; c += kEpiThreads) {
             const int m = min(c, p.M - 1);
             const int b = m / p.n_per_seq, node = m - b * p.n_per_seq;
@@ -1139,8 +1508,12 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
           ++seg;
         }
         if (*sm.abort) break;
+        if (p.epi == EPI_QKV) v_layer = g.l;
       }
       phase_arrive(P);
+      if constexpr (HD == 128) {
+        if (P.att_tc && v_layer >= 0) tc_prefetch_v<kPaged>(P, sm, v_layer, sbytes, n_issued);
+      }
     }
   }
 
@@ -1166,6 +1539,14 @@ int forward_max_stages(int ntok, int hd, size_t budget) {
   return s > kMaxStages ? kMaxStages : s;
 }
 
+// Does the persistent forward run its attention on the tensor cores?  Head
+// dim 128, the S^T and O^T columns beside the GEMM accumulators within TMEM,
+// and a ring deep enough to lend tc_free_stages and keep two.
+bool forward_att_tc(int ntok, int stages, int hd) {
+  const int F = tc_free_stages(static_cast<uint32_t>(stage_bytes(2 * ntok, 1)));
+  return hd == 128 && 4 * ntok + 4 * kTcRows <= 512 && stages >= F + 2;
+}
+
 // CTAs per SM the persistent forward can keep resident (0: not launchable).
 int forward_ctas_per_sm(int ntok, int stages, int hd) {
   const size_t smem = forward_smem_bytes(ntok, stages, hd);
@@ -1181,7 +1562,8 @@ int forward_ctas_per_sm(int ntok, int stages, int hd) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kMkThreads, smem) != cudaSuccess) return 0;
   // every resident CTA holds its accumulators in TMEM (512 columns per SM)
-  uint32_t need = 2u * 2u * static_cast<uint32_t>(ntok), cols = 32;
+  uint32_t need = 2u * 2u * static_cast<uint32_t>(ntok) + (forward_att_tc(ntok, stages, hd) ? 4u * kTcRows : 0u),
+           cols = 32;
   while (cols < need) cols <<= 1;
   const int by_tmem = static_cast<int>(512 / cols);
   return n < by_tmem ? n : by_tmem;

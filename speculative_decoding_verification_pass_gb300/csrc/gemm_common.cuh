@@ -82,6 +82,12 @@ __device__ Smem carve(uint8_t* raw, int rows_b, int stages, int ksub) {
   return s;
 }
 
+__device__ __forceinline__ uint32_t tmem_cols_pow2(uint32_t need) {
+  uint32_t c = 32;
+  while (c < need) c <<= 1;
+  return c;
+}
+
 __device__ __forceinline__ uint32_t tmem_cols_for(int ntok) {
   uint32_t need = 2u * static_cast<uint32_t>(ntok);
   uint32_t c = 32;

@@ -134,6 +134,7 @@ struct MkParams {
   int L, d, H, Hkv, hd, ffn, V, qkv_rows;
   int B, n, M, ntok, cap, stages, ssq_ld;
   int att_nch;                            // key chunks per (sequence, KV head)
+  int att_tc;                             // attention on the tensor cores (forward_att_tc)
   float eps, inv_d, scale_log2;
   const uint16_t* embed;
   const float2* rope;
@@ -167,6 +168,7 @@ struct MkParams {
 size_t forward_smem_bytes(int ntok, int stages, int hd);
 int forward_max_stages(int ntok, int hd, size_t budget);
 int forward_ctas_per_sm(int ntok, int stages, int hd);
+bool forward_att_tc(int ntok, int stages, int hd);
 cudaError_t launch_forward(const MkParams& P, int grid, int hd, cudaStream_t stream);
 
 // ------------------------------------------------------------ small kernels

@@ -134,6 +134,29 @@ def test_forward_matches_oracle_ragged_batch(cfg):
     pr.model.close()
 
 
+@pytest.mark.parametrize("tc", ["1", "0"], ids=["tcgen05", "mma_sync"])
+def test_attention_paths_match_oracle(tc, monkeypatch):
+    """Head dim 128 has two attention paths in the persistent forward: S^T
+    and O^T as tcgen05 MMAs with TMEM accumulators (the default where the
+    shape fits), and warp-level MMAs.  Both match the oracle on a ragged batch
+    of 2 (300 cached tokens: 3 key blocks) verifying a gamma=4 block, before
+    and after a rollback."""
+    monkeypatch.setenv("SPEC_ATTENTION_TC", tc)
+    cfg = SMALL[1]
+    B, cap, gamma = 2, 320, 4
+    pr = Pair(cfg, 23, B, cap)
+    pr.prefill(wl.tokens(13, B, 300, cfg.vocab))
+    blk = wl.tokens(14, B, gamma + 1, cfg.vocab)
+    _close(pr.gpu(blk), pr.oracle(blk))
+    n_acc = np.array([0, 3], np.int32)
+    sb.spec_kv_truncate(pr.kv, torch.from_numpy(n_acc).cuda(), gamma, pr.ws)
+    pr.okv.lens = OM.truncate(pr.okv.lens, n_acc, gamma)
+    blk = wl.tokens(15, B, gamma + 1, cfg.vocab)
+    _close(pr.gpu(blk), pr.oracle(blk))
+    pr.status_ok()
+    pr.model.close()
+
+
 def _bf16_ulp(x):
     """Spacing of bf16 values at |x| (8 significant bits)."""
     a = np.maximum(np.abs(x), 2.0 ** -126)
