@@ -852,19 +852,20 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
 // shared memory; each thread stores its key's 64 P values as eight 16-byte
 // words.  The first epilogue thread issues the MMAs (the GEMM issuer
 // is idle between GEMM phases) and commits them to the attention barrier.
-// Shared memory: q [64][128] and K [128][128] in the attention stage; V and
-// P in F ring stages that the weight producer leaves free until the O
-// phase's grid barrier has passed (it issues at most S - F of that phase's
-// tiles before it, and nothing of a later phase): F = 3 (V's two halves, P)
-// when a stage is under 32 KB, else 2 (V whole, P).  The cached rows of a
-// CTA's first block come early: K's during the QKV phase (the attention
-// stage's K area is not used by the GEMM phases), V's once the CTA's last QKV
-// accumulator has been read (its F stages are then free).
+// Shared memory: q [64][128] and K [128][128] in the attention stage, P over
+// K's first half once the scores are in TMEM (the next block's K loads after
+// its O^T MMAs have completed); V in F ring stages that the weight producer
+// leaves free until the O phase's grid barrier has passed (it issues at most
+// S - F of that phase's tiles before it, and nothing of a later phase):
+// F = 2 (V's two halves) when a stage is under 32 KB, else 1.  The cached
+// rows of a CTA's first block come early: K's during the QKV phase (the
+// attention stage's K area is not used by the GEMM phases), V's once the
+// CTA's last QKV accumulator has been read (its F stages are then free).
 constexpr int kTcKeys = 128;
 constexpr int kTcRows = 32;
 
 // Ring stages of sbytes bytes kept free for the attention phase.
-__host__ __device__ inline int tc_free_stages(uint32_t sbytes) { return sbytes >= 2u * 16384u ? 2 : 3; }
+__host__ __device__ inline int tc_free_stages(uint32_t sbytes) { return sbytes >= 2u * 16384u ? 1 : 2; }
 
 // Byte offset of 16-byte chunk c (of 8 in a 128-byte row) of row i in a
 // K-major tile with 128-byte swizzling: 8-row groups of 1024 bytes.
@@ -924,8 +925,8 @@ SPEC_DEVINL uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
 struct TcLayout {
   uint32_t q;       // [64 rows][128] as 2 sub-tiles [64][64] (8 KB apart)
   uint32_t k;       // [128 keys][128] as 2 sub-tiles [128][64] (16 KB apart)
-  uint32_t v0, v1;  // the V tile's two [128 keys][64 dims] sub-tiles
-  uint32_t p;       // P [128 keys][64 rows]: one 128-byte swizzled row per key
+  uint32_t v0, v1;  // the V tile's two [128 keys][64 dims] sub-tiles (v0 < v1)
+  uint32_t p;       // P [128 keys][64 rows]: one 128-byte swizzled row per key (over K's first half)
 };
 
 // n_issued: weight tiles this CTA streamed before the O phase of this layer
@@ -933,20 +934,19 @@ struct TcLayout {
 SPEC_DEVINL TcLayout tc_layout(const MkSmem& sm, uint32_t sbytes, int S, uint32_t n_issued) {
   const int F = tc_free_stages(sbytes);
   const int f0 = static_cast<int>((n_issued + static_cast<uint32_t>(S - F)) % static_cast<uint32_t>(S));
-  int va, pa;
-  if (F == 2) {  // V in one stage, P in the other
-    va = f0;
-    pa = (f0 + 1) % S;
-  } else {  // the V sub-tiles in two stages adjacent in memory, P in the third
-    va = f0 + 1 < S ? f0 : (f0 + 1) % S;
-    pa = f0 + 1 < S ? (f0 + 2) % S : f0;
-  }
   TcLayout t;
   t.q = smem_u32(sm.att);
   t.k = t.q + 16384;
-  t.v0 = smem_u32(sm.ring) + static_cast<uint32_t>(va) * sbytes;
-  t.v1 = t.v0 + (F == 2 ? 16384u : sbytes);
-  t.p = smem_u32(sm.ring) + static_cast<uint32_t>(pa) * sbytes;
+  t.p = t.k;
+  const uint32_t ring = smem_u32(sm.ring);
+  if (F == 1) {  // V whole in one stage
+    t.v0 = ring + static_cast<uint32_t>(f0) * sbytes;
+    t.v1 = t.v0 + 16384u;
+  } else {  // V's halves in two stages, the lower address first
+    const int f1 = (f0 + 1) % S;
+    t.v0 = ring + static_cast<uint32_t>(min(f0, f1)) * sbytes;
+    t.v1 = ring + static_cast<uint32_t>(max(f0, f1)) * sbytes;
+  }
   return t;
 }
 
@@ -1445,6 +1445,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
           }
           // the epilogue's other inputs, also loaded while the MMAs run
           EpiPre pre;
+          pre.rolled = true;
           if (p.epi == EPI_RESID) {
             pre.have_gn = true;
             pre.gn = f < p.N ? __ldg(p.g_next + f) : 0.f;
@@ -1454,15 +1455,15 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
             pre.fr = __ldg(p.rope + (dim < half ? dim : dim - half));
             pre.qkv = qpre;
           }
-          mbar_wait(&sm.accfull[a], (seg >> 1) & 1, sm.abort);
-          named_bar(kEpiBar, kEpiThreads);
-          if (*sm.abort) break;
-          tc_fence_after();
           const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(a * ncols);
           const uint32_t c_first = part.cta_of(t * kc);
           const uint32_t c_last = part.cta_of((t + 1) * kc - 1);
           const int nc = static_cast<int>(c_last - c_first + 1);
           const bool finisher = nc == 1 || me == c_first;
+          mbar_wait(&sm.accfull[a], (seg >> 1) & 1, sm.abort);
+          named_bar(kEpiBar, kEpiThreads);
+          if (*sm.abort) break;
+          tc_fence_after();
           if (!finisher) {
             const int slot = part.slot(me, t);
             for (int c0 = 0; c0 < p.M; c0 += 16) {

@@ -155,7 +155,28 @@ struct EpiPre {
   float2 fr{};              // EPI_QKV: RoPE frequency of this row's dimension
   const int* qkv = nullptr; // EPI_QKV: shared [3][128] per token column: KV slot, rotary
                             // position, fit flag (persistent kernel, tok0 = 0)
+  // The persistent kernel: each epilogue runs once per layer with a cold
+  // instruction cache, so its loops over the valid columns stay rolled (an
+  // unrolled body is fetched anew for every column it reaches), their
+  // operands staged in the exchange buffer ([2][16][128] floats).
+  bool rolled = false;
 };
+
+// sin and cos of the rotary angle of position pos for a dimension whose
+// frequency is fr.x + fr.y turns per position (hi + lo): pos * fr.x = t + terr
+// exactly (an fma gives the product's rounding error), whole turns are
+// removed exactly (t - rint(t) is representable), and the hardware sine and
+// cosine run on the reduced angle, |angle| <= pi (+ a few ulps), where their
+// absolute error is about 2^-21.4.  The angle so keeps ~1e-6 absolute accuracy
+// at any cached position; an unreduced fp32 angle of thousands of radians
+// would lose ~|angle| * 2^-22 to its own rounding.
+SPEC_DEVINL void rope_sincos(int pos, float2 fr, float* sn, float* cs) {
+  const float fp = static_cast<float>(pos);
+  const float t = fp * fr.x;
+  const float terr = fmaf(fp, fr.x, -t) + fp * fr.y;
+  const float frac = (t - rintf(t)) + terr;
+  __sincosf(6.28318530717958648f * frac, sn, cs);
+}
 
 // Apply the epilogue to 16 token columns [c0, c0+16) of this thread's row.
 // With have_h the residual-stream values of these columns were loaded
@@ -182,6 +203,50 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
         if (m < p.M) p.out[static_cast<long long>(m) * p.ldo + f] = v[j];
       }
     }
+    return;
+  }
+  if (p.epi == EPI_RESID && pre.rolled) {
+    // this thread's values and residual rows go to its own slots of the
+    // exchange buffer; the loop over the valid columns reads them back
+    float* xv = sm.xbuf;
+    float* xh = sm.xbuf + 16 * kTileN;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      xv[j * kTileN + r] = v[j];
+      xh[j * kTileN + r] = hv_in[j];
+    }
+    const bool fok = f < p.N;
+    const int jn = min(16, p.M - p.tok0 - c0);
+#pragma unroll 1
+    for (int j = 0; j < jn; ++j) {
+      const float hn = xh[j * kTileN + r] + xv[j * kTileN + r];
+      if (fok) {
+        const long long idx = static_cast<long long>(p.tok0 + c0 + j) * p.d + f;
+        p.h[idx] = hn;
+        const float x = hn * pre.gn;
+        const uint16_t hi = f32_to_bf16(x);
+        p.hb[idx] = hi;
+        if (p.hb_lo) p.hb_lo[idx] = f32_to_bf16(x - bf16_to_f32(hi));
+      }
+      xv[j * kTileN + r] = fok ? hn * hn : 0.f;  // this column's square, row r
+    }
+    named_bar(kEpiBar, kEpiThreads);
+    // Σh² of each valid column over the tile's 128 rows: 8 threads per
+    // column, 16 rows each, then a fixed 3-step butterfly (a fixed order)
+    {
+      const int j = e >> 3, part = e & 7;
+      float s = 0.f;
+      if (j < jn) {
+        const float* col = xv + j * kTileN + part * 16;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s += col[i];
+      }
+      s += __shfl_xor_sync(0xffffffffu, s, 4);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      if (j < jn && part == 0) p.ssq_out[static_cast<long long>(tile) * p.ssq_ld + p.tok0 + c0 + j] = s;
+    }
+    named_bar(kEpiBar, kEpiThreads);
     return;
   }
   if (p.epi == EPI_RESID) {
@@ -239,26 +304,51 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
     const bool rot = f < qdim + kdim;
     const int pr = dim < half ? r + half : r - half;
     const float2 fr = pre.have_fr ? pre.fr : p.rope[dim < half ? dim : dim - half];
+    if (pre.qkv) {
+      // the persistent forward: KV slot, rotary position and fit flag per
+      // column are in shared memory, and so are the values (the exchange
+      // buffer), so the loop over the valid columns stays rolled: this code
+      // runs once per layer, and an unrolled body is fetched anew for every
+      // column it reaches
+      const int jn = min(16, p.M - p.tok0 - c0);
+#pragma unroll 1
+      for (int j = 0; j < jn; ++j) {
+        if (f >= p.N) break;
+        const int m = p.tok0 + c0 + j;
+        float out = sm.xbuf[j * kTileN + r];
+        if (rot) {
+          float sn, cs;
+          rope_sincos(pre.qkv[128 + c0 + j], fr, &sn, &cs);
+          const float partner = sm.xbuf[j * kTileN + pr];
+          out = dim < half ? out * cs - partner * sn : out * cs + partner * sn;
+        }
+        const int slot = pre.qkv[c0 + j];
+        if (f < qdim) {
+          const long long qi = static_cast<long long>(m) * qdim + f;
+          const uint16_t hi = f32_to_bf16(out);
+          p.q[qi] = hi;
+          if (p.q_lo) p.q_lo[qi] = f32_to_bf16(out - bf16_to_f32(hi));
+        } else if (pre.qkv[256 + c0 + j] && slot < p.cap) {
+          const int kf = f < qdim + kdim ? f - qdim : f - qdim - kdim;
+          const KVMap map{p.kv_table, p.kv_max_pages, p.kv_n_pages, p.Hkv, p.cap, hd};
+          const long long idx = map.row<kKV>(m / p.n_per_seq, kf / hd, slot) + (kf % hd);
+          (f < qdim + kdim ? p.kcache : p.vcache)[idx] = f32_to_bf16(out);
+        }
+      }
+      named_bar(kEpiBar, kEpiThreads);
+      return;
+    }
     // slot = len + node index; rotary position = len + node depth (the node
     // index itself for a chain)
     int slotv[16], posv[16], okv[16];
-    if (pre.qkv) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        slotv[j] = pre.qkv[c0 + j];
-        posv[j] = pre.qkv[128 + c0 + j];
-        okv[j] = pre.qkv[256 + c0 + j];
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {  // sequence bookkeeping, loads in flight together
-        const int m = min(p.tok0 + c0 + j, p.M - 1);
-        const int b = m / p.n_per_seq;
-        const int base = ldcg_i(p.pos_base + b), node = m - b * p.n_per_seq;
-        slotv[j] = base + node;
-        posv[j] = base + (p.depth ? __ldg(p.depth + m) : node);
-        okv[j] = ldcg_i(p.seq_ok + b);
-      }
+    for (int j = 0; j < 16; ++j) {  // sequence bookkeeping, loads in flight together
+      const int m = min(p.tok0 + c0 + j, p.M - 1);
+      const int b = m / p.n_per_seq;
+      const int base = ldcg_i(p.pos_base + b), node = m - b * p.n_per_seq;
+      slotv[j] = base + node;
+      posv[j] = base + (p.depth ? __ldg(p.depth + m) : node);
+      okv[j] = ldcg_i(p.seq_ok + b);
     }
 #pragma unroll 4
     for (int j = 0; j < 16; ++j) {
@@ -268,17 +358,8 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
       float out = v[j];
       const int pos = posv[j];
       if (rot) {
-        // rotation in turns = pos * (hi + lo): pos * hi = t + terr exactly
-        // (fma), whole turns are removed exactly (t - rint(t) is representable),
-        // and sin / cos of 2 pi * frac come from sincospif on [-1, 1], so the
-        // angle keeps ~1e-7 rad absolute accuracy at any cached position
-        // (fast-math does not replace sincospif)
-        const float fp = static_cast<float>(pos);
-        const float t = fp * fr.x;
-        const float terr = fmaf(fp, fr.x, -t) + fp * fr.y;
-        const float frac = (t - rintf(t)) + terr;
         float sn, cs;
-        sincospif(2.0f * frac, &sn, &cs);
+        rope_sincos(pos, fr, &sn, &cs);
         const float partner = sm.xbuf[j * kTileN + pr];
         out = dim < half ? v[j] * cs - partner * sn : v[j] * cs + partner * sn;
       }
@@ -302,6 +383,28 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
     return;
   }
   // EPI_SWIGLU
+  if (pre.rolled) {
+    // rows 0..63 of the tile are gates, 64..127 the matching ups; every
+    // thread takes feature r % 64 for every other valid column
+#pragma unroll
+    for (int j = 0; j < 16; ++j) sm.xbuf[j * kTileN + r] = v[j];
+    named_bar(kEpiBar, kEpiThreads);
+    const int fo = static_cast<int>(tile) * 64 + (r & 63);
+    const int jn = min(16, p.M - p.tok0 - c0);
+    if (fo < p.ffn) {
+#pragma unroll 1
+      for (int j = r >> 6; j < jn; j += 2) {
+        const float g = sm.xbuf[j * kTileN + (r & 63)], u = sm.xbuf[j * kTileN + (r & 63) + 64];
+        const float a = g / (1.0f + __expf(-g)) * u;
+        const uint16_t hi = f32_to_bf16(a);
+        const long long idx = static_cast<long long>(p.tok0 + c0 + j) * p.ffn + fo;
+        p.act[idx] = hi;
+        if (p.act_lo) p.act_lo[idx] = f32_to_bf16(a - bf16_to_f32(hi));
+      }
+    }
+    named_bar(kEpiBar, kEpiThreads);
+    return;
+  }
   if (r >= 64) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) sm.xbuf[j * kTileN + r] = v[j];
