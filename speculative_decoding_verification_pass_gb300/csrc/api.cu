@@ -635,6 +635,7 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       const int grid = std::min(m->sm_count * cps, kMaxGrid);
       Q.att_nch = std::min(P.att_pairs, mk_att_chunks(grid, batch * Hkv));
       Q.att_tc = mk_att_tc_enabled() && forward_att_tc(ntok, stages, hd) ? 1 : 0;
+      Q.nacc = forward_acc_buffers(ntok, Q.att_tc != 0);
       Q.eps = c.rms_eps;
       Q.inv_d = 1.0f / d;
       Q.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));

@@ -230,8 +230,8 @@ SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
   s.full = reinterpret_cast<uint64_t*>(t);
   s.empty = s.full + kMaxStages;
   s.accfull = s.empty + kMaxStages;
-  s.accempty = s.accfull + 2;
-  s.attbar = s.accempty + 2;
+  s.accempty = s.accfull + kMkMaxAcc;
+  s.attbar = s.accempty + kMkMaxAcc;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.attbar + 1);
   s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
   s.flag = s.abort + 1;
@@ -1181,16 +1181,17 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
   const int warp = threadIdx.x >> 5;
   const uint32_t me = blockIdx.x, GR = gridDim.x;
   const int nph = 2 + kPhPerLayer * P.L;
-  // GEMM accumulators in [0, 2 ncols); the attention's S^T and O^T after them
-  const uint32_t tcols = P.att_tc ? tmem_cols_pow2(2u * static_cast<uint32_t>(ncols) + 4u * kTcRows)
-                                  : tmem_cols_for(ncols);
+  // GEMM accumulators in [0, nacc ncols); the attention's S^T and O^T after them
+  const int nacc = P.nacc;
+  const uint32_t tcols =
+      tmem_cols_pow2(static_cast<uint32_t>(nacc * ncols) + (P.att_tc ? 4u * kTcRows : 0u));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kMkMaxAcc; ++a) {
       mbar_init(&sm.accfull[a], 1);
       mbar_init(&sm.accempty[a], 4);
     }
@@ -1304,7 +1305,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
       const uint32_t idesc = idesc_bf16(kTileN, ncols);
       int stage = 0;
       uint32_t phase = 0;
-      int seg = 0;
+      int a = 0;          // accumulator buffer of the next segment
+      uint32_t apar = 0;  // its use parity
       bool ok = true;
       for (int ph = 0; ph < nph && ok; ++ph) {
         if (!is_gemm(ph_kind(ph, P.L))) continue;
@@ -1316,8 +1318,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         while (u < u1 && ok) {
           const uint32_t t = u / kc;
           const uint32_t seg_end = min(u1, (t + 1) * kc);
-          const int a = seg & 1;
-          if (!mbar_wait(&sm.accempty[a], ((seg >> 1) & 1) ^ 1u, sm.abort)) {
+          if (!mbar_wait(&sm.accempty[a], apar ^ 1u, sm.abort)) {
             ok = false;
             break;
           }
@@ -1344,7 +1345,10 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
           if (!ok) break;
           umma_commit(&sm.accfull[a]);
           u = seg_end;
-          ++seg;
+          if (++a == nacc) {
+            a = 0;
+            apar ^= 1u;
+          }
         }
       }
     }
@@ -1360,10 +1364,11 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
     gs.red = sm.red;
     gs.slots = sm.slots;
     gs.flag = sm.flag;
-    int seg = 0;
+    int a = 0;          // accumulator buffer of the next segment
+    uint32_t apar = 0;  // its use parity
     uint32_t n_issued = 0;  // weight tiles of the GEMM phases so far (this CTA)
     uint32_t att_par = 0;   // parity of the attention barrier
-    const uint32_t tmem_att = tmem_base + 2u * static_cast<uint32_t>(ncols);
+    const uint32_t tmem_att = tmem_base + static_cast<uint32_t>(nacc * ncols);
     unsigned long long* const part64 = reinterpret_cast<unsigned long long*>(P.partials);
     // read before this CTA arrives on the embedding phase; advanced after it
     const uint32_t epoch = *reinterpret_cast<volatile unsigned*>(P.epoch) & 0x7FFFFFu;
@@ -1433,7 +1438,6 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         while (u < u1) {
           const uint32_t t = u / kc;
           const uint32_t seg_end = min(u1, (t + 1) * kc);
-          const int a = seg & 1;
           // the residual stream of this tile's rows, loaded while the MMAs run
           float hv[16];
           const bool pre_h = p.epi == EPI_RESID && p.ntok <= 16;
@@ -1460,7 +1464,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
           const uint32_t c_last = part.cta_of((t + 1) * kc - 1);
           const int nc = static_cast<int>(c_last - c_first + 1);
           const bool finisher = nc == 1 || me == c_first;
-          mbar_wait(&sm.accfull[a], (seg >> 1) & 1, sm.abort);
+          mbar_wait(&sm.accfull[a], apar, sm.abort);
           named_bar(kEpiBar, kEpiThreads);
           if (*sm.abort) break;
           tc_fence_after();
@@ -1506,7 +1510,10 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
           __syncwarp();
           if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.accempty[a]);
           u = seg_end;
-          ++seg;
+          if (++a == nacc) {
+            a = 0;
+            apar ^= 1u;
+          }
         }
         if (*sm.abort) break;
         if (p.epi == EPI_QKV) v_layer = g.l;
@@ -1548,6 +1555,17 @@ bool forward_att_tc(int ntok, int stages, int hd) {
   return hd == 128 && 4 * ntok + 4 * kTcRows <= 512 && stages >= F + 2;
 }
 
+// TMEM accumulator buffers of the persistent forward: as many as fit its 512
+// columns (up to kMkMaxAcc) beside the attention's, so that a segment's MMAs
+// need not wait for the epilogue of the segment two before it (the previous
+// phase's finisher, whose epilogue ends the phase).
+int forward_acc_buffers(int ntok, bool att_tc) {
+  const int ncols = 2 * ntok, extra = att_tc ? 4 * kTcRows : 0;
+  for (int nb = kMkMaxAcc; nb > 2; --nb)
+    if (nb * ncols + extra <= 512) return nb;
+  return 2;
+}
+
 // CTAs per SM the persistent forward can keep resident (0: not launchable).
 int forward_ctas_per_sm(int ntok, int stages, int hd) {
   const size_t smem = forward_smem_bytes(ntok, stages, hd);
@@ -1563,7 +1581,8 @@ int forward_ctas_per_sm(int ntok, int stages, int hd) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kMkThreads, smem) != cudaSuccess) return 0;
   // every resident CTA holds its accumulators in TMEM (512 columns per SM)
-  uint32_t need = 2u * 2u * static_cast<uint32_t>(ntok) + (forward_att_tc(ntok, stages, hd) ? 4u * kTcRows : 0u),
+  const bool tc = forward_att_tc(ntok, stages, hd);
+  uint32_t need = static_cast<uint32_t>(forward_acc_buffers(ntok, tc) * 2 * ntok) + (tc ? 4u * kTcRows : 0u),
            cols = 32;
   while (cols < need) cols <<= 1;
   const int by_tmem = static_cast<int>(512 / cols);

@@ -128,6 +128,7 @@ int attention_cluster_size(int hd, int cap, size_t smem_limit);
 // --------------------------------------------------- persistent decode forward
 constexpr int kMkMaxLayers = 48;
 constexpr int kMkAttRows = 64;  // query rows per (sequence, KV head) of the persistent forward
+constexpr int kMkMaxAcc = 4;    // TMEM accumulator buffers of the persistent forward, at most
 struct MkParams {
   CUtensorMap xmap[6];                    // hb, hb_lo, o, o_lo, act, act_lo (box rows = ntok)
   CUtensorMap wmap[4 * kMkMaxLayers + 1]; // per layer W_qkv, W_o, W_gu, W_d; then the LM head
@@ -135,6 +136,7 @@ struct MkParams {
   int B, n, M, ntok, cap, stages, ssq_ld;
   int att_nch;                            // key chunks per (sequence, KV head)
   int att_tc;                             // attention on the tensor cores (forward_att_tc)
+  int nacc;                               // TMEM accumulator buffers, 2..kMkMaxAcc (forward_acc_buffers)
   float eps, inv_d, scale_log2;
   const uint16_t* embed;
   const float2* rope;
@@ -169,6 +171,7 @@ size_t forward_smem_bytes(int ntok, int stages, int hd);
 int forward_max_stages(int ntok, int hd, size_t budget);
 int forward_ctas_per_sm(int ntok, int stages, int hd);
 bool forward_att_tc(int ntok, int stages, int hd);
+int forward_acc_buffers(int ntok, bool att_tc);
 cudaError_t launch_forward(const MkParams& P, int grid, int hd, cudaStream_t stream);
 
 // ------------------------------------------------------------ small kernels
