@@ -30,6 +30,12 @@ SPEC_DEVINL void cp_async16(uint32_t dst, const void* src, int src_bytes) {
                : "memory");
 }
 SPEC_DEVINL void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+SPEC_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed groups are pending.
+template <int N>
+SPEC_DEVINL void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // byte offset of 16-byte chunk c of row i in a swizzled [rows][HD] bf16 tile
 template <int HD>

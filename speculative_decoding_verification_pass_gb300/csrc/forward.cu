@@ -215,11 +215,13 @@ struct MkSmem {
   int* slots;
   float* sq;        // [128] embedding partial sums
   int* qpre;        // [3][128] QKV epilogue: KV slot, rotary position, fit flag per column
+  int* au;          // [8] this CTA's first attention unit (AttUnit's fields, then a valid flag),
+                    // found during the QKV phase
 };
 
 __host__ __device__ inline size_t mk_att_bytes(int hd) { return static_cast<size_t>(384) * hd; }
 constexpr size_t kMkBarBytes = 512;
-constexpr size_t kMkTail = kMkBarBytes + 256 * 4 + 64 * 4 + 64 * 4 + 128 * 4 + 384 * 4 + 64;
+constexpr size_t kMkTail = kMkBarBytes + 256 * 4 + 64 * 4 + 64 * 4 + 128 * 4 + 384 * 4 + 8 * 4 + 64;
 
 SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
   uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023);
@@ -242,6 +244,7 @@ SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
   s.slots = reinterpret_cast<int*>(s.red + 64);
   s.sq = reinterpret_cast<float*>(s.slots + 64);
   s.qpre = reinterpret_cast<int*>(s.sq + 128);
+  s.au = s.qpre + 384;
   return s;
 }
 
@@ -853,11 +856,12 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
 // words.  The first epilogue thread issues the MMAs (the GEMM issuer
 // is idle between GEMM phases) and commits them to the attention barrier.
 // Shared memory: q [64][128] and K [128][128] in the attention stage, P over
-// K's first half once the scores are in TMEM (the next block's K loads after
-// its O^T MMAs have completed); V in F ring stages that the weight producer
-// leaves free until the O phase's grid barrier has passed (it issues at most
-// S - F of that phase's tiles before it, and nothing of a later phase):
-// F = 2 (V's two halves) when a stage is under 32 KB, else 1.  The cached
+// K's first half once the scores are in TMEM; V in F ring stages that the
+// weight producer leaves free until the O phase's grid barrier has passed (it
+// issues at most S - F of that phase's tiles before it, and nothing of a
+// later phase).  With stages of 32 KB or more, F = 3: V, and a second K and V
+// buffer, so that a block's K and V copies fly while the block before it is
+// computed; below that F = 2 (V's two halves) and one buffer.  The cached
 // rows of a CTA's first block come early: K's during the QKV phase (the
 // attention stage's K area is not used by the GEMM phases), V's once the
 // CTA's last QKV accumulator has been read (its F stages are then free).
@@ -865,7 +869,7 @@ constexpr int kTcKeys = 128;
 constexpr int kTcRows = 32;
 
 // Ring stages of sbytes bytes kept free for the attention phase.
-__host__ __device__ inline int tc_free_stages(uint32_t sbytes) { return sbytes >= 2u * 16384u ? 1 : 2; }
+__host__ __device__ inline int tc_free_stages(uint32_t sbytes) { return sbytes >= 2u * 16384u ? 3 : 2; }
 
 // Byte offset of 16-byte chunk c (of 8 in a 128-byte row) of row i in a
 // K-major tile with 128-byte swizzling: 8-row groups of 1024 bytes.
@@ -923,10 +927,11 @@ SPEC_DEVINL uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
 
 // Where the attention phase keeps its operands (shared addresses).
 struct TcLayout {
-  uint32_t q;       // [64 rows][128] as 2 sub-tiles [64][64] (8 KB apart)
-  uint32_t k;       // [128 keys][128] as 2 sub-tiles [128][64] (16 KB apart)
-  uint32_t v0, v1;  // the V tile's two [128 keys][64 dims] sub-tiles (v0 < v1)
-  uint32_t p;       // P [128 keys][64 rows]: one 128-byte swizzled row per key (over K's first half)
+  uint32_t q;             // [64 rows][128] as 2 sub-tiles [64][64] (8 KB apart)
+  uint32_t k[2];          // [128 keys][128] as 2 sub-tiles [128][64] (16 KB apart); P
+                          // [128 keys][64 rows] (one 128-byte swizzled row per key) over the first
+  uint32_t v0[2], v1[2];  // the V tile's two [128 keys][64 dims] sub-tiles (v0 < v1)
+  bool db;                // two buffers (else [1] = [0])
 };
 
 // n_issued: weight tiles this CTA streamed before the O phase of this layer
@@ -936,34 +941,58 @@ SPEC_DEVINL TcLayout tc_layout(const MkSmem& sm, uint32_t sbytes, int S, uint32_
   const int f0 = static_cast<int>((n_issued + static_cast<uint32_t>(S - F)) % static_cast<uint32_t>(S));
   TcLayout t;
   t.q = smem_u32(sm.att);
-  t.k = t.q + 16384;
-  t.p = t.k;
+  t.k[0] = t.q + 16384;
   const uint32_t ring = smem_u32(sm.ring);
-  if (F == 1) {  // V whole in one stage
-    t.v0 = ring + static_cast<uint32_t>(f0) * sbytes;
-    t.v1 = t.v0 + 16384u;
+  const auto stage = [&](int i) { return ring + static_cast<uint32_t>((f0 + i) % S) * sbytes; };
+  if (F == 3) {  // V, then the second K, then the second V: one stage each
+    t.db = true;
+    t.v0[0] = stage(0);
+    t.k[1] = stage(1);
+    t.v0[1] = stage(2);
+    t.v1[0] = t.v0[0] + 16384u;
+    t.v1[1] = t.v0[1] + 16384u;
   } else {  // V's halves in two stages, the lower address first
-    const int f1 = (f0 + 1) % S;
-    t.v0 = ring + static_cast<uint32_t>(min(f0, f1)) * sbytes;
-    t.v1 = ring + static_cast<uint32_t>(max(f0, f1)) * sbytes;
+    t.db = false;
+    t.v0[0] = min(stage(0), stage(1));
+    t.v1[0] = max(stage(0), stage(1));
+    t.k[1] = t.k[0];
+    t.v0[1] = t.v0[0];
+    t.v1[1] = t.v1[0];
   }
   return t;
 }
 
-// cp.async of 128 keys x 128 dims of one cache into [key][dim] sub-tiles
-// (sub0, sub0 + stride): `what` as in att_load_block (0 every row, zero
-// fill past kend; 1 the rows this pass does not write; 2 the rows it writes).
+// cp.async of rows [i0, i1) of the 128 keys x 128 dims of one cache's block
+// kb into [key][dim] sub-tiles (sub0, sub0 + stride), rows past kend zero
+// filled.  Thread e moves 16-byte chunk e % 16 of rows e / 16 + 8k: its
+// destinations are 1024 bytes apart.
+template <bool kPaged>
+SPEC_DEVINL void tc_load_range(uint32_t sub0, uint32_t stride, const uint16_t* cache, const KVMap& map, int b,
+                               int kvh, int kb, int kend, int i0, int i1, int e) {
+  const int c = e & 15, ir = e >> 4;
+  const uint32_t dst0 = sub0 + static_cast<uint32_t>(c >> 3) * stride + sw128_off(ir, c & 7);
+  for (int i = ir + (i0 > ir ? ((i0 - ir + 7) & ~7) : 0); i < i1; i += 8) {
+    const int key = kb + i;
+    const bool valid = key < kend;
+    const long long g = map.row<kPaged ? 2 : 1>(b, kvh, valid ? key : kb) + c * 8;
+    cp_async16(dst0 + static_cast<uint32_t>(i >> 3) * 1024u, cache + g, valid ? 16 : 0);
+  }
+}
+
+// The block's rows by `what` (as in att_load_block): 0 every row (zero fill
+// past kend); 1 the rows this pass does not write (cached keys, and the zero
+// fill); 2 the rows it writes (keys Lb .. kend - 1).
 template <bool kPaged>
 SPEC_DEVINL void tc_load_rows(uint32_t sub0, uint32_t stride, const uint16_t* cache, const KVMap& map,
                               int b, int kvh, int kb, int kend, int Lb, int what, int e) {
-  for (int idx = e; idx < kTcKeys * 16; idx += kEpiThreads) {
-    const int i = idx >> 4, c = idx & 15;  // key kb + i, dims 8c .. 8c + 7
-    const int key = kb + i;
-    const bool valid = key < kend;
-    const bool fresh = valid && key >= Lb;
-    if ((what == 1 && fresh) || (what == 2 && !fresh)) continue;
-    const long long g = map.row<kPaged ? 2 : 1>(b, kvh, valid ? key : kb) + c * 8;
-    cp_async16(sub0 + static_cast<uint32_t>(c >> 3) * stride + sw128_off(i, c & 7), cache + g, valid ? 16 : 0);
+  const int nc = min(max(Lb - kb, 0), kTcKeys), nv = min(max(kend - kb, 0), kTcKeys);
+  if (what == 0) {
+    tc_load_range<kPaged>(sub0, stride, cache, map, b, kvh, kb, kend, 0, kTcKeys, e);
+  } else if (what == 1) {
+    tc_load_range<kPaged>(sub0, stride, cache, map, b, kvh, kb, kend, 0, nc, e);
+    tc_load_range<kPaged>(sub0, stride, cache, map, b, kvh, kb, kend, nv, kTcKeys, e);
+  } else {
+    tc_load_range<kPaged>(sub0, stride, cache, map, b, kvh, kb, kend, nc, nv, e);
   }
 }
 
@@ -974,7 +1003,12 @@ template <bool kPaged>
 SPEC_DEVINL void tc_prefetch(const MkParams& P, const MkSmem& sm, int l) {
   const int e = threadIdx.x - kEpiFirstThread;
   AttUnit u;
-  if (!att_unit(P, blockIdx.x, u)) return;
+  const bool ok = att_unit(P, blockIdx.x, u);
+  if (e == 0) {  // kept for the attention phase (its sequence's length is an L2 round trip)
+    const int f[8] = {u.b, u.kvh, u.ch, u.Lb, u.kbeg, u.kend, u.nu, ok ? 1 : 0};
+    for (int i = 0; i < 8; ++i) sm.au[i] = f[i];
+  }
+  if (!ok) return;
   const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, 128};
   tc_load_rows<kPaged>(smem_u32(sm.att) + 16384, 16384, P.kc + P.layer_kv * l, map, u.b, u.kvh, u.kbeg,
                        u.kend, u.Lb, 1, e);
@@ -990,7 +1024,8 @@ SPEC_DEVINL void tc_prefetch_v(const MkParams& P, const MkSmem& sm, int l, uint3
   if (!att_unit(P, blockIdx.x, u)) return;
   const TcLayout L = tc_layout(sm, sbytes, P.stages, n_issued);
   const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, 128};
-  tc_load_rows<kPaged>(L.v0, L.v1 - L.v0, P.vc + P.layer_kv * l, map, u.b, u.kvh, u.kbeg, u.kend, u.Lb, 1, e);
+  tc_load_rows<kPaged>(L.v0[0], L.v1[0] - L.v0[0], P.vc + P.layer_kv * l, map, u.b, u.kvh, u.kbeg, u.kend, u.Lb, 1,
+                       e);
 }
 
 SPEC_DEVINL void tc_wait(uint64_t* bar, uint32_t& parity, volatile int* abort) {
@@ -1026,18 +1061,32 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
   const uint32_t id_o = idesc_bf16(HD, 2 * kTcRows) | (1u << 15) | (1u << 16);
   for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
     AttUnit u;
-    if (!att_unit(P, unit, u)) continue;  // uniform across the CTA
+    if (unit == static_cast<int>(blockIdx.x)) {  // found during the QKV phase
+      if (!sm.au[7]) continue;
+      u = AttUnit{sm.au[0], sm.au[1], sm.au[2], sm.au[3], sm.au[4], sm.au[5], sm.au[6]};
+    } else if (!att_unit(P, unit, u)) {
+      continue;  // uniform across the CTA
+    }
     for (int rbase = 0; rbase < R; rbase += kTcRows) {
       const bool first_unit = unit == static_cast<int>(blockIdx.x) && rbase == 0;
-      // q rows rbase .. rbase + 31: hi in tile rows 0..31, lo in 32..63 (zero past R)
-      for (int idx = e; idx < 2 * kTcRows * 16; idx += kEpiThreads) {
-        const int r = idx >> 4, c = idx & 15;
-        const int rr = rbase + (r & (kTcRows - 1));
-        const bool valid = rr < R;
-        const int j = valid ? rr / G : 0, g = valid ? rr % G : 0;
-        const long long off = (static_cast<long long>(u.b) * P.n + j) * qdim + (u.kvh * G + g) * HD + c * 8;
-        cp_async16(L.q + static_cast<uint32_t>(c >> 3) * 8192 + sw128_off(r, c & 7),
-                   (r < kTcRows ? P.q : P.q_lo) + off, valid ? 16 : 0);
+      // q rows rbase .. rbase + 31 (zero past R): hi in tile rows 0..31, lo in
+      // 32..63.  Thread e moves 16-byte chunk e % 16 of rows e / 16 + 8k of
+      // both halves.
+      {
+        const int c = e & 15;
+#pragma unroll
+        for (int k = 0; k < kTcRows / 8; ++k) {
+          const int r = (e >> 4) + 8 * k, rr = rbase + r;
+          const bool valid = rr < R;
+          long long off = 0;
+          if (valid) {
+            const int j = rr / G, g = rr - j * G;
+            off = (static_cast<long long>(u.b) * P.n + j) * qdim + (u.kvh * G + g) * HD + c * 8;
+          }
+          const uint32_t d = L.q + static_cast<uint32_t>(c >> 3) * 8192 + sw128_off(r, c & 7);
+          cp_async16(d, P.q + off, valid ? 16 : 0);
+          cp_async16(d + 4096u, P.q_lo + off, valid ? 16 : 0);  // row r + 32
+        }
       }
       if (e < kTcRows) {
         const int rr = rbase + e;
@@ -1048,11 +1097,18 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
       float acc[kTcRows];
 #pragma unroll
       for (int r = 0; r < kTcRows; ++r) acc[r] = 0.f;
-      for (int kb = u.kbeg; kb < u.kend; kb += kTcKeys) {
-        const bool first_block = first_unit && kb == u.kbeg;
-        tc_load_rows<kPaged>(L.k, 16384, kc, map, u.b, u.kvh, kb, u.kend, u.Lb, first_block ? 2 : 0, e);
-        tc_load_rows<kPaged>(L.v0, L.v1 - L.v0, vc, map, u.b, u.kvh, kb, u.kend, u.Lb, first_block ? 2 : 0, e);
-        cp_async_wait_all();
+      // K and V of block kb into buffer bf, as one group of copies (the first
+      // block of the CTA's first unit: its cached rows came early)
+      const auto issue = [&](int kb, int bf) {
+        const int what = first_unit && kb == u.kbeg ? 2 : 0;
+        tc_load_rows<kPaged>(L.k[bf], 16384, kc, map, u.b, u.kvh, kb, u.kend, u.Lb, what, e);
+        tc_load_rows<kPaged>(L.v0[bf], L.v1[bf] - L.v0[bf], vc, map, u.b, u.kvh, kb, u.kend, u.Lb, what, e);
+        cp_async_commit();
+      };
+      if (L.db) issue(u.kbeg, 0);
+      for (int kb = u.kbeg, bf = 0; kb < u.kend; kb += kTcKeys, bf ^= L.db ? 1 : 0) {
+        if (!L.db) issue(kb, 0);
+        cp_async_wait_group<0>();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         named_bar(kArriveBar, kEpiThreads);
@@ -1060,10 +1116,13 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk)
-            umma_bf16(tmem_att, sdesc_sw128(L.k + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+            umma_bf16(tmem_att, sdesc_sw128(L.k[bf] + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                       sdesc_sw128(L.q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_s, kk > 0 ? 1u : 0u);
           umma_commit(sm.attbar);
         }
+        // the next block's K and V fly while this one is computed (their
+        // buffer's last readers, the MMAs of block kb - 128, are done)
+        if (L.db && kb + kTcKeys < u.kend) issue(kb + kTcKeys, bf ^ 1);
         tc_wait(sm.attbar, att_par, sm.abort);
         // ---- scores of key kb + t for the 32 rows (hi + lo halves)
         float sv[kTcRows], hv2[kTcRows];
@@ -1122,7 +1181,7 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
             w[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
             w[kTcRows / 2 + i] = pack_bf16x2(sv[2 * i] - bf16lo(w[i]), sv[2 * i + 1] - bf16hi(w[i]));
           }
-          const uint32_t prow = L.p + static_cast<uint32_t>(t) * 128;
+          const uint32_t prow = L.k[bf] + static_cast<uint32_t>(t) * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((c ^ (t & 7)) << 4)),
@@ -1138,8 +1197,8 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTcKeys / 16; ++kk)
-            umma_bf16(tmem_att + 2 * kTcRows, sdesc_sw128(L.v0 + kk * 2048, L.v1 - L.v0, 1024),
-                      sdesc_sw128(L.p + kk * 2048, 8192, 1024), id_o, kk > 0 ? 1u : 0u);
+            umma_bf16(tmem_att + 2 * kTcRows, sdesc_sw128(L.v0[bf] + kk * 2048, L.v1[bf] - L.v0[bf], 1024),
+                      sdesc_sw128(L.k[bf] + kk * 2048, 8192, 1024), id_o, kk > 0 ? 1u : 0u);
           umma_commit(sm.attbar);
         }
         tc_wait(sm.attbar, att_par, sm.abort);
@@ -1162,7 +1221,10 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
         __stcg(reinterpret_cast<float2*>(P.att_ml + (ubase * kMkAttRows + rbase + e) * 2),
                make_float2(rowm[e], rowl[e]));
       named_bar(kArriveBar, kEpiThreads);  // the row statistics free for the next pass
-      if (*sm.abort) return;
+      if (*sm.abort) {
+        cp_async_wait_all();  // a block's copies may still be in flight
+        return;
+      }
     }
   }
   // the ring stages go back to the TMA loads of the O phase
@@ -1549,10 +1611,10 @@ int forward_max_stages(int ntok, int hd, size_t budget) {
 
 // Does the persistent forward run its attention on the tensor cores?  Head
 // dim 128, the S^T and O^T columns beside the GEMM accumulators within TMEM,
-// and a ring deep enough to lend tc_free_stages and keep two.
+// and a ring deep enough to lend tc_free_stages and keep one.
 bool forward_att_tc(int ntok, int stages, int hd) {
   const int F = tc_free_stages(static_cast<uint32_t>(stage_bytes(2 * ntok, 1)));
-  return hd == 128 && 4 * ntok + 4 * kTcRows <= 512 && stages >= F + 2;
+  return hd == 128 && 4 * ntok + 4 * kTcRows <= 512 && stages >= F + 1;
 }
 
 // TMEM accumulator buffers of the persistent forward: as many as fit its 512
