@@ -92,18 +92,9 @@ bool mk_att_tc_enabled() {
   return !(e && e[0] == '0');
 }
 
-// Key chunks per (sequence, KV head) of the persistent forward's attention:
-// about one unit per CTA when that leaves at least 4 chunks per pair; a batch
-// with fewer (its pairs alone nearly fill the grid) takes about 4 units per
-// CTA instead, so that one CTA does not walk a whole long sequence while
-// others idle.  Monotonic in the grid size.
-int mk_att_chunks(int grid, int pairs) {
-  pairs = std::max(1, pairs);
-  const int nch = grid / pairs;
-  return std::max(1, nch >= 4 ? nch : (4 * grid + pairs - 1) / pairs);
-}
-// The most chunks any grid up to kMaxGrid uses (the workspace's partials),
-// at most one per 64 cache slots.
+// The most key chunks a (sequence, KV head) of the persistent forward's
+// attention may be cut into (the workspace's partials): enough for about four
+// units per CTA of any grid up to kMaxGrid, at most one per 64 cache slots.
 int mk_att_chunks_max(int pairs, int slot_chunks) {
   const int p = std::max(1, pairs);
   return std::max(1, std::min(slot_chunks, std::max(kMaxGrid / p, (4 * kMaxGrid + p - 1) / p)));
@@ -633,7 +624,7 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       Q.stages = stages;
       Q.ssq_ld = P.ssq_ld;
       const int grid = std::min(m->sm_count * cps, kMaxGrid);
-      Q.att_nch = std::min(P.att_pairs, mk_att_chunks(grid, batch * Hkv));
+      Q.att_nch = P.att_pairs;  // the most chunks a sequence's keys may be cut into
       Q.att_tc = mk_att_tc_enabled() && forward_att_tc(ntok, stages, hd) ? 1 : 0;
       Q.nacc = forward_acc_buffers(ntok, Q.att_tc != 0);
       Q.eps = c.rms_eps;

@@ -217,11 +217,17 @@ struct MkSmem {
   int* qpre;        // [3][128] QKV epilogue: KV slot, rotary position, fit flag per column
   int* au;          // [8] this CTA's first attention unit (AttUnit's fields, then a valid flag),
                     // found during the QKV phase
+  int* aplan;       // [kAttPlanInts] the attention's units (att_plan)
 };
 
 __host__ __device__ inline size_t mk_att_bytes(int hd) { return static_cast<size_t>(384) * hd; }
 constexpr size_t kMkBarBytes = 512;
-constexpr size_t kMkTail = kMkBarBytes + 256 * 4 + 64 * 4 + 64 * 4 + 128 * 4 + 384 * 4 + 8 * 4 + 64;
+// The attention plan in shared memory: chunks per sequence [128], the units
+// before each sequence [129], the position base of each sequence [128], the
+// chunk length in keys.
+constexpr int kAttPlanInts = 512;
+constexpr int kPlanNu = 0, kPlanPre = 128, kPlanLb = 257, kPlanCk = 385;
+constexpr size_t kMkTail = kMkBarBytes + 256 * 4 + 64 * 4 + 64 * 4 + 128 * 4 + 384 * 4 + 8 * 4 + kAttPlanInts * 4 + 64;
 
 SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
   uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023);
@@ -245,6 +251,7 @@ SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
   s.sq = reinterpret_cast<float*>(s.slots + 64);
   s.qpre = reinterpret_cast<int*>(s.sq + 128);
   s.au = s.qpre + 384;
+  s.aplan = s.au + 8;
   return s;
 }
 
@@ -461,9 +468,12 @@ SPEC_DEVINL void embed_phase(const MkParams& P, const MkSmem& sm) {
 }
 
 // ------------------------------------------------------------- attention
-// The keys of (sequence b, KV head) are cut into P.att_nch chunks of a
-// multiple of 64 keys; a unit is one chunk, so a decode batch needs at most
-// one unit per CTA.  A unit walks its chunk in blocks of 64 keys: warp
+// Every sequence's keys are cut into chunks of the same length (a multiple of
+// the block, 64 or 128 keys), chosen for about four units per CTA and at most
+// P.att_nch chunks per sequence (the partials' slots); a unit is one chunk of
+// one KV head, and the units of a batch are numbered sequence by sequence, so
+// the CTAs share the keys evenly whatever the sequences' lengths (att_plan).
+// A unit of the warp-level path walks its chunk in blocks of 64 keys: warp
 // (slot s, query tile qt) takes keys [32 s, 32 s + 32) of every block for the
 // 16 query rows of tile qt and keeps its own online softmax state; the two
 // slots merge in shared memory into the unit's partial (max, sum, O).
@@ -516,18 +526,79 @@ SPEC_DEVINL void att_load_block(const KVLayout& lay, const uint16_t* kc, const u
 struct AttUnit {
   int b, kvh, ch, Lb, kbeg, kend, nu;
 };
-SPEC_DEVINL bool att_unit(const MkParams& P, int unit, AttUnit& u) {
-  const int nch = P.att_nch;
-  if (unit >= P.B * P.Hkv * nch) return false;
-  u.b = unit / (P.Hkv * nch);
-  u.kvh = (unit / nch) % P.Hkv;
-  u.ch = unit % nch;
-  u.Lb = __ldcg(P.pos_base + u.b);
+// The plan of this pass's attention units, by the epilogue threads of every
+// CTA alike (it depends on the sequences' position bases only, fixed from the
+// embedding phase on): the chunk length ck, then per sequence its chunks
+// ceil(Tk / ck), the units before it and its position base.
+SPEC_DEVINL void att_plan(const MkParams& P, const MkSmem& sm) {
+  const int e = threadIdx.x - kEpiFirstThread;
+  int* const pl = sm.aplan;
+  if (e < 32) {
+    int tot = 0, mx = 0;
+    for (int b = e; b < P.B; b += 32) {
+      const int Lb = __ldcg(P.pos_base + b);
+      const int Tk = min(Lb + P.n, P.cap);
+      pl[kPlanLb + b] = Lb;
+      pl[kPlanNu + b] = Tk;
+      tot += Tk;
+      mx = max(mx, Tk);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const int uk = att_unit_keys(P);
+    const long long per = (static_cast<long long>(tot) * P.Hkv + 4ll * gridDim.x - 1) / (4ll * gridDim.x);
+    int ck = static_cast<int>((per + uk - 1) / uk) * uk;
+    ck = max(ck, att_chunk_keys(mx, P.att_nch, uk));  // at most att_nch chunks a sequence
+    __syncwarp();
+    int carry = 0;
+    for (int b0 = 0; b0 < P.B; b0 += 32) {
+      const int b = b0 + e;
+      const int c = b < P.B ? (pl[kPlanNu + b] + ck - 1) / ck : 0;
+      int x = c * P.Hkv;  // inclusive scan of the units over the 32 sequences
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (e >= o) x += y;
+      }
+      if (b < P.B) {
+        pl[kPlanNu + b] = c;
+        pl[kPlanPre + b] = carry + x - c * P.Hkv;
+      }
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (e == 0) {
+      pl[kPlanPre + P.B] = carry;
+      pl[kPlanCk] = ck;
+    }
+  }
+  named_bar(kArriveBar, kEpiThreads);
+}
+
+SPEC_DEVINL int att_units(const MkSmem& sm, const MkParams& P) { return sm.aplan[kPlanPre + P.B]; }
+
+SPEC_DEVINL bool att_unit(const MkParams& P, const MkSmem& sm, int unit, AttUnit& u) {
+  const int* pl = sm.aplan;
+  if (unit >= pl[kPlanPre + P.B]) return false;
+  int lo = 0, hi = P.B - 1;  // the last sequence whose units start at or before this one
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pl[kPlanPre + mid] <= unit)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int r = unit - pl[kPlanPre + lo], nu = pl[kPlanNu + lo], ck = pl[kPlanCk];
+  u.b = lo;
+  u.kvh = r / nu;
+  u.ch = r - u.kvh * nu;
+  u.Lb = pl[kPlanLb + lo];
   const int Tk = min(u.Lb + P.n, P.cap);
-  const int ck = att_chunk_keys(Tk, nch, att_unit_keys(P));
   u.kbeg = u.ch * ck;
   u.kend = min(u.kbeg + ck, Tk);
-  u.nu = (Tk + ck - 1) / ck;  // chunks holding keys
+  u.nu = nu;
   return u.kbeg < u.kend;
 }
 
@@ -545,7 +616,7 @@ template <int HD, bool kPaged>
 SPEC_DEVINL void att_prefetch(const MkParams& P, const MkSmem& sm, int l) {
   const int e = threadIdx.x - kEpiFirstThread;
   AttUnit u;
-  if (!att_unit(P, blockIdx.x, u)) return;
+  if (!att_unit(P, sm, blockIdx.x, u)) return;
   const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, HD};
   att_load_block<HD, kPaged>(att_stage_layout(sm, HD), P.kc + P.layer_kv * l, P.vc + P.layer_kv * l, map, u.b,
                      u.kvh, u.kbeg, u.kend, u.Lb, 1, e);
@@ -658,7 +729,7 @@ SPEC_DEVINL void att_block(const MkParams& P, const KVLayout& lay, uint32_t aQ, 
 // batch needs at most one item per warp (8 KV heads x 20 rows x 2 groups at
 // batch 1, against 608 warps).
 template <int HD>
-SPEC_DEVINL void cmb_phase(const MkParams& P) {
+SPEC_DEVINL void cmb_phase(const MkParams& P, const MkSmem& sm) {
   const int e = threadIdx.x - kEpiFirstThread;
   const int w = e >> 5, lane = e & 31;
   const int G = P.H / P.Hkv;
@@ -673,9 +744,7 @@ SPEC_DEVINL void cmb_phase(const MkParams& P) {
     const int r = (it / kDG) % R;
     const int kvh = (it / (kDG * R)) % P.Hkv;
     const int b = it / (kDG * R * P.Hkv);
-    const int Tk = min(__ldcg(P.pos_base + b) + P.n, P.cap);
-    const int ck = att_chunk_keys(Tk, nch, att_unit_keys(P));
-    const int nu = (Tk + ck - 1) / ck;
+    const int nu = sm.aplan[kPlanNu + b];
     const long long ubase = (static_cast<long long>(b) * P.Hkv + kvh) * nch;
     const float2* ob = reinterpret_cast<const float2*>(P.att_o + (ubase * kMkAttRows + r) * HD + dg * 64) + lane;
     float2 acc = make_float2(0.f, 0.f);
@@ -737,11 +806,11 @@ SPEC_DEVINL void att_phase(const MkParams& P, const MkSmem& sm, int l, uint32_t 
   const uint16_t* vc = P.vc + P.layer_kv * l;
   const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, HD};
   const int nch = P.att_nch;
-  const int units = P.B * P.Hkv * nch;
+  const int units = att_units(sm, P);
   const int g8 = lane >> 2, t4 = lane & 3;
   for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
     AttUnit u;
-    if (!att_unit(P, unit, u)) continue;  // uniform across the CTA
+    if (!att_unit(P, sm, unit, u)) continue;  // uniform across the CTA
     // query rows in passes of 32 (two tiles of 16); the unit's key blocks
     // are loaded again for each pass
     for (int rbase = 0; rbase < R; rbase += 32) {
@@ -1003,7 +1072,7 @@ template <bool kPaged>
 SPEC_DEVINL void tc_prefetch(const MkParams& P, const MkSmem& sm, int l) {
   const int e = threadIdx.x - kEpiFirstThread;
   AttUnit u;
-  const bool ok = att_unit(P, blockIdx.x, u);
+  const bool ok = att_unit(P, sm, blockIdx.x, u);
   if (e == 0) {  // kept for the attention phase (its sequence's length is an L2 round trip)
     const int f[8] = {u.b, u.kvh, u.ch, u.Lb, u.kbeg, u.kend, u.nu, ok ? 1 : 0};
     for (int i = 0; i < 8; ++i) sm.au[i] = f[i];
@@ -1021,7 +1090,7 @@ template <bool kPaged>
 SPEC_DEVINL void tc_prefetch_v(const MkParams& P, const MkSmem& sm, int l, uint32_t sbytes, uint32_t n_issued) {
   const int e = threadIdx.x - kEpiFirstThread;
   AttUnit u;
-  if (!att_unit(P, blockIdx.x, u)) return;
+  if (!att_unit(P, sm, blockIdx.x, u)) return;
   const TcLayout L = tc_layout(sm, sbytes, P.stages, n_issued);
   const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, 128};
   tc_load_rows<kPaged>(L.v0[0], L.v1[0] - L.v0[0], P.vc + P.layer_kv * l, map, u.b, u.kvh, u.kbeg, u.kend, u.Lb, 1,
@@ -1050,7 +1119,7 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
   const uint16_t* vc = P.vc + P.layer_kv * l;
   const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, HD};
   const int nch = P.att_nch;
-  const int units = P.B * P.Hkv * nch;
+  const int units = att_units(sm, P);
   float* rowm = sm.rs;         // [32] running max of each row (log2 units)
   float* rowl = sm.rs + 32;    // [32] running sum
   float* alpha = sm.rs + 64;   // [32] rescale of this block
@@ -1064,7 +1133,7 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
     if (unit == static_cast<int>(blockIdx.x)) {  // found during the QKV phase
       if (!sm.au[7]) continue;
       u = AttUnit{sm.au[0], sm.au[1], sm.au[2], sm.au[3], sm.au[4], sm.au[5], sm.au[6]};
-    } else if (!att_unit(P, unit, u)) {
+    } else if (!att_unit(P, sm, unit, u)) {
       continue;  // uniform across the CTA
     }
     for (int rbase = 0; rbase < R; rbase += kTcRows) {
@@ -1454,7 +1523,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         }
       } else if (kind == PH_CMB) {
         if (!epi_wait(P, sm, ph)) break;
-        cmb_phase<HD>(P);
+        cmb_phase<HD>(P, sm);
       } else {
         if (!epi_wait(P, sm, ph)) break;
         // every CTA read the epoch before arriving on the embedding phase
@@ -1477,6 +1546,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         // QKV: per token column KV slot, rotary position and fit flag
         int* const qpre = sm.qpre;
         if (p.epi == EPI_QKV) {
+          att_plan(P, sm);
           // this layer's first key block, early
           if constexpr (HD == 128) {
             if (P.att_tc)

@@ -134,7 +134,7 @@ struct MkParams {
   CUtensorMap wmap[4 * kMkMaxLayers + 1]; // per layer W_qkv, W_o, W_gu, W_d; then the LM head
   int L, d, H, Hkv, hd, ffn, V, qkv_rows;
   int B, n, M, ntok, cap, stages, ssq_ld;
-  int att_nch;                            // key chunks per (sequence, KV head)
+  int att_nch;                            // the most key chunks per (sequence, KV head): the partials' slots
   int att_tc;                             // attention on the tensor cores (forward_att_tc)
   int nacc;                               // TMEM accumulator buffers, 2..kMkMaxAcc (forward_acc_buffers)
   float eps, inv_d, scale_log2;
