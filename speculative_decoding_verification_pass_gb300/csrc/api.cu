@@ -87,6 +87,11 @@ bool mk_enabled() {
 }
 // Its attention runs on the tensor cores where the shape allows, unless the
 // environment sets SPEC_ATTENTION_TC=0 (read per call, for comparison).
+// ... and loads its blocks with TMA unless SPEC_ATTENTION_TMA=0 (read per call).
+bool mk_att_tma_enabled() {
+  const char* e = getenv("SPEC_ATTENTION_TMA");
+  return !(e && e[0] == '0');
+}
 bool mk_att_tc_enabled() {
   const char* e = getenv("SPEC_ATTENTION_TC");
   return !(e && e[0] == '0');
@@ -176,6 +181,21 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// q (or its lo half) as a 3-D tensor [M tokens][H heads][hd]: a box of 64
+// dimensions x G heads x 32 / G tokens is 32 attention rows (token-major).
+bool make_tmap_q(CUtensorMap* m, const void* base, uint64_t M, uint64_t H, uint64_t hd, uint32_t G) {
+  auto fn = encode_fn();
+  if (!fn || G == 0 || 32 % G) return false;
+  cuuint64_t dims[3] = {hd, H, M};
+  cuuint64_t strides[2] = {hd * 2, H * hd * 2};
+  cuuint32_t box[3] = {64, G, 32 / G};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -627,6 +647,15 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       Q.att_nch = P.att_pairs;  // the most chunks a sequence's keys may be cut into
       Q.att_tc = mk_att_tc_enabled() && forward_att_tc(ntok, stages, hd) ? 1 : 0;
       Q.nacc = forward_acc_buffers(ntok, Q.att_tc != 0);
+      if (Q.att_tc && mk_att_tma_enabled() && hd == 128 && 32 % (H / Hkv) == 0) {
+        const uint64_t kv_rows = pg.table ? static_cast<uint64_t>(c.n_layers) * pg.n_pages * Hkv * SPEC_PAGE_SLOTS
+                                          : static_cast<uint64_t>(c.n_layers) * batch * Hkv * kv->capacity;
+        const uint32_t box = pg.table ? SPEC_PAGE_SLOTS : 128;
+        Q.att_tma = make_tmap(&Q.kvmap[0], kv->k, kv_rows, hd, box) && make_tmap(&Q.kvmap[1], kv->v, kv_rows, hd, box) &&
+                            make_tmap_q(&Q.qmap[0], q, M, H, hd, H / Hkv) && make_tmap_q(&Q.qmap[1], q_lo, M, H, hd, H / Hkv)
+                        ? 1
+                        : 0;
+      }
       Q.eps = c.rms_eps;
       Q.inv_d = 1.0f / d;
       Q.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));

@@ -199,6 +199,23 @@ SPEC_DEVINL void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int
       : "memory");
 }
 
+// The same with a shared-memory address, and a 3-D box.
+SPEC_DEVINL void tma_load_2d_s(uint32_t dst, const CUtensorMap* m, uint64_t* bar, int x, int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+SPEC_DEVINL void tma_load_3d_s(uint32_t dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z,
+                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 SPEC_DEVINL void tmem_alloc(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

@@ -205,6 +205,8 @@ struct MkSmem {
   uint64_t* accfull;
   uint64_t* accempty;
   uint64_t* attbar;  // tensor-core attention MMAs done
+  uint64_t* kvbar;   // [4] the attention's TMA loads: K of buffers 0, 1, then V of buffers 0, 1
+  uint64_t* qbar;    // the attention's TMA load of q
   uint32_t* tmem_slot;
   int* abort;
   int* flag;
@@ -240,7 +242,9 @@ SPEC_DEVINL MkSmem mk_carve(uint8_t* raw, size_t ring_bytes, int hd) {
   s.accfull = s.empty + kMaxStages;
   s.accempty = s.accfull + kMkMaxAcc;
   s.attbar = s.accempty + kMkMaxAcc;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.attbar + 1);
+  s.kvbar = s.attbar + 1;
+  s.qbar = s.kvbar + 4;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.qbar + 1);
   s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
   s.flag = s.abort + 1;
   s.aseq = reinterpret_cast<unsigned*>(s.flag + 1);
@@ -1065,11 +1069,63 @@ SPEC_DEVINL void tc_load_rows(uint32_t sub0, uint32_t stride, const uint16_t* ca
   }
 }
 
+// TMA loads of block kb of unit u's K (which 0) or V (1) cache of layer l
+// into the sub-tiles s0 (dimensions 0..63) and s1 (64..127), completing on
+// bar: one box of 128 rows per sub-tile, or one per 64-slot page.  Rows past
+// the chunk's end hold whatever the cache holds there (tc_zero_rows clears
+// V's).  One thread.
+template <bool kPaged>
+SPEC_DEVINL void tc_tma_kv(const MkParams& P, const AttUnit& u, int l, int kb, uint32_t s0, uint32_t s1, int which,
+                           uint64_t* bar) {
+  const CUtensorMap* m = &P.kvmap[which];
+  const uint64_t pol = l2_policy_evict_first();
+  mbar_arrive_expect_tx(bar, 2u * kTcKeys * 128u);
+  if constexpr (!kPaged) {
+    const int row = ((l * P.B + u.b) * P.Hkv + u.kvh) * P.cap + kb;
+    tma_load_2d_s(s0, m, bar, 0, row, pol);
+    tma_load_2d_s(s1, m, bar, 64, row, pol);
+  } else {
+#pragma unroll
+    for (int pg = 0; pg < 2; ++pg) {
+      const int idx = min(kb / kPageSlots + pg, P.kv_max_pages - 1);
+      int page = __ldg(P.kv_table + static_cast<long long>(u.b) * P.kv_max_pages + idx);
+      page = page < 0 ? 0 : (page >= P.kv_n_pages ? P.kv_n_pages - 1 : page);
+      const int row = ((l * P.kv_n_pages + page) * P.Hkv + u.kvh) * kPageSlots;
+      tma_load_2d_s(s0 + pg * kPageSlots * 128u, m, bar, 0, row, pol);
+      tma_load_2d_s(s1 + pg * kPageSlots * 128u, m, bar, 64, row, pol);
+    }
+  }
+}
+
+// TMA loads of the 32 query rows rbase .. rbase + 31 of unit u (token-major,
+// G heads a token; rows past the sequence are other tokens or zero): hi to
+// tile rows 0..31, lo to 32..63.  One thread.
+SPEC_DEVINL void tc_tma_q(const MkParams& P, const AttUnit& u, int rbase, uint32_t q, uint64_t* bar) {
+  const int G = P.H / P.Hkv;
+  const uint64_t pol = l2_policy_evict_first();
+  mbar_arrive_expect_tx(bar, 4u * kTcRows * 128u);
+  const int z = u.b * P.n + rbase / G, y = u.kvh * G;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    tma_load_3d_s(q + h * 8192u, &P.qmap[0], bar, 64 * h, y, z, pol);
+    tma_load_3d_s(q + h * 8192u + 4096u, &P.qmap[1], bar, 64 * h, y, z, pol);
+  }
+}
+
+// Zero rows nv .. 127 of a [128 keys][128 dims] tile (sub-tiles s0, s1).
+SPEC_DEVINL void tc_zero_rows(uint32_t s0, uint32_t s1, int nv, int e) {
+  for (int i = nv * 16 + e; i < kTcKeys * 16; i += kEpiThreads) {
+    const int row = i >> 4, c = i & 15;
+    const uint32_t a = (c < 8 ? s0 : s1) + static_cast<uint32_t>(row) * 128u + static_cast<uint32_t>(c & 7) * 16u;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+  }
+}
+
 // The cached keys of this CTA's first attention block of layer l, early
 // (during the QKV phase; the attention stage's K area is not used by the
 // GEMM phases).
 template <bool kPaged>
-SPEC_DEVINL void tc_prefetch(const MkParams& P, const MkSmem& sm, int l) {
+SPEC_DEVINL void tc_prefetch(const MkParams& P, const MkSmem& sm, int l, uint32_t& ld_pend) {
   const int e = threadIdx.x - kEpiFirstThread;
   AttUnit u;
   const bool ok = att_unit(P, sm, blockIdx.x, u);
@@ -1078,6 +1134,11 @@ SPEC_DEVINL void tc_prefetch(const MkParams& P, const MkSmem& sm, int l) {
     for (int i = 0; i < 8; ++i) sm.au[i] = f[i];
   }
   if (!ok) return;
+  if (P.att_tma) {  // the whole block (its fresh rows are reloaded after the barrier)
+    if (e == 0) tc_tma_kv<kPaged>(P, u, l, u.kbeg, smem_u32(sm.att) + 16384, smem_u32(sm.att) + 32768, 0, &sm.kvbar[0]);
+    ld_pend |= 1u;
+    return;
+  }
   const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, 128};
   tc_load_rows<kPaged>(smem_u32(sm.att) + 16384, 16384, P.kc + P.layer_kv * l, map, u.b, u.kvh, u.kbeg,
                        u.kend, u.Lb, 1, e);
@@ -1087,11 +1148,17 @@ SPEC_DEVINL void tc_prefetch(const MkParams& P, const MkSmem& sm, int l) {
 // accumulator: every MMA of the phase has then completed, and the weight
 // producer writes none of the three stages that the attention phase uses.
 template <bool kPaged>
-SPEC_DEVINL void tc_prefetch_v(const MkParams& P, const MkSmem& sm, int l, uint32_t sbytes, uint32_t n_issued) {
+SPEC_DEVINL void tc_prefetch_v(const MkParams& P, const MkSmem& sm, int l, uint32_t sbytes, uint32_t n_issued,
+                               uint32_t& ld_pend) {
   const int e = threadIdx.x - kEpiFirstThread;
   AttUnit u;
   if (!att_unit(P, sm, blockIdx.x, u)) return;
   const TcLayout L = tc_layout(sm, sbytes, P.stages, n_issued);
+  if (P.att_tma) {
+    if (e == 0) tc_tma_kv<kPaged>(P, u, l, u.kbeg, L.v0[0], L.v1[0], 1, &sm.kvbar[2]);
+    ld_pend |= 4u;
+    return;
+  }
   const KVMap map{P.kv_table, P.kv_max_pages, P.kv_n_pages, P.Hkv, P.cap, 128};
   tc_load_rows<kPaged>(L.v0[0], L.v1[0] - L.v0[0], P.vc + P.layer_kv * l, map, u.b, u.kvh, u.kbeg, u.kend, u.Lb, 1,
                        e);
@@ -1104,8 +1171,11 @@ SPEC_DEVINL void tc_wait(uint64_t* bar, uint32_t& parity, volatile int* abort) {
 }
 
 template <bool kPaged>
+// ld_par: bit i the parity of the next completion of kvbar[i] (i < 4) or
+// qbar (4); ld_pend: the same bits for TMA loads issued and not yet waited.
 SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32_t sbytes,
-                              uint32_t n_issued, uint32_t tmem_att, uint32_t& att_par) {
+                              uint32_t n_issued, uint32_t tmem_att, uint32_t& att_par, uint32_t& ld_par,
+                              uint32_t& ld_pend) {
   constexpr int HD = 128;
   const int e = threadIdx.x - kEpiFirstThread;
   const int quarter = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
@@ -1128,6 +1198,15 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
   const uint32_t id_s = idesc_bf16(kTcKeys, 2 * kTcRows);
   // A (V^T) and B (P) both MN-major
   const uint32_t id_o = idesc_bf16(HD, 2 * kTcRows) | (1u << 15) | (1u << 16);
+  // q, K and V by TMA, issued by the first epilogue thread and waited by all
+  const bool tma = P.att_tma != 0;
+  if (tma && e == 0) fence_proxy_async();  // this step's q and K/V rows (other CTAs' stores), then TMA reads
+  const auto ld_wait = [&](int i) {
+    if (mbar_wait(i < 4 ? &sm.kvbar[i] : sm.qbar, (ld_par >> i) & 1u, sm.abort)) {
+      ld_par ^= 1u << i;
+      ld_pend &= ~(1u << i);
+    }
+  };
   for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
     AttUnit u;
     if (unit == static_cast<int>(blockIdx.x)) {  // found during the QKV phase
@@ -1141,7 +1220,10 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
       // q rows rbase .. rbase + 31 (zero past R): hi in tile rows 0..31, lo in
       // 32..63.  Thread e moves 16-byte chunk e % 16 of rows e / 16 + 8k of
       // both halves.
-      {
+      if (tma) {
+        if (e == 0) tc_tma_q(P, u, rbase, L.q, sm.qbar);
+        ld_pend |= 16u;
+      } else {
         const int c = e & 15;
 #pragma unroll
         for (int k = 0; k < kTcRows / 8; ++k) {
@@ -1169,7 +1251,18 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
       // K and V of block kb into buffer bf, as one group of copies (the first
       // block of the CTA's first unit: its cached rows came early)
       const auto issue = [&](int kb, int bf) {
-        const int what = first_unit && kb == u.kbeg ? 2 : 0;
+        const bool early = first_unit && kb == u.kbeg;
+        if (tma) {
+          if (!early) {
+            if (e == 0) {
+              tc_tma_kv<kPaged>(P, u, l, kb, L.k[bf], L.k[bf] + 16384, 0, &sm.kvbar[bf]);
+              tc_tma_kv<kPaged>(P, u, l, kb, L.v0[bf], L.v1[bf], 1, &sm.kvbar[2 + bf]);
+            }
+            ld_pend |= (1u << bf) | (4u << bf);
+          }
+          return;
+        }
+        const int what = early ? 2 : 0;
         tc_load_rows<kPaged>(L.k[bf], 16384, kc, map, u.b, u.kvh, kb, u.kend, u.Lb, what, e);
         tc_load_rows<kPaged>(L.v0[bf], L.v1[bf] - L.v0[bf], vc, map, u.b, u.kvh, kb, u.kend, u.Lb, what, e);
         cp_async_commit();
@@ -1177,7 +1270,21 @@ SPEC_DEVINL void att_phase_tc(const MkParams& P, const MkSmem& sm, int l, uint32
       if (L.db) issue(u.kbeg, 0);
       for (int kb = u.kbeg, bf = 0; kb < u.kend; kb += kTcKeys, bf ^= L.db ? 1 : 0) {
         if (!L.db) issue(kb, 0);
-        cp_async_wait_group<0>();
+        if (tma) {
+          ld_wait(bf);
+          ld_wait(2 + bf);
+          if (kb == u.kbeg) ld_wait(4);
+          if (first_unit && kb == u.kbeg) {  // the early block: this step's rows now
+            tc_load_rows<kPaged>(L.k[bf], 16384, kc, map, u.b, u.kvh, kb, u.kend, u.Lb, 2, e);
+            tc_load_rows<kPaged>(L.v0[bf], L.v1[bf] - L.v0[bf], vc, map, u.b, u.kvh, kb, u.kend, u.Lb, 2, e);
+            cp_async_wait_all();
+          }
+          // V rows past the chunk's end (the cache holds anything there; their
+          // P is 0, and 0 times a NaN would not be)
+          if (u.kend - kb < kTcKeys) tc_zero_rows(L.v0[bf], L.v1[bf], u.kend - kb, e);
+        } else {
+          cp_async_wait_group<0>();
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         named_bar(kArriveBar, kEpiThreads);
@@ -1327,6 +1434,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
       mbar_init(&sm.accempty[a], 4);
     }
     mbar_init(sm.attbar, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&sm.kvbar[i], 1);
+    mbar_init(sm.qbar, 1);
     *sm.abort = 0;
     *sm.aseq = 0;
     *sm.open = 0;
@@ -1499,6 +1608,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
     uint32_t apar = 0;  // its use parity
     uint32_t n_issued = 0;  // weight tiles of the GEMM phases so far (this CTA)
     uint32_t att_par = 0;   // parity of the attention barrier
+    uint32_t ld_par = 0, ld_pend = 0;  // the attention's TMA loads (att_phase_tc)
     const uint32_t tmem_att = tmem_base + static_cast<uint32_t>(nacc * ncols);
     unsigned long long* const part64 = reinterpret_cast<unsigned long long*>(P.partials);
     // read before this CTA arrives on the embedding phase; advanced after it
@@ -1513,7 +1623,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         if (!epi_wait(P, sm, ph)) break;
         if constexpr (HD == 128) {
           if (P.att_tc) {
-            att_phase_tc<kPaged>(P, sm, (ph - 1) / kPhPerLayer, sbytes, n_issued, tmem_att, att_par);
+            att_phase_tc<kPaged>(P, sm, (ph - 1) / kPhPerLayer, sbytes, n_issued, tmem_att, att_par, ld_par,
+                                 ld_pend);
             if (*sm.abort) break;
           } else {
             att_phase<HD, kPaged>(P, sm, (ph - 1) / kPhPerLayer, sbytes);
@@ -1550,7 +1661,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
           // this layer's first key block, early
           if constexpr (HD == 128) {
             if (P.att_tc)
-              tc_prefetch<kPaged>(P, sm, g.l);
+              tc_prefetch<kPaged>(P, sm, g.l, ld_pend);
             else
               att_prefetch<HD, kPaged>(P, sm, g.l);
           } else {
@@ -1652,8 +1763,15 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
       }
       phase_arrive(P);
       if constexpr (HD == 128) {
-        if (P.att_tc && v_layer >= 0) tc_prefetch_v<kPaged>(P, sm, v_layer, sbytes, n_issued);
+        if (P.att_tc && v_layer >= 0) tc_prefetch_v<kPaged>(P, sm, v_layer, sbytes, n_issued, ld_pend);
       }
+    }
+    // after a timeout the attention's TMA loads still in flight land first
+    // (bounded waits)
+    if (*sm.abort && ld_pend) {
+      volatile int never = 0;
+      for (int i = 0; i < 5; ++i)
+        if ((ld_pend >> i) & 1u) mbar_wait(i < 4 ? &sm.kvbar[i] : sm.qbar, (ld_par >> i) & 1u, &never);
     }
   }
 

@@ -132,10 +132,13 @@ constexpr int kMkMaxAcc = 4;    // TMEM accumulator buffers of the persistent fo
 struct MkParams {
   CUtensorMap xmap[6];                    // hb, hb_lo, o, o_lo, act, act_lo (box rows = ntok)
   CUtensorMap wmap[4 * kMkMaxLayers + 1]; // per layer W_qkv, W_o, W_gu, W_d; then the LM head
+  CUtensorMap kvmap[2];                   // K, V caches of all layers as [rows][hd], boxes [64][128 | 64 rows]
+  CUtensorMap qmap[2];                    // q hi, lo as [M][H][hd], boxes [64][G][32 / G]
   int L, d, H, Hkv, hd, ffn, V, qkv_rows;
   int B, n, M, ntok, cap, stages, ssq_ld;
   int att_nch;                            // the most key chunks per (sequence, KV head): the partials' slots
   int att_tc;                             // attention on the tensor cores (forward_att_tc)
+  int att_tma;                            // ... with its q, K and V blocks as TMA loads (kvmap, qmap)
   int nacc;                               // TMEM accumulator buffers, 2..kMkMaxAcc (forward_acc_buffers)
   float eps, inv_d, scale_log2;
   const uint16_t* embed;
