@@ -134,14 +134,20 @@ def test_forward_matches_oracle_ragged_batch(cfg):
     pr.model.close()
 
 
-@pytest.mark.parametrize("tc", ["1", "0"], ids=["tcgen05", "mma_sync"])
-def test_attention_paths_match_oracle(tc, monkeypatch):
-    """Head dim 128 has two attention paths in the persistent forward: S^T
+ATT_PATHS = [("1", "1"), ("1", "0"), ("0", "1")]
+ATT_IDS = ["tcgen05_tma", "tcgen05_copies", "mma_sync"]
+
+
+@pytest.mark.parametrize("tc,tma", ATT_PATHS, ids=ATT_IDS)
+def test_attention_paths_match_oracle(tc, tma, monkeypatch):
+    """Head dim 128 has these attention paths in the persistent forward: S^T
     and O^T as tcgen05 MMAs with TMEM accumulators (the default where the
-    shape fits), and warp-level MMAs.  Both match the oracle on a ragged batch
-    of 2 (300 cached tokens: 3 key blocks) verifying a gamma=4 block, before
-    and after a rollback."""
+    shape fits), its key blocks loaded by TMA or by per-thread copies, and
+    warp-level MMAs.  Each matches the oracle on a ragged batch of 2 (300
+    cached tokens: 3 key blocks) verifying a gamma=4 block, before and after a
+    rollback."""
     monkeypatch.setenv("SPEC_ATTENTION_TC", tc)
+    monkeypatch.setenv("SPEC_ATTENTION_TMA", tma)
     cfg = SMALL[1]
     B, cap, gamma = 2, 320, 4
     pr = Pair(cfg, 23, B, cap)
@@ -153,6 +159,32 @@ def test_attention_paths_match_oracle(tc, monkeypatch):
     pr.okv.lens = OM.truncate(pr.okv.lens, n_acc, gamma)
     blk = wl.tokens(15, B, gamma + 1, cfg.vocab)
     _close(pr.gpu(blk), pr.oracle(blk))
+    pr.status_ok()
+    pr.model.close()
+
+
+@pytest.mark.parametrize("tc,tma", ATT_PATHS, ids=ATT_IDS)
+def test_stale_cache_slots_do_not_leak(tc, tma, monkeypatch):
+    """Cache slots past a sequence's length hold whatever the buffer held
+    (a rolled-back pass, never-written memory): fill them with NaN in every
+    layer, K and V, and a verify pass still matches the oracle.  The key
+    blocks of a chunk's end are read whole, so this pins the visibility mask
+    on K and the zeroed V rows."""
+    monkeypatch.setenv("SPEC_ATTENTION_TC", tc)
+    monkeypatch.setenv("SPEC_ATTENTION_TMA", tma)
+    cfg = SMALL[1]
+    B, cap, gamma = 2, 320, 4
+    pr = Pair(cfg, 29, B, cap)
+    pr.prefill(wl.tokens(17, B, 203, cfg.vocab))
+    nan = torch.tensor(0x7FC0, dtype=torch.int16).view(torch.bfloat16)
+    lens = pr.kv.len.cpu().numpy()
+    for b in range(B):
+        pr.kv.k[:, b, :, int(lens[b]):] = nan
+        pr.kv.v[:, b, :, int(lens[b]):] = nan
+    blk = wl.tokens(18, B, gamma + 1, cfg.vocab)
+    got = pr.gpu(blk)
+    assert np.isfinite(got).all()
+    _close(got, pr.oracle(blk))
     pr.status_ok()
     pr.model.close()
 
