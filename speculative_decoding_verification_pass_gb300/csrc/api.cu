@@ -757,6 +757,52 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
 
   const size_t layer_kv = pg.table ? static_cast<size_t>(pg.n_pages) * Hkv * SPEC_PAGE_SLOTS * hd
                                    : static_cast<size_t>(batch) * Hkv * kv->capacity * hd;
+  // decode shapes of head dim 128 past the persistent kernel (more than 128
+  // token rows): the attention on the tensor cores, as launches of its own
+  MkParams* tq = nullptr;
+  if (hd == 128 && P.R <= kMkAttRows && batch <= 128 && mk_att_tc_enabled()) {
+    tq = new MkParams();
+    MkParams& A = *tq;
+    A.B = batch;
+    A.n = n;
+    A.M = M;
+    A.H = H;
+    A.Hkv = Hkv;
+    A.hd = hd;
+    A.cap = kv->capacity;
+    A.stages = kStepAttStages;
+    A.att_nch = P.att_pairs;
+    A.att_tc = 1;
+    A.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));
+    A.anc = d_anc;
+    A.kc = static_cast<uint16_t*>(kv->k);
+    A.vc = static_cast<uint16_t*>(kv->v);
+    A.layer_kv = layer_kv;
+    A.kv_table = pg.table;
+    A.kv_max_pages = pg.max_pages;
+    A.kv_n_pages = pg.n_pages;
+    A.q = q;
+    A.q_lo = q_lo;
+    A.o = o;
+    A.o_lo = o_lo;
+    A.pos_base = pos_base;
+    A.status = status;
+    A.att_o = reinterpret_cast<float*>(W + P.mk_att_o);
+    A.att_ml = reinterpret_cast<float*>(W + P.mk_att_ml);
+    if (mk_att_tma_enabled() && 32 % (H / Hkv) == 0) {
+      const uint64_t kv_rows = pg.table ? static_cast<uint64_t>(c.n_layers) * pg.n_pages * Hkv * SPEC_PAGE_SLOTS
+                                        : static_cast<uint64_t>(c.n_layers) * batch * Hkv * kv->capacity;
+      const uint32_t box = pg.table ? SPEC_PAGE_SLOTS : 128;
+      A.att_tma = make_tmap(&A.kvmap[0], kv->k, kv_rows, hd, box) && make_tmap(&A.kvmap[1], kv->v, kv_rows, hd, box) &&
+                          make_tmap_q(&A.qmap[0], q, M, H, hd, H / Hkv) && make_tmap_q(&A.qmap[1], q_lo, M, H, hd, H / Hkv)
+                      ? 1
+                      : 0;
+    }
+  }
+  struct Free {
+    MkParams* p;
+    ~Free() { delete p; }
+  } free_tq{tq};
   for (int l = 0; l < c.n_layers; ++l) {
     uint16_t* kc = static_cast<uint16_t*>(kv->k) + l * layer_kv;
     uint16_t* vc = static_cast<uint16_t*>(kv->v) + l * layer_kv;
@@ -819,7 +865,10 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
         t.kind = 1;
         cudaEventRecord(t.a, st);
       }
-      SPEC_CUDA(launch_attention(a, st, pdl));
+      if (tq)
+        SPEC_CUDA(launch_attention_tc(*tq, l, m->sm_count, st));
+      else
+        SPEC_CUDA(launch_attention(a, st, pdl));
       if (cx.timing) {
         cudaEventRecord(t.b, st);
         const_cast<spec_model*>(m)->pending.push_back(t);

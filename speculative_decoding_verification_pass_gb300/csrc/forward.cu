@@ -1784,6 +1784,61 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
   }
 }
 
+// The tensor-core attention (head dim 128) of one layer as launches of its
+// own, for passes the persistent kernel does not take (more than 128 token
+// rows): one CTA per SM runs the persistent kernel's attention phase over the
+// batch's units (merge = 0), then a second launch merges the chunk partials
+// (merge = 1).  Three ring-sized stages of kStepStageBytes hold V and the
+// second K and V buffer.
+constexpr uint32_t kStepStageBytes = 36864;
+constexpr int kStepStages = kStepAttStages;
+
+template <bool kPaged>
+__global__ void __launch_bounds__(kMkThreads, 1) attn_step_kernel(const __grid_constant__ MkParams P, int l,
+                                                                  int merge) {
+  extern __shared__ uint8_t smem_raw[];
+  const MkSmem sm = mk_carve(smem_raw, static_cast<size_t>(kStepStageBytes) * kStepStages, 128);
+  const int warp = threadIdx.x >> 5;
+  const int e = threadIdx.x - kEpiFirstThread;
+  if (threadIdx.x == 0) {
+    mbar_init(sm.attbar, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&sm.kvbar[i], 1);
+    mbar_init(sm.qbar, 1);
+    *sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (!merge && warp == 1) {
+    tmem_alloc(sm.tmem_slot, 4u * kTcRows);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (e >= 0 && e < kEpiThreads) {
+    att_plan(P, sm);
+    if (merge) {
+      cmb_phase<128>(P, sm);
+    } else {
+      uint32_t att_par = 0, ld_par = 0, ld_pend = 0;
+      tc_prefetch<kPaged>(P, sm, l, ld_pend);
+      tc_prefetch_v<kPaged>(P, sm, l, kStepStageBytes, 0, ld_pend);
+      att_phase_tc<kPaged>(P, sm, l, kStepStageBytes, 0, *sm.tmem_slot, att_par, ld_par, ld_pend);
+      if (*sm.abort && ld_pend) {  // loads still in flight land first (bounded)
+        volatile int never = 0;
+        for (int i = 0; i < 5; ++i)
+          if ((ld_pend >> i) & 1u) mbar_wait(i < 4 ? &sm.kvbar[i] : sm.qbar, (ld_par >> i) & 1u, &never);
+      }
+    }
+  }
+  if (*sm.abort && threadIdx.x == 0) set_status(P.status, SPEC_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (!merge && warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(*sm.tmem_slot, 4u * kTcRows);
+  }
+}
+
 }  // namespace
 
 size_t forward_smem_bytes(int ntok, int stages, int hd) {
@@ -1859,4 +1914,33 @@ cudaError_t launch_forward(const MkParams& P, int grid, int hd, cudaStream_t str
                : cudaLaunchKernelEx(&cfg, forward_kernel<64, false>, P);
 }
 
+
+// One layer's tensor-core attention for the per-step schedule (P as for the
+// persistent kernel's attention: stages = kStepStages; grid = the SM count).
+cudaError_t launch_attention_tc(const MkParams& P, int l, int grid, cudaStream_t stream) {
+  const size_t smem = 1024 + static_cast<size_t>(kStepStageBytes) * kStepStages + mk_att_bytes(128) + kMkTail;
+  const void* fn = P.kv_table ? reinterpret_cast<const void*>(attn_step_kernel<true>)
+                              : reinterpret_cast<const void*>(attn_step_kernel<false>);
+  static PerDevice<cudaError_t> configured;
+  cudaError_t e = cudaErrorInvalidDevice;
+  if (!configured.get(
+          [&] {
+            for (const void* f : {reinterpret_cast<const void*>(attn_step_kernel<true>),
+                                  reinterpret_cast<const void*>(attn_step_kernel<false>)}) {
+              const cudaError_t r =
+                  cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+              if (r != cudaSuccess) return r;
+            }
+            return cudaSuccess;
+          },
+          &e))
+    return cudaErrorInvalidDevice;
+  if (e != cudaSuccess) return e;
+  for (int merge = 0; merge < 2; ++merge) {
+    void* args[] = {const_cast<MkParams*>(&P), &l, &merge};
+    e = cudaLaunchKernel(fn, dim3(grid), dim3(kMkThreads), args, smem, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 }  // namespace spec
