@@ -48,8 +48,8 @@ TRAFFIC = {
     # algorithmic bytes (weights, KV and logits each move once)
     "forward_kernel": {"files": ["forward.cu", "gemm_common.cuh", "attn_common.cuh", "common.cuh",
                                  "internal.h"],
-                       "source_sha1": "339255fa156d05ece2721f6c2c0f4c97c4ac9e76",
-                       "bytes_per_launch": 15344373384},
+                       "source_sha1": "38644e896e88363c725e260f044e09c8c1e58a14",
+                       "bytes_per_launch": 15425322192},
 }
 
 
