@@ -163,13 +163,14 @@ def _simulate(P, Q, gamma, trials, seed, T=1.0):
 
 def test_chi_square_v8_every_position_follows_p():
     """V=8, gamma=4, fixed (p, q) rows that differ per position; the token
-    emitted at position k (given the pass reached k) must follow P_k."""
+    emitted at position k (given the pass reached k) must follow P_k
+    (10^6 passes, the trial count the parity bar names)."""
     V, gamma = 8, 4
     g = np.random.default_rng(7)
     P = g.dirichlet(np.ones(V), size=gamma + 1)
     Q = np.clip(P[:gamma] + g.normal(0, 0.08, size=(gamma, V)), 0.01, None)
     Q /= Q.sum(1, keepdims=True)
-    res = _simulate(P, Q, gamma, 200_000, seed=11)
+    res = _simulate(P, Q, gamma, 1_000_000, seed=11)
     toks = np.array([r.tokens for r in res])
     for k in range(gamma + 1):
         col = toks[:, k]
@@ -210,6 +211,24 @@ def test_mean_tokens_per_pass_matches_printed(alpha, gamma, printed):
     n = np.array([r.n_accepted + 1 for r in res], dtype=np.float64)
     se = n.std() / np.sqrt(n.size)
     assert abs(n.mean() - printed) < 4 * se + 0.005 + 1e-9
+
+
+@pytest.mark.parametrize("alpha", [0.5, 0.8])
+def test_mean_tokens_per_pass_at_gamma_2(alpha):
+    """gamma = 2 has no printed example: the mean emitted tokens per pass of
+    the oracle's rule must equal the expanded geometric sum 1 + alpha +
+    alpha^2 (the chance of reaching each position), and the controller's
+    closed form must give the same number."""
+    from oracle import gamma as OG
+    p = np.array([0.9, 0.1])
+    q = np.array([0.9 - (1 - alpha), 0.1 + (1 - alpha)])
+    assert np.minimum(p, q).sum() == pytest.approx(alpha)
+    expect = 1.0 + alpha + alpha * alpha
+    assert OG.expected_tokens(alpha, 2) == pytest.approx(expect, abs=1e-12)
+    res = _simulate(np.tile(p, (3, 1)), np.tile(q, (2, 1)), 2, 40_000, seed=int(alpha * 10) + 2)
+    n = np.array([r.n_accepted + 1 for r in res], dtype=np.float64)
+    se = n.std() / np.sqrt(n.size)
+    assert abs(n.mean() - expect) < 4 * se + 1e-9
 
 
 def test_printed_slips_are_not_the_formula():
@@ -262,6 +281,29 @@ def test_topp_applies_to_target_rows():
     for u in np.linspace(0, 0.99, 23):
         r = A.accept(z, q, [2], [u, u], 1.0, top_p=0.8)
         assert r.n_accepted == 0 and r.tokens[0] in (0, 1)
+
+
+def test_draft_sample_pins():
+    """The draft sampler on its own: at top_p = 1, q is torch's fp64 softmax
+    of z / T; its draws with uniform u follow q (chi-square, 2e5 draws); at
+    T = 0 it is the one-hot argmax with the lowest id on ties."""
+    import torch
+    g = np.random.default_rng(23)
+    V, T = 12, 0.7
+    z = g.normal(0, 2, size=(1, V))
+    q, _, _ = A.draft_sample(z, [0.5], T, 1.0)
+    ref = torch.softmax(torch.from_numpy(z[0]) / T, dim=0).numpy()
+    np.testing.assert_allclose(q[0], ref, rtol=1e-12, atol=1e-15)
+    n = 200_000
+    u = g.random(n)
+    zz = np.repeat(z, 64, axis=0)
+    toks = np.concatenate([A.draft_sample(zz, u[i:i + 64], T, 1.0)[1] for i in range(0, n, 64)])
+    obs = np.bincount(toks, minlength=V)
+    chi = stats.chisquare(obs, ref * n)
+    assert chi.pvalue > 1e-3, chi
+    zt = np.array([[0.0, 3.0, 1.0, 3.0]])
+    q0, t0, _ = A.draft_sample(zt, [0.9], 0.0)
+    assert t0[0] == 1 and q0[0].tolist() == [0.0, 1.0, 0.0, 0.0]
 
 
 def test_draft_sample_uses_same_rule():

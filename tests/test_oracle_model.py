@@ -245,3 +245,23 @@ def test_bf16_layer_cache_returns_the_generated_values():
     for k, v in b.layer(1).items():
         np.testing.assert_array_equal(a.layer(1)[k], v)
         np.testing.assert_array_equal(a.layer(1)[k], v)   # from the cache
+
+
+# ---------------------------------------------------------------- LM head
+def test_lm_head_pins():
+    """The LM head is hidden @ head^T: equal to torch's fp64 linear; the
+    identity head returns the hidden states; a one-hot hidden state picks one
+    column of the head; the logits are linear in the head."""
+    g = np.random.default_rng(41)
+    h = g.normal(size=(5, 64))
+    Hd = g.normal(size=(300, 64))
+    Hd2 = g.normal(size=(300, 64))
+    z = Mo.lm_head(h, Hd)
+    assert z.shape == (5, 300)
+    ref = torch.nn.functional.linear(torch.from_numpy(h), torch.from_numpy(Hd)).numpy()
+    np.testing.assert_allclose(z, ref, rtol=1e-13, atol=1e-12)
+    np.testing.assert_allclose(Mo.lm_head(h, np.eye(64)), h, rtol=0, atol=0)
+    e3 = np.zeros((1, 64))
+    e3[0, 3] = 1.0
+    np.testing.assert_allclose(Mo.lm_head(e3, Hd)[0], Hd[:, 3], rtol=0, atol=0)
+    np.testing.assert_allclose(Mo.lm_head(h, Hd + Hd2), Mo.lm_head(h, Hd) + Mo.lm_head(h, Hd2), rtol=1e-12, atol=1e-12)
