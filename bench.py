@@ -48,7 +48,7 @@ TRAFFIC = {
     # algorithmic bytes (weights, KV and logits each move once)
     "forward_kernel": {"files": ["forward.cu", "gemm_common.cuh", "attn_common.cuh", "common.cuh",
                                  "internal.h"],
-                       "source_sha1": "38644e896e88363c725e260f044e09c8c1e58a14",
+                       "source_sha1": "c1788e8953357b00cea892e4662f9106eea83ba7",
                        "bytes_per_launch": 15425322192},
 }
 

@@ -155,10 +155,9 @@ struct EpiPre {
   float2 fr{};              // EPI_QKV: RoPE frequency of this row's dimension
   const int* qkv = nullptr; // EPI_QKV: shared [3][128] per token column: KV slot, rotary
                             // position, fit flag (persistent kernel, tok0 = 0)
-  // The persistent kernel: each epilogue runs once per layer with a cold
-  // instruction cache, so its loops over the valid columns stay rolled (an
-  // unrolled body is fetched anew for every column it reaches), their
-  // operands staged in the exchange buffer ([2][16][128] floats).
+  // The persistent kernel: the epilogues loop over the valid token columns
+  // only (an unrolled 16-column body ran its invalid columns predicated),
+  // their operands staged in the exchange buffer ([2][16][128] floats).
   bool rolled = false;
 };
 
@@ -307,9 +306,7 @@ __device__ void epilogue_chunk_h(const GemmParams& p, const Smem& sm, uint32_t t
     if (pre.qkv) {
       // the persistent forward: KV slot, rotary position and fit flag per
       // column are in shared memory, and so are the values (the exchange
-      // buffer), so the loop over the valid columns stays rolled: this code
-      // runs once per layer, and an unrolled body is fetched anew for every
-      // column it reaches
+      // buffer), so the loop runs over the valid columns only
       const int jn = min(16, p.M - p.tok0 - c0);
 #pragma unroll 1
       for (int j = 0; j < jn; ++j) {
