@@ -173,13 +173,17 @@ size_t spec_workspace_bytes(const spec_model_config* cfg, int batch, int gamma, 
  * capacity sets SPEC_DEV_KV_OVERFLOW, its slots beyond the capacity are not
  * written and its logits are unspecified.
  * Schedule: a decode-shaped pass (batch*(gamma+1) <= 128, (gamma+1) x query
- * heads per KV head <= 32, <= 48 layers, d_model/128 a power of two) runs as
+ * heads per KV head <= 64, <= 48 layers, d_model/128 a power of two) runs as
  * ONE persistent cooperative kernel (one CTA per SM, grid-wide barriers
  * between the pass's steps, weights streaming ahead across them); every
  * other pass (prefill chunks) runs as one kernel per step.  Setting the
  * environment variable SPEC_FORWARD_PERSISTENT=0 forces the per-step
  * schedule (read on every call).  Both give the same results up to fp32
- * summation order. */
+ * summation order.  Attention of head dim 128 in decode shapes runs on the
+ * tensor cores (S^T and O^T as tcgen05 MMAs) with its key blocks loaded by
+ * TMA; SPEC_ATTENTION_TC=0 selects warp-level MMAs instead and
+ * SPEC_ATTENTION_TMA=0 per-thread copies (both read on every call, for
+ * comparison; the results agree up to fp32 summation order). */
 int spec_verify_forward(const spec_model* model, const int32_t* d_tokens, int batch, int gamma,
                         const spec_kv_cache* kv, float* d_logits, void* d_ws, size_t ws_bytes,
                         void* stream);
