@@ -397,7 +397,7 @@ int spec_tree_masks(const int32_t* parents, int n_nodes, uint64_t* out_anc, int3
  *             node i (its children's target distribution).
  * Workspace, limits, schedules and device errors as spec_verify_forward with
  * gamma = n_nodes - 1 (the persistent schedule applies when n_nodes x query
- * heads per KV head <= 32).  The masks and depths are not checked on the
+ * heads per KV head <= 64).  The masks and depths are not checked on the
  * device: a mask bit at or above n_nodes is ignored, and a node whose mask
  * lacks its own bit does not see itself. */
 int spec_verify_forward_tree(const spec_model* model, const int32_t* d_tokens,
