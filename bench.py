@@ -48,7 +48,7 @@ TRAFFIC = {
     # algorithmic bytes (weights, KV and logits each move once)
     "forward_kernel": {"files": ["forward.cu", "gemm_common.cuh", "attn_common.cuh", "common.cuh",
                                  "internal.h"],
-                       "source_sha1": "c1788e8953357b00cea892e4662f9106eea83ba7",
+                       "source_sha1": "3d518a9e59929a1b91e1410307170eb5b5981253",
                        "bytes_per_launch": 15425322192},
 }
 

@@ -1,5 +1,5 @@
 // Persistent decode forward: the whole verification pass of a decode-shaped
-// batch (M = B*(gamma+1) <= 128 token rows, <= 32 query rows per KV head) in
+// batch (M = B*(gamma+1) <= 128 token rows, <= 64 query rows per KV head) in
 // one cooperative kernel.
 //
 // Why: the pass is a stream of 15 GB of weights through HBM ([lattice] /
@@ -8,22 +8,27 @@
 // separate kernels every boundary drains the weight stream (tail of one
 // kernel, launch and pipeline fill of the next).  Here every CTA stays
 // resident; the steps become phases separated by grid-wide barriers, and the
-// weight producer never waits on a barrier: the next phase's weight tiles keep
-// streaming into the shared-memory ring while the dependency resolves, only
-// the activation loads (which need the previous phase's output) wait.
+// weight producer runs ahead of them: up to all but two ring stages of the
+// next phase's weight tiles stream into shared memory while the dependency
+// resolves; the activation loads (which need the previous phase's output)
+// wait for the barrier.
 //
 // Phases: EMBED, then per layer QKV -> ATT -> CMB -> O -> GU -> DOWN, then
 // HEAD.  Warp roles (224 threads):
 //   warp 0 lane 0  weight producer (TMA, runs ahead across phases)
-//   warp 1         TMEM owner; lane 0 issues tcgen05.mma
+//   warp 1         TMEM owner; lane 0 issues the GEMMs' tcgen05.mma
 //   warps 2-5      GEMM epilogues (TMEM -> fused epilogue), embedding,
-//                  attention partials (ATT; the first key block prefetched
-//                  before the QKV phase ends) and their merge (CMB); they
-//                  arrive on the grid barrier for every phase
+//                  attention partials (ATT: S^T and O^T as tcgen05 MMAs with
+//                  TMA-loaded key blocks for head dim 128, warp-level MMAs
+//                  for 64; the first key block's cached rows come early) and
+//                  their merge (CMB); they arrive on the grid barrier for
+//                  every phase
 //   warp 6 lane 0  activation producer (TMA after each phase's barrier)
 // Grid barrier: one monotonic counter; phase k is complete when it holds
 // (k+1) * gridDim.x arrivals.  All waits are bounded (~2 s); a CTA that times
 // out sets the status bit, drains its own copies, frees TMEM and returns.
+// The file also holds the attention phase and its merge as launches of their
+// own (attn_step_kernel) for decode passes above 128 token rows.
 #include "attn_common.cuh"
 #include "common.cuh"
 #include "gemm_common.cuh"
