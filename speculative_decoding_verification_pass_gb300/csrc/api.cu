@@ -657,7 +657,8 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
         const uint64_t kv_rows = pg.table ? static_cast<uint64_t>(c.n_layers) * pg.n_pages * Hkv * SPEC_PAGE_SLOTS
                                           : static_cast<uint64_t>(c.n_layers) * batch * Hkv * kv->capacity;
         const uint32_t box = pg.table ? SPEC_PAGE_SLOTS : 128;
-        Q.att_tma = make_tmap(&Q.kvmap[0], kv->k, kv_rows, hd, box) && make_tmap(&Q.kvmap[1], kv->v, kv_rows, hd, box) &&
+        // the loads' row coordinates are 32-bit
+        Q.att_tma = kv_rows + 128 < (1ull << 31) && make_tmap(&Q.kvmap[0], kv->k, kv_rows, hd, box) && make_tmap(&Q.kvmap[1], kv->v, kv_rows, hd, box) &&
                             make_tmap_q(&Q.qmap[0], q, M, H, hd, H / Hkv) && make_tmap_q(&Q.qmap[1], q_lo, M, H, hd, H / Hkv)
                         ? 1
                         : 0;
@@ -799,7 +800,8 @@ static int verify_forward_impl(const spec_model* m, const int32_t* d_tokens, con
       const uint64_t kv_rows = pg.table ? static_cast<uint64_t>(c.n_layers) * pg.n_pages * Hkv * SPEC_PAGE_SLOTS
                                         : static_cast<uint64_t>(c.n_layers) * batch * Hkv * kv->capacity;
       const uint32_t box = pg.table ? SPEC_PAGE_SLOTS : 128;
-      A.att_tma = make_tmap(&A.kvmap[0], kv->k, kv_rows, hd, box) && make_tmap(&A.kvmap[1], kv->v, kv_rows, hd, box) &&
+      // the loads' row coordinates are 32-bit
+      A.att_tma = kv_rows + 128 < (1ull << 31) && make_tmap(&A.kvmap[0], kv->k, kv_rows, hd, box) && make_tmap(&A.kvmap[1], kv->v, kv_rows, hd, box) &&
                           make_tmap_q(&A.qmap[0], q, M, H, hd, H / Hkv) && make_tmap_q(&A.qmap[1], q_lo, M, H, hd, H / Hkv)
                       ? 1
                       : 0;

@@ -1086,7 +1086,8 @@ SPEC_DEVINL void tc_tma_kv(const MkParams& P, const AttUnit& u, int l, int kb, u
   const uint64_t pol = l2_policy_evict_first();
   mbar_arrive_expect_tx(bar, 2u * kTcKeys * 128u);
   if constexpr (!kPaged) {
-    const int row = ((l * P.B + u.b) * P.Hkv + u.kvh) * P.cap + kb;
+    // (below 2^31: the launcher enables these loads only then)
+    const int row = static_cast<int>(((static_cast<long long>(l) * P.B + u.b) * P.Hkv + u.kvh) * P.cap + kb);
     tma_load_2d_s(s0, m, bar, 0, row, pol);
     tma_load_2d_s(s1, m, bar, 64, row, pol);
   } else {
@@ -1095,7 +1096,8 @@ SPEC_DEVINL void tc_tma_kv(const MkParams& P, const AttUnit& u, int l, int kb, u
       const int idx = min(kb / kPageSlots + pg, P.kv_max_pages - 1);
       int page = __ldg(P.kv_table + static_cast<long long>(u.b) * P.kv_max_pages + idx);
       page = page < 0 ? 0 : (page >= P.kv_n_pages ? P.kv_n_pages - 1 : page);
-      const int row = ((l * P.kv_n_pages + page) * P.Hkv + u.kvh) * kPageSlots;
+      const int row =
+          static_cast<int>(((static_cast<long long>(l) * P.kv_n_pages + page) * P.Hkv + u.kvh) * kPageSlots);
       tma_load_2d_s(s0 + pg * kPageSlots * 128u, m, bar, 0, row, pol);
       tma_load_2d_s(s1 + pg * kPageSlots * 128u, m, bar, 64, row, pol);
     }
