@@ -40,16 +40,17 @@ METRIC = "verify-pass HBM GB/s (% of peak) and emitted tokens/s, 8B-shape γ=4, 
 # source files (concatenated in the order listed): reported only while the
 # sources are the ones that were measured.
 TRAFFIC = {
-    # one 8B-dims layer's four GEMMs x 32 + the LM head, / 129 launches
+    # batch 64 (each GEMM as two launches of 160 token rows): one 8B-dims
+    # layer's eight GEMM launches x 32 + the LM head's two, / 258 launches
     "gemm_tc_kernel": {"files": ["gemm.cu", "gemm_common.cuh", "common.cuh", "internal.h"],
-                       "source_sha1": "8e216fc32ca40f7636d65c01def4ef52f68a3a17",
-                       "bytes_per_launch": 118288036},
+                       "source_sha1": "36566c7909da3760678d86e0d9dbd8f440c8aa8e",
+                       "bytes_per_launch": 125648430},
     # a 2-layer capture with the 8B dimensions, scaled to 32 layers by the
     # algorithmic bytes (weights, KV and logits each move once)
     "forward_kernel": {"files": ["forward.cu", "gemm_common.cuh", "attn_common.cuh", "common.cuh",
                                  "internal.h"],
-                       "source_sha1": "6140a4f47b4621bde2e00641e2165989a896da5c",
-                       "bytes_per_launch": 15421350216},
+                       "source_sha1": "a165398be6c6405ba198ab3d2b8e17fe5996d671",
+                       "bytes_per_launch": 15426783985},
 }
 
 

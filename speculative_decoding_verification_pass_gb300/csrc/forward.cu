@@ -231,8 +231,8 @@ __host__ __device__ inline size_t mk_att_bytes(int hd) { return static_cast<size
 constexpr size_t kMkBarBytes = 512;
 // The attention plan in shared memory: chunks per sequence [128], the units
 // before each sequence [129], the position base of each sequence [128], the
-// chunk length in keys.
-constexpr int kAttPlanInts = 512;
+// chunk length in keys of each sequence [128].
+constexpr int kAttPlanInts = 516;
 constexpr int kPlanNu = 0, kPlanPre = 128, kPlanLb = 257, kPlanCk = 385;
 constexpr size_t kMkTail = kMkBarBytes + 256 * 4 + 64 * 4 + 64 * 4 + 128 * 4 + 384 * 4 + 8 * 4 + kAttPlanInts * 4 + 64;
 
@@ -537,9 +537,15 @@ struct AttUnit {
 };
 // The plan of this pass's attention units, by the epilogue threads of every
 // CTA alike (it depends on the sequences' position bases only, fixed from the
-// embedding phase on): the chunk length ck, then per sequence its chunks
-// ceil(Tk / ck), the units before it and its position base.
-SPEC_DEVINL void att_plan(const MkParams& P, const MkSmem& sm) {
+// embedding phase on): a chunk length ck for the batch (about four units a
+// CTA), then per sequence its chunks c = ceil(Tk / ck), the units before it,
+// its position base and its own chunk length, Tk / c rounded up to whole
+// blocks.  Chunks of one length within a sequence keep the units that a CTA
+// takes in turn (unit, unit + grid, ...) near one length: with one length for
+// the whole batch every sequence ends in a short chunk, and where the units
+// per sequence are even the CTAs of one parity took every long one.  grid:
+// the CTAs of the attention phase (the merge plans with the attention's).
+SPEC_DEVINL void att_plan(const MkParams& P, const MkSmem& sm, int grid) {
   const int e = threadIdx.x - kEpiFirstThread;
   int* const pl = sm.aplan;
   if (e < 32) {
@@ -558,14 +564,17 @@ SPEC_DEVINL void att_plan(const MkParams& P, const MkSmem& sm) {
       mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     const int uk = att_unit_keys(P);
-    const long long per = (static_cast<long long>(tot) * P.Hkv + 4ll * gridDim.x - 1) / (4ll * gridDim.x);
+    const long long per = (static_cast<long long>(tot) * P.Hkv + 4ll * grid - 1) / (4ll * grid);
     int ck = static_cast<int>((per + uk - 1) / uk) * uk;
     ck = max(ck, att_chunk_keys(mx, P.att_nch, uk));  // at most att_nch chunks a sequence
     __syncwarp();
     int carry = 0;
     for (int b0 = 0; b0 < P.B; b0 += 32) {
       const int b = b0 + e;
-      const int c = b < P.B ? (pl[kPlanNu + b] + ck - 1) / ck : 0;
+      const int Tk = b < P.B ? pl[kPlanNu + b] : 0;
+      const int c = (Tk + ck - 1) / ck;
+      // c chunks of ckb <= ck keys: (c - 1) * ckb < Tk <= c * ckb
+      const int ckb = c > 0 ? ((Tk + c - 1) / c + uk - 1) / uk * uk : uk;
       int x = c * P.Hkv;  // inclusive scan of the units over the 32 sequences
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -575,13 +584,11 @@ SPEC_DEVINL void att_plan(const MkParams& P, const MkSmem& sm) {
       if (b < P.B) {
         pl[kPlanNu + b] = c;
         pl[kPlanPre + b] = carry + x - c * P.Hkv;
+        pl[kPlanCk + b] = ckb;
       }
       carry += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (e == 0) {
-      pl[kPlanPre + P.B] = carry;
-      pl[kPlanCk] = ck;
-    }
+    if (e == 0) pl[kPlanPre + P.B] = carry;
   }
   named_bar(kArriveBar, kEpiThreads);
 }
@@ -599,7 +606,7 @@ SPEC_DEVINL bool att_unit(const MkParams& P, const MkSmem& sm, int unit, AttUnit
     else
       hi = mid - 1;
   }
-  const int r = unit - pl[kPlanPre + lo], nu = pl[kPlanNu + lo], ck = pl[kPlanCk];
+  const int r = unit - pl[kPlanPre + lo], nu = pl[kPlanNu + lo], ck = pl[kPlanCk + lo];
   u.b = lo;
   u.kvh = r / nu;
   u.ch = r - u.kvh * nu;
@@ -1664,7 +1671,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
         // QKV: per token column KV slot, rotary position and fit flag
         int* const qpre = sm.qpre;
         if (p.epi == EPI_QKV) {
-          att_plan(P, sm);
+          att_plan(P, sm, gridDim.x);
           // this layer's first key block, early
           if constexpr (HD == 128) {
             if (P.att_tc)
@@ -1794,15 +1801,14 @@ __global__ void __launch_bounds__(kMkThreads, 1) forward_kernel(const __grid_con
 // The tensor-core attention (head dim 128) of one layer as launches of its
 // own, for passes the persistent kernel does not take (more than 128 token
 // rows): one CTA per SM runs the persistent kernel's attention phase over the
-// batch's units (merge = 0), then a second launch merges the chunk partials
-// (merge = 1).  Three ring-sized stages of kStepStageBytes hold V and the
-// second K and V buffer.
+// batch's units (attn_step_kernel), then cmb_step_kernel merges the chunk
+// partials.  Three ring-sized stages of kStepStageBytes hold V and the second
+// K and V buffer.
 constexpr uint32_t kStepStageBytes = 36864;
 constexpr int kStepStages = kStepAttStages;
 
 template <bool kPaged>
-__global__ void __launch_bounds__(kMkThreads, 1) attn_step_kernel(const __grid_constant__ MkParams P, int l,
-                                                                  int merge) {
+__global__ void __launch_bounds__(kMkThreads, 1) attn_step_kernel(const __grid_constant__ MkParams P, int l) {
   extern __shared__ uint8_t smem_raw[];
   const MkSmem sm = mk_carve(smem_raw, static_cast<size_t>(kStepStageBytes) * kStepStages, 128);
   const int warp = threadIdx.x >> 5;
@@ -1814,7 +1820,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) attn_step_kernel(const __grid_c
     *sm.abort = 0;
     fence_mbar_init();
   }
-  if (!merge && warp == 1) {
+  if (warp == 1) {
     tmem_alloc(sm.tmem_slot, 4u * kTcRows);
     tmem_relinquish();
   }
@@ -1822,28 +1828,40 @@ __global__ void __launch_bounds__(kMkThreads, 1) attn_step_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   if (e >= 0 && e < kEpiThreads) {
-    att_plan(P, sm);
-    if (merge) {
-      cmb_phase<128>(P, sm);
-    } else {
-      uint32_t att_par = 0, ld_par = 0, ld_pend = 0;
-      tc_prefetch<kPaged>(P, sm, l, ld_pend);
-      tc_prefetch_v<kPaged>(P, sm, l, kStepStageBytes, 0, ld_pend);
-      att_phase_tc<kPaged>(P, sm, l, kStepStageBytes, 0, *sm.tmem_slot, att_par, ld_par, ld_pend);
-      if (*sm.abort && ld_pend) {  // loads still in flight land first (bounded)
-        volatile int never = 0;
-        for (int i = 0; i < 5; ++i)
-          if ((ld_pend >> i) & 1u) mbar_wait(i < 4 ? &sm.kvbar[i] : sm.qbar, (ld_par >> i) & 1u, &never);
-      }
+    att_plan(P, sm, gridDim.x);
+    uint32_t att_par = 0, ld_par = 0, ld_pend = 0;
+    tc_prefetch<kPaged>(P, sm, l, ld_pend);
+    tc_prefetch_v<kPaged>(P, sm, l, kStepStageBytes, 0, ld_pend);
+    att_phase_tc<kPaged>(P, sm, l, kStepStageBytes, 0, *sm.tmem_slot, att_par, ld_par, ld_pend);
+    if (*sm.abort && ld_pend) {  // loads still in flight land first (bounded)
+      volatile int never = 0;
+      for (int i = 0; i < 5; ++i)
+        if ((ld_pend >> i) & 1u) mbar_wait(i < 4 ? &sm.kvbar[i] : sm.qbar, (ld_par >> i) & 1u, &never);
     }
   }
   if (*sm.abort && threadIdx.x == 0) set_status(P.status, SPEC_DEV_TIMEOUT);
   tc_fence_before();
   __syncthreads();
-  if (!merge && warp == 1) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(*sm.tmem_slot, 4u * kTcRows);
   }
+}
+
+// The merge of attn_step_kernel's chunk partials: the persistent kernel's CMB
+// phase (one warp per (sequence, KV head, row, 64 dimensions) item, a
+// latency-bound chain of L2 loads) in CTAs that hold only the plan, so that
+// several of them share an SM instead of the attention launch's one.
+constexpr int kCmbCtasPerSm = 3;
+
+__global__ void __launch_bounds__(kGemmThreads, kCmbCtasPerSm)
+    cmb_step_kernel(const __grid_constant__ MkParams P, int att_grid) {
+  extern __shared__ uint8_t smem_raw[];
+  const MkSmem sm = mk_carve(smem_raw, 0, 0);
+  const int e = threadIdx.x - kEpiFirstThread;
+  if (e < 0) return;  // warps 0 and 1: the four warps after them take the items
+  att_plan(P, sm, att_grid);
+  cmb_phase<128>(P, sm);
 }
 
 }  // namespace
@@ -1923,7 +1941,8 @@ cudaError_t launch_forward(const MkParams& P, int grid, int hd, cudaStream_t str
 
 
 // One layer's tensor-core attention for the per-step schedule (P as for the
-// persistent kernel's attention: stages = kStepStages; grid = the SM count).
+// persistent kernel's attention: stages = kStepStages; grid = the SM count):
+// the attention launch, then the merge launch.
 cudaError_t launch_attention_tc(const MkParams& P, int l, int grid, cudaStream_t stream) {
   const size_t smem = 1024 + static_cast<size_t>(kStepStageBytes) * kStepStages + mk_att_bytes(128) + kMkTail;
   const void* fn = P.kv_table ? reinterpret_cast<const void*>(attn_step_kernel<true>)
@@ -1943,11 +1962,13 @@ cudaError_t launch_attention_tc(const MkParams& P, int l, int grid, cudaStream_t
           &e))
     return cudaErrorInvalidDevice;
   if (e != cudaSuccess) return e;
-  for (int merge = 0; merge < 2; ++merge) {
-    void* args[] = {const_cast<MkParams*>(&P), &l, &merge};
-    e = cudaLaunchKernel(fn, dim3(grid), dim3(kMkThreads), args, smem, stream);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  void* args[] = {const_cast<MkParams*>(&P), &l};
+  e = cudaLaunchKernel(fn, dim3(grid), dim3(kMkThreads), args, smem, stream);
+  if (e != cudaSuccess) return e;
+  // (the plan's chunk length depends on the attention's grid: the merge plans
+  // with it, then takes its items over kCmbCtasPerSm times as many CTAs)
+  void* cargs[] = {const_cast<MkParams*>(&P), &grid};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(cmb_step_kernel), dim3(grid * kCmbCtasPerSm),
+                          dim3(kGemmThreads), cargs, 1024 + kMkTail, stream);
 }
 }  // namespace spec

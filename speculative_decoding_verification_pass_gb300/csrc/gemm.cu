@@ -263,16 +263,29 @@ __global__ void __launch_bounds__(kThreads, 2)
         __threadfence();
       }
       if (finisher) {
+        // per 16-column chunk: the residual rows (EPI_RESID) and up to four
+        // contributors' partial sums in flight together, one L2 round trip
+        // for most tiles (a tile has about five contributors at 152 CTAs
+        // over 32 tiles)
+        const bool pre_h = p.epi == EPI_RESID;
+        const int f = static_cast<int>(t) * kTileN + r;
         for (int c0 = 0; c0 < p.ntok; c0 += 16) {
-          float own[16], acc[16];
+          float own[16], acc[16], hv[16];
+          if (pre_h) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int m = p.tok0 + c0 + j;
+              hv[j] = (m < p.M && f < p.N) ? ldcg(p.h + static_cast<long long>(m) * p.d + f) : 0.f;
+            }
+          }
           load_acc(tacc, c0, p.ntok, p.split, own);
           if (nc == 1) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[j] = own[j];
           } else {
-            fixup_sum<2>(p.partials, p.ntok, c0, r, c_first, nc, me, sm.slots, own, acc);
+            fixup_sum<4>(p.partials, p.ntok, c0, r, c_first, nc, me, sm.slots, own, acc);
           }
-          epilogue_chunk(p, sm, t, r, c0, acc);
+          epilogue_chunk_h(p, sm, t, r, c0, acc, hv, pre_h, EpiPre{});
         }
       }
       tc_fence_before();
