@@ -43,13 +43,13 @@ TRAFFIC = {
     # batch 64 (each GEMM as two launches of 160 token rows): one 8B-dims
     # layer's eight GEMM launches x 32 + the LM head's two, / 258 launches
     "gemm_tc_kernel": {"files": ["gemm.cu", "gemm_common.cuh", "common.cuh", "internal.h"],
-                       "source_sha1": "36566c7909da3760678d86e0d9dbd8f440c8aa8e",
+                       "source_sha1": "3b1ed332ec29f56b9421a63d49eda92c49aaa74c",
                        "bytes_per_launch": 125648430},
     # a 2-layer capture with the 8B dimensions, scaled to 32 layers by the
     # algorithmic bytes (weights, KV and logits each move once)
     "forward_kernel": {"files": ["forward.cu", "gemm_common.cuh", "attn_common.cuh", "common.cuh",
                                  "internal.h"],
-                       "source_sha1": "a165398be6c6405ba198ab3d2b8e17fe5996d671",
+                       "source_sha1": "3becae6f1076ad3e075db63ed1fe8ae0ccc51305",
                        "bytes_per_launch": 15426783985},
 }
 

@@ -28,7 +28,8 @@
 // (k+1) * gridDim.x arrivals.  All waits are bounded (~2 s); a CTA that times
 // out sets the status bit, drains its own copies, frees TMEM and returns.
 // The file also holds the attention phase and its merge as launches of their
-// own (attn_step_kernel) for decode passes above 128 token rows.
+// own (attn_step_kernel, cmb_step_kernel) for decode passes above 128 token
+// rows.
 #include "attn_common.cuh"
 #include "common.cuh"
 #include "gemm_common.cuh"

@@ -176,9 +176,10 @@ int forward_ctas_per_sm(int ntok, int stages, int hd);
 bool forward_att_tc(int ntok, int stages, int hd);
 int forward_acc_buffers(int ntok, bool att_tc);
 // One layer's tensor-core attention (head dim 128, at most kMkAttRows query
-// rows per KV head, at most 128 sequences) as two launches of grid CTAs: the
-// persistent kernel's attention phase, then its merge into o / o_lo.  P as for
-// the persistent kernel's attention, with stages = kStepAttStages.
+// rows per KV head, at most 128 sequences) as two launches: the persistent
+// kernel's attention phase (grid CTAs, one per SM), then its merge into o /
+// o_lo (3 x grid smaller CTAs).  P as for the persistent kernel's attention,
+// with stages = kStepAttStages.
 constexpr int kStepAttStages = 3;
 cudaError_t launch_attention_tc(const MkParams& P, int l, int grid, cudaStream_t stream);
 cudaError_t launch_forward(const MkParams& P, int grid, int hd, cudaStream_t stream);
