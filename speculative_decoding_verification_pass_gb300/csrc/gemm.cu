@@ -29,7 +29,12 @@
 //    the same number of bytes.  A tile split across CTAs is finished by the
 //    last CTA to arrive (atomic counter), which sums every contributor's
 //    fp32 partial in CTA order: deterministic, no float atomics, no waits on
-//    other CTAs.
+//    other CTAs.  With one CTA per SM (wide token tiles), the contributors
+//    that have no later segment share the finishing instead: each waits
+//    (bounded) until every contributor has arrived, then sums and runs the
+//    epilogue of every n-th 16-column chunk.  After its last MMA a finisher
+//    otherwise spends a few microseconds a chunk on the epilogue's per-column
+//    chains, ten chunks at 160 token rows, while the other CTAs have exited.
 //
 // Epilogues: EPI_STORE (fp32 logits), EPI_RESID (residual add + next norm's
 // bf16 input + sum-of-squares partials), EPI_QKV (RMSNorm scale, RoPE, q to
@@ -48,7 +53,7 @@ constexpr int kThreads = 192;
 
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const __grid_constant__ CUtensorMap tmXlo, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmXlo, const GemmParams p, int shared_finish) {
   extern __shared__ uint8_t smem_raw[];
   const int nb = p.split ? 2 * p.ntok : p.ntok;  // B rows per sub-tile: hi rows, then lo rows
   const int ncols = p.split == 1 ? 2 * p.ntok : p.ntok;  // accumulator columns (UMMA N)
@@ -240,6 +245,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t c_last = part.cta_of((t + 1) * kc - 1);
       const int nc = static_cast<int>(c_last - c_first + 1);
       bool finisher = true;
+      int chunk0 = 0, chunk_step = 1;  // this CTA's 16-column chunks: chunk0, chunk0 + chunk_step, ...
+      // shared finishing: the contributors with no later segment, a prefix
+      // of the tile's CTAs (the last one may go on into the next tile)
+      const bool sharing = shared_finish && nc > 1;
+      const int n_fin = part.start(c_last + 1) > (t + 1) * kc ? nc - 1 : nc;
       if (nc > 1) {
         const int slot = part.slot(me, t);
         float* dst = p.partials + (static_cast<long long>(me) * 2 + slot) * p.ntok * kTileN;
@@ -254,13 +264,27 @@ __global__ void __launch_bounds__(kThreads, 2)
         named_bar(kEpiBar, kEpiThreads);
         if (e == 0) {
           const int old = atomicAdd(&p.counters[t], 1);
-          const int last = old == nc - 1;
-          if (last) p.counters[t] = 0;
-          *sm.flag = last;
+          if (!sharing) {
+            const int last = old == nc - 1;
+            if (last) p.counters[t] = 0;
+            *sm.flag = last;
+          } else if (seg_end == u1) {
+            // every contributor's partials are stored once the count is nc
+            *sm.flag = wait_count(reinterpret_cast<const unsigned*>(p.counters + t), static_cast<unsigned>(nc),
+                                  sm.abort, p.status)
+                           ? 1
+                           : 0;
+          } else {
+            *sm.flag = 0;  // a later segment follows: the others finish this tile
+          }
         }
         named_bar(kEpiBar, kEpiThreads);
         finisher = *sm.flag != 0;
         __threadfence();
+        if (sharing) {
+          chunk0 = static_cast<int>(me - c_first);
+          chunk_step = n_fin;
+        }
       }
       if (finisher) {
         // per 16-column chunk: the residual rows (EPI_RESID) and up to four
@@ -269,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // over 32 tiles)
         const bool pre_h = p.epi == EPI_RESID;
         const int f = static_cast<int>(t) * kTileN + r;
-        for (int c0 = 0; c0 < p.ntok; c0 += 16) {
+        for (int c0 = chunk0 * 16; c0 < p.ntok; c0 += chunk_step * 16) {
           float own[16], acc[16], hv[16];
           if (pre_h) {
 #pragma unroll
@@ -286,6 +310,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             fixup_sum<4>(p.partials, p.ntok, c0, r, c_first, nc, me, sm.slots, own, acc);
           }
           epilogue_chunk_h(p, sm, t, r, c0, acc, hv, pre_h, EpiPre{});
+        }
+        if (sharing) {
+          // the sharers' second arrivals: the last one clears the tile's
+          // counter for the next launch (every sharer has seen nc by then)
+          named_bar(kEpiBar, kEpiThreads);
+          if (e == 0) {
+            const int old = atomicAdd(&p.counters[t], 1);
+            if (old == nc + n_fin - 1) p.counters[t] = 0;
+          }
         }
       }
       tc_fence_before();
@@ -318,6 +351,21 @@ int gemm_max_stages(int rows_b, size_t budget, int ksub) {
 cudaError_t launch_gemm(const CUtensorMap* tmW, const CUtensorMap* tmX, const CUtensorMap* tmXlo,
                         const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
   const size_t smem = gemm_smem_bytes(p.split ? 2 * p.ntok : p.ntok, p.stages, p.ksub);
+  // Shared finishing makes CTAs wait for one another: only where every CTA of
+  // the grid is resident at once, one per SM (no two fit in an SM's shared
+  // memory) and no more CTAs than SMs.
+  static PerDevice<int> sms;
+  int n_sm = 0;
+  if (!sms.get([] {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+          return 0;
+        return v;
+      },
+      &n_sm))
+    n_sm = 0;
+  int shared_finish = (smem > 116 * 1024 && n_sm > 0 && grid <= n_sm) ? 1 : 0;
   static PerDevice<cudaError_t> configured;
   cudaError_t ce = cudaErrorInvalidDevice;
   if (!configured.get([] { return cudaFuncSetAttribute(gemm_tc_kernel,
@@ -335,7 +383,7 @@ cudaError_t launch_gemm(const CUtensorMap* tmW, const CUtensorMap* tmX, const CU
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, *tmW, *tmX, *tmXlo, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, *tmW, *tmX, *tmXlo, p, shared_finish);
 }
 
 }  // namespace spec
