@@ -352,8 +352,8 @@ cudaError_t launch_gemm(const CUtensorMap* tmW, const CUtensorMap* tmX, const CU
                         const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
   const size_t smem = gemm_smem_bytes(p.split ? 2 * p.ntok : p.ntok, p.stages, p.ksub);
   // Shared finishing makes CTAs wait for one another: only where every CTA of
-  // the grid is resident at once, one per SM (no two fit in an SM's shared
-  // memory) and no more CTAs than SMs.
+  // the grid is resident at once, one per SM (no two fit in an SM's 228 KB of
+  // shared memory) and no more CTAs than SMs.
   static PerDevice<int> sms;
   int n_sm = 0;
   if (!sms.get([] {
