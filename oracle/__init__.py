@@ -27,9 +27,12 @@ gamma    -- the dynamic speculation-depth controller (rolling acceptance
 Every function cites the passage it follows.  Parity status per function:
 
 * accept.*                     pinned (worked example, exact enumeration,
-                               chi-square, alpha, E[tokens], greedy rule)
+                               chi-square, alpha, E[tokens], greedy rule;
+                               draft_sample against torch's softmax, its
+                               draws by chi-square, its T = 0 argmax)
 * model.rmsnorm/rope/attention pinned against torch library routines and
-  /swiglu                      mathematical invariants
+  /swiglu/lm_head              mathematical invariants (lm_head: torch's
+                               linear, identity and one-hot heads, linearity)
 * model.forward                pinned by invariants only (one pass equals
                                sequential passes; rollback then re-verify
                                equals a fresh pass; sublayers pinned above).
